@@ -1,0 +1,245 @@
+"""float64 reference for striped (context-parallel) paged attention.
+
+TEST INFRASTRUCTURE ONLY -- see the package docstring.  Straightforward NumPy,
+one head at a time, no blocking, fusion or reordering beyond the definitions.
+
+Readings taken where the pages leave a step open (each is listed with its
+reason in the design notes of the repository):
+
+* The striping index ``s`` is the slot offset inside a logical page.  With the
+  page size a multiple of P this gives the same partner and physical slot as
+  using the global slot number, and a partner page holds ``page_size // P``
+  slots.
+* The log-sum-exp is the natural logarithm.
+* Grouped-query heads: query head ``h`` reads KV head ``h // (Hq // Hkv)``.
+* A decode row attends every key of its row, its own (just written) key
+  included; a row of a non-decode step has a context of ``c`` keys in the pool
+  and its ``i``-th new token (0-based) additionally sees new tokens ``0..i``.
+* MLA: one latent row of ``D_qk`` values per token serves as the key; its
+  first ``D_v`` values are the value.
+* An empty key set gives output 0 and log-sum-exp -inf; merging only such
+  partials gives 0 and -inf again (padding merges to zero).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+NEG_INF = -np.inf
+
+
+# --------------------------------------------------------------------------
+# value conversion (raw input arrays -> exact float64)
+# --------------------------------------------------------------------------
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact float64 value of bfloat16 numbers given as uint16 bit patterns.
+
+    A bfloat16 is the upper half of an IEEE float32, so the value is the
+    float32 whose high 16 bits are ``bits`` and whose low 16 bits are zero.
+    """
+    b = np.asarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def raw_to_f64(raw: np.ndarray) -> np.ndarray:
+    """float64 view of an input array: uint16 means bfloat16 bits, float32 is itself."""
+    raw = np.asarray(raw)
+    if raw.dtype == np.uint16:
+        return bf16_bits_to_f64(raw)
+    if raw.dtype == np.float32 or raw.dtype == np.float64:
+        return raw.astype(np.float64)
+    raise TypeError(f"unsupported raw dtype {raw.dtype}")
+
+
+# --------------------------------------------------------------------------
+# placement (mstar PR #1124, description: striped context-parallel pool)
+# --------------------------------------------------------------------------
+
+def placement(page_row, pos: int, page_size: int, P: int):
+    """Where logical position ``pos`` of a row lives in a P-way striped pool.
+
+    The row's page table ``page_row`` lists logical page ids.  The token sits
+    in logical page ``page_row[pos // page_size]`` at offset
+    ``off = pos % page_size``.  The pool stripes each page's slots over the P
+    partners: offset ``off`` belongs to partner ``off % P`` and is that
+    partner's physical slot ``off // P`` inside the *same* page id (page ids
+    stay logical).  Returns ``(partner, page_id, physical_slot)``.
+    """
+    if P <= 0 or page_size % P != 0:
+        raise ValueError("P must divide page_size")
+    page = int(page_row[pos // page_size])
+    off = pos % page_size
+    return off % P, page, off // P
+
+
+def placement_inverse(page_row, page: int, phys: int, partner: int, page_size: int, P: int) -> int:
+    """Logical position stored at (partner, page id, physical slot); -1 if the
+    page is not in the row's table.  Offset in the page is ``phys * P + partner``."""
+    hits = np.nonzero(np.asarray(page_row) == page)[0]
+    if hits.size == 0:
+        return -1
+    return int(hits[0]) * page_size + phys * P + partner
+
+
+def stripe_positions(length: int, P: int, p: int) -> np.ndarray:
+    """Logical positions of a row of ``length`` keys that partner ``p`` holds.
+
+    Since ``page_size`` is a multiple of P, offset ``off % P == p`` is the same
+    as position ``pos % P == p``.
+    """
+    return np.arange(p, length, P, dtype=np.int64)
+
+
+def expected_pool_image(pool_raw: np.ndarray, page_row, positions, new_raw: np.ndarray,
+                        page_size: int, P: int) -> np.ndarray:
+    """Pool contents after writing new tokens through the placement.
+
+    ``pool_raw`` has the library's physical layout
+    ``[P, num_pages, H_kv, page_size // P, D]``; it is copied, and token ``t``
+    (logical position ``positions[t]``, values ``new_raw[t]`` of shape
+    ``[H_kv, D]``) is written at ``[partner, page, :, slot, :]``.  Negative
+    positions are padding tokens and are not written.
+    """
+    out = np.array(pool_raw, copy=True)
+    for t, pos in enumerate(positions):
+        if pos < 0:
+            continue
+        p, page, slot = placement(page_row, int(pos), page_size, P)
+        out[p, page, :, slot, :] = new_raw[t]
+    return out
+
+
+# --------------------------------------------------------------------------
+# attention (plain softmax definition over the logical key sequence)
+# --------------------------------------------------------------------------
+
+def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float):
+    """Softmax attention of one query token over ``m`` keys, with its LSE.
+
+    q: [Hq, Dqk], K: [m, Hkv, Dqk], V: [m, Hkv, Dv] (float64).
+    For query head h with KV head kh = h // (Hq // Hkv):
+        s_j   = scale * <q[h], K[j, kh]>
+        LSE   = ln sum_j exp(s_j)       (computed as max + ln sum exp(s - max))
+        O[h]  = sum_j exp(s_j - LSE) V[j, kh]
+    With m == 0: O = 0 and LSE = -inf.
+    Returns (O [Hq, Dv], LSE [Hq]).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    Hq = q.shape[0]
+    m, Hkv = K.shape[0], K.shape[1]
+    Dv = V.shape[2]
+    if Hq % Hkv != 0:
+        raise ValueError("query heads must be a multiple of KV heads")
+    g = Hq // Hkv
+    O = np.zeros((Hq, Dv), dtype=np.float64)
+    LSE = np.full((Hq,), NEG_INF, dtype=np.float64)
+    if m == 0:
+        return O, LSE
+    for h in range(Hq):
+        kh = h // g
+        s = scale * (K[:, kh, :] @ q[h])
+        mx = s.max()
+        w = np.exp(s - mx)
+        z = w.sum()
+        O[h] = (w @ V[:, kh, :]) / z
+        LSE[h] = mx + np.log(z)
+    return O, LSE
+
+
+def stripe_partial(q, K, V, scale: float, P: int, p: int):
+    """Partner p's partial: attention restricted to the keys j with j % P == p."""
+    idx = stripe_positions(K.shape[0], P, p)
+    return attention(q, K[idx], V[idx], scale)
+
+
+def merge(O_parts, LSE_parts):
+    """Exact merge of partials over disjoint key sets.
+
+    With M = max_i LSE_i: if M = -inf every partial is empty and the result is
+    O = 0, LSE = -inf.  Otherwise w_i = exp(LSE_i - M), LSE = M + ln sum_i w_i
+    and O = sum_i w_i O_i / sum_i w_i.  Works per head.
+    O_parts: [N, H, Dv], LSE_parts: [N, H].
+    """
+    O_parts = np.asarray(O_parts, dtype=np.float64)
+    LSE_parts = np.asarray(LSE_parts, dtype=np.float64)
+    N, H, Dv = O_parts.shape
+    O = np.zeros((H, Dv), dtype=np.float64)
+    LSE = np.full((H,), NEG_INF, dtype=np.float64)
+    for h in range(H):
+        mx = LSE_parts[:, h].max()
+        if mx == NEG_INF:
+            continue
+        w = np.exp(LSE_parts[:, h] - mx)
+        z = w.sum()
+        O[h] = (w @ O_parts[:, h, :]) / z
+        LSE[h] = mx + np.log(z)
+    return O, LSE
+
+
+def causal_own_attention(q_new, k_new, v_new, scale: float):
+    """Own-token partial of one row of a non-decode step.
+
+    New token i attends the row's new keys 0..i (the K/V the layer passes,
+    causal on equal-length query and key spans).
+    q_new: [n, Hq, Dqk], k_new: [n, Hkv, Dqk], v_new: [n, Hkv, Dv].
+    Returns (O [n, Hq, Dv], LSE [n, Hq]).
+    """
+    n = q_new.shape[0]
+    Hq, Dv = q_new.shape[1], v_new.shape[2]
+    O = np.zeros((n, Hq, Dv), dtype=np.float64)
+    LSE = np.full((n, Hq), NEG_INF, dtype=np.float64)
+    for i in range(n):
+        O[i], LSE[i] = attention(q_new[i], k_new[: i + 1], v_new[: i + 1], scale)
+    return O, LSE
+
+
+def mla_kv(latent: np.ndarray, dv: int):
+    """MLA reading: the latent row [m, 1, Dqk] is the key, its first dv values the value."""
+    return latent, latent[:, :, :dv]
+
+
+# --------------------------------------------------------------------------
+# whole step: the plain definition the striped method must reproduce
+# --------------------------------------------------------------------------
+
+def expected_step(q, k_seq, v_seq, seq_indptr, ctx_len, new_len, qo_indptr,
+                  num_real_rows: int, num_tokens: int, scale: float,
+                  rows=None, heads=None):
+    """Final merged output of a step, by the plain definition (no striping).
+
+    For real row b with ``ctx_len[b]`` keys already in the pool and
+    ``new_len[b]`` new tokens (query tokens ``qo_indptr[b]..qo_indptr[b+1]``),
+    new token i attends the row's logical keys ``0 .. ctx_len[b] + i``.
+    For a decode row (ctx = L - 1, one new token) that is all L keys.
+
+    q: [T, Hq, Dqk]; k_seq: [sum L, Hkv, Dqk]; v_seq: [sum L, Hkv, Dv] (float64),
+    row b's logical sequence at ``seq_indptr[b]:seq_indptr[b+1]``.
+    Tokens of padding rows and tokens past the last real row get O = 0,
+    LSE = -inf.  ``rows``/``heads`` restrict the work to a sample (other
+    entries stay 0 / -inf).
+    Returns (O [T, Hq, Dv], LSE [T, Hq]).
+    """
+    Hq = q.shape[1]
+    Dv = v_seq.shape[2]
+    O = np.zeros((num_tokens, Hq, Dv), dtype=np.float64)
+    LSE = np.full((num_tokens, Hq), NEG_INF, dtype=np.float64)
+    row_list = range(num_real_rows) if rows is None else rows
+    for b in row_list:
+        base = int(seq_indptr[b])
+        for i in range(int(new_len[b])):
+            t = int(qo_indptr[b]) + i
+            m = int(ctx_len[b]) + i + 1
+            Kb = k_seq[base: base + m]
+            Vb = v_seq[base: base + m]
+            if heads is None:
+                O[t], LSE[t] = attention(q[t], Kb, Vb, scale)
+            else:
+                g = Hq // Kb.shape[1]
+                for h in heads:
+                    kh = h // g
+                    o1, l1 = attention(q[t, h: h + 1], Kb[:, kh: kh + 1], Vb[:, kh: kh + 1], scale)
+                    O[t, h], LSE[t, h] = o1[0], l1[0]
+    return O, LSE
