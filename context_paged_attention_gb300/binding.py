@@ -1,0 +1,194 @@
+"""ctypes binding of libcpattn: torch tensors in, C-ABI calls out.
+
+Argument marshalling only -- every step of the computation runs in the CUDA
+library.  There is no fallback: if ``libcpattn.so`` is missing or fails to
+load, every call raises.  Tensors must be CUDA, contiguous and of the
+documented dtype; the current torch stream is used unless one is given.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build_lib import LIB
+
+DTYPE_BF16 = 0
+DTYPE_FP32 = 1
+
+_STATUS_NAMES = {
+    0: "CPATTN_OK",
+    -1: "CPATTN_ERR_INVALID_ARG",
+    -2: "CPATTN_ERR_P_NOT_DIVIDING_PAGE_SIZE",
+    -3: "CPATTN_ERR_UNSUPPORTED_SHAPE",
+    -4: "CPATTN_ERR_MISALIGNED",
+    -5: "CPATTN_ERR_WORKSPACE_TOO_SMALL",
+    -6: "CPATTN_ERR_CUDA",
+}
+
+
+class CpattnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what} failed: {_STATUS_NAMES.get(status, status)} ({status})")
+
+
+class PoolDesc(ctypes.Structure):
+    """Mirror of ``cpattn_pool_desc``."""
+
+    _fields_ = [
+        ("P", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+        ("num_pages", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("head_dim_v", ctypes.c_int32),
+        ("dtype", ctypes.c_int32),
+    ]
+
+    @property
+    def mla(self) -> bool:
+        return self.head_dim_v != self.head_dim
+
+    def pool_shape(self, value: bool = False):
+        d = self.head_dim_v if value else self.head_dim
+        return (self.P, self.num_pages, self.num_kv_heads, self.page_size // self.P, d)
+
+    def torch_dtype(self):
+        return torch.bfloat16 if self.dtype == DTYPE_BF16 else torch.float32
+
+
+_lib = None
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_i64 = ctypes.c_int64
+_sz = ctypes.c_size_t
+_f32 = ctypes.c_float
+_pdesc = ctypes.POINTER(PoolDesc)
+
+_SIGNATURES = {
+    "cpattn_version": (_i32, []),
+    "cpattn_status_string": (ctypes.c_char_p, [_i32]),
+    "cpattn_pool_bytes": (_sz, [_pdesc, _i32]),
+    "cp_kv_write": (_i32, [_pdesc, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp]),
+    "cp_paged_attn_partial": (_i32, [_pdesc, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _i32, _vp, _vp, _f32,
+                                     _vp, _vp, _vp, _sz, _vp, _vp]),
+    "cp_paged_attn_workspace_bytes": (_sz, [_pdesc, _i32, _i32, _i32]),
+    "own_token_attn": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _i32, _i32, _i32, _i32, _f32,
+                              _vp, _vp, _vp]),
+    "lse_merge": (_i32, [_i32, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _i32, _vp, _vp, _vp]),
+}
+
+
+def library_path() -> str:
+    return LIB
+
+
+def load_library(path: str | None = None):
+    """Load libcpattn.so (once).  Raises if it is missing: there is no fallback."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if lib.cpattn_version() != 1:
+        raise RuntimeError("libcpattn version mismatch")
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def version() -> int:
+    return load_library().cpattn_version()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError("tensor must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return t.data_ptr()
+
+
+def _i32_tensor(t, what):
+    if t is not None and t.dtype != torch.int32:
+        raise TypeError(f"{what} must be int32")
+    return _ptr(t)
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _check(status, what):
+    if status != 0:
+        raise CpattnError(status, what)
+
+
+def cp_kv_write(desc: PoolDesc, pool_k, pool_v, k_new, v_new, positions, qo_indptr, kv_page_indptr,
+                kv_page_indices, dev_status=None, stream=None):
+    """Write new K/V rows into the striped pool (see ``cp_kv_write`` in cpattn.h)."""
+    lib = load_library()
+    num_rows = qo_indptr.numel() - 1
+    st = lib.cp_kv_write(ctypes.byref(desc), _ptr(pool_k), _ptr(pool_v), _ptr(k_new), _ptr(v_new),
+                         _i32_tensor(positions, "positions"), _i32_tensor(qo_indptr, "qo_indptr"), num_rows,
+                         positions.numel(), _i32_tensor(kv_page_indptr, "kv_page_indptr"),
+                         _i32_tensor(kv_page_indices, "kv_page_indices"), _i32_tensor(dev_status, "dev_status"),
+                         _stream(stream))
+    _check(st, "cp_kv_write")
+
+
+def workspace_bytes(desc: PoolDesc, num_q_heads: int, num_tokens: int, max_kv_len: int) -> int:
+    return load_library().cp_paged_attn_workspace_bytes(ctypes.byref(desc), num_q_heads, num_tokens, max_kv_len)
+
+
+def cp_paged_attn_partial(desc: PoolDesc, pool_k, pool_v, q, kv_len, max_kv_len, kv_page_indptr, kv_page_indices,
+                          scale, o_part, lse_part, workspace, qo_indptr=None, num_rows=None, dev_status=None,
+                          stream=None):
+    """Per-partner partial attention over the pool (see ``cp_paged_attn_partial`` in cpattn.h)."""
+    lib = load_library()
+    T, Hq = q.shape[0], q.shape[1]
+    B = kv_len.numel() if num_rows is None else num_rows
+    st = lib.cp_paged_attn_partial(ctypes.byref(desc), _ptr(pool_k), _ptr(pool_v), _ptr(q), Hq, B, T,
+                                   _i32_tensor(qo_indptr, "qo_indptr"), _i32_tensor(kv_len, "kv_len"),
+                                   int(max_kv_len), _i32_tensor(kv_page_indptr, "kv_page_indptr"),
+                                   _i32_tensor(kv_page_indices, "kv_page_indices"), float(scale), _ptr(o_part),
+                                   _ptr(lse_part), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                   _i32_tensor(dev_status, "dev_status"), _stream(stream))
+    _check(st, "cp_paged_attn_partial")
+
+
+def own_token_attn(q, k_new, v_new, qo_indptr, num_real_rows, max_q_len, scale, o_own, lse_own, stream=None):
+    """Causal attention of the step's new tokens (see ``own_token_attn`` in cpattn.h)."""
+    lib = load_library()
+    T, Hq, D = q.shape
+    Hkv = k_new.shape[1]
+    Dv = D if v_new is None else v_new.shape[2]
+    dt = DTYPE_BF16 if q.dtype == torch.bfloat16 else DTYPE_FP32
+    st = lib.own_token_attn(_ptr(q), _ptr(k_new), _ptr(v_new), Hq, Hkv, D, Dv, dt,
+                            _i32_tensor(qo_indptr, "qo_indptr"), qo_indptr.numel() - 1, int(num_real_rows), T,
+                            int(max_q_len), float(scale), _ptr(o_own), _ptr(lse_own), _stream(stream))
+    _check(st, "own_token_attn")
+
+
+def lse_merge(o_parts, lse_parts, out, lse_out=None, stream=None):
+    """Exact merge of partials ``o_parts [N, T, H, Dv]`` / ``lse_parts [N, T, H]`` into ``out``."""
+    lib = load_library()
+    N, T, H, Dv = o_parts.shape
+    dt = DTYPE_BF16 if out.dtype == torch.bfloat16 else DTYPE_FP32
+    st = lib.lse_merge(N, _ptr(o_parts), _ptr(lse_parts), T * H * Dv, T * H, T, H, Dv, dt, _ptr(out),
+                       _ptr(lse_out), _stream(stream))
+    _check(st, "lse_merge")

@@ -1,0 +1,242 @@
+// C ABI of libcpattn (declared in include/cpattn.h): argument checks on the
+// host, then the kernel launches.  Nothing here allocates, synchronises or
+// keeps state between calls.
+#include <cstdint>
+
+#include "cpattn.h"
+#include "launch.h"
+
+using namespace cpattn;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int dtype_bytes(int dtype) {
+  if (dtype == CPATTN_DTYPE_BF16) return 2;
+  if (dtype == CPATTN_DTYPE_FP32) return 4;
+  return 0;
+}
+
+// Common descriptor checks.  mla: head_dim != head_dim_v (value = prefix of the key row).
+int check_desc(const cpattn_pool_desc* d) {
+  if (d == nullptr) return CPATTN_ERR_INVALID_ARG;
+  if (d->P < 1 || d->page_size < 1 || d->page_size % d->P != 0) return CPATTN_ERR_P_NOT_DIVIDING_PAGE_SIZE;
+  if (d->num_pages < 1 || d->num_kv_heads < 1 || d->head_dim < 1 || d->head_dim_v < 1)
+    return CPATTN_ERR_INVALID_ARG;
+  const int eb = dtype_bytes(d->dtype);
+  if (eb == 0) return CPATTN_ERR_INVALID_ARG;
+  if ((d->head_dim * eb) % 16 != 0 || (d->head_dim_v * eb) % 16 != 0) return CPATTN_ERR_UNSUPPORTED_SHAPE;
+  if (d->head_dim_v > d->head_dim) return CPATTN_ERR_UNSUPPORTED_SHAPE;
+  return CPATTN_OK;
+}
+
+bool is_mla(const cpattn_pool_desc* d) { return d->head_dim_v != d->head_dim; }
+
+}  // namespace
+
+extern "C" {
+
+int cpattn_version(void) { return CPATTN_VERSION; }
+
+const char* cpattn_status_string(int status) {
+  switch (status) {
+    case CPATTN_OK: return "ok";
+    case CPATTN_ERR_INVALID_ARG: return "invalid argument";
+    case CPATTN_ERR_P_NOT_DIVIDING_PAGE_SIZE: return "P must be >= 1 and divide page_size";
+    case CPATTN_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (head dims / group size)";
+    case CPATTN_ERR_MISALIGNED: return "device pointer not 16-byte aligned";
+    case CPATTN_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case CPATTN_ERR_CUDA: return "CUDA launch failed";
+    default: return "unknown status";
+  }
+}
+
+size_t cpattn_pool_bytes(const cpattn_pool_desc* d, int which_v) {
+  if (check_desc(d) != CPATTN_OK) return 0;
+  const size_t rows = static_cast<size_t>(d->P) * d->num_pages * d->num_kv_heads * (d->page_size / d->P);
+  return rows * (which_v ? d->head_dim_v : d->head_dim) * dtype_bytes(d->dtype);
+}
+
+int cp_kv_write(const cpattn_pool_desc* desc, void* pool_k, void* pool_v, const void* k_new, const void* v_new,
+                const int32_t* positions, const int32_t* qo_indptr, int32_t num_rows, int32_t num_tokens,
+                const int32_t* kv_page_indptr, const int32_t* kv_page_indices, int32_t* dev_status,
+                cudaStream_t stream) {
+  int st = check_desc(desc);
+  if (st != CPATTN_OK) return st;
+  if (num_rows < 0 || num_tokens < 0) return CPATTN_ERR_INVALID_ARG;
+  if (num_tokens == 0) return CPATTN_OK;
+  const bool mla = is_mla(desc);
+  if (pool_k == nullptr || k_new == nullptr || positions == nullptr || qo_indptr == nullptr ||
+      kv_page_indptr == nullptr || kv_page_indices == nullptr || num_rows < 1)
+    return CPATTN_ERR_INVALID_ARG;
+  if (!mla && (pool_v == nullptr || v_new == nullptr)) return CPATTN_ERR_INVALID_ARG;
+  if (mla && (pool_v != nullptr || v_new != nullptr)) return CPATTN_ERR_INVALID_ARG;
+  if (!aligned16(pool_k) || !aligned16(pool_v) || !aligned16(k_new) || !aligned16(v_new))
+    return CPATTN_ERR_MISALIGNED;
+  const int eb = dtype_bytes(desc->dtype);
+  WriteArgs a;
+  a.pool_k = pool_k;
+  a.pool_v = pool_v;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.positions = positions;
+  a.qo_indptr = qo_indptr;
+  a.page_indptr = kv_page_indptr;
+  a.page_indices = kv_page_indices;
+  a.dev_status = dev_status;
+  a.P = desc->P;
+  a.page_size = desc->page_size;
+  a.num_pages = desc->num_pages;
+  a.num_kv_heads = desc->num_kv_heads;
+  a.num_rows = num_rows;
+  a.num_tokens = num_tokens;
+  a.row_bytes_k = desc->head_dim * eb;
+  a.row_bytes_v = mla ? 0 : desc->head_dim_v * eb;
+  return launch_kv_write(a, stream) == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+}
+
+size_t cp_paged_attn_workspace_bytes(const cpattn_pool_desc* desc, int32_t num_q_heads, int32_t num_tokens,
+                                     int32_t max_kv_len) {
+  if (check_desc(desc) != CPATTN_OK || num_q_heads < 1 || num_tokens < 0 || max_kv_len < 0) return 0;
+  if (num_q_heads % desc->num_kv_heads != 0) return 0;
+  PartialPlan plan;
+  if (!plan_partial(is_mla(desc), desc->P, desc->page_size, desc->num_kv_heads, num_q_heads, desc->head_dim,
+                    num_tokens, max_kv_len, dtype_bytes(desc->dtype), &plan))
+    return 0;
+  return plan.bytes();
+}
+
+int cp_paged_attn_partial(const cpattn_pool_desc* desc, const void* pool_k, const void* pool_v, const void* q,
+                          int32_t num_q_heads, int32_t num_rows, int32_t num_tokens, const int32_t* qo_indptr,
+                          const int32_t* kv_len, int32_t max_kv_len, const int32_t* kv_page_indptr,
+                          const int32_t* kv_page_indices, float scale, float* o_part, float* lse_part,
+                          void* workspace, size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream) {
+  int st = check_desc(desc);
+  if (st != CPATTN_OK) return st;
+  if (num_q_heads < 1 || num_rows < 0 || num_tokens < 0 || max_kv_len < 0) return CPATTN_ERR_INVALID_ARG;
+  if (num_q_heads % desc->num_kv_heads != 0) return CPATTN_ERR_INVALID_ARG;
+  if (qo_indptr == nullptr && num_tokens != num_rows) return CPATTN_ERR_INVALID_ARG;
+  if (num_tokens == 0) return CPATTN_OK;
+  const bool mla = is_mla(desc);
+  if (pool_k == nullptr || q == nullptr || o_part == nullptr || lse_part == nullptr || num_rows < 1 ||
+      kv_len == nullptr || kv_page_indptr == nullptr || kv_page_indices == nullptr)
+    return CPATTN_ERR_INVALID_ARG;
+  if (!mla && pool_v == nullptr) return CPATTN_ERR_INVALID_ARG;
+  if (mla && pool_v != nullptr && pool_v != pool_k) return CPATTN_ERR_INVALID_ARG;
+  if (!aligned16(pool_k) || !aligned16(pool_v) || !aligned16(q) || !aligned16(o_part) ||
+      !aligned16(workspace))
+    return CPATTN_ERR_MISALIGNED;
+  if (mla && desc->dtype != CPATTN_DTYPE_BF16) return CPATTN_ERR_UNSUPPORTED_SHAPE;
+
+  PartialPlan plan;
+  if (!plan_partial(mla, desc->P, desc->page_size, desc->num_kv_heads, num_q_heads, desc->head_dim, num_tokens,
+                    max_kv_len, dtype_bytes(desc->dtype), &plan))
+    return CPATTN_ERR_UNSUPPORTED_SHAPE;
+  const size_t need = plan.bytes();
+  if (workspace == nullptr || workspace_bytes < need) return CPATTN_ERR_WORKSPACE_TOO_SMALL;
+
+  auto al = [](size_t x) { return (x + 255) / 256 * 256; };
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  PartialArgs a;
+  a.ws_o = reinterpret_cast<float*>(ws);
+  a.ws_lse = reinterpret_cast<float*>(ws + al(plan.ws_o_floats * 4));
+  a.ws_cnt = reinterpret_cast<int32_t*>(ws + al(plan.ws_o_floats * 4) + al(plan.ws_lse_floats * 4));
+  a.pool_k = pool_k;
+  a.pool_v = mla ? pool_k : pool_v;
+  a.q = q;
+  a.o_part = o_part;
+  a.lse_part = lse_part;
+  a.qo_indptr = qo_indptr;
+  a.kv_len = kv_len;
+  a.page_indptr = kv_page_indptr;
+  a.page_indices = kv_page_indices;
+  a.dev_status = dev_status;
+  a.P = desc->P;
+  a.page_size = desc->page_size;
+  a.ps_l = desc->page_size / desc->P;
+  a.num_pages = desc->num_pages;
+  a.num_kv_heads = desc->num_kv_heads;
+  a.num_q_heads = num_q_heads;
+  a.head_dim = desc->head_dim;
+  a.head_dim_v = desc->head_dim_v;
+  a.num_rows = num_rows;
+  a.num_tokens = num_tokens;
+  a.max_kv_len = max_kv_len;
+  a.seg = plan.seg;
+  a.chunk = plan.chunk;
+  a.max_chunks = plan.max_chunks;
+  a.scale = scale;
+
+  // tickets of multi-chunk stripes start from zero
+  if (plan.max_chunks > 1) {
+    if (cudaMemsetAsync(a.ws_cnt, 0, plan.ws_cnt_ints * sizeof(int32_t), stream) != cudaSuccess)
+      return CPATTN_ERR_CUDA;
+  }
+  cudaError_t err = cudaSuccess;
+  if (mla) return launch_mla_partial(a, stream, &err);
+  return launch_gqa_partial(a, desc->dtype == CPATTN_DTYPE_BF16, stream, &err);
+}
+
+int own_token_attn(const void* q, const void* k_new, const void* v_new, int32_t num_q_heads, int32_t num_kv_heads,
+                   int32_t head_dim, int32_t head_dim_v, int32_t dtype, const int32_t* qo_indptr,
+                   int32_t num_rows_bucket, int32_t num_real_rows, int32_t num_tokens, int32_t max_q_len,
+                   float scale, float* o_own, float* lse_own, cudaStream_t stream) {
+  const int eb = dtype_bytes(dtype);
+  if (eb == 0 || num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads != 0 || num_tokens < 0 ||
+      num_rows_bucket < 1 || num_real_rows < 0 || num_real_rows > num_rows_bucket || max_q_len < 0)
+    return CPATTN_ERR_INVALID_ARG;
+  if (head_dim != head_dim_v) return CPATTN_ERR_UNSUPPORTED_SHAPE;
+  if (num_tokens == 0) return CPATTN_OK;
+  if (q == nullptr || k_new == nullptr || qo_indptr == nullptr || o_own == nullptr || lse_own == nullptr)
+    return CPATTN_ERR_INVALID_ARG;
+  if (v_new == nullptr) v_new = k_new;  // value = prefix (here: all) of the key row
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(o_own)) return CPATTN_ERR_MISALIGNED;
+  OwnArgs a;
+  a.q = q;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.o_own = o_own;
+  a.lse_own = lse_own;
+  a.qo_indptr = qo_indptr;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.num_rows_bucket = num_rows_bucket;
+  a.num_real_rows = num_real_rows;
+  a.num_tokens = num_tokens;
+  a.max_q_len = max_q_len;
+  a.scale = scale;
+  cudaError_t err = cudaSuccess;
+  return launch_own_token(a, dtype == CPATTN_DTYPE_BF16, stream, &err);
+}
+
+int lse_merge(int32_t num_partials, const float* o_parts, const float* lse_parts, int64_t stride_o,
+              int64_t stride_lse, int32_t num_tokens, int32_t num_heads, int32_t head_dim_v, int32_t out_dtype,
+              void* out, float* lse_out, cudaStream_t stream) {
+  if (num_partials < 1 || num_tokens < 0 || num_heads < 1 || head_dim_v < 4 || head_dim_v % 4 != 0)
+    return CPATTN_ERR_INVALID_ARG;
+  if (out_dtype != CPATTN_DTYPE_BF16 && out_dtype != CPATTN_DTYPE_FP32) return CPATTN_ERR_INVALID_ARG;
+  if (num_tokens == 0) return CPATTN_OK;
+  if (o_parts == nullptr || lse_parts == nullptr || out == nullptr) return CPATTN_ERR_INVALID_ARG;
+  const int64_t per_o = static_cast<int64_t>(num_tokens) * num_heads * head_dim_v;
+  const int64_t per_l = static_cast<int64_t>(num_tokens) * num_heads;
+  if (num_partials > 1 && (stride_o < per_o || stride_lse < per_l)) return CPATTN_ERR_INVALID_ARG;
+  if (!aligned16(o_parts) || !aligned16(out) || (stride_o % 4) != 0) return CPATTN_ERR_MISALIGNED;
+  if (out_dtype == CPATTN_DTYPE_BF16 && (head_dim_v % 8) != 0) return CPATTN_ERR_UNSUPPORTED_SHAPE;
+  MergeArgs a;
+  a.num_partials = num_partials;
+  a.o_parts = o_parts;
+  a.lse_parts = lse_parts;
+  a.stride_o = stride_o;
+  a.stride_lse = stride_lse;
+  a.num_tokens = num_tokens;
+  a.num_heads = num_heads;
+  a.head_dim_v = head_dim_v;
+  a.out_bf16 = out_dtype == CPATTN_DTYPE_BF16;
+  a.out = out;
+  a.lse_out = lse_out;
+  return launch_lse_merge(a, stream) == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+}
+
+}  // extern "C"

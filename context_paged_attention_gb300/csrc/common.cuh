@@ -1,0 +1,78 @@
+// Internal helpers shared by the libcpattn kernels (not part of the C ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "cpattn.h"
+
+namespace cpattn {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Record the first device-detected inconsistency (0 stays 0 until something happens).
+__device__ __forceinline__ void report(int32_t* status, int code) {
+  if (status != nullptr) atomicCAS(status, 0, code);
+}
+
+// Two bfloat16 values packed in a 32-bit word -> float (exact).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// A 16-byte chunk of elements of type T, widened to float.
+template <typename T>
+struct Chunk16;
+
+template <>
+struct Chunk16<__nv_bfloat16> {
+  static constexpr int N = 8;
+  __device__ __forceinline__ static void widen(const uint4& u, float* f) {
+    f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x);
+    f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
+    f[4] = bf16_lo(u.z); f[5] = bf16_hi(u.z);
+    f[6] = bf16_lo(u.w); f[7] = bf16_hi(u.w);
+  }
+};
+
+template <>
+struct Chunk16<float> {
+  static constexpr int N = 4;
+  __device__ __forceinline__ static void widen(const uint4& u, float* f) {
+    f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+  }
+};
+
+// 16-byte asynchronous global -> shared copy (bypasses L1).
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// Row of token t: the b in [0, num_rows) with indptr[b] <= t < indptr[b+1]
+// (indptr non-decreasing, t < indptr[num_rows]).  Empty rows are skipped.
+__device__ __forceinline__ int find_row(const int32_t* __restrict__ indptr, int num_rows, int t) {
+  int lo = 0, hi = num_rows - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(indptr + mid) <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Online-softmax state merge in the log2 domain: (m, l) absorbs (m2, l2);
+// returns the factors the two accumulators are scaled by.
+__device__ __forceinline__ void softmax_merge_factors(float m, float m2, float& mn, float& a, float& b) {
+  mn = fmaxf(m, m2);
+  a = (m == -INFINITY) ? 0.f : exp2f(m - mn);
+  b = (m2 == -INFINITY) ? 0.f : exp2f(m2 - mn);
+}
+
+}  // namespace cpattn

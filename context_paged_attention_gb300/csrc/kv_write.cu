@@ -1,0 +1,79 @@
+// cp_kv_write: copy a step's new K/V rows into the P-way striped paged pool.
+//
+// Placement (mstar PR #1124 "Context / Sequence Parallel 1/5", description):
+// offset off of a logical page belongs to partner off % P at physical slot
+// off / P of the same page id.  The review thread of that PR shows the failure
+// this kernel must avoid: taking the slot at the logical page size, which makes
+// every partner write every token at offsets up to page_size - 1.
+//
+// One thread moves one 16-byte chunk of one (token, KV head) row; the chunks of
+// a row are adjacent threads, so both the read of k_new and the write into the
+// pool are coalesced 16-byte accesses.
+#include "common.cuh"
+#include "launch.h"
+
+namespace cpattn {
+
+__global__ void __launch_bounds__(256) kv_write_kernel(const WriteArgs a, int chunks_per_row) {
+  const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t per_token = static_cast<int64_t>(a.num_kv_heads) * chunks_per_row;
+  const int64_t total = per_token * a.num_tokens;
+  if (gid >= total) return;
+  const int t = static_cast<int>(gid / per_token);
+  const int rem = static_cast<int>(gid - static_cast<int64_t>(t) * per_token);
+  const int h = rem / chunks_per_row;
+  const int c = rem - h * chunks_per_row;
+
+  const int end = __ldg(a.qo_indptr + a.num_rows);
+  if (t >= end) return;  // padding token past the last row
+  const int pos = __ldg(a.positions + t);
+  if (pos < 0) return;  // padding token
+  const int b = find_row(a.qo_indptr, a.num_rows, t);
+
+  const int page_idx = pos / a.page_size;
+  const int pbeg = __ldg(a.page_indptr + b);
+  const int pend = __ldg(a.page_indptr + b + 1);
+  if (page_idx >= pend - pbeg) {
+    if (c == 0 && h == 0) report(a.dev_status, CPATTN_DEV_POS_PAST_TABLE);
+    return;
+  }
+  const int page = __ldg(a.page_indices + pbeg + page_idx);
+  if (page < 0 || page >= a.num_pages) {
+    if (c == 0 && h == 0) report(a.dev_status, CPATTN_DEV_PAGE_OUT_OF_RANGE);
+    return;
+  }
+  const int off = pos - page_idx * a.page_size;
+  const int partner = off % a.P;
+  const int slot = off / a.P;
+  const int ps_l = a.page_size / a.P;
+  // row index inside the pool tensor [P][num_pages][H][ps_l]
+  const int64_t prow =
+      ((static_cast<int64_t>(partner) * a.num_pages + page) * a.num_kv_heads + h) * ps_l + slot;
+  const int64_t srow = static_cast<int64_t>(t) * a.num_kv_heads + h;
+
+  if (c * 16 < a.row_bytes_k) {
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.k_new) +
+                                                      srow * a.row_bytes_k) + c;
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.pool_k) + prow * a.row_bytes_k) + c;
+    *dst = __ldg(src);
+  }
+  if (a.pool_v != nullptr && c * 16 < a.row_bytes_v) {
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.v_new) +
+                                                      srow * a.row_bytes_v) + c;
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.pool_v) + prow * a.row_bytes_v) + c;
+    *dst = __ldg(src);
+  }
+}
+
+cudaError_t launch_kv_write(const WriteArgs& a, cudaStream_t s) {
+  const int rb = a.row_bytes_k > a.row_bytes_v ? a.row_bytes_k : a.row_bytes_v;
+  const int chunks = rb / 16;
+  const int64_t total = static_cast<int64_t>(a.num_tokens) * a.num_kv_heads * chunks;
+  if (total == 0) return cudaSuccess;
+  const int threads = 256;
+  const int64_t blocks = (total + threads - 1) / threads;
+  kv_write_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(a, chunks);
+  return cudaGetLastError();
+}
+
+}  // namespace cpattn

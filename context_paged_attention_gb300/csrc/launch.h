@@ -1,0 +1,87 @@
+// Host-side launchers of the libcpattn kernels (internal; the C ABI is in cpattn.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace cpattn {
+
+struct WriteArgs {
+  void* pool_k;
+  void* pool_v;
+  const void* k_new;
+  const void* v_new;
+  const int32_t* positions;
+  const int32_t* qo_indptr;
+  const int32_t* page_indptr;
+  const int32_t* page_indices;
+  int32_t* dev_status;
+  int P, page_size, num_pages, num_kv_heads, num_rows, num_tokens;
+  int row_bytes_k, row_bytes_v;  // bytes of one head's K / V row
+};
+cudaError_t launch_kv_write(const WriteArgs& a, cudaStream_t s);
+
+struct MergeArgs {
+  int num_partials;
+  const float* o_parts;
+  const float* lse_parts;
+  int64_t stride_o, stride_lse;
+  int num_tokens, num_heads, head_dim_v;
+  int out_bf16;
+  void* out;
+  float* lse_out;
+};
+cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t s);
+
+// Shared by every partial-attention kernel.
+struct PartialArgs {
+  const void* pool_k;
+  const void* pool_v;  // == pool_k for MLA (value = prefix of the latent row)
+  const void* q;
+  float* o_part;
+  float* lse_part;
+  const int32_t* qo_indptr;  // may be null: one token a row
+  const int32_t* kv_len;
+  const int32_t* page_indptr;
+  const int32_t* page_indices;
+  int32_t* dev_status;
+  // workspace (split-KV partials)
+  float* ws_o;
+  float* ws_lse;
+  int32_t* ws_cnt;
+  int P, page_size, ps_l, num_pages, num_kv_heads, num_q_heads, head_dim, head_dim_v;
+  int num_rows, num_tokens, max_kv_len;
+  int seg;         // tokens per staged segment (divides ps_l)
+  int chunk;       // stripe tokens per CTA (multiple of seg)
+  int max_chunks;  // chunks per (token, partner, kv head), = grid.x
+  float scale;
+};
+
+// Geometry of a partial launch (shared by workspace sizing and the launch).
+struct PartialPlan {
+  int seg, chunk, max_chunks;
+  size_t ws_o_floats, ws_lse_floats, ws_cnt_ints;
+  size_t bytes() const;
+};
+// Returns false if the shape is unsupported.
+bool plan_partial(int mla, int P, int page_size, int num_kv_heads, int num_q_heads, int head_dim,
+                  int num_tokens, int max_kv_len, int dtype_bytes, PartialPlan* plan);
+
+// status: 0 ok, CPATTN_ERR_UNSUPPORTED_SHAPE, or the cudaError via *err
+int launch_gqa_partial(const PartialArgs& a, int dtype_bf16, cudaStream_t s, cudaError_t* err);
+int launch_mla_partial(const PartialArgs& a, cudaStream_t s, cudaError_t* err);
+
+struct OwnArgs {
+  const void* q;
+  const void* k_new;
+  const void* v_new;
+  float* o_own;
+  float* lse_own;
+  const int32_t* qo_indptr;
+  int num_q_heads, num_kv_heads, head_dim, num_rows_bucket, num_real_rows, num_tokens, max_q_len;
+  float scale;
+};
+int launch_own_token(const OwnArgs& a, int dtype_bf16, cudaStream_t s, cudaError_t* err);
+
+}  // namespace cpattn

@@ -1,0 +1,117 @@
+"""One attention step over a striped pool, orchestrated through the C ABI.
+
+A decode step (one new token a row) is: ``cp_kv_write`` of the new K/V, then
+``cp_paged_attn_partial`` over each row's full length, then ``lse_merge`` of
+the P partner partials.  A non-decode step attends the pool for the context
+only and its new tokens apart: ``cp_kv_write``, ``cp_paged_attn_partial``
+(kv_len = context), ``own_token_attn``, then ``lse_merge`` of P + 1 partials
+(mstar PR #1124 "Context / Sequence Parallel 1/5", description; vLLM "[Core]
+Add explicit layer parallel plans", _forward_with_dcp).
+
+This module only allocates device buffers and sequences the library calls;
+all arithmetic runs in libcpattn.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import binding as B
+
+
+def _to_torch(a: np.ndarray, device) -> torch.Tensor:
+    """Host array -> device tensor; uint16 arrays are bfloat16 bit patterns."""
+    if a.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+def desc_for(w) -> B.PoolDesc:
+    return B.PoolDesc(P=w.P, page_size=w.page_size, num_pages=w.num_pages, num_kv_heads=w.num_kv_heads,
+                      head_dim=w.head_dim, head_dim_v=w.head_dim_v,
+                      dtype=B.DTYPE_BF16 if w.dtype == "bf16" else B.DTYPE_FP32)
+
+
+class StripedAttention:
+    """Device state of one workload: the striped pool, the step's inputs and outputs.
+
+    ``w`` is a ``workloads.Workload``.  The pool is filled with NaN (so any read
+    of an unwritten slot would surface) and then with every row's context
+    through ``cp_kv_write``; ``run_step`` then performs the step.
+    """
+
+    def __init__(self, w, device="cuda", fill_history=True, out_dtype=None):
+        self.w = w
+        self.device = torch.device(device)
+        self.desc = desc_for(w)
+        dt = self.desc.torch_dtype()
+        nan = float("nan")
+        self.pool_k = torch.full(self.desc.pool_shape(False), nan, dtype=dt, device=self.device)
+        self.pool_v = None if w.mla else torch.full(self.desc.pool_shape(True), nan, dtype=dt, device=self.device)
+        self.dev_status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        # step inputs
+        self.q = _to_torch(w.q, self.device)
+        self.k_new = _to_torch(w.k_new, self.device)
+        self.v_new = None if w.v_new is None else _to_torch(w.v_new, self.device)
+        self.positions = _to_torch(w.positions, self.device)
+        self.qo_indptr = _to_torch(w.qo_indptr, self.device)
+        self.kv_len = _to_torch(w.kv_len, self.device)
+        self.page_indptr = _to_torch(w.kv_page_indptr, self.device)
+        self.page_indices = _to_torch(w.kv_page_indices, self.device)
+        self.max_kv_len = int(max(1, w.kv_len.max(initial=0)))
+        self.max_q_len = int(w.new_len.max(initial=0))
+        # outputs
+        T, Hq, Dv, P = w.num_tokens, w.num_q_heads, w.head_dim_v, w.P
+        nparts = P if w.decode else P + 1
+        self.o_parts = torch.empty((nparts, T, Hq, Dv), dtype=torch.float32, device=self.device)
+        self.lse_parts = torch.empty((nparts, T, Hq), dtype=torch.float32, device=self.device)
+        odt = out_dtype if out_dtype is not None else dt
+        self.out = torch.empty((T, Hq, Dv), dtype=odt, device=self.device)
+        self.lse = torch.empty((T, Hq), dtype=torch.float32, device=self.device)
+        ws = B.workspace_bytes(self.desc, Hq, T, self.max_kv_len)
+        self.workspace = torch.empty((max(ws, 256),), dtype=torch.uint8, device=self.device)
+        if fill_history:
+            self.fill_history()
+
+    def fill_history(self):
+        """Write every real row's context (positions 0 .. ctx-1) through cp_kv_write."""
+        from .workloads import history_tokens
+
+        qo, pos, k, v = history_tokens(self.w)
+        if len(pos) == 0:
+            return
+        B.cp_kv_write(self.desc, self.pool_k, self.pool_v, _to_torch(k, self.device),
+                      None if v is None else _to_torch(v, self.device), _to_torch(pos, self.device),
+                      _to_torch(qo, self.device), self.page_indptr, self.page_indices, dev_status=self.dev_status)
+
+    # -- the step's calls
+    def write_new(self, stream=None):
+        B.cp_kv_write(self.desc, self.pool_k, self.pool_v, self.k_new, self.v_new, self.positions, self.qo_indptr,
+                      self.page_indptr, self.page_indices, dev_status=self.dev_status, stream=stream)
+
+    def partial(self, stream=None):
+        P = self.w.P
+        B.cp_paged_attn_partial(self.desc, self.pool_k, self.pool_v, self.q, self.kv_len, self.max_kv_len,
+                                self.page_indptr, self.page_indices, self.w.scale, self.o_parts[:P],
+                                self.lse_parts[:P], self.workspace, qo_indptr=self.qo_indptr,
+                                num_rows=self.w.num_rows, dev_status=self.dev_status, stream=stream)
+
+    def own(self, stream=None):
+        P = self.w.P
+        B.own_token_attn(self.q, self.k_new, self.v_new, self.qo_indptr, self.w.num_real_rows, self.max_q_len,
+                         self.w.scale, self.o_parts[P], self.lse_parts[P], stream=stream)
+
+    def merge(self, stream=None):
+        B.lse_merge(self.o_parts, self.lse_parts, self.out, self.lse, stream=stream)
+
+    def run_step(self, stream=None):
+        self.write_new(stream)
+        self.partial(stream)
+        if not self.w.decode:
+            self.own(stream)
+        self.merge(stream)
+        return self.out, self.lse
+
+    def status(self) -> int:
+        return int(self.dev_status.item())

@@ -105,9 +105,10 @@ class Workload:
     @property
     def kv_len(self) -> np.ndarray:
         """Keys each row's queries see in the pool (decode: incl. the new token)."""
-        if self.decode:
-            return (self.ctx_len + self.new_len).astype(np.int32)
-        return self.ctx_len.astype(np.int32)
+        kv = self.ctx_len + self.new_len if self.decode else self.ctx_len.copy()
+        kv = kv.astype(np.int32)
+        kv[self.num_real_rows:] = 0  # padding rows own no keys (their tables point at the sink page)
+        return kv
 
     @property
     def seq_len(self) -> np.ndarray:

@@ -1,0 +1,128 @@
+"""The C-ABI library: it builds, loads, exports every declared symbol, and its
+host-side argument checks return the documented status codes (no GPU needed:
+every call here fails validation before anything is launched)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from context_paged_attention_gb300 import binding as B
+from context_paged_attention_gb300 import build_lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "cpattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_lib.build()
+    return B.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:CPATTN_API\s+)?(?:int|size_t|const char\s*\*)\s+(\w+)\s*\(", text, flags=re.M)
+    return names
+
+
+def test_header_declares_the_boundary():
+    names = set(declared_functions())
+    for n in ["cp_kv_write", "cp_paged_attn_partial", "own_token_attn", "lse_merge",
+              "cp_paged_attn_workspace_bytes", "cpattn_version", "cpattn_status_string", "cpattn_pool_bytes"]:
+        assert n in names, n
+
+
+def test_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in cpattn.h but not exported"
+
+
+def test_version_and_status_strings(lib):
+    assert lib.cpattn_version() == 1
+    assert lib.cpattn_status_string(0) == b"ok"
+    assert b"divide" in lib.cpattn_status_string(-2)
+    assert lib.cpattn_status_string(-999) == b"unknown status"
+
+
+def _desc(**kw):
+    d = dict(P=4, page_size=16, num_pages=10, num_kv_heads=8, head_dim=128, head_dim_v=128, dtype=B.DTYPE_BF16)
+    d.update(kw)
+    return B.PoolDesc(**d)
+
+
+FAKE = 0x10000  # never dereferenced: these calls fail host validation first
+
+
+def test_pool_bytes(lib):
+    d = _desc()
+    assert lib.cpattn_pool_bytes(ctypes.byref(d), 0) == 4 * 10 * 8 * 4 * 128 * 2
+    mla = _desc(num_kv_heads=1, head_dim=576, head_dim_v=512, page_size=64)
+    assert lib.cpattn_pool_bytes(ctypes.byref(mla), 0) == 4 * 10 * 1 * 16 * 576 * 2
+    assert lib.cpattn_pool_bytes(ctypes.byref(_desc(P=3)), 0) == 0
+
+
+@pytest.mark.parametrize("P,ps", [(3, 16), (0, 16), (32, 16), (-1, 8)])
+def test_p_must_divide_page_size(lib, P, ps):
+    d = _desc(P=P, page_size=ps)
+    st = lib.cp_kv_write(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, FAKE, FAKE, None, None)
+    assert st == -2
+    st = lib.cp_paged_attn_partial(ctypes.byref(d), FAKE, FAKE, FAKE, 32, 1, 1, None, FAKE, 100, FAKE, FAKE, 0.1,
+                                   FAKE, FAKE, FAKE, 1 << 30, None, None)
+    assert st == -2
+
+
+def test_invalid_and_misaligned(lib):
+    d = _desc()
+    # null pool
+    assert lib.cp_kv_write(ctypes.byref(d), None, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, FAKE, FAKE, None, None) == -1
+    # misaligned k_new
+    assert lib.cp_kv_write(ctypes.byref(d), FAKE, FAKE, FAKE + 2, FAKE, FAKE, FAKE, 1, 1, FAKE, FAKE, None,
+                           None) == -4
+    # MLA pools take no V
+    mla = _desc(num_kv_heads=1, head_dim=576, head_dim_v=512, page_size=64)
+    assert lib.cp_kv_write(ctypes.byref(mla), FAKE, FAKE, FAKE, None, FAKE, FAKE, 1, 1, FAKE, FAKE, None,
+                           None) == -1
+    # query heads not a multiple of KV heads
+    assert lib.cp_paged_attn_partial(ctypes.byref(d), FAKE, FAKE, FAKE, 30, 1, 1, None, FAKE, 100, FAKE, FAKE, 0.1,
+                                     FAKE, FAKE, FAKE, 1 << 30, None, None) == -1
+    # one token a row needs num_tokens == num_rows when qo_indptr is NULL
+    assert lib.cp_paged_attn_partial(ctypes.byref(d), FAKE, FAKE, FAKE, 32, 2, 3, None, FAKE, 100, FAKE, FAKE, 0.1,
+                                     FAKE, FAKE, FAKE, 1 << 30, None, None) == -1
+    # head_dim_v above head_dim, and rows that are not 16-byte multiples
+    assert lib.cp_paged_attn_partial(ctypes.byref(_desc(head_dim_v=256)), FAKE, FAKE, FAKE, 32, 1, 1, None, FAKE,
+                                     100, FAKE, FAKE, 0.1, FAKE, FAKE, FAKE, 1 << 30, None, None) == -3
+    assert lib.cp_paged_attn_partial(ctypes.byref(_desc(head_dim=4, head_dim_v=4)), FAKE, FAKE, FAKE, 32, 1, 1,
+                                     None, FAKE, 100, FAKE, FAKE, 0.1, FAKE, FAKE, FAKE, 1 << 30, None, None) == -3
+    # merge: bad counts / dims
+    assert lib.lse_merge(0, FAKE, FAKE, 0, 0, 1, 1, 128, 0, FAKE, None, None) == -1
+    assert lib.lse_merge(2, FAKE, FAKE, 10, 1, 1, 1, 128, 0, FAKE, None, None) == -1
+    assert lib.lse_merge(1, FAKE, FAKE, 0, 0, 1, 1, 6, 0, FAKE, None, None) == -1
+    # own-token: real rows beyond the bucket
+    assert lib.own_token_attn(FAKE, FAKE, FAKE, 32, 8, 128, 128, 0, FAKE, 4, 5, 16, 8, 0.1, FAKE, FAKE,
+                              None) == -1
+
+
+def test_workspace_sizing(lib):
+    d = _desc()
+    small = lib.cp_paged_attn_workspace_bytes(ctypes.byref(d), 32, 64, 256)
+    big = lib.cp_paged_attn_workspace_bytes(ctypes.byref(d), 32, 64, 8192)
+    assert small > 0 and big > small
+    assert lib.cp_paged_attn_workspace_bytes(ctypes.byref(d), 30, 64, 8192) == 0
+    # too-small workspace is refused before any launch
+    assert lib.cp_paged_attn_partial(ctypes.byref(d), FAKE, FAKE, FAKE, 32, 64, 64, None, FAKE, 8192, FAKE, FAKE,
+                                     0.1, FAKE, FAKE, FAKE, big - 1, None, None) == -5
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    torch = pytest.importorskip("torch")
+    x = torch.zeros(4)
+    with pytest.raises(ValueError):
+        B._ptr(x)
+
+
+def test_missing_library_is_loud(tmp_path):
+    with pytest.raises(RuntimeError):
+        B.load_library(str(tmp_path / "nope.so"))

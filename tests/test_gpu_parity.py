@@ -1,0 +1,228 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle.
+
+Bars: bit-exact pool contents after cp_kv_write; final outputs within max-abs
+1e-2 (bf16 output) and LSE within 1e-3 (fp32 workloads: 1e-5 for both);
+per-partner fp32 partials within 1e-4 (bf16 inputs) / 1e-5 (fp32 inputs).
+Padding tokens must come out exactly 0 / -inf, and NaN planted in padding
+rows, padding tokens, the sink page and unwritten pool slots must reach no
+real output.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from context_paged_attention_gb300 import workloads as W
+from helpers import OracleView, assert_close, assert_close_lse, f64, raw, tolerances
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+def _att(w, **kw):
+    from context_paged_attention_gb300.step import StripedAttention
+
+    return StripedAttention(w, device="cuda", **kw)
+
+
+SMALL = {
+    "tiny_fp32": lambda: W.tiny_fp32(),
+    "gqa_decode": lambda: W.gqa_decode(seed=21, batch=6, len_lo=20, len_hi=5000),
+    "gqa_decode_padded": lambda: W.gqa_decode(seed=22, batch=5, len_lo=1, len_hi=900, padding_spans=[1, 1, 1]),
+    "long_gqa_decode": lambda: W.long_gqa_decode(seed=23, batch=2, len_lo=3000, len_hi=20000),
+    "mla_decode": lambda: W.mla_decode(seed=24, batch=3, len_lo=100, len_hi=5000),
+    "mixed_step": lambda: W.mixed_step(seed=25, n_decode=4, n_extend=3, dec_ctx=(1, 3000), ext_new=(2, 40),
+                                       ext_ctx=(0, 1500), token_multiple=64),
+    "mixed_padded": lambda: W.mixed_step(seed=26, n_decode=3, n_extend=3, dec_ctx=(5, 700), ext_new=(2, 17),
+                                         ext_ctx=(0, 0), padding_spans=[0, 4, 0, 2], token_multiple=32),
+    "gqa_P1": lambda: W.build_workload("gqa_P1", dtype="bf16", P=1, page_size=16, num_q_heads=16,
+                                       num_kv_heads=8, head_dim=128, ctx_len=[0, 15, 16, 700, 33],
+                                       new_len=[1] * 5, seed=27),
+    "gqa_g1_d64": lambda: W.build_workload("gqa_g1_d64", dtype="bf16", P=2, page_size=8, num_q_heads=4,
+                                           num_kv_heads=4, head_dim=64, ctx_len=[3, 400, 1], new_len=[1] * 3,
+                                           seed=28),
+    "gqa_P16_ps16": lambda: W.build_workload("gqa_P16_ps16", dtype="bf16", P=16, page_size=16, num_q_heads=16,
+                                             num_kv_heads=2, head_dim=128, ctx_len=[5, 40, 2000], new_len=[1] * 3,
+                                             seed=29),
+}
+
+
+@pytest.fixture(scope="module", params=sorted(SMALL))
+def small(request):
+    w = SMALL[request.param]()
+    att = _att(w)
+    att.run_step()
+    torch.cuda.synchronize()
+    return w, att
+
+
+def _expected_pool(w, which_v=False):
+    """Oracle image: NaN pool, every row's context and the step's new tokens written by the placement."""
+    dt_nan = W.nan_pool((1,), w.dtype)[0]
+    shape = W.pool_v_shape(w) if which_v else W.pool_shape(w)
+    pool = np.full(shape, dt_nan, dtype=np.uint16 if w.dtype == "bf16" else np.float32)
+    src = w.v_seq if which_v else w.k_seq
+    for b in range(w.num_real_rows):
+        L = int(w.ctx_len[b] + w.new_len[b])
+        s0 = int(w.seq_indptr[b])
+        rows = w.kv_page_indices[w.kv_page_indptr[b]: w.kv_page_indptr[b + 1]]
+        pool = oracle.expected_pool_image(pool, rows, np.arange(L), src[s0: s0 + L], w.page_size, w.P)
+    return pool
+
+
+def _bits(a):
+    return a.view(np.uint32) if a.dtype == np.float32 else a
+
+
+def test_kv_write_bit_exact(small):
+    w, att = small
+    got = raw(att.pool_k)
+    want = _expected_pool(w)
+    assert np.array_equal(_bits(got), _bits(want)), "pool_k differs from the placement image"
+    if not w.mla:
+        assert np.array_equal(_bits(raw(att.pool_v)), _bits(_expected_pool(w, True)))
+    assert att.status() == 0
+
+
+def test_partner_partials(small):
+    w, att = small
+    ov = OracleView(w)
+    tol = 1e-5 if w.dtype == "fp32" else 1e-4
+    o_parts = att.o_parts.cpu().numpy().astype(np.float64)
+    l_parts = att.lse_parts.cpu().numpy().astype(np.float64)
+    for t in range(w.num_tokens):
+        for p in range(w.P):
+            O, L = ov.stripe(t, p)
+            assert_close(o_parts[p, t], O, tol, f"O part p={p} t={t}")
+            assert_close_lse(l_parts[p, t], L, tol, f"LSE part p={p} t={t}")
+
+
+def test_step_matches_oracle(small):
+    w, att = small
+    ov = OracleView(w)
+    O, L = ov.final()
+    tol_o, tol_l = tolerances(w)
+    got_o = f64(att.out)
+    got_l = att.lse.cpu().numpy().astype(np.float64)
+    assert_close(got_o, O, tol_o, "merged output")
+    assert_close_lse(got_l, L, tol_l, "merged LSE")
+    # padding tokens merge to exactly 0 / -inf
+    t0 = int(w.qo_indptr[w.num_real_rows])
+    assert np.all(got_o[t0:] == 0) and np.all(got_l[t0:] == -np.inf)
+
+
+def test_own_token_partial(small):
+    w, att = small
+    if w.decode:
+        pytest.skip("decode steps attend the pool only")
+    ov = OracleView(w)
+    o_own = att.o_parts[w.P].cpu().numpy().astype(np.float64)
+    l_own = att.lse_parts[w.P].cpu().numpy().astype(np.float64)
+    for b in range(w.num_real_rows):
+        s0 = int(w.seq_indptr[b])
+        c, n = int(w.ctx_len[b]), int(w.new_len[b])
+        K = oracle.raw_to_f64(w.k_seq[s0 + c: s0 + c + n])
+        V = oracle.raw_to_f64(w.v_seq[s0 + c: s0 + c + n])
+        t0 = int(w.qo_indptr[b])
+        O, L = oracle.causal_own_attention(ov.q[t0: t0 + n], K, V, w.scale)
+        assert_close(o_own[t0: t0 + n], O, 1e-4, f"own O row {b}")
+        assert_close_lse(l_own[t0: t0 + n], L, 1e-4, f"own LSE row {b}")
+    t0 = int(w.qo_indptr[w.num_real_rows])
+    assert np.all(o_own[t0:] == 0) and np.all(l_own[t0:] == -np.inf)
+
+
+def test_repeat_step_is_stable(small):
+    """Running the step again (same write, same tables) gives bit-identical outputs."""
+    w, att = small
+    first = raw(att.out).copy()
+    att.run_step()
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(raw(att.out)), _bits(first))
+
+
+# ---------------------------------------------------------------- full-size workloads
+
+FULL = {
+    "gqa_decode": (W.gqa_decode, None),
+    "long_gqa_decode": (W.long_gqa_decode, [0, 5]),
+    "mla_decode": (W.mla_decode, [0, 7, 19, 31]),
+    "mixed_step": (W.mixed_step, [0, 17, 47, 48, 55, 63]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(FULL))
+def test_full_size_sampled(name):
+    fn, rows = FULL[name]
+    w = fn()
+    att = _att(w)
+    att.run_step()
+    torch.cuda.synchronize()
+    assert att.status() == 0
+    got_o = f64(att.out)
+    got_l = att.lse.cpu().numpy().astype(np.float64)
+    # properties over every output: finite for real tokens, exact 0 / -inf for padding
+    t_end = int(w.qo_indptr[w.num_real_rows])
+    assert np.all(np.isfinite(got_o[:t_end])) and np.all(np.isfinite(got_l[:t_end]))
+    assert np.all(got_o[t_end:] == 0) and np.all(got_l[t_end:] == -np.inf)
+    assert np.all(np.abs(got_o[:t_end]) <= 7.0)  # convex combination of N(0,1) draws
+    ov = OracleView(w)
+    tol_o, tol_l = tolerances(w)
+    row_list = range(w.num_real_rows) if rows is None else rows
+    rng = np.random.default_rng(7)
+    for b in row_list:
+        heads = None if rows is None else sorted(rng.choice(w.num_q_heads, size=8, replace=False).tolist())
+        O, L = ov.final_row(b, heads)
+        t0, n = int(w.qo_indptr[b]), int(w.new_len[b])
+        sel_o = got_o[t0: t0 + n] if heads is None else got_o[t0: t0 + n][:, heads]
+        sel_l = got_l[t0: t0 + n] if heads is None else got_l[t0: t0 + n][:, heads]
+        assert_close(sel_o, O, tol_o, f"{name} row {b} O")
+        assert_close_lse(sel_l, L, tol_l, f"{name} row {b} LSE")
+
+
+# ---------------------------------------------------------------- device-side checks
+
+def test_bad_page_id_is_reported_not_read():
+    """A page id outside the pool is skipped and reported; other rows are unaffected."""
+    w = W.gqa_decode(seed=31, batch=4, len_lo=100, len_hi=400)
+    att = _att(w)
+    att.run_step()
+    torch.cuda.synchronize()
+    good = raw(att.out).copy()
+    b = 2
+    idx = att.page_indices.clone()
+    idx[int(w.kv_page_indptr[b])] = w.num_pages + 1000  # far outside the pool
+    att.page_indices = idx
+    att.partial()
+    att.merge()
+    torch.cuda.synchronize()
+    assert att.status() == 1  # CPATTN_DEV_PAGE_OUT_OF_RANGE
+    out = raw(att.out)
+    for r in range(w.num_rows):
+        if r != b:
+            assert np.array_equal(_bits(out[r]), _bits(good[r]))
+
+
+def test_kv_len_past_table_is_reported():
+    w = W.gqa_decode(seed=32, batch=3, len_lo=50, len_hi=90)
+    att = _att(w)
+    att.run_step()
+    torch.cuda.synchronize()
+    kv = att.kv_len.clone()
+    kv[1] = int(w.kv_len[1]) + 10 * w.page_size  # beyond the row's page table
+    att.kv_len = kv
+    att.max_kv_len = int(kv.max().item())
+    from context_paged_attention_gb300 import binding as B
+
+    ws = B.workspace_bytes(att.desc, w.num_q_heads, w.num_tokens, att.max_kv_len)
+    att.workspace = torch.empty((max(ws, 256),), dtype=torch.uint8, device="cuda")
+    att.partial()
+    torch.cuda.synchronize()
+    assert att.status() == 2  # CPATTN_DEV_POS_PAST_TABLE
