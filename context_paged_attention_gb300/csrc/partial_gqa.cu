@@ -174,7 +174,7 @@ static int launch_gqa_t(const PartialArgs& a, cudaStream_t s, cudaError_t* err) 
   const size_t comb = GqaLaneState<T, D, G>::merge_smem_bytes(kGqaWarps);
   const size_t smem = ring > comb ? ring : comb;
   auto kern = gqa_partial_kernel<T, D, G>;
-  if (smem > 48 * 1024) {
+  if (smem > 32 * 1024) {  // the kernel also has a little static shared memory
     *err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (*err != cudaSuccess) return CPATTN_ERR_CUDA;
   }
