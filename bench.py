@@ -1,0 +1,507 @@
+#!/usr/bin/env python
+"""Benchmark of one striped paged attention step on GB300.
+
+A step is the whole hot path over one batch: ``cp_kv_write`` of the step's
+new K/V into the P-way striped pool, ``cp_paged_attn_partial`` (every
+partner's partial with its log-sum-exp), ``own_token_attn`` for non-decode
+workloads, and ``lse_merge`` of the partials.  Metric: algorithmic KV bytes the
+step reads (every visible key and value once) per second, plus decode
+tokens/s; inputs (the KV pool, 1.14 GB for the default workload) are larger
+than L2, so no flush is needed between steps.
+
+Default workload: GQA decode, batch 64, 32 query / 8 KV heads, head_dim 128,
+page 16, P = 4, context lengths uniform in [512, 8192], bf16, fp32 LSE.
+
+``--impl reference`` times the float64 CPU oracle on the host cores instead
+(the pages publish no implementation or figures to run); under torchrun only
+rank 0 runs it.  ``--gpus N`` under torchrun runs N independent replicas (the
+path has no cross-GPU step on one box): whole-job value = sum of the ranks'
+bytes over the slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KV-read HBM GB/s (% of peak) and decode tokens/s, striped paged attn + merge"
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
+PARTIAL_SOURCES = ["partial_gqa.cu", "gqa_core.cuh", "split_combine.cuh", "common.cuh", "partial_mla_fma.cu"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="gqa_decode",
+                    choices=["tiny_fp32", "gqa_decode", "long_gqa_decode", "mla_decode", "mixed_step"])
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
+    ap.add_argument("--no-clocks", action="store_true", help="do not sample nvidia-smi")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- workloads
+
+def make_workload(name):
+    from context_paged_attention_gb300 import workloads as W
+
+    return W.WORKLOADS[{"tiny_fp32": 1, "gqa_decode": 2, "long_gqa_decode": 3, "mla_decode": 4,
+                        "mixed_step": 5}[name]]()
+
+
+def describe(w):
+    lens = w.ctx_len[: w.num_real_rows] + w.new_len[: w.num_real_rows]
+    return {
+        "workload": f"{w.name}: {w.num_real_rows} rows, {w.num_q_heads}q/{w.num_kv_heads}kv heads, "
+                    f"D {w.head_dim}/{w.head_dim_v}, page {w.page_size}, P {w.P}, {w.dtype}",
+        "rows": int(w.num_real_rows),
+        "tokens": int(w.num_tokens),
+        "q_heads": w.num_q_heads,
+        "kv_heads": w.num_kv_heads,
+        "head_dim": w.head_dim,
+        "head_dim_v": w.head_dim_v,
+        "page_size": w.page_size,
+        "P": w.P,
+        "kv_len_mean": float(lens.mean()),
+        "kv_bytes_per_step": int(w.kv_bytes_read()),
+        "l2": "inputs larger than L2 (KV pool read each step exceeds 129 MB); no flush",
+        "seed": w.meta.get("seed"),
+    }
+
+
+def algorithmic_bytes(w):
+    """Bytes each kernel must move at minimum, per launch."""
+    esz = 2 if w.dtype == "bf16" else 4
+    T, Hq, D, Dv, P = w.num_tokens, w.num_q_heads, w.head_dim, w.head_dim_v, w.P
+    kv = w.kv_bytes_read()
+    q = T * Hq * D * esz
+    part_out = P * T * Hq * (Dv + 1) * 4
+    return {"partial": kv + q + part_out, "kv": kv}
+
+
+# ---------------------------------------------------------------- environment
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest():
+    h = hashlib.sha256()
+    for name in PARTIAL_SOURCES:
+        with open(os.path.join(ROOT, "context_paged_attention_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel sources still match."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    digest = source_digest()
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            kv = dict(x.split("=", 1) for x in line.split())
+            if kv.get("kernel") == kernel and kv.get("workload") == workload and kv.get("source") == digest:
+                return int(kv["dram_bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms in the background."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_id):
+        self.samples = []
+        self.proc = None
+        self.device_id = device_id
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.device_id)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        used = inside if inside else [min(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[1]]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[0]) for p in used if num(p[0]) is not None]
+        smax = [num(p[1]) for p in used if num(p[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in used for i in range(4) if p[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(used), "window_samples": len(inside)}
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+def _oracle_row_task(task):
+    """One row of the decode step by the float64 oracle (runs in a spawned worker)."""
+    import numpy as np
+
+    import oracle
+
+    q_raw, k_raw, v_raw, scale, dv, mla = task
+    t0 = time.perf_counter()
+    q = oracle.raw_to_f64(q_raw)
+    K = oracle.raw_to_f64(k_raw)
+    V = K[:, :, :dv] if mla else oracle.raw_to_f64(v_raw)
+    for i in range(q.shape[0]):
+        oracle.attention(q[i], K[: K.shape[0] - q.shape[0] + i + 1], V[: K.shape[0] - q.shape[0] + i + 1], scale)
+    del np
+    return time.perf_counter() - t0
+
+
+def oracle_tasks(w, max_keys=None):
+    """Per-row oracle tasks (the step's real rows), optionally a prefix of rows bounded by total keys."""
+    tasks, keys, nbytes = [], 0, 0
+    esz = 2 if w.dtype == "bf16" else 4
+    per_key = w.num_kv_heads * (w.head_dim + (0 if w.mla else w.head_dim_v)) * esz
+    for b in range(w.num_real_rows):
+        c, n = int(w.ctx_len[b]), int(w.new_len[b])
+        s0 = int(w.seq_indptr[b])
+        t0 = int(w.qo_indptr[b])
+        m = c + n
+        tasks.append((w.q[t0: t0 + n], w.k_seq[s0: s0 + m], None if w.mla else w.v_seq[s0: s0 + m], w.scale,
+                      w.head_dim_v, w.mla))
+        kv = int(w.kv_len[b]) if w.decode else c + n
+        keys += kv
+        nbytes += kv * per_key
+        if max_keys is not None and keys >= max_keys:
+            break
+    return tasks, nbytes
+
+
+class OraclePool:
+    """Spawned single-threaded workers, one per host core (BLAS threads pinned to 1)."""
+
+    def __init__(self):
+        import multiprocessing as mp
+
+        self.cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+        saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+        for k in saved:
+            os.environ[k] = "1"
+        self.pool = mp.get_context("spawn").Pool(self.cores)
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+
+    def run(self, tasks):
+        t0 = time.perf_counter()
+        self.pool.map(_oracle_row_task, tasks, chunksize=1)
+        return time.perf_counter() - t0
+
+    def close(self):
+        self.pool.terminate()
+
+
+def sample_keys(w):
+    """Bound the oracle sample to roughly 10-30 s of single-core float64 work."""
+    per_key_cost = w.num_q_heads * (w.head_dim + w.head_dim_v) * 8  # bytes of float64 traffic per key per step
+    budget_bytes = 6e10  # ~ 20 s of single-core float64 streaming at ~3 GB/s
+    return max(1, int(budget_bytes / per_key_cost))
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import __graft_entry__
+    from context_paged_attention_gb300.step import StripedAttention
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    torch.cuda.set_device(local_rank)
+    __graft_entry__.build()
+
+    # the oracle workers are spawned before the first GPU call
+    opool = OraclePool() if (rank == 0 and not args.no_cpu_baseline) else None
+
+    w = make_workload(args.config)
+    att = StripedAttention(w, device=f"cuda:{local_rank}")
+    torch.cuda.synchronize()
+    if att.status() != 0:
+        raise RuntimeError(f"device status {att.status()} after filling the pool")
+    alg = algorithmic_bytes(w)
+    stream = torch.cuda.current_stream()
+
+    def step(ev0=None, ev1=None):
+        att.write_new()
+        if ev0 is not None:
+            ev0.record(stream)
+        att.partial()
+        if ev1 is not None:
+            ev1.record(stream)
+        if not w.decode:
+            att.own()
+        att.merge()
+
+    sampler = None
+    if not args.no_clocks and rank == 0:
+        sampler = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+        sampler.start()
+        time.sleep(0.3)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    K = args.steps
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    start.record(stream)
+    for i in range(K):
+        step(e0[i], e1[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    total_ms = start.elapsed_time(end)
+    partial_ms = sum(e0[i].elapsed_time(e1[i]) for i in range(K)) / K
+    if sampler is not None:
+        time.sleep(0.25)
+        sampler.stop()
+    if att.status() != 0:
+        raise RuntimeError(f"device status {att.status()} during the timed steps")
+
+    # end-to-end through the public API with host buffers (pinned), copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        e2e = time_e2e(att, w, args, stream)
+
+    if dist is not None:
+        t = torch.tensor([total_ms, e2e["ms_per_step"] if e2e else 0.0], device=f"cuda:{local_rank}")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, e2e_ms = float(t[0]), float(t[1])
+        if e2e:
+            e2e["ms_per_step"] = e2e_ms
+    ms = total_ms / K
+    kv_bytes = alg["kv"]
+    value = world * kv_bytes / (ms * 1e-3) / 1e9
+    peak, peak_src = load_peaks()
+
+    if rank != 0:
+        return
+    achieved = alg["partial"] / (partial_ms * 1e-3) / 1e9
+    traffic = recorded_traffic("gqa_partial" if not w.mla else "mla_partial", args.config)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic (seeded N(0,1) values, uniform lengths, random page permutation)",
+        "config": describe(w) | {"parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "frac_of_peak": round(value / world / peak, 4),
+        "peak_source": f"{peak_src} hbm_gbs {peak}",
+        "decode_tokens_per_s": round(world * int(w.qo_indptr[w.num_real_rows]) / (ms * 1e-3), 1),
+        "roofline": {
+            "kernel": "cp_paged_attn_partial (GQA CUDA-core split-KV)" if not w.mla else
+                      "cp_paged_attn_partial (MLA)",
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "algorithmic_bytes": alg["partial"],
+            "ms_per_launch": round(partial_ms, 5),
+            "peak_note": f"of {peak_src}",
+        },
+        "gpu_launches": K * (4 if not w.decode else 3),
+        "launch_note": "per step: kv_write, partial, merge kernels (+own_token for mixed steps) and one "
+                       "4-byte-per-slot cudaMemsetAsync of the split tickets",
+    }
+    if e2e is not None:
+        line["e2e"] = {"value": round(world * kv_bytes / (e2e["ms_per_step"] * 1e-3) / 1e9, 2), "unit": "GB/s",
+                       "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                       "ms_per_step": round(e2e["ms_per_step"], 5)}
+    if sampler is not None:
+        line["clocks"] = sampler.summary(t_wall0, t_wall1)
+    if opool is not None:
+        tasks, nbytes = oracle_tasks(w, sample_keys(w))
+        secs = opool.run(tasks)
+        opool.close()
+        line["cpu_baseline"] = {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": opool.cores,
+                                "kind": "oracle",
+                                "sample": f"float64 oracle over {len(tasks)} of {w.num_real_rows} rows of the same "
+                                          f"step ({nbytes / 1e9:.3f} GB of KV), one spawned single-threaded "
+                                          f"worker per core, {secs:.2f} s"}
+    print(json.dumps(line), flush=True)
+
+
+def time_e2e(att, w, args, stream):
+    """Same step through the public API, inputs copied from pinned host buffers each step."""
+    import torch
+
+    names = ["q", "k_new", "v_new", "positions", "qo_indptr", "kv_len", "page_indptr", "page_indices"]
+    host = {}
+    h2d = 0
+    for n in names:
+        t = getattr(att, n)
+        if t is None:
+            continue
+        host[n] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        host[n].copy_(t)
+        h2d += t.numel() * t.element_size()
+    out_h = torch.empty(att.out.shape, dtype=att.out.dtype, pin_memory=True)
+    lse_h = torch.empty(att.lse.shape, dtype=att.lse.dtype, pin_memory=True)
+    d2h = att.out.numel() * att.out.element_size() + att.lse.numel() * att.lse.element_size()
+
+    def e2e_step():
+        for n, h in host.items():
+            getattr(att, n).copy_(h, non_blocking=True)
+        att.run_step()
+        out_h.copy_(att.out, non_blocking=True)
+        lse_h.copy_(att.lse, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    return {"ms_per_step": start.elapsed_time(end) / args.steps, "h2d": h2d, "d2h": d2h}
+
+
+# ---------------------------------------------------------------- reference arm (the oracle)
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    opool = OraclePool()
+    w = make_workload(args.config)
+    tasks, nbytes = oracle_tasks(w, sample_keys(w) // 4)
+    for _ in range(args.warmup):
+        opool.run(tasks[: max(1, len(tasks) // 8)])
+    # time K bounded steps, scaled down so the whole run stays within a few minutes
+    per = opool.run(tasks)
+    budget = 120.0
+    k = max(1, min(args.steps, int(budget / max(per, 1e-3))))
+    secs = per
+    for _ in range(k - 1):
+        secs += opool.run(tasks)
+    opool.close()
+    ms = secs / k * 1e3
+    value = nbytes / (secs / k) / 1e9
+    sample = (f"float64 oracle over {len(tasks)} of {w.num_real_rows} rows ({nbytes / 1e9:.3f} GB of KV) per step, "
+              f"{k} timed steps, one spawned single-threaded worker per core")
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": k,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) values, uniform lengths, random page permutation)",
+        "config": describe(w),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": opool.cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local_rank}"))
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
