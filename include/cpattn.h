@@ -178,6 +178,42 @@ CPATTN_API size_t cp_paged_attn_workspace_bytes(const cpattn_pool_desc* desc, in
                                      int32_t num_tokens, int32_t max_kv_len);
 
 /*
+ * cp_paged_attn_partial_noalloc -- cp_paged_attn_partial for callers that
+ * cannot allocate device memory.  The pages have no counterpart: this is a
+ * convenience of this library.
+ *
+ * Some callers cannot call cudaMalloc: a plugin that is handed raw input and
+ * output pointers but no allocator, a runtime whose memory pool owns the whole
+ * GPU, or a step that must not allocate once it has started.  This call takes
+ * the same inputs and outputs as cp_paged_attn_partial but no workspace: the
+ * split-KV scratch is a fixed 16 MiB __device__ array inside libcpattn (every
+ * GPU that loads the library holds it until the process exits; see
+ * cp_paged_attn_noalloc_scratch_bytes).
+ *   - Returns CPATTN_ERR_WORKSPACE_TOO_SMALL, launching nothing, when
+ *     cp_paged_attn_workspace_bytes(desc, num_q_heads, num_tokens, max_kv_len)
+ *     exceeds that size.
+ *   - Allocates nothing; all calls share the one array, which keeps the last
+ *     call's contents.  Each call clears what must start at zero on `stream`.
+ *     Calls whose kernels can overlap on the GPU (other streams, other host
+ *     threads) race on the array: order them on one stream.
+ *   - The first call on each device looks up the array's device address with
+ *     that device current and caches it; make that first call before any
+ *     stream capture begins.
+ * Results equal those of cp_paged_attn_partial with a caller workspace.
+ */
+CPATTN_API int cp_paged_attn_partial_noalloc(const cpattn_pool_desc* desc, const void* pool_k,
+                                             const void* pool_v, const void* q, int32_t num_q_heads,
+                                             int32_t num_rows, int32_t num_tokens,
+                                             const int32_t* qo_indptr, const int32_t* kv_len,
+                                             int32_t max_kv_len, const int32_t* kv_page_indptr,
+                                             const int32_t* kv_page_indices, float scale,
+                                             float* o_part, float* lse_part, int32_t* dev_status,
+                                             cudaStream_t stream);
+
+/* Size in bytes of the library-owned scratch behind cp_paged_attn_partial_noalloc. */
+CPATTN_API size_t cp_paged_attn_noalloc_scratch_bytes(void);
+
+/*
  * own_token_attn -- causal attention of a step's new tokens over the K/V the
  * layer passes (mstar PR #1124 "Context / Sequence Parallel 1/5",
  * description: a step that is not one token a row attends its own tokens
