@@ -39,7 +39,11 @@ if ROOT not in sys.path:
 METRIC = "KV-read HBM GB/s (% of peak) and decode tokens/s, striped paged attn + merge"
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
-PARTIAL_SOURCES = ["partial_gqa.cu", "gqa_core.cuh", "split_combine.cuh", "common.cuh", "partial_mla_fma.cu"]
+# sources whose digest keys the recorded ncu traffic of each partial kernel
+KERNEL_SOURCES = {
+    "gqa_partial": ["partial_gqa.cu", "partial_gqa_mma.cu", "gqa_core.cuh", "split_combine.cuh", "common.cuh"],
+    "mla_partial": ["partial_gqa.cu", "partial_mla_fma.cu", "split_combine.cuh", "common.cuh"],
+}
 
 
 def parse_args():
@@ -107,9 +111,9 @@ def load_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def source_digest():
+def source_digest(kernel="gqa_partial"):
     h = hashlib.sha256()
-    for name in PARTIAL_SOURCES:
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "context_paged_attention_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -119,7 +123,7 @@ def recorded_traffic(kernel, workload):
     """DRAM bytes per launch from the committed ncu summary, if the kernel sources still match."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
-    digest = source_digest()
+    digest = source_digest(kernel)
     with open(TRAFFIC_FILE) as f:
         for line in f:
             line = line.strip()
@@ -365,8 +369,9 @@ def run_ours(args, rank, world, local_rank):
         "peak_source": f"{peak_src} hbm_gbs {peak}",
         "decode_tokens_per_s": round(world * int(w.qo_indptr[w.num_real_rows]) / (ms * 1e-3), 1),
         "roofline": {
-            "kernel": "cp_paged_attn_partial (GQA CUDA-core split-KV)" if not w.mla else
-                      "cp_paged_attn_partial (MLA)",
+            "kernel": ("cp_paged_attn_partial (MLA)" if w.mla else
+                       "cp_paged_attn_partial (GQA, mma.sync tensor cores, split-KV)" if w.dtype == "bf16" else
+                       "cp_paged_attn_partial (GQA, CUDA cores, split-KV)"),
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,

@@ -199,8 +199,7 @@ int launch_gqa_partial(const PartialArgs& a, int dtype_bf16, cudaStream_t s, cud
   const int G = a.num_q_heads / a.num_kv_heads;
   if (a.head_dim != a.head_dim_v) return CPATTN_ERR_UNSUPPORTED_SHAPE;
   if (dtype_bf16) {
-    if (a.head_dim == 128) return dispatch_g<__nv_bfloat16, 128>(a, G, s, err);
-    if (a.head_dim == 64) return dispatch_g<__nv_bfloat16, 64>(a, G, s, err);
+    return launch_gqa_partial_mma(a, s, err);  // bf16 pools: tensor-core path (partial_gqa_mma.cu)
   } else {
     if (a.head_dim == 128) return dispatch_g<float, 128>(a, G, s, err);
     if (a.head_dim == 64) return dispatch_g<float, 64>(a, G, s, err);
@@ -222,7 +221,6 @@ size_t PartialPlan::bytes() const {
 
 bool plan_partial(int mla, int P, int page_size, int num_kv_heads, int num_q_heads, int head_dim,
                   int num_tokens, int max_kv_len, int dtype_bytes, PartialPlan* plan) {
-  (void)dtype_bytes;
   (void)head_dim;
   const int ps_l = page_size / P;
   const int G = num_q_heads / num_kv_heads;
@@ -234,8 +232,15 @@ bool plan_partial(int mla, int P, int page_size, int num_kv_heads, int num_q_hea
   if (mla) {
     chunk = 1024;
     unit = plan->seg;
+  } else if (dtype_bytes == 2) {
+    // tensor-core path: 16-key stages, 4 warps; about four chunks on the
+    // longest stripe, within [1024, 2048] keys (long enough to amortise a CTA's
+    // start and merge, short enough to balance rows of unequal length)
+    chunk = (max_stripe + 3) / 4;
+    chunk = chunk < 1024 ? 1024 : (chunk > 2048 ? 2048 : chunk);
+    unit = 64;
   } else {
-    // about eight chunks on the longest stripe, within [256, 2048] keys
+    // CUDA-core path: about eight chunks on the longest stripe, within [256, 2048] keys
     chunk = (max_stripe + 7) / 8;
     chunk = chunk < 256 ? 256 : (chunk > 2048 ? 2048 : chunk);
     unit = plan->seg * kGqaWarps;

@@ -1,0 +1,408 @@
+// cp_paged_attn_partial, GQA path on tensor cores (bf16 pools).
+//
+// Same work split and partner addressing as the CUDA-core path (see
+// partial_gqa.cu): CTA = (chunk, partner p, KV head h, query token t); partner
+// p's stripe slot k is logical position k * P + p at physical slot
+// k % (page_size / P) of the row's page k / (page_size / P) (mstar PR #1124
+// "Context / Sequence Parallel 1/5", description: logical slot s on partner
+// s % P at physical slot s / P, page ids logical).
+//
+// The chunk's page ids are checked once and staged in shared memory.  Per
+// warp: stages of 16 keys (gathered from as many page runs as needed) are
+// copied with 16-byte cp.async into an XOR-swizzled ring (chunk c of row r at
+// c ^ (r & 7), so ldmatrix rows never share banks).  The G query heads of the
+// KV head form the rows of a 16-row A tile (rows >= G are zero), so
+//   S = Q K^T  : 2 n-tiles (8 keys) x D/16 k-steps of mma.m16n8k16 (bf16 -> f32)
+//   O += P V   : D/8 n-tiles x 1 k-step (16 keys), P re-packed from the S
+//                accumulators in registers (their layout is the A layout) as
+//                a bf16 hi + lo pair, so P V keeps fp32-grade accuracy.
+// The tile is only G/16 full: decode reads each key once, so the contraction
+// is tiny and the kernel stays bound by HBM; the tensor cores only take the
+// multiply-adds off the issue slots (tcgen05 needs M >= 64 rows, a decode group
+// has 1..16).  Online softmax in the log2 domain with a lazily raised running
+// max (raised only when a block exceeds it by more than 8, which keeps every
+// probability <= 2^8 and the result exact).
+#include "gqa_core.cuh"
+#include "launch.h"
+#include "split_combine.cuh"
+
+namespace cpattn {
+
+constexpr int kMmaWarps = 4;
+constexpr int kMmaStages = 3;
+constexpr int kMmaKeys = 16;  // keys per stage
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// x ~= hi + lo with hi, lo bfloat16 pairs: lo carries the rounding error of hi,
+// so hi + lo matches x to about 2^-17 relative (two bf16 MMAs give fp32-grade P V).
+__device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16(x0, x1);
+  lo = pack_bf16(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xffff0000u));
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(const PartialArgs a) {
+  constexpr int NW = kMmaWarps;
+  constexpr int NST = kMmaStages;
+  constexpr int KT = kMmaKeys;
+  constexpr int ROWB = D * 2;
+  constexpr int CH = ROWB / 16;          // 16-byte chunks per row
+  constexpr int STAGE_B = KT * ROWB;     // K (or V) bytes per stage
+  constexpr int KSTEPS = D / 16;
+  constexpr int NT = D / 8;              // n-tiles of the output
+  constexpr int ITERS = KT * CH / 32;    // cp.async rounds per stage
+  static_assert(G >= 1 && G <= 16, "group size");
+  static_assert(NT % 4 == 0, "head dim");
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ uint32_t s_vmask[NW][NST];  // which of a stage's 16 keys were copied
+
+  const int c = blockIdx.x;
+  const int p = blockIdx.y / a.num_kv_heads;
+  const int h = blockIdx.y - p * a.num_kv_heads;
+  const int t = blockIdx.z;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int P = a.P;
+  const int quad = lane >> 2;  // row of the accumulator fragments
+  const int qi = lane & 3;
+
+  int b = -1;
+  if (a.qo_indptr != nullptr) {
+    if (t < __ldg(a.qo_indptr + a.num_rows)) b = find_row(a.qo_indptr, a.num_rows, t);
+  } else if (t < a.num_rows) {
+    b = t;
+  }
+  int n_p = 0;
+  if (b >= 0) {
+    int L = __ldg(a.kv_len + b);
+    if (L > a.max_kv_len) {
+      if (c == 0 && threadIdx.x == 0) report(a.dev_status, CPATTN_DEV_POS_PAST_TABLE);
+      L = a.max_kv_len;
+    }
+    n_p = (L > p) ? (L - p + P - 1) / P : 0;
+  }
+  const int nchunks = n_p > 0 ? (n_p + a.chunk - 1) / a.chunk : 1;
+  if (c >= nchunks) return;
+  const int k_begin = c * a.chunk;
+  const int k_end = min(n_p, k_begin + a.chunk);
+  const int nstage = k_end > k_begin ? (k_end - k_begin + KT - 1) / KT : 0;
+  const int my_n = nstage > warp ? (nstage - warp + NW - 1) / NW : 0;
+
+  // ---- Q fragments (A operand), rows = the G heads of this KV head
+  uint32_t qa[KSTEPS][4];
+  {
+    const uint32_t* qw = reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(a.q) +
+                                                           (static_cast<int64_t>(t) * a.num_q_heads + h * G) * ROWB);
+    const bool r0ok = b >= 0 && quad < G;
+    const bool r1ok = b >= 0 && quad + 8 < G;
+#pragma unroll
+    for (int s = 0; s < KSTEPS; ++s) {
+      const int w0 = s * 8 + qi;  // word of dims (16s + 2qi, +1)
+      qa[s][0] = r0ok ? __ldg(qw + quad * (D / 2) + w0) : 0u;
+      qa[s][1] = r1ok ? __ldg(qw + (quad + 8) * (D / 2) + w0) : 0u;
+      qa[s][2] = r0ok ? __ldg(qw + quad * (D / 2) + w0 + 4) : 0u;
+      qa[s][3] = r1ok ? __ldg(qw + (quad + 8) * (D / 2) + w0 + 4) : 0u;
+    }
+  }
+
+  uint8_t* ring = smem + static_cast<size_t>(warp) * NST * STAGE_B * 2;
+  const uint8_t* poolk = static_cast<const uint8_t*>(a.pool_k);
+  const uint8_t* poolv = static_cast<const uint8_t*>(a.pool_v);
+
+  // The chunk's page ids, checked once and staged in shared memory (-1 = not
+  // covered by the row's table or outside the pool), so issuing a stage never
+  // waits on a dependent global load.
+  int* spg = reinterpret_cast<int*>(smem + static_cast<size_t>(NW) * NST * STAGE_B * 2);
+  const int j0 = k_begin / a.ps_l;
+  if (nstage > 0) {
+    const int j1 = (k_end - 1) / a.ps_l;
+    int pb = 0, npages = 0;
+    if (b >= 0) {
+      pb = __ldg(a.page_indptr + b);
+      npages = __ldg(a.page_indptr + b + 1) - pb;
+    }
+    for (int x = threadIdx.x; x <= j1 - j0; x += blockDim.x) {
+      const int j = j0 + x;
+      int pg = -1;
+      if (j >= npages) {
+        report(a.dev_status, CPATTN_DEV_POS_PAST_TABLE);
+      } else {
+        pg = __ldg(a.page_indices + pb + j);
+        if (pg < 0 || pg >= a.num_pages) {
+          report(a.dev_status, CPATTN_DEV_PAGE_OUT_OF_RANGE);
+          pg = -1;
+        }
+      }
+      spg[x] = pg;
+    }
+  }
+  __syncthreads();
+  const int64_t head_row0 = static_cast<int64_t>(p) * a.num_pages * a.num_kv_heads + h;
+
+  // pool row of stripe slot k, or -1 if past the stripe or on a rejected page
+  auto row_of = [&](int k) -> int64_t {
+    if (k >= k_end) return -1;
+    const int j = k / a.ps_l;
+    const int pg = spg[j - j0];
+    if (pg < 0) return -1;
+    return (head_row0 + static_cast<int64_t>(pg) * a.num_kv_heads) * a.ps_l + (k - j * a.ps_l);
+  };
+
+  auto issue = [&](int i) {
+    if (i < my_n) {
+      const int k0 = k_begin + (warp + i * NW) * KT;
+      const int64_t myrow = row_of(k0 + (lane & (KT - 1)));  // lanes 0..15 and 16..31 both cover the 16 keys
+      const uint32_t vm = __ballot_sync(0xffffffffu, myrow >= 0) & 0xffffu;
+      if (lane == 0) s_vmask[warp][i % NST] = vm;
+      uint8_t* sk = ring + (i % NST) * STAGE_B * 2;
+      uint8_t* sv = sk + STAGE_B;
+#pragma unroll
+      for (int it = 0; it < ITERS; ++it) {
+        const int idx = it * 32 + lane;
+        const int key = idx / CH;
+        const int ch = idx - key * CH;
+        const int64_t row = __shfl_sync(0xffffffffu, myrow, key);
+        const int soff = (key * CH + (ch ^ (key & 7))) * 16;
+        if (row >= 0) {
+          cp_async16(sk + soff, poolk + row * ROWB + ch * 16);
+          cp_async16(sv + soff, poolv + row * ROWB + ch * 16);
+        } else {
+          *reinterpret_cast<uint4*>(sv + soff) = make_uint4(0u, 0u, 0u, 0u);  // masked keys: value 0, never NaN
+        }
+      }
+    }
+    cp_async_commit();
+  };
+
+  float o[NT][4];
+#pragma unroll
+  for (int u = 0; u < NT; ++u) o[u][0] = o[u][1] = o[u][2] = o[u][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  const float sl = a.scale * kLog2e;
+  const int mrow = lane & 7;
+  const int mi = lane >> 3;  // which of the 4 matrices of an ldmatrix.x4 this lane addresses
+
+#pragma unroll
+  for (int i = 0; i < NST - 1; ++i) issue(i);
+
+  for (int i = 0; i < my_n; ++i) {
+    cp_async_wait<NST - 2>();
+    __syncwarp();
+    issue(i + NST - 1);  // refills the stage consumed in step i - 1
+
+    const uint32_t sk = smem_u32(ring + (i % NST) * STAGE_B * 2);
+    const uint32_t sv = sk + STAGE_B;
+    const uint32_t vm = s_vmask[warp][i % NST];
+
+    // S = Q K^T for the 16 keys (two n-tiles), even / odd k-steps in two MMA chains
+    float s[2][4], s_alt[2][4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[j][e] = s_alt[j][e] = 0.f;
+#pragma unroll
+    for (int s2 = 0; s2 < KSTEPS; s2 += 2) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int key = j * 8 + mrow;
+        const int ch = s2 * 2 + mi;  // chunks 2*s2 .. 2*s2+3 cover k-steps s2, s2+1
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(sk + (key * CH + (ch ^ (key & 7))) * 16, b0, b1, b2, b3);
+        mma_bf16(s[j], qa[s2], b0, b1);
+        mma_bf16(s_alt[j], qa[s2 + 1], b2, b3);
+      }
+    }
+    // mask keys past the stripe end (or on a rejected page), scale into the log2 domain
+    float bm0 = -INFINITY, bm1 = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const bool ok = (vm >> (j * 8 + 2 * qi + e)) & 1u;
+        s[j][e] = ok ? (s[j][e] + s_alt[j][e]) * sl : -INFINITY;
+        s[j][e + 2] = ok ? (s[j][e + 2] + s_alt[j][e + 2]) * sl : -INFINITY;
+        bm0 = fmaxf(bm0, s[j][e]);
+        bm1 = fmaxf(bm1, s[j][e + 2]);
+      }
+    }
+    bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, 1));
+    bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, 2));
+    bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, 1));
+    bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, 2));
+    const bool up0 = bm0 > m0 + 8.f;
+    const bool up1 = bm1 > m1 + 8.f;
+    if (__any_sync(0xffffffffu, up0 || up1)) {
+      const float a0 = up0 ? exp2f(m0 - bm0) : 1.f;
+      const float a1 = up1 ? exp2f(m1 - bm1) : 1.f;
+      if (up0) m0 = bm0;
+      if (up1) m1 = bm1;
+      l0 *= a0;
+      l1 *= a1;
+#pragma unroll
+      for (int u = 0; u < NT; ++u) {
+        o[u][0] *= a0;
+        o[u][1] *= a0;
+        o[u][2] *= a1;
+        o[u][3] *= a1;
+      }
+    }
+    uint32_t pa[4], pl[4];
+    {
+      const float p00 = exp2f(s[0][0] - m0), p01 = exp2f(s[0][1] - m0);
+      const float p02 = exp2f(s[0][2] - m1), p03 = exp2f(s[0][3] - m1);
+      const float p10 = exp2f(s[1][0] - m0), p11 = exp2f(s[1][1] - m0);
+      const float p12 = exp2f(s[1][2] - m1), p13 = exp2f(s[1][3] - m1);
+      l0 += (p00 + p01) + (p10 + p11);
+      l1 += (p02 + p03) + (p12 + p13);
+      split_bf16(p00, p01, pa[0], pl[0]);
+      split_bf16(p02, p03, pa[1], pl[1]);
+      split_bf16(p10, p11, pa[2], pl[2]);
+      split_bf16(p12, p13, pa[3], pl[3]);
+    }
+    // O += P V  (V rows via ldmatrix.trans: two n-tiles of 8 dims per instruction)
+    {
+      const int key = (mi & 1) * 8 + mrow;
+#pragma unroll
+      for (int u = 0; u < NT; u += 4) {
+        uint32_t bv[2][4];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int ch = u + 2 * hh + (mi >> 1);  // 16-byte chunk = 8-dim group
+          ldsm_x4_t(sv + (key * CH + (ch ^ (key & 7))) * 16, bv[hh][0], bv[hh][1], bv[hh][2], bv[hh][3]);
+        }
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          mma_bf16(o[u + 2 * hh], pa, bv[hh][0], bv[hh][1]);
+          mma_bf16(o[u + 2 * hh + 1], pa, bv[hh][2], bv[hh][3]);
+        }
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          mma_bf16(o[u + 2 * hh], pl, bv[hh][0], bv[hh][1]);
+          mma_bf16(o[u + 2 * hh + 1], pl, bv[hh][2], bv[hh][3]);
+        }
+      }
+    }
+  }
+  cp_async_wait<0>();
+
+  // ---- per-warp state -> shared memory (rows < G only), then the cross-warp merge
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  __syncthreads();
+  float* sm = reinterpret_cast<float*>(smem);
+  float* sm_o = sm;                       // [NW][G][D]
+  float* sm_m = sm_o + NW * G * D;        // [NW][G]
+  float* sm_l = sm_m + NW * G;            // [NW][G]
+  if (quad < G) {
+#pragma unroll
+    for (int u = 0; u < NT; ++u) {
+      sm_o[(warp * G + quad) * D + u * 8 + 2 * qi] = o[u][0];
+      sm_o[(warp * G + quad) * D + u * 8 + 2 * qi + 1] = o[u][1];
+    }
+    if (qi == 0) {
+      sm_m[warp * G + quad] = m0;
+      sm_l[warp * G + quad] = l0;
+    }
+  }
+  if (quad + 8 < G) {
+#pragma unroll
+    for (int u = 0; u < NT; ++u) {
+      sm_o[(warp * G + quad + 8) * D + u * 8 + 2 * qi] = o[u][2];
+      sm_o[(warp * G + quad + 8) * D + u * 8 + 2 * qi + 1] = o[u][3];
+    }
+    if (qi == 0) {
+      sm_m[warp * G + quad + 8] = m1;
+      sm_l[warp * G + quad + 8] = l1;
+    }
+  }
+  __syncthreads();
+
+  const int64_t orow0 = (static_cast<int64_t>(p) * a.num_tokens + t) * a.num_q_heads + h * G;
+  const int64_t slot = (static_cast<int64_t>(t) * P + p) * a.num_kv_heads + h;
+  const bool single = (nchunks == 1);
+  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+    const int g = idx / D;
+    const int d = idx - g * D;
+    float out, lse;
+    merge_stored<D, G>(sm, NW, g, d, out, lse);
+    if (single) {
+      a.o_part[(orow0 + g) * D + d] = out;
+      if (d == 0) a.lse_part[orow0 + g] = lse;
+    } else {
+      const int64_t wrow = (slot * a.max_chunks + c) * G + g;
+      a.ws_o[wrow * D + d] = out;
+      if (d == 0) a.ws_lse[wrow] = lse;
+    }
+  }
+  if (single) return;
+  if (!take_ticket(a.ws_cnt + slot, nchunks)) return;
+  merge_chunks(a, slot, nchunks, G, D, a.o_part + orow0 * D, a.lse_part + orow0);
+  if (threadIdx.x == 0) a.ws_cnt[slot] = 0;  // ready for the next call
+}
+
+template <int D, int G>
+static int launch_mma_t(const PartialArgs& a, cudaStream_t s, cudaError_t* err) {
+  const size_t ring = static_cast<size_t>(kMmaWarps) * kMmaStages * kMmaKeys * D * 2 * 2;
+  const size_t comb = (static_cast<size_t>(kMmaWarps) * G * D + 2 * kMmaWarps * G) * sizeof(float);
+  const size_t pages = (static_cast<size_t>(a.chunk) / a.ps_l + 2) * sizeof(int);
+  const size_t smem = (ring > comb ? ring : comb) + pages;
+  auto kern = gqa_partial_mma_kernel<D, G>;
+  *err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (*err != cudaSuccess) return CPATTN_ERR_CUDA;
+  dim3 grid(a.max_chunks, a.P * a.num_kv_heads, a.num_tokens);
+  kern<<<grid, kMmaWarps * 32, smem, s>>>(a);
+  *err = cudaGetLastError();
+  return *err == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+}
+
+template <int D>
+static int mma_dispatch_g(const PartialArgs& a, int G, cudaStream_t s, cudaError_t* err) {
+  switch (G) {
+    case 1: return launch_mma_t<D, 1>(a, s, err);
+    case 2: return launch_mma_t<D, 2>(a, s, err);
+    case 4: return launch_mma_t<D, 4>(a, s, err);
+    case 8: return launch_mma_t<D, 8>(a, s, err);
+    case 16: return launch_mma_t<D, 16>(a, s, err);
+    default: return CPATTN_ERR_UNSUPPORTED_SHAPE;
+  }
+}
+
+int launch_gqa_partial_mma(const PartialArgs& a, cudaStream_t s, cudaError_t* err) {
+  const int G = a.num_q_heads / a.num_kv_heads;
+  if (a.head_dim != a.head_dim_v) return CPATTN_ERR_UNSUPPORTED_SHAPE;
+  if (a.head_dim == 128) return mma_dispatch_g<128>(a, G, s, err);
+  if (a.head_dim == 64) return mma_dispatch_g<64>(a, G, s, err);
+  return CPATTN_ERR_UNSUPPORTED_SHAPE;
+}
+
+}  // namespace cpattn

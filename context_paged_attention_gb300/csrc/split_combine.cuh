@@ -14,19 +14,22 @@
 namespace cpattn {
 
 // Returns true in every thread of the CTA that must do the final merge.
-// Call after this CTA's workspace stores; all threads must call it.
+// Call after this CTA's workspace stores; all threads must call it.  The
+// barrier orders every thread's stores before thread 0's device-scope fence,
+// which (being cumulative) publishes them before the ticket; the last CTA's
+// thread 0 fences again before the barrier that releases its readers.
 __device__ __forceinline__ bool take_ticket(int32_t* counter, int arrivals_needed) {
   __shared__ int s_last;
-  __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
+    __threadfence();
     const int ticket = atomicAdd(counter, 1);
-    s_last = (ticket == arrivals_needed - 1);
+    const bool last = (ticket == arrivals_needed - 1);
+    if (last) __threadfence();
+    s_last = last;
   }
   __syncthreads();
-  const bool last = s_last != 0;
-  if (last) __threadfence();
-  return last;
+  return s_last != 0;
 }
 
 // Merge nchunks workspace partials of one (token, partner, KV head) slot.
