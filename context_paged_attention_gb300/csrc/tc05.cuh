@@ -1,0 +1,166 @@
+// Blackwell tensor-core (tcgen05 / TMEM) building blocks, sm_100 family.
+//
+// Operand tiles live in shared memory in the swizzled layouts the tensor core
+// reads directly; the accumulator lives in tensor memory (TMEM, 128 lanes x 512
+// 32-bit columns per SM), is written by tcgen05.mma issued from one thread,
+// and read back by the warps with tcgen05.ld (warp w sees lanes 32w..32w+31).
+//
+// Layouts used here (bf16 operands):
+// * K-major, 128-byte swizzle ("SW128K"): a tile of R rows x 64 K-elements is
+//   R x 128 B; 16-byte chunk c of row r sits at r*128 + ((c ^ (r & 7)) * 16).
+//   Wider K is a sequence of such 64-element column blocks.  Stride between
+//   8-row groups (SBO) = 1024 B.  A 16-element K step inside a block is a
+//   +32 B start offset.
+// * MN-major, 128-byte swizzle ("SW128MN"): the same physical tile read with
+//   the 64-element, 128-byte rows along M/N and the rows along K (e.g. value
+//   rows [key][dim] used as the B operand of P V).  8-row K groups are 1024 B
+//   apart; 64-element M/N blocks are `block_stride` bytes apart.
+// * K-major, 64-byte swizzle ("SW64K"): rows of 32 K-elements (64 B); chunk c
+//   of row r at r*64 + ((c ^ ((r >> 1) & 3)) * 16); SBO = 512 B.
+// Every tile base is 1024-byte aligned.
+#pragma once
+
+#include <stdint.h>
+
+namespace cpattn {
+namespace tc05 {
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// --- shared-memory matrix descriptors -------------------------------------
+// bits 0-13 start >> 4, 16-29 leading byte offset >> 4, 32-45 stride byte
+// offset >> 4, 46-47 descriptor version (1), 61-63 swizzle mode.
+constexpr uint64_t kSwizzle128 = 2;
+constexpr uint64_t kSwizzle64 = 4;
+
+__device__ __forceinline__ uint64_t make_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint64_t swz) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= swz << 61;
+  return d;
+}
+
+// K-major SW128 operand; saddr already includes the +32 B per K step.
+__device__ __forceinline__ uint64_t desc_k128(uint32_t saddr) { return make_desc(saddr, 16, 1024, kSwizzle128); }
+// K-major SW64 operand.
+__device__ __forceinline__ uint64_t desc_k64(uint32_t saddr) { return make_desc(saddr, 16, 512, kSwizzle64); }
+// MN-major SW128 operand: 64-element M/N blocks `block_stride` bytes apart,
+// 8-row K groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t desc_mn128(uint32_t saddr, uint32_t block_stride) {
+  return make_desc(saddr, block_stride, 1024, kSwizzle128);
+}
+
+// --- instruction descriptor (kind::f16, bf16 x bf16 -> f32) ------------------
+// bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format,
+// 15 A major (1 = MN), 16 B major (1 = MN), 17-22 N >> 3, 24-28 M >> 4.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (a_mn ? 1u << 15 : 0u) | (b_mn ? 1u << 16 : 0u) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// --- MMA, commit -------------------------------------------------------------
+__device__ __forceinline__ void mma_ss(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
+      : "memory");
+}
+
+// Arrive once on the mbarrier when every MMA issued so far by this thread is done.
+__device__ __forceinline__ void commit(uint32_t mbar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(mbar)
+               : "memory");
+}
+
+// --- TMEM allocation (one full warp) -----------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// --- fences ------------------------------------------------------------------
+__device__ __forceinline__ void fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+}
+__device__ __forceinline__ void fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+}
+// Make this thread's generic-proxy shared-memory stores visible to the tensor core.
+__device__ __forceinline__ void fence_smem_to_async() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
+// --- mbarrier -----------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(mbar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+// Bounded wait for the phase with parity `parity` to complete.  Returns false
+// if it did not complete within `max_tries` polls (the caller reports it).
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, uint32_t max_tries = 1u << 24) {
+  for (uint32_t i = 0; i < max_tries; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(mbar), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+// --- TMEM loads / stores (32 lanes x 32 bits, repeated over columns) ---------
+// Each thread of the warp gets 16 (or 32) consecutive columns of its lane.
+__device__ __forceinline__ void ld_x16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void st_x16(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16};\n" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])));
+}
+__device__ __forceinline__ void ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
+__device__ __forceinline__ void st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
+
+// TMEM address of (lane, column).
+__device__ __forceinline__ uint32_t taddr(uint32_t base, uint32_t lane, uint32_t col) {
+  return base + (lane << 16) + col;
+}
+
+// Byte offset of 16-byte chunk c of row r in a SW128 tile (rows of 128 B).
+__host__ __device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t c) { return r * 128u + ((c ^ (r & 7u)) << 4); }
+// Byte offset of 16-byte chunk c of row r in a SW64 tile (rows of 64 B).
+__host__ __device__ __forceinline__ uint32_t sw64(uint32_t r, uint32_t c) {
+  return r * 64u + ((c ^ ((r >> 1) & 3u)) << 4);
+}
+
+}  // namespace tc05
+}  // namespace cpattn

@@ -1,0 +1,41 @@
+/*
+ * cpattn_selftest.h -- device self-test of libcpattn's tensor-core plumbing.
+ *
+ * The pages have no counterpart: this checks, against a plain matmul in a
+ * test, that the shared-memory operand layouts, tcgen05 descriptors, TMEM
+ * allocation and tcgen05.ld read-back used by the attention kernels produce
+ * the product they are meant to.  Same conventions as cpattn.h (device
+ * pointers, caller's stream, negative status on bad arguments).
+ */
+#ifndef CPATTN_SELFTEST_H_
+#define CPATTN_SELFTEST_H_
+
+#include <stdint.h>
+
+#include "cpattn.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * One 128-row tile, bf16 inputs (row-major in global memory), fp32 output
+ * D [128][N] (row-major):
+ *   variant 0: D = A B^T, A [128][K], B [N][K]; both staged K-major with the
+ *              128-byte swizzle (the Q K^T pattern).  N in 16..256 step 16,
+ *              K in {64, 128, 192, 256}.
+ *   variant 1: D = A B, A [128][32] K-major with the 64-byte swizzle, B [32][N]
+ *              read M/N-major from 128-byte-swizzled rows (the P V pattern).
+ *              N in {64, 128, 192, 256}.
+ *   variant 2: variant 1 with the two descriptor strides exchanged (a check
+ *              of which field carries which stride).
+ * A completion wait that times out stores 4 in *dev_status (if not NULL).
+ */
+CPATTN_API int cpattn_umma_selftest(int variant, const void* A, const void* B, float* D, int N, int K,
+                                    int32_t* dev_status, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CPATTN_SELFTEST_H_ */

@@ -22,7 +22,10 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    text = ""
+    for name in sorted(os.listdir(os.path.dirname(HEADER))):
+        if name.endswith(".h"):
+            text += open(os.path.join(os.path.dirname(HEADER), name)).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     names = re.findall(r"^\s*(?:CPATTN_API\s+)?(?:int|size_t|const char\s*\*)\s+(\w+)\s*\(", text, flags=re.M)
     return names
