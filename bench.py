@@ -42,7 +42,7 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
 # sources whose digest keys the recorded ncu traffic of each partial kernel
 KERNEL_SOURCES = {
     "gqa_partial": ["partial_gqa.cu", "partial_gqa_mma.cu", "gqa_core.cuh", "split_combine.cuh", "common.cuh"],
-    "mla_partial": ["partial_gqa.cu", "partial_mla_fma.cu", "split_combine.cuh", "common.cuh"],
+    "mla_partial": ["partial_gqa.cu", "partial_mla_tc.cu", "tc05.cuh", "split_combine.cuh", "common.cuh"],
 }
 
 

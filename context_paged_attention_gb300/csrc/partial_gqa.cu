@@ -230,8 +230,8 @@ bool plan_partial(int mla, int P, int page_size, int num_kv_heads, int num_q_hea
   int chunk;
   int unit;
   if (mla) {
-    chunk = 1024;
-    unit = plan->seg;
+    chunk = mla_tc_chunk(ps_l);
+    unit = 32;
   } else if (dtype_bytes == 2) {
     // tensor-core path: 16-key stages, 4 warps; about four chunks on the
     // longest stripe, within [1024, 2048] keys (long enough to amortise a CTA's

@@ -123,6 +123,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, uint32
   return false;
 }
 
+// --- TMA (tensor-map bulk copies into shared memory) -------------------------
+// Register `bytes` of expected transaction on the mbarrier and arrive once.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t mbar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(mbar), "r"(bytes) : "memory");
+}
+// 2-D tiled copy of the box at (x, y) (x = innermost, in elements) into dst;
+// completion is counted in bytes on the mbarrier.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y, uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(mbar)
+      : "memory");
+}
+
 // --- TMEM loads / stores (32 lanes x 32 bits, repeated over columns) ---------
 // Each thread of the warp gets 16 (or 32) consecutive columns of its lane.
 __device__ __forceinline__ void ld_x16(uint32_t taddr, float (&v)[16]) {

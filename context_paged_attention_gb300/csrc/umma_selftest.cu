@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(128) umma_selftest_kernel(int variant, const _
       for (int i = 0; i < 16; ++i) dst[i] = v[i];
     }
   } else if (tid == 0) {
-    report(status, 4);
+    report(status, CPATTN_DEV_TC_TIMEOUT);
   }
   tc05::fence_before_sync();
   __syncthreads();

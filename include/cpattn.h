@@ -83,6 +83,7 @@ extern "C" {
 #define CPATTN_DEV_PAGE_OUT_OF_RANGE 1   /* page id outside [0, num_pages) */
 #define CPATTN_DEV_POS_PAST_TABLE 2      /* position beyond the row's page table */
 #define CPATTN_DEV_BAD_INDPTR 3          /* qo_indptr not within [0, num_tokens] */
+#define CPATTN_DEV_TC_TIMEOUT 4          /* a tensor-core completion wait ran out; that CTA's output is not written */
 
 /* element types */
 #define CPATTN_DTYPE_BF16 0
