@@ -71,6 +71,7 @@ bool plan_partial(int mla, int P, int page_size, int num_kv_heads, int num_q_hea
 // status: 0 ok, CPATTN_ERR_UNSUPPORTED_SHAPE, or the cudaError via *err
 int launch_gqa_partial(const PartialArgs& a, int dtype_bf16, cudaStream_t s, cudaError_t* err);
 int launch_gqa_partial_mma(const PartialArgs& a, cudaStream_t s, cudaError_t* err);
+int launch_gqa_partial_ext(const PartialArgs& a, cudaStream_t s, cudaError_t* err);
 int launch_mla_partial(const PartialArgs& a, cudaStream_t s, cudaError_t* err);
 int mla_tc_chunk(int ps_l);  // keys per CTA of the MLA tensor-core kernel
 

@@ -1,4 +1,5 @@
-// cp_paged_attn_partial, GQA path on tensor cores (bf16 pools).
+// cp_paged_attn_partial, GQA path on tensor cores (bf16 pools), rows of one
+// query token (rows of several tokens: partial_gqa_ext.cu).
 //
 // Same work split and partner addressing as the CUDA-core path (see
 // partial_gqa.cu): CTA = (chunk, partner p, KV head h, query token t); partner
@@ -24,6 +25,7 @@
 // probability <= 2^8 and the result exact).
 #include "gqa_core.cuh"
 #include "launch.h"
+#include "mma_sync.cuh"
 #include "split_combine.cuh"
 
 namespace cpattn {
@@ -31,42 +33,6 @@ namespace cpattn {
 constexpr int kMmaWarps = 4;
 constexpr int kMmaStages = 3;
 constexpr int kMmaKeys = 16;  // keys per stage
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];\n"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];\n"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-// x ~= hi + lo with hi, lo bfloat16 pairs: lo carries the rounding error of hi,
-// so hi + lo matches x to about 2^-17 relative (two bf16 MMAs give fp32-grade P V).
-__device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  hi = pack_bf16(x0, x1);
-  lo = pack_bf16(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xffff0000u));
-}
 
 template <int D, int G>
 __global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(const PartialArgs a) {
@@ -96,7 +62,11 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(cons
 
   int b = -1;
   if (a.qo_indptr != nullptr) {
-    if (t < __ldg(a.qo_indptr + a.num_rows)) b = find_row(a.qo_indptr, a.num_rows, t);
+    if (t < __ldg(a.qo_indptr + a.num_rows)) {
+      b = find_row(a.qo_indptr, a.num_rows, t);
+      // rows of two or more tokens belong to the multi-token kernel (partial_gqa_ext.cu)
+      if (__ldg(a.qo_indptr + b + 1) - __ldg(a.qo_indptr + b) >= 2) return;
+    }
   } else if (t < a.num_rows) {
     b = t;
   }
@@ -400,9 +370,12 @@ static int mma_dispatch_g(const PartialArgs& a, int G, cudaStream_t s, cudaError
 int launch_gqa_partial_mma(const PartialArgs& a, cudaStream_t s, cudaError_t* err) {
   const int G = a.num_q_heads / a.num_kv_heads;
   if (a.head_dim != a.head_dim_v) return CPATTN_ERR_UNSUPPORTED_SHAPE;
-  if (a.head_dim == 128) return mma_dispatch_g<128>(a, G, s, err);
-  if (a.head_dim == 64) return mma_dispatch_g<64>(a, G, s, err);
-  return CPATTN_ERR_UNSUPPORTED_SHAPE;
+  int st = CPATTN_ERR_UNSUPPORTED_SHAPE;
+  if (a.head_dim == 128) st = mma_dispatch_g<128>(a, G, s, err);
+  if (a.head_dim == 64) st = mma_dispatch_g<64>(a, G, s, err);
+  // ragged rows may hold several tokens: those rows go to the multi-token kernel
+  if (st == CPATTN_OK && a.qo_indptr != nullptr) st = launch_gqa_partial_ext(a, s, err);
+  return st;
 }
 
 }  // namespace cpattn

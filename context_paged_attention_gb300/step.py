@@ -92,9 +92,12 @@ class StripedAttention:
 
     def partial(self, stream=None):
         P = self.w.P
+        # one token a row (a decode step): the call takes no token -> row map
+        one_per_row = self.w.decode and self.w.num_tokens == self.w.num_rows
         B.cp_paged_attn_partial(self.desc, self.pool_k, self.pool_v, self.q, self.kv_len, self.max_kv_len,
                                 self.page_indptr, self.page_indices, self.w.scale, self.o_parts[:P],
-                                self.lse_parts[:P], self.workspace, qo_indptr=self.qo_indptr,
+                                self.lse_parts[:P], self.workspace,
+                                qo_indptr=None if one_per_row else self.qo_indptr,
                                 num_rows=self.w.num_rows, dev_status=self.dev_status, stream=stream)
 
     def own(self, stream=None):
