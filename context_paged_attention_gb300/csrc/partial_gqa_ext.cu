@@ -61,6 +61,14 @@ __global__ void __launch_bounds__(kExtWarps * 32, 2) gqa_partial_ext_kernel(cons
   const int t_lo = blockIdx.z * QB;
   const int t_real = __ldg(a.qo_indptr + a.num_rows);
   const int t_hi = min(t_lo + QB, t_real);
+  if (c == 0) {
+    // padding tokens past the last row: this (partner, KV head)'s 0 / -inf
+    for (int tok = max(t_lo, t_real); tok < min(t_lo + QB, a.num_tokens); ++tok) {
+      const int64_t orow0 = (static_cast<int64_t>(p) * a.num_tokens + tok) * a.num_q_heads + h * G;
+      for (int x = tid; x < G * D; x += blockDim.x) a.o_part[orow0 * D + x] = 0.f;
+      if (tid < G) a.lse_part[orow0 + tid] = -INFINITY;
+    }
+  }
   if (t_lo >= t_hi) return;
 
   for (int b = find_row(a.qo_indptr, a.num_rows, t_lo); b < a.num_rows; ++b) {

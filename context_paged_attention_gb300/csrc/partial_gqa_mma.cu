@@ -53,22 +53,21 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(cons
   const int c = blockIdx.x;
   const int p = blockIdx.y / a.num_kv_heads;
   const int h = blockIdx.y - p * a.num_kv_heads;
-  const int t = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int P = a.P;
   const int quad = lane >> 2;  // row of the accumulator fragments
   const int qi = lane & 3;
 
-  int b = -1;
+  // one CTA column per row: with a token -> row map only rows of exactly one
+  // token are handled here (rows of two or more tokens: partial_gqa_ext.cu,
+  // which also writes the padding tokens past the last row); without a map
+  // row b is token b
+  int b = blockIdx.z;
+  int t = b;
   if (a.qo_indptr != nullptr) {
-    if (t < __ldg(a.qo_indptr + a.num_rows)) {
-      b = find_row(a.qo_indptr, a.num_rows, t);
-      // rows of two or more tokens belong to the multi-token kernel (partial_gqa_ext.cu)
-      if (__ldg(a.qo_indptr + b + 1) - __ldg(a.qo_indptr + b) >= 2) return;
-    }
-  } else if (t < a.num_rows) {
-    b = t;
+    t = __ldg(a.qo_indptr + b);
+    if (__ldg(a.qo_indptr + b + 1) - t != 1) return;
   }
   int n_p = 0;
   if (b >= 0) {
@@ -349,7 +348,7 @@ static int launch_mma_t(const PartialArgs& a, cudaStream_t s, cudaError_t* err) 
   auto kern = gqa_partial_mma_kernel<D, G>;
   *err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (*err != cudaSuccess) return CPATTN_ERR_CUDA;
-  dim3 grid(a.max_chunks, a.P * a.num_kv_heads, a.num_tokens);
+  dim3 grid(a.max_chunks, a.P * a.num_kv_heads, a.qo_indptr != nullptr ? a.num_rows : a.num_tokens);
   kern<<<grid, kMmaWarps * 32, smem, s>>>(a);
   *err = cudaGetLastError();
   return *err == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
