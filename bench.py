@@ -41,7 +41,8 @@ FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
 # sources whose digest keys the recorded ncu traffic of each partial kernel
 KERNEL_SOURCES = {
-    "gqa_partial": ["partial_gqa.cu", "partial_gqa_mma.cu", "gqa_core.cuh", "split_combine.cuh", "common.cuh"],
+    "gqa_partial": ["partial_gqa.cu", "partial_gqa_mma.cu", "partial_gqa_ext_tc.cu", "gqa_core.cuh",
+                    "split_combine.cuh", "common.cuh", "tc05.cuh", "mma_sync.cuh"],
     "mla_partial": ["partial_gqa.cu", "partial_mla_tc.cu", "tc05.cuh", "split_combine.cuh", "common.cuh"],
 }
 
@@ -135,35 +136,105 @@ def recorded_traffic(kernel, workload):
     return None
 
 
+_REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                "hw_thermal_slowdown": 0x40}
+
+
+class _Nvml:
+    """Read-only NVML queries through ctypes: SM clock, its maximum, power and
+    the active clock-event reasons of one GPU (found by its UUID)."""
+
+    def __init__(self, uuid: str):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        u = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        if self.lib.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(self.h)) != 0:
+            raise RuntimeError("no NVML handle for " + u)
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def read(self):
+        ct = self.ct
+        sm, mx, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        self.lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(sm))       # NVML_CLOCK_SM
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ct.byref(mx))
+        self.lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(mw))
+        self.reasons_fn(self.h, ct.byref(rs))
+        return float(sm.value), float(mx.value), mw.value / 1000.0, int(rs.value)
+
+
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 100 ms in the background."""
+    """SM clocks and clock-event reasons sampled in the background.
+
+    NVML (read-only) polled every 5 ms, so that even a timed region of a few
+    tens of milliseconds holds several samples; ``nvidia-smi -lms 100`` if
+    NVML cannot be opened.  Samples are (wall time, sm MHz, max MHz, reasons set).
+    """
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
+    SMI_NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self, device_id):
+    def __init__(self, device_index: int, uuid: str | None = None, period_s: float = 0.005):
         self.samples = []
         self.proc = None
-        self.device_id = device_id
+        self.device_index = device_index
+        self.uuid = uuid
+        self.period = period_s
+        self.source = None
+        self._stop = threading.Event()
 
     def start(self):
+        nv = None
+        if self.uuid:
+            try:
+                nv = _Nvml(self.uuid)
+                nv.read()
+            except Exception:
+                nv = None
+        if nv is not None:
+            self.source = "nvml 5 ms"
+            threading.Thread(target=self._poll, args=(nv,), daemon=True).start()
+            return
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
-                 "-i", str(self.device_id)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-i", str(self.device_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
             return
+        self.source = "nvidia-smi 100 ms"
         threading.Thread(target=self._read, daemon=True).start()
 
+    def _poll(self, nv):
+        while not self._stop.is_set():
+            try:
+                sm, mx, _, bits = nv.read()
+            except Exception:
+                return
+            reasons = {n for n, b in _REASON_BITS.items() if bits & b}
+            self.samples.append((time.time(), sm, mx, reasons))
+            self._stop.wait(self.period)
+
     def _read(self):
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
         for line in self.proc.stdout:
             parts = [x.strip() for x in line.split(",")]
             if len(parts) >= 8:
-                self.samples.append((time.time(), parts))
+                reasons = {self.SMI_NAMES[i] for i in range(4) if parts[4 + i].lower() == "active"}
+                self.samples.append((time.time(), num(parts[0]), num(parts[1]), reasons))
 
     def stop(self):
+        self._stop.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -173,22 +244,14 @@ class ClockSampler:
 
     def summary(self, t0, t1):
         if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
-        used = inside if inside else [min(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[1]]
-
-        def num(x):
-            try:
-                return float(x)
-            except ValueError:
-                return None
-
-        sm = [num(p[0]) for p in used if num(p[0]) is not None]
-        smax = [num(p[1]) for p in used if num(p[1]) is not None]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for p in used for i in range(4) if p[4 + i].lower() == "active"})
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": self.source}
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        used = inside if inside else [min(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))]
+        sm = [s[1] for s in used if s[1] is not None]
+        smax = [s[2] for s in used if s[2] is not None]
+        reasons = sorted(set().union(*[s[3] for s in used]))
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": reasons, "samples": len(used), "window_samples": len(inside)}
+                "reasons": reasons, "samples": len(used), "window_samples": len(inside), "source": self.source}
 
 
 # ---------------------------------------------------------------- CPU oracle timing
@@ -301,7 +364,11 @@ def run_ours(args, rank, world, local_rank):
 
     sampler = None
     if not args.no_clocks and rank == 0:
-        sampler = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+        try:
+            uuid = str(torch.cuda.get_device_properties(local_rank).uuid)
+        except Exception:
+            uuid = None
+        sampler = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else 0, uuid)
         sampler.start()
         time.sleep(0.3)
 

@@ -46,6 +46,7 @@ class PoolDesc(ctypes.Structure):
         ("head_dim", ctypes.c_int32),
         ("head_dim_v", ctypes.c_int32),
         ("dtype", ctypes.c_int32),
+        ("interleave", ctypes.c_int32),
     ]
 
     @property
@@ -99,7 +100,7 @@ def load_library(path: str | None = None):
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
-    if lib.cpattn_version() != 1:
+    if lib.cpattn_version() != 2:
         raise RuntimeError("libcpattn version mismatch")
     if path is None:
         _lib = lib

@@ -18,10 +18,14 @@ int dtype_bytes(int dtype) {
   return 0;
 }
 
+// Interleave size: 0 in the descriptor means 1 (plain striping).
+int interleave_of(const cpattn_pool_desc* d) { return d->interleave > 1 ? d->interleave : 1; }
+
 // Common descriptor checks.  mla: head_dim != head_dim_v (value = prefix of the key row).
 int check_desc(const cpattn_pool_desc* d) {
   if (d == nullptr) return CPATTN_ERR_INVALID_ARG;
-  if (d->P < 1 || d->page_size < 1 || d->page_size % d->P != 0) return CPATTN_ERR_P_NOT_DIVIDING_PAGE_SIZE;
+  if (d->P < 1 || d->page_size < 1 || d->interleave < 0 || d->page_size % (d->P * interleave_of(d)) != 0)
+    return CPATTN_ERR_P_NOT_DIVIDING_PAGE_SIZE;
   if (d->num_pages < 1 || d->num_kv_heads < 1 || d->head_dim < 1 || d->head_dim_v < 1)
     return CPATTN_ERR_INVALID_ARG;
   const int eb = dtype_bytes(d->dtype);
@@ -43,7 +47,7 @@ const char* cpattn_status_string(int status) {
   switch (status) {
     case CPATTN_OK: return "ok";
     case CPATTN_ERR_INVALID_ARG: return "invalid argument";
-    case CPATTN_ERR_P_NOT_DIVIDING_PAGE_SIZE: return "P must be >= 1 and divide page_size";
+    case CPATTN_ERR_P_NOT_DIVIDING_PAGE_SIZE: return "P and interleave must be >= 1 and P * interleave divide page_size";
     case CPATTN_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (head dims / group size)";
     case CPATTN_ERR_MISALIGNED: return "device pointer not 16-byte aligned";
     case CPATTN_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
@@ -86,6 +90,7 @@ int cp_kv_write(const cpattn_pool_desc* desc, void* pool_k, void* pool_v, const 
   a.page_indices = kv_page_indices;
   a.dev_status = dev_status;
   a.P = desc->P;
+  a.interleave = interleave_of(desc);
   a.page_size = desc->page_size;
   a.num_pages = desc->num_pages;
   a.num_kv_heads = desc->num_kv_heads;
@@ -101,7 +106,7 @@ size_t cp_paged_attn_workspace_bytes(const cpattn_pool_desc* desc, int32_t num_q
   if (check_desc(desc) != CPATTN_OK || num_q_heads < 1 || num_tokens < 0 || max_kv_len < 0) return 0;
   if (num_q_heads % desc->num_kv_heads != 0) return 0;
   PartialPlan plan;
-  if (!plan_partial(is_mla(desc), desc->P, desc->page_size, desc->num_kv_heads, num_q_heads, desc->head_dim,
+  if (!plan_partial(is_mla(desc), desc->P, interleave_of(desc), desc->page_size, desc->num_kv_heads, num_q_heads, desc->head_dim,
                     num_tokens, max_kv_len, dtype_bytes(desc->dtype), &plan))
     return 0;
   return plan.bytes();
@@ -130,7 +135,7 @@ int cp_paged_attn_partial(const cpattn_pool_desc* desc, const void* pool_k, cons
   if (mla && desc->dtype != CPATTN_DTYPE_BF16) return CPATTN_ERR_UNSUPPORTED_SHAPE;
 
   PartialPlan plan;
-  if (!plan_partial(mla, desc->P, desc->page_size, desc->num_kv_heads, num_q_heads, desc->head_dim, num_tokens,
+  if (!plan_partial(mla, desc->P, interleave_of(desc), desc->page_size, desc->num_kv_heads, num_q_heads, desc->head_dim, num_tokens,
                     max_kv_len, dtype_bytes(desc->dtype), &plan))
     return CPATTN_ERR_UNSUPPORTED_SHAPE;
   const size_t need = plan.bytes();
@@ -153,6 +158,7 @@ int cp_paged_attn_partial(const cpattn_pool_desc* desc, const void* pool_k, cons
   a.page_indices = kv_page_indices;
   a.dev_status = dev_status;
   a.P = desc->P;
+  a.interleave = interleave_of(desc);
   a.page_size = desc->page_size;
   a.ps_l = desc->page_size / desc->P;
   a.num_pages = desc->num_pages;

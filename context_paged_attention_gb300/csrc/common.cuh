@@ -67,6 +67,21 @@ __device__ __forceinline__ int find_row(const int32_t* __restrict__ indptr, int 
   return lo;
 }
 
+// Keys of a row of L positions that partner p holds when runs of I
+// consecutive positions go round the P partners (I = 1: positions p, p + P, ...).
+// Those keys fill the partner's physical slots 0 .. n - 1 in stripe order.
+__host__ __device__ __forceinline__ int stripe_len(int L, int p, int P, int I) {
+  const int groups = L / I;  // whole runs
+  const int mine = groups > p ? (groups - p + P - 1) / P : 0;
+  return mine * I + (groups % P == p ? L - groups * I : 0);
+}
+
+// Upper bound of stripe_len over the partners (exact for I = 1).
+__host__ __device__ __forceinline__ int max_stripe_len(int L, int P, int I) {
+  const int runs = (L + I * P - 1) / (I * P);
+  return runs * I < L ? runs * I : L;
+}
+
 // Online-softmax state merge in the log2 domain: (m, l) absorbs (m2, l2);
 // returns the factors the two accumulators are scaled by.
 __device__ __forceinline__ void softmax_merge_factors(float m, float m2, float& mn, float& a, float& b) {

@@ -2,7 +2,9 @@
 //
 // Placement (mstar PR #1124 "Context / Sequence Parallel 1/5", description):
 // offset off of a logical page belongs to partner off % P at physical slot
-// off / P of the same page id.  The review thread of that PR shows the failure
+// off / P of the same page id.  With an interleave size I (vLLM's
+// cp_kv_cache_interleave_size), runs of I offsets go together: partner
+// (off / I) % P, physical slot (off / (I * P)) * I + off % I.  The review thread of that PR shows the failure
 // this kernel must avoid: taking the slot at the logical page size, which makes
 // every partner write every token at offsets up to page_size - 1.
 //
@@ -43,8 +45,9 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const WriteArgs a, int ch
     return;
   }
   const int off = pos - page_idx * a.page_size;
-  const int partner = off % a.P;
-  const int slot = off / a.P;
+  const int run = off / a.interleave;
+  const int partner = run % a.P;
+  const int slot = (run / a.P) * a.interleave + (off - run * a.interleave);
   const int ps_l = a.page_size / a.P;
   // row index inside the pool tensor [P][num_pages][H][ps_l]
   const int64_t prow =

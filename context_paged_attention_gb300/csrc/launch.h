@@ -17,7 +17,7 @@ struct WriteArgs {
   const int32_t* page_indptr;
   const int32_t* page_indices;
   int32_t* dev_status;
-  int P, page_size, num_pages, num_kv_heads, num_rows, num_tokens;
+  int P, interleave, page_size, num_pages, num_kv_heads, num_rows, num_tokens;
   int row_bytes_k, row_bytes_v;  // bytes of one head's K / V row
 };
 cudaError_t launch_kv_write(const WriteArgs& a, cudaStream_t s);
@@ -50,7 +50,7 @@ struct PartialArgs {
   float* ws_o;
   float* ws_lse;
   int32_t* ws_cnt;
-  int P, page_size, ps_l, num_pages, num_kv_heads, num_q_heads, head_dim, head_dim_v;
+  int P, interleave, page_size, ps_l, num_pages, num_kv_heads, num_q_heads, head_dim, head_dim_v;
   int num_rows, num_tokens, max_kv_len;
   int seg;         // tokens per staged segment (divides ps_l)
   int chunk;       // stripe tokens per CTA (multiple of seg)
@@ -65,7 +65,7 @@ struct PartialPlan {
   size_t bytes() const;
 };
 // Returns false if the shape is unsupported.
-bool plan_partial(int mla, int P, int page_size, int num_kv_heads, int num_q_heads, int head_dim,
+bool plan_partial(int mla, int P, int interleave, int page_size, int num_kv_heads, int num_q_heads, int head_dim,
                   int num_tokens, int max_kv_len, int dtype_bytes, PartialPlan* plan);
 
 // status: 0 ok, CPATTN_ERR_UNSUPPORTED_SHAPE, or the cudaError via *err

@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_partial_kernel(const Parti
       if (c == 0 && threadIdx.x == 0) report(a.dev_status, CPATTN_DEV_POS_PAST_TABLE);
       L = a.max_kv_len;
     }
-    n_p = (L > p) ? (L - p + P - 1) / P : 0;
+    n_p = stripe_len(L, p, P, a.interleave);
   }
   const int nchunks = n_p > 0 ? (n_p + a.chunk - 1) / a.chunk : 1;
   if (c >= nchunks) return;
@@ -219,14 +219,14 @@ size_t PartialPlan::bytes() const {
   return al(ws_o_floats * 4) + al(ws_lse_floats * 4) + al(ws_cnt_ints * 4);
 }
 
-bool plan_partial(int mla, int P, int page_size, int num_kv_heads, int num_q_heads, int head_dim,
+bool plan_partial(int mla, int P, int interleave, int page_size, int num_kv_heads, int num_q_heads, int head_dim,
                   int num_tokens, int max_kv_len, int dtype_bytes, PartialPlan* plan) {
   (void)head_dim;
   const int ps_l = page_size / P;
   const int G = num_q_heads / num_kv_heads;
   const int Dv = mla ? 512 : head_dim;
   plan->seg = pick_seg(ps_l, mla ? 16 : kSegMax);
-  const int max_stripe = (max_kv_len + P - 1) / P;
+  const int max_stripe = max_stripe_len(max_kv_len, P, interleave);
   int chunk;
   int unit;
   if (mla) {

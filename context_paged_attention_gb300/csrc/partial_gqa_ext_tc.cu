@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
       if (c == 0 && tid == 0) report(a.dev_status, CPATTN_DEV_POS_PAST_TABLE);
       L = a.max_kv_len;
     }
-    const int n_p = (L > p) ? (L - p + P - 1) / P : 0;
+    const int n_p = stripe_len(L, p, P, a.interleave);
     const int nchunks = n_p > 0 ? (n_p + a.chunk - 1) / a.chunk : 1;
     if (c >= nchunks) continue;
     const int k_begin = c * a.chunk;

@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(cons
       if (c == 0 && threadIdx.x == 0) report(a.dev_status, CPATTN_DEV_POS_PAST_TABLE);
       L = a.max_kv_len;
     }
-    n_p = (L > p) ? (L - p + P - 1) / P : 0;
+    n_p = stripe_len(L, p, P, a.interleave);
   }
   const int nchunks = n_p > 0 ? (n_p + a.chunk - 1) / a.chunk : 1;
   if (c >= nchunks) return;

@@ -30,7 +30,8 @@ def _to_torch(a: np.ndarray, device) -> torch.Tensor:
 def desc_for(w) -> B.PoolDesc:
     return B.PoolDesc(P=w.P, page_size=w.page_size, num_pages=w.num_pages, num_kv_heads=w.num_kv_heads,
                       head_dim=w.head_dim, head_dim_v=w.head_dim_v,
-                      dtype=B.DTYPE_BF16 if w.dtype == "bf16" else B.DTYPE_FP32)
+                      dtype=B.DTYPE_BF16 if w.dtype == "bf16" else B.DTYPE_FP32,
+                      interleave=w.interleave)
 
 
 class StripedAttention:

@@ -25,6 +25,7 @@ bfloat16 arrays are carried as uint16 bit patterns.
 from __future__ import annotations
 
 import math
+import dataclasses
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -97,6 +98,7 @@ class Workload:
     k_new: np.ndarray
     v_new: np.ndarray | None
     meta: dict = field(default_factory=dict)
+    interleave: int = 1  # runs of this many consecutive page offsets share a partner
 
     @property
     def sink_page(self) -> int:
@@ -120,6 +122,15 @@ class Workload:
         keys = int(self.kv_len[: self.num_real_rows].astype(np.int64).sum())
         per_key = self.num_kv_heads * (self.head_dim + (0 if self.mla else self.head_dim_v)) * esz
         return keys * per_key
+
+
+def interleaved(w: Workload, interleave: int) -> Workload:
+    """The same step over a pool whose pages move runs of ``interleave``
+    consecutive offsets to one partner; the inputs are unchanged."""
+    if interleave < 1 or w.page_size % (w.P * interleave) != 0:
+        raise ValueError("P * interleave must divide page_size")
+    name = w.name if interleave == 1 else f"{w.name}_I{interleave}"
+    return dataclasses.replace(w, interleave=interleave, name=name)
 
 
 def _values(rng, shape, dtype):

@@ -44,7 +44,12 @@
  *   pool_v: [P][num_pages][num_kv_heads][page_size / P][head_dim_v]
  * Logical position pos of a row whose page table is pages[] lives in page id
  * pages[pos / page_size] at offset off = pos % page_size, i.e. partner
- * off % P, physical slot off / P.  P must divide page_size.  MLA pools keep one
+ * off % P, physical slot off / P.  P must divide page_size.
+ * With an interleave size I > 1 (the vLLM page "[Core] Add explicit layer
+ * parallel plans", FlashAttentionMetadataBuilder: cp_kv_cache_interleave_size)
+ * runs of I consecutive offsets stay together: partner (off / I) % P,
+ * physical slot (off / (I * P)) * I + off % I, and I * P must divide
+ * page_size.  I = 1 is the plain striping.  MLA pools keep one
  * latent row per token (num_kv_heads = 1, head_dim = 576) and no pool_v: the
  * value is the first head_dim_v values of the latent row (pool_v == NULL).
  */
@@ -60,7 +65,7 @@
 extern "C" {
 #endif
 
-#define CPATTN_VERSION 1
+#define CPATTN_VERSION 2
 
 /* exported symbols (the library is built with hidden visibility otherwise) */
 #if defined(__GNUC__)
@@ -72,7 +77,7 @@ extern "C" {
 /* status codes */
 #define CPATTN_OK 0
 #define CPATTN_ERR_INVALID_ARG (-1)               /* null pointer, bad count or size */
-#define CPATTN_ERR_P_NOT_DIVIDING_PAGE_SIZE (-2)  /* P < 1 or page_size % P != 0 */
+#define CPATTN_ERR_P_NOT_DIVIDING_PAGE_SIZE (-2)  /* P < 1, interleave < 0 or page_size % (P * I) != 0 */
 #define CPATTN_ERR_UNSUPPORTED_SHAPE (-3)         /* head dims / group size not compiled */
 #define CPATTN_ERR_MISALIGNED (-4)                /* a device pointer not 16-byte aligned */
 #define CPATTN_ERR_WORKSPACE_TOO_SMALL (-5)       /* workspace_bytes below the requirement */
@@ -97,6 +102,7 @@ typedef struct cpattn_pool_desc {
   int32_t head_dim;     /* key width (MLA: latent + rope, 576) */
   int32_t head_dim_v;   /* value width (== head_dim for GQA; MLA: 512) */
   int32_t dtype;        /* CPATTN_DTYPE_* of pool, q and new K/V */
+  int32_t interleave;   /* interleave size I (0 or 1: plain striping); I * P divides page_size */
 } cpattn_pool_desc;
 
 /* Library version (CPATTN_VERSION) -- lets a binding check it loaded the right .so. */

@@ -10,6 +10,9 @@ reason in the design notes of the repository):
   page size a multiple of P this gives the same partner and physical slot as
   using the global slot number, and a partner page holds ``page_size // P``
   slots.
+* An interleave size I (named by the vLLM page, cp_kv_cache_interleave_size,
+  without a formula) moves runs of I consecutive offsets together: partner
+  ``(off // I) % P``, physical slot ``(off // (I * P)) * I + off % I``.
 * The log-sum-exp is the natural logarithm.
 * Grouped-query heads: query head ``h`` reads KV head ``h // (Hq // Hkv)``.
 * A decode row attends every key of its row, its own (just written) key
@@ -56,7 +59,7 @@ def raw_to_f64(raw: np.ndarray) -> np.ndarray:
 # placement (mstar PR #1124, description: striped context-parallel pool)
 # --------------------------------------------------------------------------
 
-def placement(page_row, pos: int, page_size: int, P: int):
+def placement(page_row, pos: int, page_size: int, P: int, interleave: int = 1):
     """Where logical position ``pos`` of a row lives in a P-way striped pool.
 
     The row's page table ``page_row`` lists logical page ids.  The token sits
@@ -65,34 +68,45 @@ def placement(page_row, pos: int, page_size: int, P: int):
     partners: offset ``off`` belongs to partner ``off % P`` and is that
     partner's physical slot ``off // P`` inside the *same* page id (page ids
     stay logical).  Returns ``(partner, page_id, physical_slot)``.
+
+    With an interleave size I > 1 (vLLM's cp_kv_cache_interleave_size), runs
+    of I consecutive offsets go to one partner: offset ``off`` belongs to
+    partner ``(off // I) % P`` at physical slot ``(off // (I * P)) * I + off % I``
+    (I = 1 is the striping above).  I * P must divide the page size.
     """
-    if P <= 0 or page_size % P != 0:
-        raise ValueError("P must divide page_size")
+    if P <= 0 or interleave <= 0 or page_size % (P * interleave) != 0:
+        raise ValueError("P * interleave must divide page_size")
     page = int(page_row[pos // page_size])
     off = pos % page_size
-    return off % P, page, off // P
+    grp = off // interleave
+    return grp % P, page, (grp // P) * interleave + off % interleave
 
 
-def placement_inverse(page_row, page: int, phys: int, partner: int, page_size: int, P: int) -> int:
+def placement_inverse(page_row, page: int, phys: int, partner: int, page_size: int, P: int,
+                      interleave: int = 1) -> int:
     """Logical position stored at (partner, page id, physical slot); -1 if the
-    page is not in the row's table.  Offset in the page is ``phys * P + partner``."""
+    page is not in the row's table.  Offset in the page is
+    ``((phys // I) * P + partner) * I + phys % I`` (``phys * P + partner`` for I = 1)."""
     hits = np.nonzero(np.asarray(page_row) == page)[0]
     if hits.size == 0:
         return -1
-    return int(hits[0]) * page_size + phys * P + partner
+    off = ((phys // interleave) * P + partner) * interleave + phys % interleave
+    return int(hits[0]) * page_size + off
 
 
-def stripe_positions(length: int, P: int, p: int) -> np.ndarray:
-    """Logical positions of a row of ``length`` keys that partner ``p`` holds.
+def stripe_positions(length: int, P: int, p: int, interleave: int = 1) -> np.ndarray:
+    """Logical positions of a row of ``length`` keys that partner ``p`` holds,
+    in the order of the partner's physical slots.
 
-    Since ``page_size`` is a multiple of P, offset ``off % P == p`` is the same
-    as position ``pos % P == p``.
+    Since ``page_size`` is a multiple of P * I, the partner of an offset is
+    the partner of the position: ``(pos // I) % P``.
     """
-    return np.arange(p, length, P, dtype=np.int64)
+    pos = np.arange(length, dtype=np.int64)
+    return pos[(pos // interleave) % P == p]
 
 
 def expected_pool_image(pool_raw: np.ndarray, page_row, positions, new_raw: np.ndarray,
-                        page_size: int, P: int) -> np.ndarray:
+                        page_size: int, P: int, interleave: int = 1) -> np.ndarray:
     """Pool contents after writing new tokens through the placement.
 
     ``pool_raw`` has the library's physical layout
@@ -105,7 +119,7 @@ def expected_pool_image(pool_raw: np.ndarray, page_row, positions, new_raw: np.n
     for t, pos in enumerate(positions):
         if pos < 0:
             continue
-        p, page, slot = placement(page_row, int(pos), page_size, P)
+        p, page, slot = placement(page_row, int(pos), page_size, P, interleave)
         out[p, page, :, slot, :] = new_raw[t]
     return out
 
@@ -149,9 +163,10 @@ def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float):
     return O, LSE
 
 
-def stripe_partial(q, K, V, scale: float, P: int, p: int):
-    """Partner p's partial: attention restricted to the keys j with j % P == p."""
-    idx = stripe_positions(K.shape[0], P, p)
+def stripe_partial(q, K, V, scale: float, P: int, p: int, interleave: int = 1):
+    """Partner p's partial: attention restricted to the keys partner p holds
+    (j % P == p; with interleave I, (j // I) % P == p)."""
+    idx = stripe_positions(K.shape[0], P, p, interleave)
     return attention(q, K[idx], V[idx], scale)
 
 

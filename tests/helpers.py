@@ -58,10 +58,10 @@ class OracleView:
             L = np.zeros((len(heads),))
             for i, h in enumerate(heads):
                 o, l_ = oracle.stripe_partial(q[i: i + 1], K[:, kh[i]: kh[i] + 1], V[:, kh[i]: kh[i] + 1],
-                                              w.scale, w.P, p)
+                                              w.scale, w.P, p, w.interleave)
                 O[i], L[i] = o[0], l_[0]
             return O, L
-        return oracle.stripe_partial(q, K, V, w.scale, w.P, p)
+        return oracle.stripe_partial(q, K, V, w.scale, w.P, p, w.interleave)
 
     def final(self, rows=None, heads=None):
         w = self.w

@@ -44,7 +44,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.cpattn_version() == 1
+    assert lib.cpattn_version() == 2
     assert lib.cpattn_status_string(0) == b"ok"
     assert b"divide" in lib.cpattn_status_string(-2)
     assert lib.cpattn_status_string(-999) == b"unknown status"
@@ -75,6 +75,22 @@ def test_p_must_divide_page_size(lib, P, ps):
     st = lib.cp_paged_attn_partial(ctypes.byref(d), FAKE, FAKE, FAKE, 32, 1, 1, None, FAKE, 100, FAKE, FAKE, 0.1,
                                    FAKE, FAKE, FAKE, 1 << 30, None, None)
     assert st == -2
+
+
+@pytest.mark.parametrize("I", [3, -1, 8, 5])
+def test_interleave_times_p_must_divide_page_size(lib, I):
+    d = _desc(interleave=I)  # P 4, page 16: I in {0, 1, 2, 4} only
+    st = lib.cp_kv_write(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, FAKE, FAKE, None, None)
+    assert st == -2
+    assert lib.cp_paged_attn_workspace_bytes(ctypes.byref(d), 32, 64, 256) == 0
+    assert lib.cpattn_pool_bytes(ctypes.byref(d), 0) == 0
+
+
+@pytest.mark.parametrize("I", [0, 1, 2, 4])
+def test_interleave_accepted(lib, I):
+    d = _desc(interleave=I)
+    assert lib.cpattn_pool_bytes(ctypes.byref(d), 0) == 4 * 10 * 8 * 4 * 128 * 2
+    assert lib.cp_paged_attn_workspace_bytes(ctypes.byref(d), 32, 64, 8192) > 0
 
 
 def test_invalid_and_misaligned(lib):

@@ -28,3 +28,22 @@ def test_peaks_fallback(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     peak, src = bench.load_peaks()
     assert src == "fallback" and peak == bench.FALLBACK_HBM_GBS
+
+
+def test_clock_summary_window_and_reasons():
+    s = bench.ClockSampler(0)
+    s.samples = [(0.5, 1900.0, 2070.0, set()), (1.0, 2070.0, 2070.0, set()), (1.5, 2050.0, 2070.0, {"sw_power_cap"}),
+                 (2.0, 2070.0, 2070.0, set()), (3.0, 1000.0, 2070.0, {"hw_slowdown"})]
+    out = s.summary(0.9, 2.1)
+    assert out["window_samples"] == 3 and out["sm_mhz"] == 2070.0 and out["sm_max_mhz"] == 2070.0
+    assert out["reasons"] == ["sw_power_cap"]
+    # no sample inside the window: the nearest one stands in, and says so
+    out = s.summary(2.6, 2.7)
+    assert out["window_samples"] == 0 and out["samples"] == 1 and out["reasons"] == ["hw_slowdown"]
+
+
+def test_clock_reason_bits():
+    # NVML clock-event reason masks (nvml.h): SwPowerCap 0x4, HwSlowdown 0x8,
+    # SwThermalSlowdown 0x20, HwThermalSlowdown 0x40
+    assert bench._REASON_BITS == {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                                  "hw_thermal_slowdown": 0x40}

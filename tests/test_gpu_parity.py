@@ -56,6 +56,15 @@ SMALL = {
     "gqa_g1_d64": lambda: W.build_workload("gqa_g1_d64", dtype="bf16", P=2, page_size=8, num_q_heads=4,
                                            num_kv_heads=4, head_dim=64, ctx_len=[3, 400, 1], new_len=[1] * 3,
                                            seed=28),
+    # interleaved pools: runs of I page offsets per partner (I * P = page size is whole-run pages)
+    "tiny_fp32_I4": lambda: W.interleaved(W.tiny_fp32(), 4),
+    "gqa_decode_I2": lambda: W.interleaved(W.gqa_decode(seed=33, batch=5, len_lo=1, len_hi=3000), 2),
+    "gqa_decode_I4": lambda: W.interleaved(W.gqa_decode(seed=34, batch=5, len_lo=1, len_hi=3000,
+                                                        padding_spans=[2, 1]), 4),
+    "mla_decode_I16": lambda: W.interleaved(W.mla_decode(seed=35, batch=3, len_lo=1, len_hi=9000), 16),
+    "mla_decode_I2": lambda: W.interleaved(W.mla_decode(seed=36, batch=3, len_lo=30, len_hi=3000), 2),
+    "mixed_I2": lambda: W.interleaved(W.mixed_step(seed=37, n_decode=3, n_extend=3, dec_ctx=(1, 2000),
+                                                   ext_new=(2, 40), ext_ctx=(0, 1500), token_multiple=64), 2),
     "gqa_P16_ps16": lambda: W.build_workload("gqa_P16_ps16", dtype="bf16", P=16, page_size=16, num_q_heads=16,
                                              num_kv_heads=2, head_dim=128, ctx_len=[5, 40, 2000], new_len=[1] * 3,
                                              seed=29),
@@ -81,7 +90,8 @@ def _expected_pool(w, which_v=False):
         L = int(w.ctx_len[b] + w.new_len[b])
         s0 = int(w.seq_indptr[b])
         rows = w.kv_page_indices[w.kv_page_indptr[b]: w.kv_page_indptr[b + 1]]
-        pool = oracle.expected_pool_image(pool, rows, np.arange(L), src[s0: s0 + L], w.page_size, w.P)
+        pool = oracle.expected_pool_image(pool, rows, np.arange(L), src[s0: s0 + L], w.page_size, w.P,
+                                            w.interleave)
     return pool
 
 

@@ -40,6 +40,51 @@ def pin_placement_golden():
         assert got == (int(p), int(page), int(slot)), (pos, got)
 
 
+def pin_placement_golden_interleaved():
+    page_row = [3, 6]
+    for pos, p, page, slot in _rows("placement_ps8_P2_I2.txt"):
+        got = oracle.placement(page_row, int(pos), 8, 2, 2)
+        assert got == (int(p), int(page), int(slot)), (pos, got)
+
+
+def pin_placement_bijection_interleaved(seed=10):
+    """Bijection and inverse with interleave sizes; I = 1 reproduces the striping."""
+    rng = np.random.default_rng(seed)
+    for ps, P, I in [(16, 2, 2), (16, 4, 4), (64, 4, 2), (64, 8, 8), (32, 1, 4)]:
+        pages = rng.permutation(30)[:4]
+        seen = set()
+        for pos in range(ps * len(pages)):
+            p, page, slot = oracle.placement(pages, pos, ps, P, I)
+            assert 0 <= p < P and 0 <= slot < ps // P
+            assert (p, page, slot) not in seen
+            seen.add((p, page, slot))
+            assert oracle.placement_inverse(pages, page, slot, p, ps, P, I) == pos
+            assert oracle.placement(pages, pos, ps, P, 1) == oracle.placement(pages, pos, ps, P)
+        # each partner's positions, in physical-slot order, are its stripe
+        for p in range(P):
+            sp = oracle.stripe_positions(ps * len(pages), P, p, I)
+            slots = [oracle.placement(pages, int(x), ps, P, I) for x in sp]
+            assert all(s[0] == p for s in slots)
+            order = [(list(pages).index(s[1]), s[2]) for s in slots]
+            assert order == sorted(order)
+
+
+def pin_merge_interleaved_equals_one(seed=11):
+    """Partials over interleaved stripes merge to the P = 1 result too."""
+    rng = np.random.default_rng(seed)
+    Hq, Hkv, D = 4, 2, 8
+    for m in [1, 5, 33, 100]:
+        q = rng.standard_normal((Hq, D))
+        K = rng.standard_normal((m, Hkv, D)) * 2
+        V = rng.standard_normal((m, Hkv, D))
+        O1, L1 = oracle.attention(q, K, V, 0.4)
+        for P, I in [(2, 2), (4, 4), (3, 2)]:
+            parts = [oracle.stripe_partial(q, K, V, 0.4, P, p, I) for p in range(P)]
+            O, L = oracle.merge([o for o, _ in parts], [l for _, l in parts])
+            np.testing.assert_allclose(O, O1, atol=1e-12)
+            np.testing.assert_allclose(L, L1, atol=1e-12)
+
+
 def pin_placement_bijection(seed=0):
     """Brute force over every slot of a row's pages: the map is injective, each
     partner page gets page_size // P slots, and the inverse recovers pos."""
@@ -329,7 +374,8 @@ def pin_bf16_bits():
 
 
 PINS = [
-    pin_placement_golden, pin_placement_bijection, pin_stripe_positions, pin_pool_image_golden,
+    pin_placement_golden, pin_placement_golden_interleaved, pin_placement_bijection,
+    pin_placement_bijection_interleaved, pin_merge_interleaved_equals_one, pin_stripe_positions, pin_pool_image_golden,
     pin_pool_image_sentinel, pin_attention_brute, pin_attention_closed_forms,
     pin_attention_library, pin_merge_golden, pin_merge_p_way_equals_one, pin_merge_any_split,
     pin_merge_empty, pin_own_token_plus_context, pin_expected_step_mixed, pin_mla_kv,
@@ -344,7 +390,7 @@ def test_oracle_pin(pin):
 
 # ---------------------------------------------------------------- planted mistakes
 
-def _blocked_placement(page_row, pos, page_size, P):
+def _blocked_placement(page_row, pos, page_size, P, interleave=1):
     # plausible mistake: contiguous blocks per partner instead of striping
     page = int(page_row[pos // page_size])
     off = pos % page_size
@@ -352,7 +398,7 @@ def _blocked_placement(page_row, pos, page_size, P):
     return off // ps_l, page, off % ps_l
 
 
-def _logical_page_size_placement(page_row, pos, page_size, P):
+def _logical_page_size_placement(page_row, pos, page_size, P, interleave=1):
     # the review's resident-plan bug: offset taken at the logical page size
     page = int(page_row[pos // page_size])
     off = pos % page_size
