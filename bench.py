@@ -58,6 +58,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
     ap.add_argument("--no-clocks", action="store_true", help="do not sample nvidia-smi")
+    ap.add_argument("--path", choices=["fused", "unfused"], default="fused",
+                    help="fused: partials merged inside the partial launch; unfused: partial + lse_merge")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
     return ap.parse_args()
 
 
@@ -90,14 +93,31 @@ def describe(w):
     }
 
 
-def algorithmic_bytes(w):
-    """Bytes each kernel must move at minimum, per launch."""
+def algorithmic_bytes(w, fused=True):
+    """Bytes the partial launch must move at minimum: every visible key once,
+    the queries, and its outputs -- the P partials (unfused), or the merged
+    output and LSE plus the own-token partial it folds in (fused)."""
     esz = 2 if w.dtype == "bf16" else 4
     T, Hq, D, Dv, P = w.num_tokens, w.num_q_heads, w.head_dim, w.head_dim_v, w.P
     kv = w.kv_bytes_read()
     q = T * Hq * D * esz
-    part_out = P * T * Hq * (Dv + 1) * 4
-    return {"partial": kv + q + part_out, "kv": kv}
+    if fused:
+        out = T * Hq * (Dv * esz + 4) + (0 if w.decode else T * Hq * (Dv + 1) * 4)
+    else:
+        out = P * T * Hq * (Dv + 1) * 4
+    return {"partial": kv + q + out, "kv": kv}
+
+
+def launches_per_step(w, fused=True):
+    """Kernels of one step: kv_write, the partial (a second kernel for the
+    multi-token rows of a non-decode step), own_token (non-decode), and
+    lse_merge (unfused only)."""
+    n = 1 + 1
+    if not w.decode:
+        n += 2
+    if not fused:
+        n += 1
+    return n
 
 
 # ---------------------------------------------------------------- environment
@@ -315,6 +335,14 @@ class OraclePool:
         self.pool.map(_oracle_row_task, tasks, chunksize=1)
         return time.perf_counter() - t0
 
+    def run_for(self, tasks, min_s=5.0, max_passes=20):
+        """Repeat the sample until at least min_s of wall time (at most max_passes): (seconds, passes)."""
+        secs, passes = 0.0, 0
+        while passes < max_passes and (passes == 0 or secs < min_s):
+            secs += self.run(tasks)
+            passes += 1
+        return secs, passes
+
     def close(self):
         self.pool.terminate()
 
@@ -348,11 +376,21 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     if att.status() != 0:
         raise RuntimeError(f"device status {att.status()} after filling the pool")
-    alg = algorithmic_bytes(w)
+    fused = args.path == "fused"
+    alg = algorithmic_bytes(w, fused)
     stream = torch.cuda.current_stream()
 
     def step(ev0=None, ev1=None):
         att.write_new()
+        if fused:
+            if not w.decode:
+                att.own()
+            if ev0 is not None:
+                ev0.record(stream)
+            att.fused()
+            if ev1 is not None:
+                ev1.record(stream)
+            return
         if ev0 is not None:
             ev0.record(stream)
         att.partial()
@@ -401,7 +439,24 @@ def run_ours(args, rank, world, local_rank):
     # end-to-end through the public API with host buffers (pinned), copies inside the timed region
     e2e = None
     if not args.no_e2e:
-        e2e = time_e2e(att, w, args, stream)
+        e2e = time_e2e(att, w, args, stream, fused)
+
+    # the same fused step captured once as a CUDA graph and replayed K times
+    graph = None
+    if fused and not args.no_graph:
+        att.capture()
+        for _ in range(args.warmup):
+            att.replay()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        g0.record(stream)
+        for _ in range(K):
+            att.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        gms = g0.elapsed_time(g1) / K
+        graph = {"ms_per_step": round(gms, 5), "value": round(world * alg["kv"] / (gms * 1e-3) / 1e9, 2),
+                 "unit": "GB/s", "note": "informational: the same step replayed from one captured CUDA graph"}
 
     if dist is not None:
         t = torch.tensor([total_ms, e2e["ms_per_step"] if e2e else 0.0], device=f"cuda:{local_rank}")
@@ -436,9 +491,10 @@ def run_ours(args, rank, world, local_rank):
         "peak_source": f"{peak_src} hbm_gbs {peak}",
         "decode_tokens_per_s": round(world * int(w.qo_indptr[w.num_real_rows]) / (ms * 1e-3), 1),
         "roofline": {
-            "kernel": ("cp_paged_attn_partial (MLA)" if w.mla else
-                       "cp_paged_attn_partial (GQA, mma.sync tensor cores, split-KV)" if w.dtype == "bf16" else
-                       "cp_paged_attn_partial (GQA, CUDA cores, split-KV)"),
+            "kernel": ("cp_paged_attn_fused" if fused else "cp_paged_attn_partial") +
+                      (" (MLA, tcgen05)" if w.mla else
+                       " (GQA, mma.sync decode rows + tcgen05 multi-token rows)" if w.dtype == "bf16" else
+                       " (GQA, CUDA cores)"),
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,
@@ -449,10 +505,14 @@ def run_ours(args, rank, world, local_rank):
             "ms_per_launch": round(partial_ms, 5),
             "peak_note": f"of {peak_src}",
         },
-        "gpu_launches": K * (4 if not w.decode else 3),
-        "launch_note": "per step: kv_write, partial, merge kernels (+own_token for mixed steps) and one "
-                       "4-byte-per-slot cudaMemsetAsync of the split tickets",
+        "gpu_launches": K * launches_per_step(w, fused),
+        "launch_note": "per step: " + ("kv_write, the fused partial+merge" if fused else "kv_write, partial, lse_merge") +
+                       (" (+ own_token and the multi-token-row partial kernel for non-decode steps)" if not w.decode
+                        else "") + "; plus one cudaMemsetAsync of the split tickets",
+        "path": args.path,
     }
+    if graph is not None:
+        line["graph"] = graph
     if e2e is not None:
         line["e2e"] = {"value": round(world * kv_bytes / (e2e["ms_per_step"] * 1e-3) / 1e9, 2), "unit": "GB/s",
                        "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
@@ -461,17 +521,17 @@ def run_ours(args, rank, world, local_rank):
         line["clocks"] = sampler.summary(t_wall0, t_wall1)
     if opool is not None:
         tasks, nbytes = oracle_tasks(w, sample_keys(w))
-        secs = opool.run(tasks)
+        secs, passes = opool.run_for(tasks)
         opool.close()
-        line["cpu_baseline"] = {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": opool.cores,
-                                "kind": "oracle",
+        line["cpu_baseline"] = {"value": round(passes * nbytes / secs / 1e9, 4), "unit": "GB/s",
+                                "cores": opool.cores, "kind": "oracle",
                                 "sample": f"float64 oracle over {len(tasks)} of {w.num_real_rows} rows of the same "
-                                          f"step ({nbytes / 1e9:.3f} GB of KV), one spawned single-threaded "
-                                          f"worker per core, {secs:.2f} s"}
+                                          f"step ({nbytes / 1e9:.3f} GB of KV), {passes} pass(es), one spawned "
+                                          f"single-threaded worker per core, {secs:.2f} s"}
     print(json.dumps(line), flush=True)
 
 
-def time_e2e(att, w, args, stream):
+def time_e2e(att, w, args, stream, fused=True):
     """Same step through the public API, inputs copied from pinned host buffers each step."""
     import torch
 
@@ -492,7 +552,10 @@ def time_e2e(att, w, args, stream):
     def e2e_step():
         for n, h in host.items():
             getattr(att, n).copy_(h, non_blocking=True)
-        att.run_step()
+        if fused:
+            att.run_step_fused()
+        else:
+            att.run_step()
         out_h.copy_(att.out, non_blocking=True)
         lse_h.copy_(att.lse, non_blocking=True)
 

@@ -39,6 +39,110 @@ bool is_mla(const cpattn_pool_desc* d) { return d->head_dim_v != d->head_dim; }
 
 }  // namespace
 
+namespace {
+
+// Output side of a partial launch: per-partner partials (o_part / lse_part)
+// or, fused, the merged output.
+struct FusedOut {
+  int fused = 0;
+  const float* extra_o = nullptr;
+  const float* extra_lse = nullptr;
+  void* out = nullptr;
+  int out_bf16 = 0;
+  float* lse_out = nullptr;
+};
+
+size_t partial_workspace(const cpattn_pool_desc* desc, int fused, int32_t num_q_heads, int32_t num_tokens,
+                         int32_t max_kv_len) {
+  if (check_desc(desc) != CPATTN_OK || num_q_heads < 1 || num_tokens < 0 || max_kv_len < 0) return 0;
+  if (num_q_heads % desc->num_kv_heads != 0) return 0;
+  PartialPlan plan;
+  if (!plan_partial(is_mla(desc), fused, desc->P, interleave_of(desc), desc->page_size, desc->num_kv_heads,
+                    num_q_heads, desc->head_dim, num_tokens, max_kv_len, dtype_bytes(desc->dtype), &plan))
+    return 0;
+  return plan.bytes();
+}
+
+int run_partial(const cpattn_pool_desc* desc, const void* pool_k, const void* pool_v, const void* q,
+                int32_t num_q_heads, int32_t num_rows, int32_t num_tokens, const int32_t* qo_indptr,
+                const int32_t* kv_len, int32_t max_kv_len, const int32_t* kv_page_indptr,
+                const int32_t* kv_page_indices, float scale, float* o_part, float* lse_part, const FusedOut& f,
+                void* workspace, size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream) {
+  int st = check_desc(desc);
+  if (st != CPATTN_OK) return st;
+  if (num_q_heads < 1 || num_rows < 0 || num_tokens < 0 || max_kv_len < 0) return CPATTN_ERR_INVALID_ARG;
+  if (num_q_heads % desc->num_kv_heads != 0) return CPATTN_ERR_INVALID_ARG;
+  if (qo_indptr == nullptr && num_tokens != num_rows) return CPATTN_ERR_INVALID_ARG;
+  if (num_tokens == 0) return CPATTN_OK;
+  const bool mla = is_mla(desc);
+  if (pool_k == nullptr || q == nullptr || num_rows < 1 || kv_len == nullptr || kv_page_indptr == nullptr ||
+      kv_page_indices == nullptr)
+    return CPATTN_ERR_INVALID_ARG;
+  if (!f.fused && (o_part == nullptr || lse_part == nullptr)) return CPATTN_ERR_INVALID_ARG;
+  if (!mla && pool_v == nullptr) return CPATTN_ERR_INVALID_ARG;
+  if (mla && pool_v != nullptr && pool_v != pool_k) return CPATTN_ERR_INVALID_ARG;
+  if (!aligned16(pool_k) || !aligned16(pool_v) || !aligned16(q) || !aligned16(o_part) || !aligned16(workspace))
+    return CPATTN_ERR_MISALIGNED;
+  if (mla && desc->dtype != CPATTN_DTYPE_BF16) return CPATTN_ERR_UNSUPPORTED_SHAPE;
+
+  PartialPlan plan;
+  if (!plan_partial(mla, f.fused, desc->P, interleave_of(desc), desc->page_size, desc->num_kv_heads, num_q_heads,
+                    desc->head_dim, num_tokens, max_kv_len, dtype_bytes(desc->dtype), &plan))
+    return CPATTN_ERR_UNSUPPORTED_SHAPE;
+  const size_t need = plan.bytes();
+  if (workspace == nullptr || workspace_bytes < need) return CPATTN_ERR_WORKSPACE_TOO_SMALL;
+
+  auto al = [](size_t x) { return (x + 255) / 256 * 256; };
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  PartialArgs a;
+  a.ws_o = reinterpret_cast<float*>(ws);
+  a.ws_lse = reinterpret_cast<float*>(ws + al(plan.ws_o_floats * 4));
+  a.ws_cnt = reinterpret_cast<int32_t*>(ws + al(plan.ws_o_floats * 4) + al(plan.ws_lse_floats * 4));
+  a.pool_k = pool_k;
+  a.pool_v = mla ? pool_k : pool_v;
+  a.q = q;
+  a.o_part = o_part;
+  a.lse_part = lse_part;
+  a.qo_indptr = qo_indptr;
+  a.kv_len = kv_len;
+  a.page_indptr = kv_page_indptr;
+  a.page_indices = kv_page_indices;
+  a.dev_status = dev_status;
+  a.P = desc->P;
+  a.interleave = interleave_of(desc);
+  a.page_size = desc->page_size;
+  a.ps_l = desc->page_size / desc->P;
+  a.num_pages = desc->num_pages;
+  a.num_kv_heads = desc->num_kv_heads;
+  a.num_q_heads = num_q_heads;
+  a.head_dim = desc->head_dim;
+  a.head_dim_v = desc->head_dim_v;
+  a.num_rows = num_rows;
+  a.num_tokens = num_tokens;
+  a.max_kv_len = max_kv_len;
+  a.seg = plan.seg;
+  a.chunk = plan.chunk;
+  a.max_chunks = plan.max_chunks;
+  a.scale = scale;
+  a.fused = f.fused;
+  a.extra_o = f.extra_o;
+  a.extra_lse = f.extra_lse;
+  a.out = f.out;
+  a.out_bf16 = f.out_bf16;
+  a.lse_out = f.lse_out;
+
+  // tickets start from zero (each call's last arrivals also reset them)
+  if (plan.max_chunks > 1 || f.fused) {
+    if (cudaMemsetAsync(a.ws_cnt, 0, plan.ws_cnt_ints * sizeof(int32_t), stream) != cudaSuccess)
+      return CPATTN_ERR_CUDA;
+  }
+  cudaError_t err = cudaSuccess;
+  if (mla) return launch_mla_partial(a, stream, &err);
+  return launch_gqa_partial(a, desc->dtype == CPATTN_DTYPE_BF16, stream, &err);
+}
+
+}  // namespace
+
 extern "C" {
 
 int cpattn_version(void) { return CPATTN_VERSION; }
@@ -103,13 +207,12 @@ int cp_kv_write(const cpattn_pool_desc* desc, void* pool_k, void* pool_v, const 
 
 size_t cp_paged_attn_workspace_bytes(const cpattn_pool_desc* desc, int32_t num_q_heads, int32_t num_tokens,
                                      int32_t max_kv_len) {
-  if (check_desc(desc) != CPATTN_OK || num_q_heads < 1 || num_tokens < 0 || max_kv_len < 0) return 0;
-  if (num_q_heads % desc->num_kv_heads != 0) return 0;
-  PartialPlan plan;
-  if (!plan_partial(is_mla(desc), desc->P, interleave_of(desc), desc->page_size, desc->num_kv_heads, num_q_heads, desc->head_dim,
-                    num_tokens, max_kv_len, dtype_bytes(desc->dtype), &plan))
-    return 0;
-  return plan.bytes();
+  return partial_workspace(desc, 0, num_q_heads, num_tokens, max_kv_len);
+}
+
+size_t cp_paged_attn_fused_workspace_bytes(const cpattn_pool_desc* desc, int32_t num_q_heads, int32_t num_tokens,
+                                           int32_t max_kv_len) {
+  return partial_workspace(desc, 1, num_q_heads, num_tokens, max_kv_len);
 }
 
 int cp_paged_attn_partial(const cpattn_pool_desc* desc, const void* pool_k, const void* pool_v, const void* q,
@@ -117,71 +220,35 @@ int cp_paged_attn_partial(const cpattn_pool_desc* desc, const void* pool_k, cons
                           const int32_t* kv_len, int32_t max_kv_len, const int32_t* kv_page_indptr,
                           const int32_t* kv_page_indices, float scale, float* o_part, float* lse_part,
                           void* workspace, size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream) {
-  int st = check_desc(desc);
+  FusedOut none;
+  return run_partial(desc, pool_k, pool_v, q, num_q_heads, num_rows, num_tokens, qo_indptr, kv_len, max_kv_len,
+                     kv_page_indptr, kv_page_indices, scale, o_part, lse_part, none, workspace, workspace_bytes,
+                     dev_status, stream);
+}
+
+int cp_paged_attn_fused(const cpattn_pool_desc* desc, const void* pool_k, const void* pool_v, const void* q,
+                        int32_t num_q_heads, int32_t num_rows, int32_t num_tokens, const int32_t* qo_indptr,
+                        const int32_t* kv_len, int32_t max_kv_len, const int32_t* kv_page_indptr,
+                        const int32_t* kv_page_indices, float scale, const float* extra_o, const float* extra_lse,
+                        int32_t out_dtype, void* out, float* lse_out, void* workspace, size_t workspace_bytes,
+                        int32_t* dev_status, cudaStream_t stream) {
+  const int st = check_desc(desc);
   if (st != CPATTN_OK) return st;
-  if (num_q_heads < 1 || num_rows < 0 || num_tokens < 0 || max_kv_len < 0) return CPATTN_ERR_INVALID_ARG;
-  if (num_q_heads % desc->num_kv_heads != 0) return CPATTN_ERR_INVALID_ARG;
-  if (qo_indptr == nullptr && num_tokens != num_rows) return CPATTN_ERR_INVALID_ARG;
-  if (num_tokens == 0) return CPATTN_OK;
-  const bool mla = is_mla(desc);
-  if (pool_k == nullptr || q == nullptr || o_part == nullptr || lse_part == nullptr || num_rows < 1 ||
-      kv_len == nullptr || kv_page_indptr == nullptr || kv_page_indices == nullptr)
-    return CPATTN_ERR_INVALID_ARG;
-  if (!mla && pool_v == nullptr) return CPATTN_ERR_INVALID_ARG;
-  if (mla && pool_v != nullptr && pool_v != pool_k) return CPATTN_ERR_INVALID_ARG;
-  if (!aligned16(pool_k) || !aligned16(pool_v) || !aligned16(q) || !aligned16(o_part) ||
-      !aligned16(workspace))
-    return CPATTN_ERR_MISALIGNED;
-  if (mla && desc->dtype != CPATTN_DTYPE_BF16) return CPATTN_ERR_UNSUPPORTED_SHAPE;
-
-  PartialPlan plan;
-  if (!plan_partial(mla, desc->P, interleave_of(desc), desc->page_size, desc->num_kv_heads, num_q_heads, desc->head_dim, num_tokens,
-                    max_kv_len, dtype_bytes(desc->dtype), &plan))
-    return CPATTN_ERR_UNSUPPORTED_SHAPE;
-  const size_t need = plan.bytes();
-  if (workspace == nullptr || workspace_bytes < need) return CPATTN_ERR_WORKSPACE_TOO_SMALL;
-
-  auto al = [](size_t x) { return (x + 255) / 256 * 256; };
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  PartialArgs a;
-  a.ws_o = reinterpret_cast<float*>(ws);
-  a.ws_lse = reinterpret_cast<float*>(ws + al(plan.ws_o_floats * 4));
-  a.ws_cnt = reinterpret_cast<int32_t*>(ws + al(plan.ws_o_floats * 4) + al(plan.ws_lse_floats * 4));
-  a.pool_k = pool_k;
-  a.pool_v = mla ? pool_k : pool_v;
-  a.q = q;
-  a.o_part = o_part;
-  a.lse_part = lse_part;
-  a.qo_indptr = qo_indptr;
-  a.kv_len = kv_len;
-  a.page_indptr = kv_page_indptr;
-  a.page_indices = kv_page_indices;
-  a.dev_status = dev_status;
-  a.P = desc->P;
-  a.interleave = interleave_of(desc);
-  a.page_size = desc->page_size;
-  a.ps_l = desc->page_size / desc->P;
-  a.num_pages = desc->num_pages;
-  a.num_kv_heads = desc->num_kv_heads;
-  a.num_q_heads = num_q_heads;
-  a.head_dim = desc->head_dim;
-  a.head_dim_v = desc->head_dim_v;
-  a.num_rows = num_rows;
-  a.num_tokens = num_tokens;
-  a.max_kv_len = max_kv_len;
-  a.seg = plan.seg;
-  a.chunk = plan.chunk;
-  a.max_chunks = plan.max_chunks;
-  a.scale = scale;
-
-  // tickets of multi-chunk stripes start from zero
-  if (plan.max_chunks > 1) {
-    if (cudaMemsetAsync(a.ws_cnt, 0, plan.ws_cnt_ints * sizeof(int32_t), stream) != cudaSuccess)
-      return CPATTN_ERR_CUDA;
-  }
-  cudaError_t err = cudaSuccess;
-  if (mla) return launch_mla_partial(a, stream, &err);
-  return launch_gqa_partial(a, desc->dtype == CPATTN_DTYPE_BF16, stream, &err);
+  if (out_dtype != CPATTN_DTYPE_BF16 && out_dtype != CPATTN_DTYPE_FP32) return CPATTN_ERR_INVALID_ARG;
+  if ((extra_o == nullptr) != (extra_lse == nullptr)) return CPATTN_ERR_INVALID_ARG;
+  if (num_tokens > 0 && out == nullptr) return CPATTN_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(extra_o)) return CPATTN_ERR_MISALIGNED;
+  if (out_dtype == CPATTN_DTYPE_BF16 && (desc->head_dim_v % 8) != 0) return CPATTN_ERR_UNSUPPORTED_SHAPE;
+  FusedOut f;
+  f.fused = 1;
+  f.extra_o = extra_o;
+  f.extra_lse = extra_lse;
+  f.out = out;
+  f.out_bf16 = out_dtype == CPATTN_DTYPE_BF16;
+  f.lse_out = lse_out;
+  return run_partial(desc, pool_k, pool_v, q, num_q_heads, num_rows, num_tokens, qo_indptr, kv_len, max_kv_len,
+                     kv_page_indptr, kv_page_indices, scale, nullptr, nullptr, f, workspace, workspace_bytes,
+                     dev_status, stream);
 }
 
 int own_token_attn(const void* q, const void* k_new, const void* v_new, int32_t num_q_heads, int32_t num_kv_heads,

@@ -5,7 +5,24 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace cpattn {
+
+// Raise a kernel's dynamic shared-memory limit once per device (and again
+// only if a launch needs more), so that launches recorded into a CUDA graph
+// make no attribute call.  One `cache` per kernel instantiation.
+template <typename Kernel>
+inline cudaError_t ensure_smem(Kernel kern, size_t bytes, std::atomic<int> (&cache)[64]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::atomic<int>& c = cache[dev & 63];
+  if (c.load(std::memory_order_acquire) >= static_cast<int>(bytes)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess) c.store(static_cast<int>(bytes), std::memory_order_release);
+  return e;
+}
 
 struct WriteArgs {
   void* pool_k;
@@ -56,6 +73,14 @@ struct PartialArgs {
   int chunk;       // stripe tokens per CTA (multiple of seg)
   int max_chunks;  // chunks per (token, partner, kv head), = grid.x
   float scale;
+  // fused calls: partials stay in the workspace and the last CTA of each
+  // (token, KV head) writes the merged output (o_part / lse_part unused)
+  int fused;
+  const float* extra_o;    // [T][Hq][Dv] fp32 partial merged in too, or null
+  const float* extra_lse;  // [T][Hq]
+  void* out;               // [T][Hq][Dv], bf16 when out_bf16 else fp32
+  int out_bf16;
+  float* lse_out;          // [T][Hq] or null
 };
 
 // Geometry of a partial launch (shared by workspace sizing and the launch).
@@ -65,7 +90,7 @@ struct PartialPlan {
   size_t bytes() const;
 };
 // Returns false if the shape is unsupported.
-bool plan_partial(int mla, int P, int interleave, int page_size, int num_kv_heads, int num_q_heads, int head_dim,
+bool plan_partial(int mla, int fused, int P, int interleave, int page_size, int num_kv_heads, int num_q_heads, int head_dim,
                   int num_tokens, int max_kv_len, int dtype_bytes, PartialPlan* plan);
 
 // status: 0 ok, CPATTN_ERR_UNSUPPORTED_SHAPE, or the cudaError via *err

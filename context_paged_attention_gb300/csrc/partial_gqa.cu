@@ -48,8 +48,9 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_partial_kernel(const Parti
     b = t;
   }
   int n_p = 0;
+  int L = 0;  // keys of the row (clamped to max_kv_len)
   if (b >= 0) {
-    int L = __ldg(a.kv_len + b);
+    L = __ldg(a.kv_len + b);
     if (L > a.max_kv_len) {
       if (c == 0 && threadIdx.x == 0) report(a.dev_status, CPATTN_DEV_POS_PAST_TABLE);
       L = a.max_kv_len;
@@ -146,7 +147,7 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_partial_kernel(const Parti
 
   const int64_t orow0 = (static_cast<int64_t>(p) * a.num_tokens + t) * a.num_q_heads + h * G;
   const int64_t slot = (static_cast<int64_t>(t) * P + p) * a.num_kv_heads + h;  // (t, p, h)
-  const bool single = (nchunks == 1);
+  const bool single = !a.fused && nchunks == 1;
   for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
     const int g = idx / D;
     const int d = idx - g * D;
@@ -162,6 +163,10 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_partial_kernel(const Parti
     }
   }
   if (single) return;
+  if (a.fused) {
+    fused_finish(a, t, h, L, G, D, sm);
+    return;
+  }
   if (!take_ticket(a.ws_cnt + slot, nchunks)) return;
   merge_chunks(a, slot, nchunks, G, D, a.o_part + orow0 * D, a.lse_part + orow0);
   if (threadIdx.x == 0) a.ws_cnt[slot] = 0;  // ready for the next call
@@ -175,7 +180,8 @@ static int launch_gqa_t(const PartialArgs& a, cudaStream_t s, cudaError_t* err) 
   const size_t smem = ring > comb ? ring : comb;
   auto kern = gqa_partial_kernel<T, D, G>;
   if (smem > 32 * 1024) {  // the kernel also has a little static shared memory
-    *err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    static std::atomic<int> smem_set[64];
+    *err = ensure_smem(kern, smem, smem_set);
     if (*err != cudaSuccess) return CPATTN_ERR_CUDA;
   }
   dim3 grid(a.max_chunks, a.P * a.num_kv_heads, a.num_tokens);
@@ -219,7 +225,7 @@ size_t PartialPlan::bytes() const {
   return al(ws_o_floats * 4) + al(ws_lse_floats * 4) + al(ws_cnt_ints * 4);
 }
 
-bool plan_partial(int mla, int P, int interleave, int page_size, int num_kv_heads, int num_q_heads, int head_dim,
+bool plan_partial(int mla, int fused, int P, int interleave, int page_size, int num_kv_heads, int num_q_heads, int head_dim,
                   int num_tokens, int max_kv_len, int dtype_bytes, PartialPlan* plan) {
   (void)head_dim;
   const int ps_l = page_size / P;
@@ -249,7 +255,7 @@ bool plan_partial(int mla, int P, int interleave, int page_size, int num_kv_head
   plan->chunk = chunk;
   plan->max_chunks = max_stripe > 0 ? (max_stripe + chunk - 1) / chunk : 1;
   const size_t slots = static_cast<size_t>(num_tokens) * P * num_kv_heads;
-  if (plan->max_chunks > 1) {
+  if (plan->max_chunks > 1 || fused) {
     plan->ws_o_floats = slots * plan->max_chunks * G * Dv;
     plan->ws_lse_floats = slots * plan->max_chunks * G;
   } else {

@@ -79,7 +79,11 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
   const int t_lo = blockIdx.z * QB;
   const int t_real = __ldg(a.qo_indptr + a.num_rows);
   const int t_hi = min(t_lo + QB, t_real);
-  if (c == 0) {
+  if (c == 0 && a.fused) {
+    // padding tokens past the last row: final output 0 / -inf (written once, by partner 0)
+    if (p == 0)
+      for (int tok = max(t_lo, t_real); tok < min(t_lo + QB, a.num_tokens); ++tok) fused_zero_token(a, tok, h, G, D);
+  } else if (c == 0) {
     // padding tokens past the last row: this (partner, KV head)'s 0 / -inf
     for (int tok = max(t_lo, t_real); tok < min(t_lo + QB, a.num_tokens); ++tok) {
       const int64_t orow0 = (static_cast<int64_t>(p) * a.num_tokens + tok) * a.num_q_heads + h * G;
@@ -323,7 +327,7 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
 
     // ---- row `tid`: normalised output and LSE, to o_part or the workspace.
     // Every lane runs the (warp-collective) TMEM loads; only valid rows store.
-    const bool single = (nchunks == 1);
+    const bool single = !a.fused && nchunks == 1;
     {
       const bool empty = (l == 0.f);
       const float inv = empty ? 0.f : 1.f / l;
@@ -362,7 +366,16 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
       if (my_ok) *ldst = lse;
     }
     tc05::fence_before_sync();
-    if (!single) {
+    if (a.fused) {
+      // one ticket per (segment, KV head): every chunk of every partner
+      const int64_t pair0 = static_cast<int64_t>(s0) * a.num_kv_heads + h;
+      int arrivals = 0;
+      for (int pp = 0; pp < P; ++pp) arrivals += chunks_of(a, L, pp);
+      if (take_ticket(a.ws_cnt + pair0, arrivals)) {
+        for (int tok = s0; tok < s1; ++tok) merge_partners(a, tok, h, L, G, D, reinterpret_cast<float*>(sKV));
+        if (tid == 0) a.ws_cnt[pair0] = 0;
+      }
+    } else if (!single) {
       const int64_t slot0 = (static_cast<int64_t>(s0) * P + p) * a.num_kv_heads + h;
       if (take_ticket(a.ws_cnt + slot0, nchunks)) {
         for (int tok = s0; tok < s1; ++tok) {
@@ -388,7 +401,8 @@ static int launch_ext_tc_t(const PartialArgs& a, cudaStream_t s, cudaError_t* er
   const size_t smem = ExtTcLayout<D>::smem_bytes(page_slots);
   if (smem > 227 * 1024) return CPATTN_ERR_UNSUPPORTED_SHAPE;
   auto kern = gqa_partial_ext_tc_kernel<D, G>;
-  *err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  static std::atomic<int> smem_set[64];
+  *err = ensure_smem(kern, smem, smem_set);
   if (*err != cudaSuccess) return CPATTN_ERR_CUDA;
   dim3 grid(a.max_chunks, a.P * a.num_kv_heads, (a.num_tokens + QB - 1) / QB);
   kern<<<grid, 128, smem, s>>>(a);

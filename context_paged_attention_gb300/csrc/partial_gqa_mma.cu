@@ -70,8 +70,9 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(cons
     if (__ldg(a.qo_indptr + b + 1) - t != 1) return;
   }
   int n_p = 0;
+  int L = 0;  // keys of the row (clamped to max_kv_len)
   if (b >= 0) {
-    int L = __ldg(a.kv_len + b);
+    L = __ldg(a.kv_len + b);
     if (L > a.max_kv_len) {
       if (c == 0 && threadIdx.x == 0) report(a.dev_status, CPATTN_DEV_POS_PAST_TABLE);
       L = a.max_kv_len;
@@ -318,7 +319,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(cons
 
   const int64_t orow0 = (static_cast<int64_t>(p) * a.num_tokens + t) * a.num_q_heads + h * G;
   const int64_t slot = (static_cast<int64_t>(t) * P + p) * a.num_kv_heads + h;
-  const bool single = (nchunks == 1);
+  const bool single = !a.fused && nchunks == 1;
   for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
     const int g = idx / D;
     const int d = idx - g * D;
@@ -334,6 +335,10 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(cons
     }
   }
   if (single) return;
+  if (a.fused) {
+    fused_finish(a, t, h, L, G, D, sm);
+    return;
+  }
   if (!take_ticket(a.ws_cnt + slot, nchunks)) return;
   merge_chunks(a, slot, nchunks, G, D, a.o_part + orow0 * D, a.lse_part + orow0);
   if (threadIdx.x == 0) a.ws_cnt[slot] = 0;  // ready for the next call
@@ -346,7 +351,8 @@ static int launch_mma_t(const PartialArgs& a, cudaStream_t s, cudaError_t* err) 
   const size_t pages = (static_cast<size_t>(a.chunk) / a.ps_l + 2) * sizeof(int);
   const size_t smem = (ring > comb ? ring : comb) + pages;
   auto kern = gqa_partial_mma_kernel<D, G>;
-  *err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  static std::atomic<int> smem_set[64];
+  *err = ensure_smem(kern, smem, smem_set);
   if (*err != cudaSuccess) return CPATTN_ERR_CUDA;
   dim3 grid(a.max_chunks, a.P * a.num_kv_heads, a.qo_indptr != nullptr ? a.num_rows : a.num_tokens);
   kern<<<grid, kMmaWarps * 32, smem, s>>>(a);

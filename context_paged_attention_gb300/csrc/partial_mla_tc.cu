@@ -96,8 +96,9 @@ __global__ void __launch_bounds__(128, 1)
     b = t;
   }
   int n_p = 0;
+  int L = 0;  // keys of the row (clamped to max_kv_len)
   if (b >= 0) {
-    int L = __ldg(a.kv_len + b);
+    L = __ldg(a.kv_len + b);
     if (L > a.max_kv_len) {
       if (c == 0 && tid == 0) report(a.dev_status, CPATTN_DEV_POS_PAST_TABLE);
       L = a.max_kv_len;
@@ -113,9 +114,15 @@ __global__ void __launch_bounds__(128, 1)
   const int64_t orow = (static_cast<int64_t>(p) * a.num_tokens + t) * a.num_q_heads + tid;  // head tid
   const int64_t slot = static_cast<int64_t>(t) * P + p;
   if (ntiles == 0) {  // empty stripe (or padding token): 0 / -inf
-    float4* dst = reinterpret_cast<float4*>(a.o_part + orow * kDv);
+    const int64_t wrow = (slot * a.max_chunks + c) * kHeads + tid;
+    float4* dst = reinterpret_cast<float4*>(a.fused ? a.ws_o + wrow * kDv : a.o_part + orow * kDv);
     for (int e = 0; e < kDv / 4; ++e) dst[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-    a.lse_part[orow] = -INFINITY;
+    if (a.fused) {
+      a.ws_lse[wrow] = -INFINITY;
+      fused_finish(a, t, 0, L, kHeads, kDv, reinterpret_cast<float*>(sQ));
+    } else {
+      a.lse_part[orow] = -INFINITY;
+    }
     return;
   }
 
@@ -390,7 +397,7 @@ __global__ void __launch_bounds__(128, 1)
     if (tid == 0) report(a.dev_status, CPATTN_DEV_TC_TIMEOUT);
   } else {
     // ---- normalised partial of head `tid`: to o_part directly, or to the workspace
-    const bool single = (nchunks == 1);
+    const bool single = !a.fused && nchunks == 1;
     const float inv = lr > 0.f ? 1.f / lr : 0.f;
     const float lse = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
     float* dst = single ? a.o_part + orow * kDv : a.ws_o + ((slot * a.max_chunks + c) * kHeads + tid) * kDv;
@@ -419,7 +426,12 @@ __global__ void __launch_bounds__(128, 1)
   tc05::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc05::tmem_dealloc(tbase, 512);
-  if (!alive || nchunks == 1) return;
+  if (!alive) return;
+  if (a.fused) {
+    fused_finish(a, t, 0, L, kHeads, kDv, reinterpret_cast<float*>(sQ));
+    return;
+  }
+  if (nchunks == 1) return;
   if (!take_ticket(a.ws_cnt + slot, nchunks)) return;
   const int64_t orow0 = (static_cast<int64_t>(p) * a.num_tokens + t) * a.num_q_heads;
   merge_chunks(a, slot, nchunks, kHeads, kDv, a.o_part + orow0 * kDv, a.lse_part + orow0);
@@ -486,7 +498,8 @@ int launch_mla_partial(const PartialArgs& a, cudaStream_t s, cudaError_t* err) {
           encode_rows(&map_q, a.q, static_cast<uint64_t>(a.num_tokens) * kHeads, kHeads);
   }
   auto kern = tma ? mla_partial_tc_kernel<true> : mla_partial_tc_kernel<false>;
-  *err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
+  static std::atomic<int> smem_set[2][64];
+  *err = ensure_smem(kern, kSmemBytes, smem_set[tma ? 1 : 0]);
   if (*err != cudaSuccess) return CPATTN_ERR_CUDA;
   dim3 grid(a.max_chunks, a.P, a.num_tokens);
   kern<<<grid, 128, kSmemBytes, s>>>(a, map_kv, map_q, box_rows);

@@ -6,6 +6,14 @@
 // ticket, and the last CTA to arrive merges the chunk partials (exact LSE
 // merge, as lse_merge does for partners) into o_part / lse_part.  No
 // spin-wait: the last arrival does the work, the others just exit.
+//
+// Fused calls (cp_paged_attn_fused) go one level further: every chunk CTA of
+// every partner of a (token, KV head) stores its partial in the workspace and
+// arrives on one ticket for the pair; the last one merges all of them (and an
+// optional precomputed partial, e.g. the own-token one) into the final
+// output.  The exact merge is associative, so this equals merging the
+// partners' partials (mstar PR #1124 "Context / Sequence Parallel 1/5",
+// description: the partials and their LSEs are combined exactly).
 #pragma once
 
 #include "common.cuh"
@@ -57,6 +65,132 @@ __device__ __forceinline__ void merge_chunks(const PartialArgs& a, int64_t slot,
     o_out[static_cast<int64_t>(g) * Dv + d] = empty ? 0.f : acc / wsum;
     if (d == 0) lse_out[g] = empty ? -INFINITY : mx + logf(wsum);
   }
+}
+
+// Chunk CTAs of partner p's stripe of a row of L keys (an empty stripe still
+// has its chunk 0, which stores the empty partial).
+__device__ __forceinline__ int chunks_of(const PartialArgs& a, int L, int p) {
+  const int n = stripe_len(L, p, a.P, a.interleave);
+  return n > 0 ? (n + a.chunk - 1) / a.chunk : 1;
+}
+
+// Arrivals on the ticket of a fused (token, KV head) pair.
+__device__ __forceinline__ int fused_arrivals(const PartialArgs& a, int L) {
+  int n = 0;
+  for (int p = 0; p < a.P; ++p) n += chunks_of(a, L, p);
+  return n;
+}
+
+// Final output of (token t, KV head h) from every partner's chunk partials in
+// the workspace (rows ((t * P + p) * Hkv + h) * max_chunks + c) and the
+// optional extra partial; written as bf16 (round to nearest even) or fp32.
+// Two passes: the per-head max and weight sum (one thread a head), then the
+// weighted sum over float4 groups of the value dims.  Dv % 4 == 0.  scratch:
+// 2 * Hg floats of shared memory the CTA no longer uses.
+__device__ __forceinline__ void merge_partners(const PartialArgs& a, int t, int h, int L, int Hg, int Dv,
+                                               float* scratch) {
+  float* s_mx = scratch;
+  float* s_inv = scratch + Hg;
+  const int64_t hq0 = static_cast<int64_t>(t) * a.num_q_heads + h * Hg;  // first query-head row of the pair
+  const int64_t wt0 = static_cast<int64_t>(t) * a.P * a.num_kv_heads + h;  // (t, p = 0, h)
+  __syncthreads();  // s_mx / s_inv may still be read from a previous token
+  for (int g = threadIdx.x; g < Hg; g += blockDim.x) {
+    float mx = a.extra_lse != nullptr ? __ldg(a.extra_lse + hq0 + g) : -INFINITY;
+    for (int p = 0; p < a.P; ++p) {
+      const int64_t w0 = (wt0 + static_cast<int64_t>(p) * a.num_kv_heads) * a.max_chunks;
+      const int nc = chunks_of(a, L, p);
+      for (int c = 0; c < nc; ++c) mx = fmaxf(mx, __ldcg(a.ws_lse + (w0 + c) * Hg + g));
+    }
+    float wsum = 0.f;
+    if (mx != -INFINITY) {
+      for (int p = 0; p < a.P; ++p) {
+        const int64_t w0 = (wt0 + static_cast<int64_t>(p) * a.num_kv_heads) * a.max_chunks;
+        const int nc = chunks_of(a, L, p);
+        for (int c = 0; c < nc; ++c) {
+          const float lc = __ldcg(a.ws_lse + (w0 + c) * Hg + g);
+          if (lc != -INFINITY) wsum += expf(lc - mx);
+        }
+      }
+      if (a.extra_lse != nullptr) {
+        const float le = __ldg(a.extra_lse + hq0 + g);
+        if (le != -INFINITY) wsum += expf(le - mx);
+      }
+    }
+    const bool empty = (wsum == 0.f);
+    s_mx[g] = mx;
+    s_inv[g] = empty ? 0.f : 1.f / wsum;
+    if (a.lse_out != nullptr) a.lse_out[hq0 + g] = empty ? -INFINITY : mx + logf(wsum);
+  }
+  __syncthreads();
+  const int D4 = Dv / 4;
+  for (int idx = threadIdx.x; idx < Hg * D4; idx += blockDim.x) {
+    const int g = idx / D4;
+    const int d = (idx - g * D4) * 4;
+    const float mx = s_mx[g];
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (mx != -INFINITY) {
+      for (int p = 0; p < a.P; ++p) {
+        const int64_t w0 = (wt0 + static_cast<int64_t>(p) * a.num_kv_heads) * a.max_chunks;
+        const int nc = chunks_of(a, L, p);
+        for (int c = 0; c < nc; ++c) {
+          const int64_t wrow = (w0 + c) * Hg + g;
+          const float lc = __ldcg(a.ws_lse + wrow);
+          if (lc == -INFINITY) continue;  // empty partial: its output row is not read
+          const float w = expf(lc - mx);
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(a.ws_o + wrow * Dv + d));
+          acc.x = fmaf(w, v.x, acc.x);
+          acc.y = fmaf(w, v.y, acc.y);
+          acc.z = fmaf(w, v.z, acc.z);
+          acc.w = fmaf(w, v.w, acc.w);
+        }
+      }
+      if (a.extra_lse != nullptr) {
+        const float le = __ldg(a.extra_lse + hq0 + g);
+        if (le != -INFINITY) {
+          const float w = expf(le - mx);
+          const float4 v = __ldg(reinterpret_cast<const float4*>(a.extra_o + (hq0 + g) * Dv + d));
+          acc.x = fmaf(w, v.x, acc.x);
+          acc.y = fmaf(w, v.y, acc.y);
+          acc.z = fmaf(w, v.z, acc.z);
+          acc.w = fmaf(w, v.w, acc.w);
+        }
+      }
+    }
+    const float inv = s_inv[g];
+    const int64_t oi = (hq0 + g) * Dv + d;
+    if (a.out_bf16) {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + oi) = pk;
+    } else {
+      *reinterpret_cast<float4*>(static_cast<float*>(a.out) + oi) =
+          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    }
+  }
+}
+
+// Fused finish of one CTA (all threads call, after their workspace stores):
+// arrive on the pair's ticket; the last arrival merges and re-arms the ticket.
+__device__ __forceinline__ void fused_finish(const PartialArgs& a, int t, int h, int L, int Hg, int Dv,
+                                             float* scratch) {
+  const int64_t pair = static_cast<int64_t>(t) * a.num_kv_heads + h;
+  if (!take_ticket(a.ws_cnt + pair, fused_arrivals(a, L))) return;
+  merge_partners(a, t, h, L, Hg, Dv, scratch);
+  if (threadIdx.x == 0) a.ws_cnt[pair] = 0;
+}
+
+// Output rows of padding tokens (fused calls): 0 and -inf.
+__device__ __forceinline__ void fused_zero_token(const PartialArgs& a, int t, int h, int Hg, int Dv) {
+  const int64_t hq0 = static_cast<int64_t>(t) * a.num_q_heads + h * Hg;
+  for (int idx = threadIdx.x; idx < Hg * Dv; idx += blockDim.x) {
+    if (a.out_bf16) static_cast<__nv_bfloat16*>(a.out)[hq0 * Dv + idx] = __float2bfloat16_rn(0.f);
+    else static_cast<float*>(a.out)[hq0 * Dv + idx] = 0.f;
+  }
+  if (a.lse_out != nullptr)
+    for (int g = threadIdx.x; g < Hg; g += blockDim.x) a.lse_out[hq0 + g] = -INFINITY;
 }
 
 }  // namespace cpattn

@@ -72,6 +72,8 @@ class StripedAttention:
         self.lse = torch.empty((T, Hq), dtype=torch.float32, device=self.device)
         ws = B.workspace_bytes(self.desc, Hq, T, self.max_kv_len)
         self.workspace = torch.empty((max(ws, 256),), dtype=torch.uint8, device=self.device)
+        self._fused_ws = None
+        self.graph = None
         if fill_history:
             self.fill_history()
 
@@ -115,6 +117,50 @@ class StripedAttention:
         if not self.w.decode:
             self.own(stream)
         self.merge(stream)
+        return self.out, self.lse
+
+    # -- fused path: partials of every partner merged inside the partial launch
+    def fused(self, stream=None, out=None, lse=None):
+        """All partners' partials and their merge in one launch; a non-decode
+        step folds in the own-token partial (computed first by ``own``).
+        ``out``/``lse`` default to this object's output buffers."""
+        if self._fused_ws is None:
+            n = B.fused_workspace_bytes(self.desc, self.w.num_q_heads, self.w.num_tokens, self.max_kv_len)
+            self._fused_ws = torch.empty((max(n, 256),), dtype=torch.uint8, device=self.device)
+        P = self.w.P
+        one_per_row = self.w.decode and self.w.num_tokens == self.w.num_rows
+        extra_o = None if self.w.decode else self.o_parts[P]
+        extra_lse = None if self.w.decode else self.lse_parts[P]
+        B.cp_paged_attn_fused(self.desc, self.pool_k, self.pool_v, self.q, self.kv_len, self.max_kv_len,
+                              self.page_indptr, self.page_indices, self.w.scale,
+                              self.out if out is None else out, self._fused_ws,
+                              lse_out=self.lse if lse is None else lse, extra_o=extra_o, extra_lse=extra_lse,
+                              qo_indptr=None if one_per_row else self.qo_indptr, num_rows=self.w.num_rows,
+                              dev_status=self.dev_status, stream=stream)
+
+    def run_step_fused(self, stream=None, out=None, lse=None):
+        self.write_new(stream)
+        if not self.w.decode:
+            self.own(stream)
+        self.fused(stream, out, lse)
+        return (self.out if out is None else out), (self.lse if lse is None else lse)
+
+    def capture(self):
+        """Record the fused step into a CUDA graph over this object's buffers
+        (a captured bucket: later steps refill the same inputs and replay)."""
+        side = torch.cuda.Stream(device=self.device)
+        side.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(side):
+            self.run_step_fused(side)  # first call outside capture: workspace and kernel attributes
+        torch.cuda.current_stream(self.device).wait_stream(side)
+        torch.cuda.synchronize(self.device)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.run_step_fused(torch.cuda.current_stream(self.device))
+        return self.graph
+
+    def replay(self):
+        self.graph.replay()
         return self.out, self.lse
 
     def status(self) -> int:

@@ -185,6 +185,50 @@ CPATTN_API size_t cp_paged_attn_workspace_bytes(const cpattn_pool_desc* desc, in
                                      int32_t num_tokens, int32_t max_kv_len);
 
 /*
+ * cp_paged_attn_fused -- the partials of all P partners and their exact merge
+ * in one launch: the final attention output of every query token.
+ *
+ * The method computes one partial (output, LSE) per partner over its stripe
+ * and combines them exactly (mstar PR #1124 "Context / Sequence Parallel
+ * 1/5", description: each partner returns its partial with its log-sum-exp,
+ * merged on the device; vLLM "[Core] Add explicit layer parallel plans",
+ * _forward_with_dcp: merge_attn_states of the context and query partials).
+ * Here the merge is fused into the partial kernels: every chunk of every
+ * partner leaves its partial in the workspace and the last CTA of each
+ * (token, KV head) merges them.  The exact merge is associative, so the
+ * result is the one cp_paged_attn_partial followed by lse_merge gives, with
+ * one launch and no [P, T, Hq, Dv] partial tensor round trip.  Pages give the
+ * captured buckets of a step (fixed shapes, replayed as a graph); this call
+ * makes no host synchronisation and no allocation, so it can be captured.
+ *
+ * Arguments as cp_paged_attn_partial, except:
+ *   extra_o, extra_lse  optional precomputed partial merged in too
+ *               ([num_tokens][num_q_heads][head_dim_v] fp32 and
+ *               [num_tokens][num_q_heads] fp32, e.g. own_token_attn's); both
+ *               NULL or both set
+ *   out_dtype   CPATTN_DTYPE_BF16 (round to nearest even) or CPATTN_DTYPE_FP32
+ *   out         [num_tokens][num_q_heads][head_dim_v] of out_dtype
+ *   lse_out     [num_tokens][num_q_heads] fp32 natural-log LSE, or NULL
+ *   workspace   cp_paged_attn_fused_workspace_bytes(...) bytes or more.
+ * Tokens of no row, of padding rows (kv_len 0) and empty stripes merge to
+ * output 0 and LSE -inf unless the extra partial covers them.  max_kv_len may
+ * be a capacity (a captured bucket's largest length): shorter rows only leave
+ * idle CTAs.
+ */
+CPATTN_API int cp_paged_attn_fused(const cpattn_pool_desc* desc, const void* pool_k,
+                                   const void* pool_v, const void* q, int32_t num_q_heads,
+                                   int32_t num_rows, int32_t num_tokens, const int32_t* qo_indptr,
+                                   const int32_t* kv_len, int32_t max_kv_len,
+                                   const int32_t* kv_page_indptr, const int32_t* kv_page_indices,
+                                   float scale, const float* extra_o, const float* extra_lse,
+                                   int32_t out_dtype, void* out, float* lse_out, void* workspace,
+                                   size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream);
+
+/* Workspace bytes cp_paged_attn_fused needs for these sizes (0 on bad args). */
+CPATTN_API size_t cp_paged_attn_fused_workspace_bytes(const cpattn_pool_desc* desc, int32_t num_q_heads,
+                                                      int32_t num_tokens, int32_t max_kv_len);
+
+/*
  * cp_paged_attn_partial_noalloc -- cp_paged_attn_partial for callers that
  * cannot allocate device memory.  The pages have no counterpart: this is a
  * convenience of this library.

@@ -47,3 +47,16 @@ def test_clock_reason_bits():
     # SwThermalSlowdown 0x20, HwThermalSlowdown 0x40
     assert bench._REASON_BITS == {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
                                   "hw_thermal_slowdown": 0x40}
+
+
+def test_launch_counts_and_bytes():
+    from context_paged_attention_gb300 import workloads as W
+
+    dec = W.tiny_fp32()
+    mixed = W.mixed_step(seed=1, n_decode=2, n_extend=2, dec_ctx=(1, 50), ext_new=(2, 5), ext_ctx=(0, 30),
+                         token_multiple=16)
+    assert bench.launches_per_step(dec, True) == 2 and bench.launches_per_step(dec, False) == 3
+    assert bench.launches_per_step(mixed, True) == 4 and bench.launches_per_step(mixed, False) == 5
+    # fused: merged output instead of P partials; the KV bytes are the same
+    f, u = bench.algorithmic_bytes(dec, True), bench.algorithmic_bytes(dec, False)
+    assert f["kv"] == u["kv"] == dec.kv_bytes_read() and f["partial"] < u["partial"]

@@ -8,6 +8,8 @@ rows, padding tokens, the sink page and unwritten pool slots must reach no
 real output.
 """
 
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -152,6 +154,26 @@ def test_step_matches_oracle(small):
     assert np.all(got_o[t0:] == 0) and np.all(got_l[t0:] == -np.inf)
 
 
+def test_fused_step_matches_oracle(small):
+    """Partials merged inside the partial launch: same bar as partial + lse_merge."""
+    w, att = small
+    out = torch.empty_like(att.out)
+    lse = torch.empty_like(att.lse)
+    att.run_step_fused(out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert att.status() == 0
+    O, L = OracleView(w).final()
+    tol_o, tol_l = tolerances(w)
+    got_o = f64(out)
+    got_l = lse.cpu().numpy().astype(np.float64)
+    assert_close(got_o, O, tol_o, "fused output")
+    assert_close_lse(got_l, L, tol_l, "fused LSE")
+    t0 = int(w.qo_indptr[w.num_real_rows])
+    assert np.all(got_o[t0:] == 0) and np.all(got_l[t0:] == -np.inf)
+    # and against the two-launch path on the device (same partials, another merge order)
+    assert_close(got_o, f64(att.out), tol_o, "fused vs partial + merge")
+
+
 def test_own_token_partial(small):
     w, att = small
     if w.decode:
@@ -189,6 +211,34 @@ FULL = {
     "mla_decode": (W.mla_decode, [0, 7, 19, 31]),
     "mixed_step": (W.mixed_step, [0, 17, 47, 48, 55, 63]),
 }
+
+
+@pytest.mark.parametrize("name", ["gqa_decode", "mixed_step", "mla_decode"])
+def test_graph_replay(name):
+    """The fused step captured as a CUDA graph: replays equal the eager call
+    bit for bit, and a replay after refilling the inputs gives the new step."""
+    w = SMALL[name]()
+    att = _att(w)
+    out0, lse0 = att.run_step_fused()
+    ref_o, ref_l = out0.clone(), lse0.clone()
+    att.capture()
+    for _ in range(2):
+        o, l_ = att.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(o.view(torch.int16) if o.dtype == torch.bfloat16 else o,
+                           ref_o.view(torch.int16) if ref_o.dtype == torch.bfloat16 else ref_o)
+        assert torch.equal(l_, ref_l)
+    # new step values in the captured buffers: queries doubled (exact in bf16)
+    att.q.mul_(2)
+    o, l_ = att.replay()
+    torch.cuda.synchronize()
+    assert att.status() == 0
+    q2 = W.f32_to_bf16_bits(2 * oracle.raw_to_f64(w.q).astype(np.float32)) if w.dtype == "bf16" else 2 * w.q
+    w2 = dataclasses.replace(w, q=q2)
+    O, L = OracleView(w2).final()
+    tol_o, tol_l = tolerances(w)
+    assert_close(f64(o), O, tol_o, "replayed output")
+    assert_close_lse(l_.cpu().numpy().astype(np.float64), L, tol_l, "replayed LSE")
 
 
 @pytest.mark.parametrize("name", sorted(FULL))
