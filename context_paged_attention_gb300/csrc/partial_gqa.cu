@@ -254,6 +254,14 @@ bool plan_partial(int mla, int fused, int P, int interleave, int page_size, int 
   chunk = (chunk + unit - 1) / unit * unit;
   plan->chunk = chunk;
   plan->max_chunks = max_stripe > 0 ? (max_stripe + chunk - 1) / chunk : 1;
+  if (fused) {
+    // the last CTA of a (token, KV head) merges in shared memory it no longer
+    // uses; the smallest such region: MLA's Q tile, the bf16 kernels' K/V
+    // rings (multi-token kernel at D 64), the fp32 kernel's ring (page runs
+    // of one row at D 64)
+    const int cap_floats = mla ? 36000 : (dtype_bytes == 2 ? 6000 : 3000);
+    if (merge_scratch_floats(G, P, plan->max_chunks) > cap_floats) return false;
+  }
   const size_t slots = static_cast<size_t>(num_tokens) * P * num_kv_heads;
   if (plan->max_chunks > 1 || fused) {
     plan->ws_o_floats = slots * plan->max_chunks * G * Dv;

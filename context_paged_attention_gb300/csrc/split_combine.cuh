@@ -81,80 +81,96 @@ __device__ __forceinline__ int fused_arrivals(const PartialArgs& a, int L) {
   return n;
 }
 
+// Shared-memory floats merge_partners needs: the Hg x (P * max_chunks + 1)
+// weight table and two per-head values.
+__host__ __device__ __forceinline__ int merge_scratch_floats(int Hg, int P, int max_chunks) {
+  return Hg * (P * max_chunks + 1) + 2 * Hg;
+}
+
 // Final output of (token t, KV head h) from every partner's chunk partials in
 // the workspace (rows ((t * P + p) * Hkv + h) * max_chunks + c) and the
 // optional extra partial; written as bf16 (round to nearest even) or fp32.
-// Two passes: the per-head max and weight sum (one thread a head), then the
-// weighted sum over float4 groups of the value dims.  Dv % 4 == 0.  scratch:
-// 2 * Hg floats of shared memory the CTA no longer uses.
+// Entry e = p * max_chunks + c (e = P * max_chunks: the extra partial).
+//   1. all threads load the entries' LSEs at once into a [Hg][E] table
+//      (-inf for chunks the partner does not have: their rows are stale);
+//   2. one warp per head turns them into weights exp(lse - max) and the
+//      head's LSE with shuffle reductions;
+//   3. each thread sums weight * row over the entries for a float4 group of
+//      value dims, the loads unrolled so several are in flight.
+// scratch: merge_scratch_floats(Hg, P, max_chunks) floats of shared memory
+// the CTA no longer uses.  Dv % 4 == 0.
 __device__ __forceinline__ void merge_partners(const PartialArgs& a, int t, int h, int L, int Hg, int Dv,
                                                float* scratch) {
-  float* s_mx = scratch;
-  float* s_inv = scratch + Hg;
+  const int E = a.P * a.max_chunks + 1;
+  float* wt = scratch;              // [Hg][E]
+  float* s_inv = scratch + Hg * E;  // [Hg]
   const int64_t hq0 = static_cast<int64_t>(t) * a.num_q_heads + h * Hg;  // first query-head row of the pair
   const int64_t wt0 = static_cast<int64_t>(t) * a.P * a.num_kv_heads + h;  // (t, p = 0, h)
-  __syncthreads();  // s_mx / s_inv may still be read from a previous token
-  for (int g = threadIdx.x; g < Hg; g += blockDim.x) {
-    float mx = a.extra_lse != nullptr ? __ldg(a.extra_lse + hq0 + g) : -INFINITY;
-    for (int p = 0; p < a.P; ++p) {
-      const int64_t w0 = (wt0 + static_cast<int64_t>(p) * a.num_kv_heads) * a.max_chunks;
-      const int nc = chunks_of(a, L, p);
-      for (int c = 0; c < nc; ++c) mx = fmaxf(mx, __ldcg(a.ws_lse + (w0 + c) * Hg + g));
+  __syncthreads();  // the scratch may still be read from a previous token
+  for (int idx = threadIdx.x; idx < Hg * E; idx += blockDim.x) {
+    const int g = idx / E;
+    const int e = idx - g * E;
+    float lse = -INFINITY;
+    if (e == E - 1) {
+      if (a.extra_lse != nullptr) lse = __ldg(a.extra_lse + hq0 + g);
+    } else {
+      const int p = e / a.max_chunks;
+      const int c = e - p * a.max_chunks;
+      if (c < chunks_of(a, L, p))
+        lse = __ldcg(a.ws_lse + ((wt0 + static_cast<int64_t>(p) * a.num_kv_heads) * a.max_chunks + c) * Hg + g);
     }
-    float wsum = 0.f;
-    if (mx != -INFINITY) {
-      for (int p = 0; p < a.P; ++p) {
-        const int64_t w0 = (wt0 + static_cast<int64_t>(p) * a.num_kv_heads) * a.max_chunks;
-        const int nc = chunks_of(a, L, p);
-        for (int c = 0; c < nc; ++c) {
-          const float lc = __ldcg(a.ws_lse + (w0 + c) * Hg + g);
-          if (lc != -INFINITY) wsum += expf(lc - mx);
-        }
-      }
-      if (a.extra_lse != nullptr) {
-        const float le = __ldg(a.extra_lse + hq0 + g);
-        if (le != -INFINITY) wsum += expf(le - mx);
-      }
+    wt[idx] = lse;
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  for (int g = warp; g < Hg; g += nwarps) {
+    float mx = -INFINITY;
+    for (int e = lane; e < E; e += 32) mx = fmaxf(mx, wt[g * E + e]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float sum = 0.f;
+    for (int e = lane; e < E; e += 32) {
+      const float l = wt[g * E + e];
+      const float w = (mx == -INFINITY || l == -INFINITY) ? 0.f : expf(l - mx);
+      wt[g * E + e] = w;
+      sum += w;
     }
-    const bool empty = (wsum == 0.f);
-    s_mx[g] = mx;
-    s_inv[g] = empty ? 0.f : 1.f / wsum;
-    if (a.lse_out != nullptr) a.lse_out[hq0 + g] = empty ? -INFINITY : mx + logf(wsum);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane == 0) {
+      const bool empty = (sum == 0.f);
+      s_inv[g] = empty ? 0.f : 1.f / sum;
+      if (a.lse_out != nullptr) a.lse_out[hq0 + g] = empty ? -INFINITY : mx + logf(sum);
+    }
   }
   __syncthreads();
   const int D4 = Dv / 4;
   for (int idx = threadIdx.x; idx < Hg * D4; idx += blockDim.x) {
     const int g = idx / D4;
     const int d = (idx - g * D4) * 4;
-    const float mx = s_mx[g];
+    const float* wg = wt + g * E;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (mx != -INFINITY) {
-      for (int p = 0; p < a.P; ++p) {
-        const int64_t w0 = (wt0 + static_cast<int64_t>(p) * a.num_kv_heads) * a.max_chunks;
-        const int nc = chunks_of(a, L, p);
-        for (int c = 0; c < nc; ++c) {
-          const int64_t wrow = (w0 + c) * Hg + g;
-          const float lc = __ldcg(a.ws_lse + wrow);
-          if (lc == -INFINITY) continue;  // empty partial: its output row is not read
-          const float w = expf(lc - mx);
-          const float4 v = __ldcg(reinterpret_cast<const float4*>(a.ws_o + wrow * Dv + d));
-          acc.x = fmaf(w, v.x, acc.x);
-          acc.y = fmaf(w, v.y, acc.y);
-          acc.z = fmaf(w, v.z, acc.z);
-          acc.w = fmaf(w, v.w, acc.w);
-        }
+#pragma unroll 4
+    for (int e = 0; e < E - 1; ++e) {
+      const float w = wg[e];
+      if (w != 0.f) {  // rows of absent chunks are never read
+        const int p = e / a.max_chunks;
+        const int c = e - p * a.max_chunks;
+        const int64_t wrow = ((wt0 + static_cast<int64_t>(p) * a.num_kv_heads) * a.max_chunks + c) * Hg + g;
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(a.ws_o + wrow * Dv + d));
+        acc.x = fmaf(w, v.x, acc.x);
+        acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z);
+        acc.w = fmaf(w, v.w, acc.w);
       }
-      if (a.extra_lse != nullptr) {
-        const float le = __ldg(a.extra_lse + hq0 + g);
-        if (le != -INFINITY) {
-          const float w = expf(le - mx);
-          const float4 v = __ldg(reinterpret_cast<const float4*>(a.extra_o + (hq0 + g) * Dv + d));
-          acc.x = fmaf(w, v.x, acc.x);
-          acc.y = fmaf(w, v.y, acc.y);
-          acc.z = fmaf(w, v.z, acc.z);
-          acc.w = fmaf(w, v.w, acc.w);
-        }
-      }
+    }
+    if (wg[E - 1] != 0.f) {
+      const float w = wg[E - 1];
+      const float4 v = __ldg(reinterpret_cast<const float4*>(a.extra_o + (hq0 + g) * Dv + d));
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
     }
     const float inv = s_inv[g];
     const int64_t oi = (hq0 + g) * Dv + d;

@@ -16,7 +16,9 @@ Every function follows a passage of the source pages:
 * vLLM "[Core] Add explicit layer parallel plans",
   ``vllm/v1/attention/backends/flash_attn.py``, ``FlashAttentionImpl.
   _forward_with_dcp`` -- context partial over the paged cache, own-token
-  partial with ``cu_seqlens_k = cu_seqlens_q`` (causal), ``merge_attn_states``.
+  partial with ``cu_seqlens_k = cu_seqlens_q`` (causal), ``merge_attn_states``,
+  the per-tensor ``k_descale`` / ``v_descale`` of an FP8 KV cache, and the
+  interleave size ``cp_kv_cache_interleave_size`` (FlashAttentionMetadataBuilder).
 
 Pinning status (what each function is checked against, in
 ``tests/test_oracle_pins.py``): every public function has at least one pin
@@ -26,10 +28,16 @@ No function here is "parity unpinned".
 """
 
 from .reference import (  # noqa: F401
+    E4M3_MAX,
     NEG_INF,
     attention,
     bf16_bits_to_f64,
     causal_own_attention,
+    e4m3_dequantize,
+    e4m3_encode,
+    e4m3_quantize,
+    e4m3_table,
+    e4m3_value,
     expected_pool_image,
     expected_step,
     merge,

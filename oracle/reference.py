@@ -22,6 +22,11 @@ reason in the design notes of the repository):
   first ``D_v`` values are the value.
 * An empty key set gives output 0 and log-sum-exp -inf; merging only such
   partials gives 0 and -inf again (padding merges to zero).
+* FP8 pools (the vLLM page passes per-tensor ``k_descale`` / ``v_descale`` to
+  the attention call): keys and values are stored as OCP FP8 E4M3 codes of
+  ``x / descale`` (quotient in float32, rounded to the nearest E4M3 value,
+  ties to even, magnitudes past 448 saturated to 448) and read back as
+  ``code value * descale``; queries stay in their own type.
 """
 
 from __future__ import annotations
@@ -34,6 +39,70 @@ NEG_INF = -np.inf
 # --------------------------------------------------------------------------
 # value conversion (raw input arrays -> exact float64)
 # --------------------------------------------------------------------------
+
+E4M3_MAX = 448.0
+
+
+def e4m3_value(code: int) -> float:
+    """Value of an FP8 E4M3 code (OCP 8-bit floating point, E4M3 variant):
+    sign bit, 4 exponent bits with bias 7, 3 mantissa bits; exponent 0 holds
+    the subnormals m/8 * 2^-6; no infinities; S.1111.111 is NaN."""
+    code = int(code) & 0xFF
+    sign = -1.0 if code & 0x80 else 1.0
+    e = (code >> 3) & 0xF
+    m = code & 0x7
+    if e == 0xF and m == 0x7:
+        return float("nan")
+    if e == 0:
+        return sign * (m / 8.0) * 2.0 ** -6
+    return sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+def e4m3_table() -> np.ndarray:
+    """float64 values of all 256 codes (NaN for the two NaN codes)."""
+    return np.array([e4m3_value(c) for c in range(256)], dtype=np.float64)
+
+
+def e4m3_encode(x: float) -> int:
+    """Nearest E4M3 code to x: ties go to the even code, magnitudes beyond
+    448 saturate to 448, NaN gives 0x7F.  Written as a search over the 127
+    non-negative finite codes, whose values increase with the code."""
+    x = float(x)
+    if x != x:
+        return 0x7F
+    neg = np.signbit(x)
+    a = min(abs(x), E4M3_MAX)
+    vals = [e4m3_value(c) for c in range(0x7F)]  # codes 0x00 .. 0x7E
+    lo = max(c for c in range(0x7F) if vals[c] <= a)
+    if vals[lo] == a or lo == 0x7E:
+        code = lo
+    else:
+        hi = lo + 1
+        d_lo, d_hi = a - vals[lo], vals[hi] - a
+        code = lo if d_lo < d_hi else hi if d_hi < d_lo else (lo if lo % 2 == 0 else hi)
+    return code | (0x80 if neg else 0)
+
+
+def e4m3_quantize(x_raw: np.ndarray, descale: float) -> np.ndarray:
+    """Codes stored for raw values (bf16 bits or float32) with a per-tensor
+    descale: E4M3 code of float32(x) / float32(descale), the quotient rounded
+    to float32 first."""
+    x = raw_to_f64(x_raw).astype(np.float32)
+    qt = (x / np.float32(descale)).astype(np.float32)
+    flat = qt.reshape(-1)
+    out = np.empty(flat.shape, dtype=np.uint8)
+    memo = {}
+    for i, v in enumerate(flat):
+        key = v.tobytes()
+        if key not in memo:
+            memo[key] = e4m3_encode(float(v))
+        out[i] = memo[key]
+    return out.reshape(qt.shape)
+
+
+def e4m3_dequantize(codes: np.ndarray, descale: float) -> np.ndarray:
+    """float64 values of stored codes: code value * descale."""
+    return e4m3_table()[np.asarray(codes, dtype=np.uint8)] * float(descale)
 
 def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     """Exact float64 value of bfloat16 numbers given as uint16 bit patterns.

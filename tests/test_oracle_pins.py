@@ -373,7 +373,69 @@ def pin_bf16_bits():
     np.testing.assert_array_equal(got, [1.0, -2.0, 0.333984375, 2.0 ** -133])
 
 
+def pin_e4m3_closed_forms():
+    """Values fixed by the E4M3 format: bias 7, 3 mantissa bits, subnormals
+    m/8 * 2^-6, largest finite 1.75 * 2^8 = 448, S.1111.111 = NaN."""
+    v = oracle.e4m3_value
+    assert v(0x7E) == 448.0 and v(0xFE) == -448.0 and oracle.E4M3_MAX == 448.0
+    assert v(0x08) == 2.0 ** -6 and v(0x01) == 2.0 ** -9 and v(0x07) == 7 * 2.0 ** -9
+    assert v(0x38) == 1.0 and v(0x40) == 2.0 and v(0x30) == 0.5 and v(0x3C) == 1.5 and v(0x77) == 240.0
+    assert math.isnan(v(0x7F)) and math.isnan(v(0xFF))
+    assert v(0x00) == 0.0 and v(0x80) == 0.0 and math.copysign(1.0, v(0x80)) == -1.0
+    vals = oracle.e4m3_table()[:0x7F]
+    assert np.all(np.diff(vals) > 0)  # non-negative finite codes increase with their value
+
+
+def pin_e4m3_library():
+    """Decode of all 256 codes and round-to-nearest-even encode of in-range
+    values (random and every midpoint) agree with torch.float8_e4m3fn."""
+    torch = pytest.importorskip("torch")
+    table = oracle.e4m3_table()
+    lib = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(lib), np.isnan(table))
+    fin = ~np.isnan(table)
+    assert np.array_equal(lib[fin], table[fin])
+    rng = np.random.default_rng(12)
+    pos = table[:0x7F]
+    mids = (pos[:-1] + pos[1:]) / 2
+    x = np.concatenate([rng.standard_normal(3000) * 40, rng.standard_normal(500) * 0.01, mids, -mids,
+                        mids * (1 + 2.0 ** -20), mids * (1 - 2.0 ** -20)]).astype(np.float32)
+    x = x[np.abs(x) <= 448]
+    mine = np.array([oracle.e4m3_encode(float(v)) for v in x], dtype=np.uint8)
+    theirs = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(mine, theirs), int((mine != theirs).sum())
+
+
+def pin_e4m3_rounding_and_saturation():
+    enc = oracle.e4m3_encode
+    assert enc(1e9) == 0x7E and enc(-1e9) == 0xFE and enc(449.0) == 0x7E and enc(464.0) == 0x7E
+    assert enc(float("inf")) == 0x7E and enc(float("nan")) == 0x7F
+    assert enc(0.0) == 0x00 and enc(-0.0) == 0x80
+    assert enc(1.0625) == 0x38 and enc(1.1875) == 0x3A  # midpoints: to the even code
+    assert enc(1.0625 * (1 + 1e-6)) == 0x39 and enc(1.1875 * (1 - 1e-6)) == 0x39
+    assert enc(2.0 ** -10) == 0x00 and enc(2.0 ** -10 * 1.001) == 0x01  # half the smallest subnormal
+    assert enc(-3 * 2.0 ** -10) == 0x82  # -1.5 * 2^-9: tie between codes 1 and 2, to 2
+    for c in range(0x7F):
+        assert enc(oracle.e4m3_value(c)) == c and enc(oracle.e4m3_value(c | 0x80)) == (c | 0x80)
+
+
+def pin_e4m3_quantize_error():
+    """Quantise -> dequantise stays within half a unit of the last place: 2^-4
+    relative for normal codes, 2^-10 * descale absolute below 2^-6 * descale."""
+    rng = np.random.default_rng(13)
+    x = W.f32_to_bf16_bits(rng.standard_normal(4000).astype(np.float32) * 3)
+    xf = oracle.raw_to_f64(x)
+    for descale in [0.0123, 0.0625, 1.0]:
+        back = oracle.e4m3_dequantize(oracle.e4m3_quantize(x, descale), descale)
+        inr = np.abs(xf) <= 448 * descale
+        err = np.abs(back - xf)[inr]
+        bound = np.maximum(np.abs(xf[inr]) * 2.0 ** -4, 2.0 ** -10 * descale) * (1 + 1e-6)
+        assert np.all(err <= bound)
+        assert np.all(np.abs(back[~inr]) == 448 * descale)
+
+
 PINS = [
+    pin_e4m3_closed_forms, pin_e4m3_library, pin_e4m3_rounding_and_saturation, pin_e4m3_quantize_error,
     pin_placement_golden, pin_placement_golden_interleaved, pin_placement_bijection,
     pin_placement_bijection_interleaved, pin_merge_interleaved_equals_one, pin_stripe_positions, pin_pool_image_golden,
     pin_pool_image_sentinel, pin_attention_brute, pin_attention_closed_forms,
@@ -451,7 +513,37 @@ def _causal_off_by_one(q_new, k_new, v_new, scale):
 
 _ORIG_ATTENTION = R.attention
 
+def _e4m3_bias_8(code):
+    code = int(code) & 0xFF
+    e, m = (code >> 3) & 0xF, code & 7
+    sign = -1.0 if code & 0x80 else 1.0
+    if e == 0xF and m == 7:
+        return float("nan")
+    return sign * ((m / 8.0) * 2.0 ** -7 if e == 0 else (1 + m / 8.0) * 2.0 ** (e - 8))
+
+
+def _e4m3_ties_away(x):
+    x = float(x)
+    if x != x:
+        return 0x7F
+    a = min(abs(x), 448.0)
+    vals = [R.e4m3_value(c) for c in range(0x7F)]
+    lo = max(c for c in range(0x7F) if vals[c] <= a)
+    code = lo if (vals[lo] == a or lo == 0x7E) else (lo if a - vals[lo] < vals[lo + 1] - a else lo + 1)
+    return code | (0x80 if np.signbit(x) else 0)
+
+
+_ORIG_E4M3_ENCODE = R.e4m3_encode
+
+
+def _e4m3_no_saturation(x):
+    return 0x7F if abs(float(x)) > 448.0 else _ORIG_E4M3_ENCODE(x)
+
+
 MUTATIONS = {
+    "e4m3_exponent_bias_8": ("e4m3_value", _e4m3_bias_8),
+    "e4m3_ties_away_from_zero": ("e4m3_encode", _e4m3_ties_away),
+    "e4m3_no_saturation": ("e4m3_encode", _e4m3_no_saturation),
     "blocked_placement": ("placement", _blocked_placement),
     "logical_page_size_offset": ("placement", _logical_page_size_placement),
     "wrong_gqa_head_map": ("attention", _attention_wrong_head_map),
