@@ -17,6 +17,8 @@ from .build_lib import LIB
 
 DTYPE_BF16 = 0
 DTYPE_FP32 = 1
+DTYPE_FP8_E4M3 = 2  # pools only
+FP8_NAN_CODE = 0x7F
 
 _STATUS_NAMES = {
     0: "CPATTN_OK",
@@ -47,6 +49,9 @@ class PoolDesc(ctypes.Structure):
         ("head_dim_v", ctypes.c_int32),
         ("dtype", ctypes.c_int32),
         ("interleave", ctypes.c_int32),
+        ("kv_dtype", ctypes.c_int32),
+        ("k_descale", ctypes.c_float),
+        ("v_descale", ctypes.c_float),
     ]
 
     @property
@@ -58,7 +63,16 @@ class PoolDesc(ctypes.Structure):
         return (self.P, self.num_pages, self.num_kv_heads, self.page_size // self.P, d)
 
     def torch_dtype(self):
+        """Type of queries, new K/V and outputs."""
         return torch.bfloat16 if self.dtype == DTYPE_BF16 else torch.float32
+
+    @property
+    def fp8(self) -> bool:
+        return self.kv_dtype == DTYPE_FP8_E4M3
+
+    def pool_torch_dtype(self):
+        """Element type of pool_k / pool_v tensors (E4M3 codes as uint8)."""
+        return torch.uint8 if self.fp8 else self.torch_dtype()
 
 
 _lib = None
@@ -103,7 +117,7 @@ def load_library(path: str | None = None):
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
-    if lib.cpattn_version() != 2:
+    if lib.cpattn_version() != 3:
         raise RuntimeError("libcpattn version mismatch")
     if path is None:
         _lib = lib

@@ -21,7 +21,17 @@ int dtype_bytes(int dtype) {
 // Interleave size: 0 in the descriptor means 1 (plain striping).
 int interleave_of(const cpattn_pool_desc* d) { return d->interleave > 1 ? d->interleave : 1; }
 
-// Common descriptor checks.  mla: head_dim != head_dim_v (value = prefix of the key row).
+// Pool element type: kv_dtype 0 means the layer's dtype.
+int kv_dtype_of(const cpattn_pool_desc* d) { return d->kv_dtype == 0 ? d->dtype : d->kv_dtype; }
+
+int kv_bytes(const cpattn_pool_desc* d) {
+  const int kt = kv_dtype_of(d);
+  return kt == CPATTN_DTYPE_FP8_E4M3 ? 1 : dtype_bytes(kt);
+}
+
+bool is_fp8(const cpattn_pool_desc* d) { return kv_dtype_of(d) == CPATTN_DTYPE_FP8_E4M3; }
+
+// Common descriptor checks.
 int check_desc(const cpattn_pool_desc* d) {
   if (d == nullptr) return CPATTN_ERR_INVALID_ARG;
   if (d->P < 1 || d->page_size < 1 || d->interleave < 0 || d->page_size % (d->P * interleave_of(d)) != 0)
@@ -30,7 +40,16 @@ int check_desc(const cpattn_pool_desc* d) {
     return CPATTN_ERR_INVALID_ARG;
   const int eb = dtype_bytes(d->dtype);
   if (eb == 0) return CPATTN_ERR_INVALID_ARG;
+  const int kt = kv_dtype_of(d);
+  if (kt != d->dtype && kt != CPATTN_DTYPE_FP8_E4M3) return CPATTN_ERR_INVALID_ARG;
+  if (kt == CPATTN_DTYPE_FP8_E4M3) {
+    if (d->dtype != CPATTN_DTYPE_BF16) return CPATTN_ERR_UNSUPPORTED_SHAPE;
+    const float ks = d->k_descale, vs = d->v_descale;
+    if (!(ks > 0.f && ks <= 3.0e38f) || !(vs > 0.f && vs <= 3.0e38f)) return CPATTN_ERR_INVALID_ARG;
+  }
+  const int kb = kv_bytes(d);
   if ((d->head_dim * eb) % 16 != 0 || (d->head_dim_v * eb) % 16 != 0) return CPATTN_ERR_UNSUPPORTED_SHAPE;
+  if ((d->head_dim * kb) % 16 != 0 || (d->head_dim_v * kb) % 16 != 0) return CPATTN_ERR_UNSUPPORTED_SHAPE;
   if (d->head_dim_v > d->head_dim) return CPATTN_ERR_UNSUPPORTED_SHAPE;
   return CPATTN_OK;
 }
@@ -84,6 +103,8 @@ int run_partial(const cpattn_pool_desc* desc, const void* pool_k, const void* po
   if (!aligned16(pool_k) || !aligned16(pool_v) || !aligned16(q) || !aligned16(o_part) || !aligned16(workspace))
     return CPATTN_ERR_MISALIGNED;
   if (mla && desc->dtype != CPATTN_DTYPE_BF16) return CPATTN_ERR_UNSUPPORTED_SHAPE;
+  // E4M3 pools: GQA rows of one token (the decode kernel); no MLA, no ragged rows
+  if (is_fp8(desc) && (mla || qo_indptr != nullptr)) return CPATTN_ERR_UNSUPPORTED_SHAPE;
 
   PartialPlan plan;
   if (!plan_partial(mla, f.fused, desc->P, interleave_of(desc), desc->page_size, desc->num_kv_heads, num_q_heads,
@@ -124,6 +145,9 @@ int run_partial(const cpattn_pool_desc* desc, const void* pool_k, const void* po
   a.chunk = plan.chunk;
   a.max_chunks = plan.max_chunks;
   a.scale = scale;
+  a.kv_fp8 = is_fp8(desc);
+  a.k_descale = desc->k_descale;
+  a.v_descale = desc->v_descale;
   a.fused = f.fused;
   a.extra_o = f.extra_o;
   a.extra_lse = f.extra_lse;
@@ -163,7 +187,7 @@ const char* cpattn_status_string(int status) {
 size_t cpattn_pool_bytes(const cpattn_pool_desc* d, int which_v) {
   if (check_desc(d) != CPATTN_OK) return 0;
   const size_t rows = static_cast<size_t>(d->P) * d->num_pages * d->num_kv_heads * (d->page_size / d->P);
-  return rows * (which_v ? d->head_dim_v : d->head_dim) * dtype_bytes(d->dtype);
+  return rows * (which_v ? d->head_dim_v : d->head_dim) * kv_bytes(d);
 }
 
 int cp_kv_write(const cpattn_pool_desc* desc, void* pool_k, void* pool_v, const void* k_new, const void* v_new,
@@ -200,8 +224,14 @@ int cp_kv_write(const cpattn_pool_desc* desc, void* pool_k, void* pool_v, const 
   a.num_kv_heads = desc->num_kv_heads;
   a.num_rows = num_rows;
   a.num_tokens = num_tokens;
-  a.row_bytes_k = desc->head_dim * eb;
-  a.row_bytes_v = mla ? 0 : desc->head_dim_v * eb;
+  const int kb = kv_bytes(desc);
+  a.row_bytes_k = desc->head_dim * kb;
+  a.row_bytes_v = mla ? 0 : desc->head_dim_v * kb;
+  a.src_row_bytes_k = desc->head_dim * eb;
+  a.src_row_bytes_v = mla ? 0 : desc->head_dim_v * eb;
+  a.quant_fp8 = is_fp8(desc);
+  a.k_descale = desc->k_descale;
+  a.v_descale = desc->v_descale;
   return launch_kv_write(a, stream) == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
 }
 

@@ -11,10 +11,38 @@
 // One thread moves one 16-byte chunk of one (token, KV head) row; the chunks of
 // a row are adjacent threads, so both the read of k_new and the write into the
 // pool are coalesced 16-byte accesses.
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 #include "launch.h"
 
 namespace cpattn {
+
+// E4M3 codes of 16 bf16 values (byte offset src_off of src, chunk c) divided
+// by the descale: IEEE float32 quotient, then round to nearest even with
+// saturation to +-448 (cvt ... satfinite).
+__device__ __forceinline__ void store_fp8_chunk(const void* src, int64_t src_off, void* dst, int64_t dst_off, int c,
+                                                float descale) {
+  const uint4* s = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(src) + src_off) + 2 * c;
+  const uint4 w0 = __ldg(s), w1 = __ldg(s + 1);
+  const uint32_t in[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+  uint32_t out[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const uint32_t pair = in[2 * i + j];
+      const float lo = __fdiv_rn(bf16_lo(pair), descale);
+      const float hi = __fdiv_rn(bf16_hi(pair), descale);
+      const uint32_t b0 = __nv_cvt_float_to_fp8(lo, __NV_SATFINITE, __NV_E4M3);
+      const uint32_t b1 = __nv_cvt_float_to_fp8(hi, __NV_SATFINITE, __NV_E4M3);
+      word |= (b0 | (b1 << 8)) << (16 * j);
+    }
+    out[i] = word;
+  }
+  *(reinterpret_cast<uint4*>(static_cast<uint8_t*>(dst) + dst_off) + c) = make_uint4(out[0], out[1], out[2], out[3]);
+}
 
 __global__ void __launch_bounds__(256) kv_write_kernel(const WriteArgs a, int chunks_per_row) {
   const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -54,6 +82,14 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const WriteArgs a, int ch
       ((static_cast<int64_t>(partner) * a.num_pages + page) * a.num_kv_heads + h) * ps_l + slot;
   const int64_t srow = static_cast<int64_t>(t) * a.num_kv_heads + h;
 
+  if (a.quant_fp8) {
+    // 16 codes of the pool row from 16 bf16 values of the new row
+    if (c * 16 < a.row_bytes_k) store_fp8_chunk(a.k_new, srow * a.src_row_bytes_k, a.pool_k, prow * a.row_bytes_k, c,
+                                               a.k_descale);
+    if (a.pool_v != nullptr && c * 16 < a.row_bytes_v)
+      store_fp8_chunk(a.v_new, srow * a.src_row_bytes_v, a.pool_v, prow * a.row_bytes_v, c, a.v_descale);
+    return;
+  }
   if (c * 16 < a.row_bytes_k) {
     const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.k_new) +
                                                       srow * a.row_bytes_k) + c;

@@ -35,7 +35,10 @@ struct WriteArgs {
   const int32_t* page_indices;
   int32_t* dev_status;
   int P, interleave, page_size, num_pages, num_kv_heads, num_rows, num_tokens;
-  int row_bytes_k, row_bytes_v;  // bytes of one head's K / V row
+  int row_bytes_k, row_bytes_v;  // bytes of one head's K / V row in the pool
+  int src_row_bytes_k, src_row_bytes_v;  // ... in k_new / v_new
+  int quant_fp8;                 // pool holds E4M3 codes of x / descale
+  float k_descale, v_descale;
 };
 cudaError_t launch_kv_write(const WriteArgs& a, cudaStream_t s);
 
@@ -73,6 +76,8 @@ struct PartialArgs {
   int chunk;       // stripe tokens per CTA (multiple of seg)
   int max_chunks;  // chunks per (token, partner, kv head), = grid.x
   float scale;
+  int kv_fp8;                 // pool holds E4M3 codes: key = code * k_descale, value = code * v_descale
+  float k_descale, v_descale;
   // fused calls: partials stay in the workspace and the last CTA of each
   // (token, KV head) writes the merged output (o_part / lse_part unused)
   int fused;

@@ -32,19 +32,37 @@ namespace cpattn {
 
 constexpr int kMmaWarps = 4;
 constexpr int kMmaStages = 3;
+constexpr int kMmaStagesF8 = 4;  // E4M3 pools: half the bytes a stage, one stage deeper
 constexpr int kMmaKeys = 16;  // keys per stage
 
-template <int D, int G>
+// Shared memory of one CTA: the warps' cp.async rings of pool rows, then (E4M3
+// pools) each warp's float16 copy of the stage it works on.
+template <int D, bool F8>
+struct MmaSmem {
+  static constexpr int NST = F8 ? kMmaStagesF8 : kMmaStages;
+  static constexpr int SRC_ROWB = F8 ? D : 2 * D;                    // bytes of a pool row
+  static constexpr int RING_STAGE = kMmaKeys * SRC_ROWB;             // K (or V) bytes per ring stage
+  static constexpr int STAGE16 = kMmaKeys * 2 * D;                   // K (or V) bytes of a 16-bit stage
+  static constexpr size_t RING = static_cast<size_t>(kMmaWarps) * NST * RING_STAGE * 2;
+  static constexpr size_t STAGING = F8 ? static_cast<size_t>(kMmaWarps) * STAGE16 * 2 : 0;
+  static constexpr size_t MAIN = RING + STAGING;
+};
+
+template <int D, int G, bool F8>
 __global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(const PartialArgs a) {
+  using SM = MmaSmem<D, F8>;
   constexpr int NW = kMmaWarps;
-  constexpr int NST = kMmaStages;
+  constexpr int NST = SM::NST;
   constexpr int KT = kMmaKeys;
-  constexpr int ROWB = D * 2;
-  constexpr int CH = ROWB / 16;          // 16-byte chunks per row
-  constexpr int STAGE_B = KT * ROWB;     // K (or V) bytes per stage
+  constexpr int ROWB = D * 2;            // bytes of a 16-bit row (the MMA operand layout)
+  constexpr int CH = ROWB / 16;          // 16-byte chunks per 16-bit row
+  constexpr int SRC_ROWB = SM::SRC_ROWB;
+  constexpr int SRC_CH = SRC_ROWB / 16;  // 16-byte chunks per pool row
+  constexpr int RING_STAGE = SM::RING_STAGE;
+  constexpr int STAGE_B = SM::STAGE16;   // K (or V) bytes per 16-bit stage
   constexpr int KSTEPS = D / 16;
   constexpr int NT = D / 8;              // n-tiles of the output
-  constexpr int ITERS = KT * CH / 32;    // cp.async rounds per stage
+  constexpr int ITERS = KT * SRC_CH / 32;  // cp.async rounds per stage
   static_assert(G >= 1 && G <= 16, "group size");
   static_assert(NT % 4 == 0, "head dim");
   extern __shared__ __align__(128) uint8_t smem[];
@@ -100,17 +118,22 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(cons
       qa[s][1] = r1ok ? __ldg(qw + (quad + 8) * (D / 2) + w0) : 0u;
       qa[s][2] = r0ok ? __ldg(qw + quad * (D / 2) + w0 + 4) : 0u;
       qa[s][3] = r1ok ? __ldg(qw + (quad + 8) * (D / 2) + w0 + 4) : 0u;
+      if constexpr (F8) {  // E4M3 pools: the MMAs run on float16 operands
+#pragma unroll
+        for (int r = 0; r < 4; ++r) qa[s][r] = bf16x2_to_f16x2(qa[s][r]);
+      }
     }
   }
 
-  uint8_t* ring = smem + static_cast<size_t>(warp) * NST * STAGE_B * 2;
+  uint8_t* ring = smem + static_cast<size_t>(warp) * NST * RING_STAGE * 2;
+  uint8_t* stage16 = smem + SM::RING + static_cast<size_t>(warp) * STAGE_B * 2;  // E4M3 pools only
   const uint8_t* poolk = static_cast<const uint8_t*>(a.pool_k);
   const uint8_t* poolv = static_cast<const uint8_t*>(a.pool_v);
 
   // The chunk's page ids, checked once and staged in shared memory (-1 = not
   // covered by the row's table or outside the pool), so issuing a stage never
   // waits on a dependent global load.
-  int* spg = reinterpret_cast<int*>(smem + static_cast<size_t>(NW) * NST * STAGE_B * 2);
+  int* spg = reinterpret_cast<int*>(smem + SM::MAIN);
   const int j0 = k_begin / a.ps_l;
   if (nstage > 0) {
     const int j1 = (k_end - 1) / a.ps_l;
@@ -152,18 +175,19 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(cons
       const int64_t myrow = row_of(k0 + (lane & (KT - 1)));  // lanes 0..15 and 16..31 both cover the 16 keys
       const uint32_t vm = __ballot_sync(0xffffffffu, myrow >= 0) & 0xffffu;
       if (lane == 0) s_vmask[warp][i % NST] = vm;
-      uint8_t* sk = ring + (i % NST) * STAGE_B * 2;
-      uint8_t* sv = sk + STAGE_B;
+      uint8_t* sk = ring + (i % NST) * RING_STAGE * 2;
+      uint8_t* sv = sk + RING_STAGE;
 #pragma unroll
       for (int it = 0; it < ITERS; ++it) {
         const int idx = it * 32 + lane;
-        const int key = idx / CH;
-        const int ch = idx - key * CH;
+        const int key = idx / SRC_CH;
+        const int ch = idx - key * SRC_CH;
         const int64_t row = __shfl_sync(0xffffffffu, myrow, key);
-        const int soff = (key * CH + (ch ^ (key & 7))) * 16;
+        // bf16: the MMA layout directly; E4M3: plain rows, converted per stage
+        const int soff = F8 ? idx * 16 : (key * CH + (ch ^ (key & 7))) * 16;
         if (row >= 0) {
-          cp_async16(sk + soff, poolk + row * ROWB + ch * 16);
-          cp_async16(sv + soff, poolv + row * ROWB + ch * 16);
+          cp_async16(sk + soff, poolk + row * SRC_ROWB + ch * 16);
+          cp_async16(sv + soff, poolv + row * SRC_ROWB + ch * 16);
         } else {
           *reinterpret_cast<uint4*>(sv + soff) = make_uint4(0u, 0u, 0u, 0u);  // masked keys: value 0, never NaN
         }
@@ -176,7 +200,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(cons
 #pragma unroll
   for (int u = 0; u < NT; ++u) o[u][0] = o[u][1] = o[u][2] = o[u][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  const float sl = a.scale * kLog2e;
+  const float sl = a.scale * kLog2e * (F8 ? a.k_descale : 1.f);
   const int mrow = lane & 7;
   const int mi = lane >> 3;  // which of the 4 matrices of an ldmatrix.x4 this lane addresses
 
@@ -188,8 +212,32 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(cons
     __syncwarp();
     issue(i + NST - 1);  // refills the stage consumed in step i - 1
 
-    const uint32_t sk = smem_u32(ring + (i % NST) * STAGE_B * 2);
-    const uint32_t sv = sk + STAGE_B;
+    uint32_t sk, sv;
+    if constexpr (F8) {
+      // the stage's E4M3 codes -> float16 rows in the MMA layout (exact)
+      const uint8_t* rk = ring + (i % NST) * RING_STAGE * 2;
+#pragma unroll
+      for (int it = 0; it < 2 * ITERS; ++it) {
+        const int x = it * 32 + lane;          // K chunks, then V chunks
+        const int kv = x / (KT * SRC_CH);
+        const int idx = x - kv * (KT * SRC_CH);
+        const int key = idx / SRC_CH;
+        const int c8 = idx - key * SRC_CH;     // 16 codes: dims 16 c8 .. 16 c8 + 15
+        const uint4 w = *reinterpret_cast<const uint4*>(rk + kv * RING_STAGE + idx * 16);
+        uint8_t* dst = stage16 + kv * STAGE_B + key * CH * 16;
+        const uint4 h0 = make_uint4(e4m3x2_to_f16x2(w.x), e4m3x2_to_f16x2(w.x >> 16), e4m3x2_to_f16x2(w.y),
+                                    e4m3x2_to_f16x2(w.y >> 16));
+        const uint4 h1 = make_uint4(e4m3x2_to_f16x2(w.z), e4m3x2_to_f16x2(w.z >> 16), e4m3x2_to_f16x2(w.w),
+                                    e4m3x2_to_f16x2(w.w >> 16));
+        *reinterpret_cast<uint4*>(dst + ((2 * c8) ^ (key & 7)) * 16) = h0;
+        *reinterpret_cast<uint4*>(dst + ((2 * c8 + 1) ^ (key & 7)) * 16) = h1;
+      }
+      __syncwarp();
+      sk = smem_u32(stage16);
+    } else {
+      sk = smem_u32(ring + (i % NST) * RING_STAGE * 2);
+    }
+    sv = sk + STAGE_B;
     const uint32_t vm = s_vmask[warp][i % NST];
 
     // S = Q K^T for the 16 keys (two n-tiles), even / odd k-steps in two MMA chains
@@ -206,8 +254,8 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(cons
         const int ch = s2 * 2 + mi;  // chunks 2*s2 .. 2*s2+3 cover k-steps s2, s2+1
         uint32_t b0, b1, b2, b3;
         ldsm_x4(sk + (key * CH + (ch ^ (key & 7))) * 16, b0, b1, b2, b3);
-        mma_bf16(s[j], qa[s2], b0, b1);
-        mma_bf16(s_alt[j], qa[s2 + 1], b2, b3);
+        mma16<F8>(s[j], qa[s2], b0, b1);
+        mma16<F8>(s_alt[j], qa[s2 + 1], b2, b3);
       }
     }
     // mask keys past the stripe end (or on a rejected page), scale into the log2 domain
@@ -252,10 +300,10 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(cons
       const float p12 = exp2f(s[1][2] - m1), p13 = exp2f(s[1][3] - m1);
       l0 += (p00 + p01) + (p10 + p11);
       l1 += (p02 + p03) + (p12 + p13);
-      split_bf16(p00, p01, pa[0], pl[0]);
-      split_bf16(p02, p03, pa[1], pl[1]);
-      split_bf16(p10, p11, pa[2], pl[2]);
-      split_bf16(p12, p13, pa[3], pl[3]);
+      split16<F8>(p00, p01, pa[0], pl[0]);
+      split16<F8>(p02, p03, pa[1], pl[1]);
+      split16<F8>(p10, p11, pa[2], pl[2]);
+      split16<F8>(p12, p13, pa[3], pl[3]);
     }
     // O += P V  (V rows via ldmatrix.trans: two n-tiles of 8 dims per instruction)
     {
@@ -270,19 +318,28 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(cons
         }
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          mma_bf16(o[u + 2 * hh], pa, bv[hh][0], bv[hh][1]);
-          mma_bf16(o[u + 2 * hh + 1], pa, bv[hh][2], bv[hh][3]);
+          mma16<F8>(o[u + 2 * hh], pa, bv[hh][0], bv[hh][1]);
+          mma16<F8>(o[u + 2 * hh + 1], pa, bv[hh][2], bv[hh][3]);
         }
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          mma_bf16(o[u + 2 * hh], pl, bv[hh][0], bv[hh][1]);
-          mma_bf16(o[u + 2 * hh + 1], pl, bv[hh][2], bv[hh][3]);
+          mma16<F8>(o[u + 2 * hh], pl, bv[hh][0], bv[hh][1]);
+          mma16<F8>(o[u + 2 * hh + 1], pl, bv[hh][2], bv[hh][3]);
         }
       }
     }
   }
   cp_async_wait<0>();
 
+  if constexpr (F8) {  // value = code * v_descale
+#pragma unroll
+    for (int u = 0; u < NT; ++u) {
+      o[u][0] *= a.v_descale;
+      o[u][1] *= a.v_descale;
+      o[u][2] *= a.v_descale;
+      o[u][3] *= a.v_descale;
+    }
+  }
   // ---- per-warp state -> shared memory (rows < G only), then the cross-warp merge
   l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
   l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
@@ -344,13 +401,13 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(cons
   if (threadIdx.x == 0) a.ws_cnt[slot] = 0;  // ready for the next call
 }
 
-template <int D, int G>
+template <int D, int G, bool F8>
 static int launch_mma_t(const PartialArgs& a, cudaStream_t s, cudaError_t* err) {
-  const size_t ring = static_cast<size_t>(kMmaWarps) * kMmaStages * kMmaKeys * D * 2 * 2;
+  using SM = MmaSmem<D, F8>;
   const size_t comb = (static_cast<size_t>(kMmaWarps) * G * D + 2 * kMmaWarps * G) * sizeof(float);
   const size_t pages = (static_cast<size_t>(a.chunk) / a.ps_l + 2) * sizeof(int);
-  const size_t smem = (ring > comb ? ring : comb) + pages;
-  auto kern = gqa_partial_mma_kernel<D, G>;
+  const size_t smem = (SM::MAIN > comb ? SM::MAIN : comb) + pages;
+  auto kern = gqa_partial_mma_kernel<D, G, F8>;
   static std::atomic<int> smem_set[64];
   *err = ensure_smem(kern, smem, smem_set);
   if (*err != cudaSuccess) return CPATTN_ERR_CUDA;
@@ -360,14 +417,14 @@ static int launch_mma_t(const PartialArgs& a, cudaStream_t s, cudaError_t* err) 
   return *err == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
 }
 
-template <int D>
+template <int D, bool F8>
 static int mma_dispatch_g(const PartialArgs& a, int G, cudaStream_t s, cudaError_t* err) {
   switch (G) {
-    case 1: return launch_mma_t<D, 1>(a, s, err);
-    case 2: return launch_mma_t<D, 2>(a, s, err);
-    case 4: return launch_mma_t<D, 4>(a, s, err);
-    case 8: return launch_mma_t<D, 8>(a, s, err);
-    case 16: return launch_mma_t<D, 16>(a, s, err);
+    case 1: return launch_mma_t<D, 1, F8>(a, s, err);
+    case 2: return launch_mma_t<D, 2, F8>(a, s, err);
+    case 4: return launch_mma_t<D, 4, F8>(a, s, err);
+    case 8: return launch_mma_t<D, 8, F8>(a, s, err);
+    case 16: return launch_mma_t<D, 16, F8>(a, s, err);
     default: return CPATTN_ERR_UNSUPPORTED_SHAPE;
   }
 }
@@ -376,8 +433,15 @@ int launch_gqa_partial_mma(const PartialArgs& a, cudaStream_t s, cudaError_t* er
   const int G = a.num_q_heads / a.num_kv_heads;
   if (a.head_dim != a.head_dim_v) return CPATTN_ERR_UNSUPPORTED_SHAPE;
   int st = CPATTN_ERR_UNSUPPORTED_SHAPE;
-  if (a.head_dim == 128) st = mma_dispatch_g<128>(a, G, s, err);
-  if (a.head_dim == 64) st = mma_dispatch_g<64>(a, G, s, err);
+  if (a.kv_fp8) {
+    // E4M3 pools: rows of one token only (the multi-token kernel reads bf16 pools)
+    if (a.qo_indptr != nullptr) return CPATTN_ERR_UNSUPPORTED_SHAPE;
+    if (a.head_dim == 128) st = mma_dispatch_g<128, true>(a, G, s, err);
+    if (a.head_dim == 64) st = mma_dispatch_g<64, true>(a, G, s, err);
+    return st;
+  }
+  if (a.head_dim == 128) st = mma_dispatch_g<128, false>(a, G, s, err);
+  if (a.head_dim == 64) st = mma_dispatch_g<64, false>(a, G, s, err);
   // ragged rows may hold several tokens: those rows go to the multi-token kernel
   if (st == CPATTN_OK && a.qo_indptr != nullptr) st = launch_gqa_partial_ext(a, s, err);
   return st;

@@ -28,10 +28,12 @@ def _to_torch(a: np.ndarray, device) -> torch.Tensor:
 
 
 def desc_for(w) -> B.PoolDesc:
+    fp8 = getattr(w, "kv_dtype", "same") == "fp8"
     return B.PoolDesc(P=w.P, page_size=w.page_size, num_pages=w.num_pages, num_kv_heads=w.num_kv_heads,
                       head_dim=w.head_dim, head_dim_v=w.head_dim_v,
                       dtype=B.DTYPE_BF16 if w.dtype == "bf16" else B.DTYPE_FP32,
-                      interleave=w.interleave)
+                      interleave=w.interleave, kv_dtype=B.DTYPE_FP8_E4M3 if fp8 else 0,
+                      k_descale=w.k_descale if fp8 else 0.0, v_descale=w.v_descale if fp8 else 0.0)
 
 
 class StripedAttention:
@@ -47,9 +49,10 @@ class StripedAttention:
         self.device = torch.device(device)
         self.desc = desc_for(w)
         dt = self.desc.torch_dtype()
-        nan = float("nan")
-        self.pool_k = torch.full(self.desc.pool_shape(False), nan, dtype=dt, device=self.device)
-        self.pool_v = None if w.mla else torch.full(self.desc.pool_shape(True), nan, dtype=dt, device=self.device)
+        pdt = self.desc.pool_torch_dtype()
+        nan = B.FP8_NAN_CODE if self.desc.fp8 else float("nan")
+        self.pool_k = torch.full(self.desc.pool_shape(False), nan, dtype=pdt, device=self.device)
+        self.pool_v = None if w.mla else torch.full(self.desc.pool_shape(True), nan, dtype=pdt, device=self.device)
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=self.device)
         # step inputs
         self.q = _to_torch(w.q, self.device)

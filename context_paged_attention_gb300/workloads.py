@@ -99,6 +99,9 @@ class Workload:
     v_new: np.ndarray | None
     meta: dict = field(default_factory=dict)
     interleave: int = 1  # runs of this many consecutive page offsets share a partner
+    kv_dtype: str = "same"  # "fp8": the pool holds E4M3 codes of K / k_descale and V / v_descale
+    k_descale: float = 0.0
+    v_descale: float = 0.0
 
     @property
     def sink_page(self) -> int:
@@ -131,6 +134,15 @@ def interleaved(w: Workload, interleave: int) -> Workload:
         raise ValueError("P * interleave must divide page_size")
     name = w.name if interleave == 1 else f"{w.name}_I{interleave}"
     return dataclasses.replace(w, interleave=interleave, name=name)
+
+
+def fp8_pool(w: Workload, k_descale: float, v_descale: float) -> Workload:
+    """The same step with the pool kept as FP8 E4M3 codes and per-tensor
+    descales (inputs unchanged; a bf16 layer only)."""
+    if w.dtype != "bf16" or w.mla:
+        raise ValueError("FP8 pools are for bf16 GQA layers")
+    return dataclasses.replace(w, kv_dtype="fp8", k_descale=float(k_descale), v_descale=float(v_descale),
+                               name=f"{w.name}_fp8")
 
 
 def _values(rng, shape, dtype):
@@ -245,6 +257,12 @@ def gqa_decode(seed=2, batch=64, len_lo=512, len_hi=8192, padding_spans=None):
                           num_kv_heads=8, head_dim=128, ctx_len=L - 1,
                           new_len=np.ones(batch, np.int64), padding_spans=padding_spans,
                           rng=rng, seed=seed)
+
+
+def gqa_decode_fp8(seed=2, batch=64, len_lo=512, len_hi=8192, padding_spans=None):
+    """The GQA decode step over an FP8 E4M3 pool: per-tensor descales about
+    amax / 448 of the N(0, 1) draws (k 0.0123, v 0.0137)."""
+    return fp8_pool(gqa_decode(seed, batch, len_lo, len_hi, padding_spans), 0.0123, 0.0137)
 
 
 def long_gqa_decode(seed=3, batch=8, len_lo=65536, len_hi=131072):

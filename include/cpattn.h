@@ -35,6 +35,13 @@
  * - Device pointers must be 16-byte aligned (CPATTN_ERR_MISALIGNED), and every
  *   row of head_dim values must be a multiple of 16 bytes.
  * - Element types: CPATTN_DTYPE_BF16 (bfloat16 values) or CPATTN_DTYPE_FP32.
+ *   A bf16 layer may keep its pool in CPATTN_DTYPE_FP8_E4M3 (kv_dtype of the
+ *   descriptor): the vLLM page "[Core] Add explicit layer parallel plans"
+ *   passes per-tensor k_descale / v_descale to the attention call of an FP8
+ *   cache.  A stored code is the OCP FP8 E4M3 value nearest to x / descale
+ *   (IEEE float32 quotient, round to nearest even, magnitudes past 448
+ *   saturated to 448); a read key or value is code value * descale.  Queries,
+ *   new K/V and outputs stay bf16; the pool bytes halve.
  *   Partial outputs and log-sum-exps are always fp32.  Log-sum-exps use the
  *   natural logarithm; an empty key set gives output 0 and LSE -inf.
  *
@@ -65,7 +72,7 @@
 extern "C" {
 #endif
 
-#define CPATTN_VERSION 2
+#define CPATTN_VERSION 3
 
 /* exported symbols (the library is built with hidden visibility otherwise) */
 #if defined(__GNUC__)
@@ -93,6 +100,7 @@ extern "C" {
 /* element types */
 #define CPATTN_DTYPE_BF16 0
 #define CPATTN_DTYPE_FP32 1
+#define CPATTN_DTYPE_FP8_E4M3 2 /* pools only (kv_dtype), with a bf16 layer */
 
 typedef struct cpattn_pool_desc {
   int32_t P;            /* partners (stripes); divides page_size */
@@ -103,6 +111,10 @@ typedef struct cpattn_pool_desc {
   int32_t head_dim_v;   /* value width (== head_dim for GQA; MLA: 512) */
   int32_t dtype;        /* CPATTN_DTYPE_* of pool, q and new K/V */
   int32_t interleave;   /* interleave size I (0 or 1: plain striping); I * P divides page_size */
+  int32_t kv_dtype;     /* element type of pool_k / pool_v: 0 or dtype (the same), or
+                           CPATTN_DTYPE_FP8_E4M3 with dtype CPATTN_DTYPE_BF16 */
+  float k_descale;      /* FP8 pools: key = code value * k_descale (finite, > 0) */
+  float v_descale;      /* FP8 pools: value = code value * v_descale (finite, > 0) */
 } cpattn_pool_desc;
 
 /* Library version (CPATTN_VERSION) -- lets a binding check it loaded the right .so. */

@@ -31,6 +31,8 @@ reason in the design notes of the repository):
 
 from __future__ import annotations
 
+import bisect
+
 import numpy as np
 
 NEG_INF = -np.inf
@@ -63,17 +65,18 @@ def e4m3_table() -> np.ndarray:
     return np.array([e4m3_value(c) for c in range(256)], dtype=np.float64)
 
 
-def e4m3_encode(x: float) -> int:
+def e4m3_encode(x: float, _vals=None) -> int:
     """Nearest E4M3 code to x: ties go to the even code, magnitudes beyond
     448 saturate to 448, NaN gives 0x7F.  Written as a search over the 127
-    non-negative finite codes, whose values increase with the code."""
+    non-negative finite codes, whose values increase with the code
+    (``_vals``: their values, when the caller already has them)."""
     x = float(x)
     if x != x:
         return 0x7F
     neg = np.signbit(x)
     a = min(abs(x), E4M3_MAX)
-    vals = [e4m3_value(c) for c in range(0x7F)]  # codes 0x00 .. 0x7E
-    lo = max(c for c in range(0x7F) if vals[c] <= a)
+    vals = _vals if _vals is not None else [e4m3_value(c) for c in range(0x7F)]  # codes 0x00 .. 0x7E
+    lo = bisect.bisect_right(vals, a) - 1  # largest code whose value is <= a
     if vals[lo] == a or lo == 0x7E:
         code = lo
     else:
@@ -89,15 +92,11 @@ def e4m3_quantize(x_raw: np.ndarray, descale: float) -> np.ndarray:
     to float32 first."""
     x = raw_to_f64(x_raw).astype(np.float32)
     qt = (x / np.float32(descale)).astype(np.float32)
-    flat = qt.reshape(-1)
-    out = np.empty(flat.shape, dtype=np.uint8)
-    memo = {}
-    for i, v in enumerate(flat):
-        key = v.tobytes()
-        if key not in memo:
-            memo[key] = e4m3_encode(float(v))
-        out[i] = memo[key]
-    return out.reshape(qt.shape)
+    vals = [e4m3_value(c) for c in range(0x7F)]
+    # each distinct quotient is encoded once (bf16 inputs have few distinct values)
+    uniq, inv = np.unique(qt.reshape(-1), return_inverse=True)
+    codes = np.array([e4m3_encode(float(v), vals) for v in uniq], dtype=np.uint8)
+    return codes[inv].reshape(qt.shape)
 
 
 def e4m3_dequantize(codes: np.ndarray, descale: float) -> np.ndarray:

@@ -28,6 +28,10 @@ class OracleView:
     def row_kv(self, b, m):
         w = self.w
         s0 = int(w.seq_indptr[b])
+        if w.kv_dtype == "fp8":  # the pool holds E4M3 codes: read back code * descale
+            K = oracle.e4m3_dequantize(oracle.e4m3_quantize(w.k_seq[s0: s0 + m], w.k_descale), w.k_descale)
+            V = oracle.e4m3_dequantize(oracle.e4m3_quantize(w.v_seq[s0: s0 + m], w.v_descale), w.v_descale)
+            return K, V
         K = oracle.raw_to_f64(w.k_seq[s0: s0 + m])
         if w.mla:
             return oracle.mla_kv(K, w.head_dim_v)
@@ -65,8 +69,12 @@ class OracleView:
 
     def final(self, rows=None, heads=None):
         w = self.w
-        k = oracle.raw_to_f64(w.k_seq)
-        v = oracle.mla_kv(k, w.head_dim_v)[1] if w.mla else oracle.raw_to_f64(w.v_seq)
+        if w.kv_dtype == "fp8":  # keys and values as the pool returns them
+            k = oracle.e4m3_dequantize(oracle.e4m3_quantize(w.k_seq, w.k_descale), w.k_descale)
+            v = oracle.e4m3_dequantize(oracle.e4m3_quantize(w.v_seq, w.v_descale), w.v_descale)
+        else:
+            k = oracle.raw_to_f64(w.k_seq)
+            v = oracle.mla_kv(k, w.head_dim_v)[1] if w.mla else oracle.raw_to_f64(w.v_seq)
         return oracle.expected_step(self.q, k, v, w.seq_indptr, w.ctx_len, w.new_len, w.qo_indptr,
                                     w.num_real_rows, w.num_tokens, w.scale, rows=rows, heads=heads)
 

@@ -44,7 +44,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.cpattn_version() == 2
+    assert lib.cpattn_version() == 3
     assert lib.cpattn_status_string(0) == b"ok"
     assert b"divide" in lib.cpattn_status_string(-2)
     assert lib.cpattn_status_string(-999) == b"unknown status"
@@ -122,6 +122,28 @@ def test_invalid_and_misaligned(lib):
     # own-token: real rows beyond the bucket
     assert lib.own_token_attn(FAKE, FAKE, FAKE, 32, 8, 128, 128, 0, FAKE, 4, 5, 16, 8, 0.1, FAKE, FAKE,
                               None) == -1
+
+
+def test_fp8_descriptor_checks(lib):
+    fp8 = dict(kv_dtype=2, k_descale=0.0123, v_descale=0.0137)
+    d = _desc(**fp8)
+    assert lib.cpattn_pool_bytes(ctypes.byref(d), 0) == 4 * 10 * 8 * 4 * 128  # one byte a code
+    assert lib.cp_paged_attn_workspace_bytes(ctypes.byref(d), 32, 64, 8192) > 0
+    # FP8 pools belong to bf16 layers; descales must be finite and positive
+    assert lib.cpattn_pool_bytes(ctypes.byref(_desc(dtype=B.DTYPE_FP32, **fp8)), 0) == 0
+    for ks in [0.0, -1.0, float("nan"), float("inf")]:
+        bad = _desc(kv_dtype=2, k_descale=ks, v_descale=0.5)
+        assert lib.cp_kv_write(ctypes.byref(bad), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, FAKE, FAKE, None,
+                               None) == -1
+    # an unknown pool type, and a pool type other than the layer's that is not FP8
+    assert lib.cpattn_pool_bytes(ctypes.byref(_desc(kv_dtype=7)), 0) == 0
+    assert lib.cpattn_pool_bytes(ctypes.byref(_desc(kv_dtype=1)), 0) == 0
+    # kv_dtype 0 and kv_dtype == dtype mean the same pool
+    assert lib.cpattn_pool_bytes(ctypes.byref(_desc(kv_dtype=0)), 0) == \
+        lib.cpattn_pool_bytes(ctypes.byref(_desc(kv_dtype=B.DTYPE_BF16)), 0)
+    # E4M3 pools with ragged multi-token rows are not supported (refused before any launch)
+    assert lib.cp_paged_attn_partial(ctypes.byref(d), FAKE, FAKE, FAKE, 32, 2, 3, FAKE, FAKE, 100, FAKE, FAKE, 0.1,
+                                     FAKE, FAKE, FAKE, 1 << 30, None, None) == -3
 
 
 def test_fused_argument_checks(lib):

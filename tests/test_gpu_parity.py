@@ -67,6 +67,14 @@ SMALL = {
     "mla_decode_I2": lambda: W.interleaved(W.mla_decode(seed=36, batch=3, len_lo=30, len_hi=3000), 2),
     "mixed_I2": lambda: W.interleaved(W.mixed_step(seed=37, n_decode=3, n_extend=3, dec_ctx=(1, 2000),
                                                    ext_new=(2, 40), ext_ctx=(0, 1500), token_multiple=64), 2),
+    # FP8 E4M3 pools with per-tensor descales (decode rows)
+    "gqa_decode_fp8": lambda: W.gqa_decode_fp8(seed=38, batch=6, len_lo=20, len_hi=5000),
+    "gqa_decode_fp8_I2_pad": lambda: W.interleaved(W.gqa_decode_fp8(seed=39, batch=5, len_lo=1, len_hi=2000,
+                                                                    padding_spans=[1, 1]), 2),
+    "gqa_fp8_g1_d64": lambda: W.fp8_pool(W.build_workload("gqa_fp8_g1_d64", dtype="bf16", P=2, page_size=8,
+                                                          num_q_heads=4, num_kv_heads=4, head_dim=64,
+                                                          ctx_len=[3, 400, 1], new_len=[1] * 3, seed=40),
+                                         0.0091, 0.0213),
     "gqa_P16_ps16": lambda: W.build_workload("gqa_P16_ps16", dtype="bf16", P=16, page_size=16, num_q_heads=16,
                                              num_kv_heads=2, head_dim=128, ctx_len=[5, 40, 2000], new_len=[1] * 3,
                                              seed=29),
@@ -84,16 +92,23 @@ def small(request):
 
 def _expected_pool(w, which_v=False):
     """Oracle image: NaN pool, every row's context and the step's new tokens written by the placement."""
-    dt_nan = W.nan_pool((1,), w.dtype)[0]
     shape = W.pool_v_shape(w) if which_v else W.pool_shape(w)
-    pool = np.full(shape, dt_nan, dtype=np.uint16 if w.dtype == "bf16" else np.float32)
+    fp8 = w.kv_dtype == "fp8"
+    if fp8:
+        pool = np.full(shape, 0x7F, dtype=np.uint8)  # the E4M3 NaN code
+    else:
+        dt_nan = W.nan_pool((1,), w.dtype)[0]
+        pool = np.full(shape, dt_nan, dtype=np.uint16 if w.dtype == "bf16" else np.float32)
     src = w.v_seq if which_v else w.k_seq
+    descale = w.v_descale if which_v else w.k_descale
     for b in range(w.num_real_rows):
         L = int(w.ctx_len[b] + w.new_len[b])
         s0 = int(w.seq_indptr[b])
         rows = w.kv_page_indices[w.kv_page_indptr[b]: w.kv_page_indptr[b + 1]]
-        pool = oracle.expected_pool_image(pool, rows, np.arange(L), src[s0: s0 + L], w.page_size, w.P,
-                                            w.interleave)
+        vals = src[s0: s0 + L]
+        if fp8:
+            vals = oracle.e4m3_quantize(vals, descale)
+        pool = oracle.expected_pool_image(pool, rows, np.arange(L), vals, w.page_size, w.P, w.interleave)
     return pool
 
 
@@ -207,6 +222,7 @@ def test_repeat_step_is_stable(small):
 
 FULL = {
     "gqa_decode": (W.gqa_decode, None),
+    "gqa_decode_fp8": (W.gqa_decode_fp8, [0, 9, 63]),
     "long_gqa_decode": (W.long_gqa_decode, [0, 5]),
     "mla_decode": (W.mla_decode, [0, 7, 19, 31]),
     "mixed_step": (W.mixed_step, [0, 17, 47, 48, 55, 63]),

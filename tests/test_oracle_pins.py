@@ -522,7 +522,7 @@ def _e4m3_bias_8(code):
     return sign * ((m / 8.0) * 2.0 ** -7 if e == 0 else (1 + m / 8.0) * 2.0 ** (e - 8))
 
 
-def _e4m3_ties_away(x):
+def _e4m3_ties_away(x, _vals=None):
     x = float(x)
     if x != x:
         return 0x7F
@@ -536,8 +536,8 @@ def _e4m3_ties_away(x):
 _ORIG_E4M3_ENCODE = R.e4m3_encode
 
 
-def _e4m3_no_saturation(x):
-    return 0x7F if abs(float(x)) > 448.0 else _ORIG_E4M3_ENCODE(x)
+def _e4m3_no_saturation(x, _vals=None):
+    return 0x7F if abs(float(x)) > 448.0 else _ORIG_E4M3_ENCODE(x, _vals)
 
 
 MUTATIONS = {
