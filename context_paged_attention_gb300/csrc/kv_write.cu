@@ -11,16 +11,30 @@
 // One thread moves one 16-byte chunk of one (token, KV head) row; the chunks of
 // a row are adjacent threads, so both the read of k_new and the write into the
 // pool are coalesced 16-byte accesses.
-#include <cuda_fp8.h>
-
 #include "common.cuh"
 #include "launch.h"
 
 namespace cpattn {
 
+// E4M3 code of a float32 value, rounded once to the nearest E4M3 value (ties
+// to the even code), magnitudes of 448 and more (and infinities) saturated to
+// 448, NaN to 0x7F.  Written from the format: normal codes are the float32
+// exponent rebiased from 127 to 7 and the mantissa rounded to 3 bits;
+// below 2^-6 the codes are the multiples m * 2^-9 (m = 0..8).
+__device__ __forceinline__ uint32_t e4m3_rn_satfinite(float x) {
+  const uint32_t u = __float_as_uint(x);
+  const uint32_t sign = (u >> 24) & 0x80u;
+  const float ax = fabsf(x);
+  if (ax != ax) return 0x7Fu;
+  if (ax >= 448.f) return sign | 0x7Eu;
+  if (ax < 0.015625f) return sign | static_cast<uint32_t>(__float2int_rn(ax * 512.f));  // exact scaling
+  const uint32_t bits = u & 0x7fffffffu;
+  const uint32_t r = (bits + 0x7ffffu + ((bits >> 20) & 1u)) >> 20;  // exponent | 3 mantissa bits, to nearest even
+  return sign | (r - ((127u - 7u) << 3));
+}
+
 // E4M3 codes of 16 bf16 values (byte offset src_off of src, chunk c) divided
-// by the descale: IEEE float32 quotient, then round to nearest even with
-// saturation to +-448 (cvt ... satfinite).
+// by the descale: IEEE float32 quotient, then e4m3_rn_satfinite.
 __device__ __forceinline__ void store_fp8_chunk(const void* src, int64_t src_off, void* dst, int64_t dst_off, int c,
                                                 float descale) {
   const uint4* s = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(src) + src_off) + 2 * c;
@@ -35,8 +49,8 @@ __device__ __forceinline__ void store_fp8_chunk(const void* src, int64_t src_off
       const uint32_t pair = in[2 * i + j];
       const float lo = __fdiv_rn(bf16_lo(pair), descale);
       const float hi = __fdiv_rn(bf16_hi(pair), descale);
-      const uint32_t b0 = __nv_cvt_float_to_fp8(lo, __NV_SATFINITE, __NV_E4M3);
-      const uint32_t b1 = __nv_cvt_float_to_fp8(hi, __NV_SATFINITE, __NV_E4M3);
+      const uint32_t b0 = e4m3_rn_satfinite(lo);
+      const uint32_t b1 = e4m3_rn_satfinite(hi);
       word |= (b0 | (b1 << 8)) << (16 * j);
     }
     out[i] = word;
