@@ -93,9 +93,10 @@ def e4m3_quantize(x_raw: np.ndarray, descale: float) -> np.ndarray:
     x = raw_to_f64(x_raw).astype(np.float32)
     qt = (x / np.float32(descale)).astype(np.float32)
     vals = [e4m3_value(c) for c in range(0x7F)]
-    # each distinct quotient is encoded once (bf16 inputs have few distinct values)
-    uniq, inv = np.unique(qt.reshape(-1), return_inverse=True)
-    codes = np.array([e4m3_encode(float(v), vals) for v in uniq], dtype=np.uint8)
+    # each distinct quotient is encoded once (bf16 inputs have few distinct
+    # values); distinct by bit pattern, so -0.0 keeps its sign (code 0x80)
+    uniq, inv = np.unique(qt.reshape(-1).view(np.uint32), return_inverse=True)
+    codes = np.array([e4m3_encode(float(v), vals) for v in uniq.view(np.float32)], dtype=np.uint8)
     return codes[inv].reshape(qt.shape)
 
 

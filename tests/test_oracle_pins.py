@@ -432,6 +432,9 @@ def pin_e4m3_quantize_error():
         bound = np.maximum(np.abs(xf[inr]) * 2.0 ** -4, 2.0 ** -10 * descale) * (1 + 1e-6)
         assert np.all(err <= bound)
         assert np.all(np.abs(back[~inr]) == 448 * descale)
+    # signed zeros keep their sign bit (S.0000.000), next to each other or not
+    z = np.array([0x8000, 0x0000, 0x8000, 0x3F80], dtype=np.uint16)  # bf16 -0, +0, -0, 1.0
+    assert list(oracle.e4m3_quantize(z, 0.5)) == [0x80, 0x00, 0x80, 0x40]
 
 
 PINS = [
