@@ -91,7 +91,7 @@ _SIGNATURES = {
     "cp_paged_attn_partial": (_i32, [_pdesc, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _i32, _vp, _vp, _f32,
                                      _vp, _vp, _vp, _sz, _vp, _vp]),
     "cp_paged_attn_workspace_bytes": (_sz, [_pdesc, _i32, _i32, _i32]),
-    "cp_paged_attn_fused": (_i32, [_pdesc, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _i32, _vp, _vp, _f32,
+    "cp_paged_attn_fused": (_i32, [_pdesc, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _f32,
                                    _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp, _vp]),
     "cp_paged_attn_fused_workspace_bytes": (_sz, [_pdesc, _i32, _i32, _i32]),
     "own_token_attn": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _i32, _i32, _i32, _i32, _f32,
@@ -196,7 +196,7 @@ def fused_workspace_bytes(desc: PoolDesc, num_q_heads: int, num_tokens: int, max
 
 def cp_paged_attn_fused(desc: PoolDesc, pool_k, pool_v, q, kv_len, max_kv_len, kv_page_indptr, kv_page_indices,
                         scale, out, workspace, lse_out=None, extra_o=None, extra_lse=None, qo_indptr=None,
-                        num_rows=None, dev_status=None, stream=None):
+                        num_rows=None, row_order=None, dev_status=None, stream=None):
     """All partners' partials and their merge in one launch (see ``cp_paged_attn_fused`` in cpattn.h)."""
     lib = load_library()
     T, Hq = q.shape[0], q.shape[1]
@@ -205,7 +205,8 @@ def cp_paged_attn_fused(desc: PoolDesc, pool_k, pool_v, q, kv_len, max_kv_len, k
     st = lib.cp_paged_attn_fused(ctypes.byref(desc), _ptr(pool_k), _ptr(pool_v), _ptr(q), Hq, B, T,
                                  _i32_tensor(qo_indptr, "qo_indptr"), _i32_tensor(kv_len, "kv_len"),
                                  int(max_kv_len), _i32_tensor(kv_page_indptr, "kv_page_indptr"),
-                                 _i32_tensor(kv_page_indices, "kv_page_indices"), float(scale), _ptr(extra_o),
+                                 _i32_tensor(kv_page_indices, "kv_page_indices"),
+                                 _i32_tensor(row_order, "row_order"), float(scale), _ptr(extra_o),
                                  _ptr(extra_lse), dt, _ptr(out), _ptr(lse_out), _ptr(workspace),
                                  workspace.numel() * workspace.element_size(),
                                  _i32_tensor(dev_status, "dev_status"), _stream(stream))

@@ -69,6 +69,7 @@ struct FusedOut {
   void* out = nullptr;
   int out_bf16 = 0;
   float* lse_out = nullptr;
+  const int32_t* row_order = nullptr;
 };
 
 size_t partial_workspace(const cpattn_pool_desc* desc, int fused, int32_t num_q_heads, int32_t num_tokens,
@@ -113,12 +114,28 @@ int run_partial(const cpattn_pool_desc* desc, const void* pool_k, const void* po
   const size_t need = plan.bytes();
   if (workspace == nullptr || workspace_bytes < need) return CPATTN_ERR_WORKSPACE_TOO_SMALL;
 
+  // workspace: chunk partials, chunk LSEs, partner partials, partner LSEs
+  // (fused), then the two ticket arrays side by side (one memset)
   auto al = [](size_t x) { return (x + 255) / 256 * 256; };
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   PartialArgs a;
-  a.ws_o = reinterpret_cast<float*>(ws);
-  a.ws_lse = reinterpret_cast<float*>(ws + al(plan.ws_o_floats * 4));
-  a.ws_cnt = reinterpret_cast<int32_t*>(ws + al(plan.ws_o_floats * 4) + al(plan.ws_lse_floats * 4));
+  size_t off = 0;
+  a.ws_o = reinterpret_cast<float*>(ws + off);
+  off += al(plan.ws_o_floats * 4);
+  a.ws_lse = reinterpret_cast<float*>(ws + off);
+  off += al(plan.ws_lse_floats * 4);
+  float* ws_part = reinterpret_cast<float*>(ws + off);
+  off += al(plan.ws_part_floats * 4);
+  float* ws_part_lse = reinterpret_cast<float*>(ws + off);
+  off += al(plan.ws_part_lse_floats * 4);
+  a.ws_cnt = reinterpret_cast<int32_t*>(ws + off);
+  const size_t cnt_bytes = al(plan.ws_cnt_ints * 4);
+  a.ws_pair = reinterpret_cast<int32_t*>(ws + off + cnt_bytes);
+  const size_t ticket_bytes = cnt_bytes + plan.ws_pair_ints * 4;
+  if (f.fused) {
+    o_part = ws_part;
+    lse_part = ws_part_lse;
+  }
   a.pool_k = pool_k;
   a.pool_v = mla ? pool_k : pool_v;
   a.q = q;
@@ -154,11 +171,11 @@ int run_partial(const cpattn_pool_desc* desc, const void* pool_k, const void* po
   a.out = f.out;
   a.out_bf16 = f.out_bf16;
   a.lse_out = f.lse_out;
+  a.row_order = f.row_order;
 
   // tickets start from zero (each call's last arrivals also reset them)
   if (plan.max_chunks > 1 || f.fused) {
-    if (cudaMemsetAsync(a.ws_cnt, 0, plan.ws_cnt_ints * sizeof(int32_t), stream) != cudaSuccess)
-      return CPATTN_ERR_CUDA;
+    if (cudaMemsetAsync(a.ws_cnt, 0, ticket_bytes, stream) != cudaSuccess) return CPATTN_ERR_CUDA;
   }
   cudaError_t err = cudaSuccess;
   if (mla) return launch_mla_partial(a, stream, &err);
@@ -259,7 +276,8 @@ int cp_paged_attn_partial(const cpattn_pool_desc* desc, const void* pool_k, cons
 int cp_paged_attn_fused(const cpattn_pool_desc* desc, const void* pool_k, const void* pool_v, const void* q,
                         int32_t num_q_heads, int32_t num_rows, int32_t num_tokens, const int32_t* qo_indptr,
                         const int32_t* kv_len, int32_t max_kv_len, const int32_t* kv_page_indptr,
-                        const int32_t* kv_page_indices, float scale, const float* extra_o, const float* extra_lse,
+                        const int32_t* kv_page_indices, const int32_t* row_order, float scale,
+                        const float* extra_o, const float* extra_lse,
                         int32_t out_dtype, void* out, float* lse_out, void* workspace, size_t workspace_bytes,
                         int32_t* dev_status, cudaStream_t stream) {
   const int st = check_desc(desc);
@@ -276,6 +294,7 @@ int cp_paged_attn_fused(const cpattn_pool_desc* desc, const void* pool_k, const 
   f.out = out;
   f.out_bf16 = out_dtype == CPATTN_DTYPE_BF16;
   f.lse_out = lse_out;
+  f.row_order = qo_indptr == nullptr ? row_order : nullptr;
   return run_partial(desc, pool_k, pool_v, q, num_q_heads, num_rows, num_tokens, qo_indptr, kv_len, max_kv_len,
                      kv_page_indptr, kv_page_indices, scale, nullptr, nullptr, f, workspace, workspace_bytes,
                      dev_status, stream);

@@ -82,6 +82,18 @@ __host__ __device__ __forceinline__ int max_stripe_len(int L, int P, int I) {
   return runs * I < L ? runs * I : L;
 }
 
+// Row (or token) that grid slot z works on under an optional dispatch order;
+// an entry outside [0, n) is reported (CPATTN_DEV_BAD_INDPTR) and gives -1.
+__device__ __forceinline__ int ordered_row(const int32_t* __restrict__ order, int z, int n, int32_t* dev_status) {
+  if (order == nullptr) return z;
+  const int b = __ldg(order + z);
+  if (b < 0 || b >= n) {
+    if (threadIdx.x == 0) report(dev_status, CPATTN_DEV_BAD_INDPTR);
+    return -1;
+  }
+  return b;
+}
+
 // Online-softmax state merge in the log2 domain: (m, l) absorbs (m2, l2);
 // returns the factors the two accumulators are scaled by.
 __device__ __forceinline__ void softmax_merge_factors(float m, float m2, float& mn, float& a, float& b) {

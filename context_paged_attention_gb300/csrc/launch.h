@@ -69,7 +69,8 @@ struct PartialArgs {
   // workspace (split-KV partials)
   float* ws_o;
   float* ws_lse;
-  int32_t* ws_cnt;
+  int32_t* ws_cnt;   // [T * P * Hkv] chunk tickets
+  int32_t* ws_pair;  // [T * Hkv] partner tickets (fused calls)
   int P, interleave, page_size, ps_l, num_pages, num_kv_heads, num_q_heads, head_dim, head_dim_v;
   int num_rows, num_tokens, max_kv_len;
   int seg;         // tokens per staged segment (divides ps_l)
@@ -78,20 +79,26 @@ struct PartialArgs {
   float scale;
   int kv_fp8;                 // pool holds E4M3 codes: key = code * k_descale, value = code * v_descale
   float k_descale, v_descale;
-  // fused calls: partials stay in the workspace and the last CTA of each
-  // (token, KV head) writes the merged output (o_part / lse_part unused)
+  // fused calls: o_part / lse_part point into the workspace, and the last
+  // partner to finish a (token, KV head) writes the merged output
   int fused;
   const float* extra_o;    // [T][Hq][Dv] fp32 partial merged in too, or null
   const float* extra_lse;  // [T][Hq]
   void* out;               // [T][Hq][Dv], bf16 when out_bf16 else fp32
   int out_bf16;
   float* lse_out;          // [T][Hq] or null
+  // dispatch order of the grid's row axis (a permutation, e.g. longest rows
+  // first so the last wave holds the short ones), or null: natural order.
+  // Used where the grid's z axis walks rows (one token a row); ignored by
+  // the multi-token kernel.
+  const int32_t* row_order;
 };
 
 // Geometry of a partial launch (shared by workspace sizing and the launch).
 struct PartialPlan {
   int seg, chunk, max_chunks;
   size_t ws_o_floats, ws_lse_floats, ws_cnt_ints;
+  size_t ws_part_floats, ws_part_lse_floats, ws_pair_ints;  // fused calls: partner partials, pair tickets
   size_t bytes() const;
 };
 // Returns false if the shape is unsupported.

@@ -35,7 +35,9 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_partial_kernel(const Parti
   const int c = blockIdx.x;
   const int p = blockIdx.y / a.num_kv_heads;
   const int h = blockIdx.y - p * a.num_kv_heads;
-  const int t = blockIdx.z;
+  // token of this grid slot (a dispatch order applies when tokens are rows)
+  const int t = a.qo_indptr == nullptr ? ordered_row(a.row_order, blockIdx.z, gridDim.z, a.dev_status) : blockIdx.z;
+  if (t < 0) return;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int P = a.P;
@@ -147,7 +149,7 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_partial_kernel(const Parti
 
   const int64_t orow0 = (static_cast<int64_t>(p) * a.num_tokens + t) * a.num_q_heads + h * G;
   const int64_t slot = (static_cast<int64_t>(t) * P + p) * a.num_kv_heads + h;  // (t, p, h)
-  const bool single = !a.fused && nchunks == 1;
+  const bool single = (nchunks == 1);
   for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
     const int g = idx / D;
     const int d = idx - g * D;
@@ -162,14 +164,12 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_partial_kernel(const Parti
       if (d == 0) a.ws_lse[wrow] = lse;
     }
   }
-  if (single) return;
-  if (a.fused) {
-    fused_finish(a, t, h, L, G, D, sm);
-    return;
+  if (!single) {
+    if (!take_ticket(a.ws_cnt + slot, nchunks)) return;
+    merge_chunks(a, slot, nchunks, G, D, a.o_part + orow0 * D, a.lse_part + orow0);
+    if (threadIdx.x == 0) a.ws_cnt[slot] = 0;  // ready for the next call
   }
-  if (!take_ticket(a.ws_cnt + slot, nchunks)) return;
-  merge_chunks(a, slot, nchunks, G, D, a.o_part + orow0 * D, a.lse_part + orow0);
-  if (threadIdx.x == 0) a.ws_cnt[slot] = 0;  // ready for the next call
+  if (a.fused) pair_finish(a, t, h, G, D, sm);
 }
 
 template <typename T, int D, int G>
@@ -222,7 +222,8 @@ static int pick_seg(int ps_l, int lim) {
 
 size_t PartialPlan::bytes() const {
   auto al = [](size_t x) { return (x + 255) / 256 * 256; };
-  return al(ws_o_floats * 4) + al(ws_lse_floats * 4) + al(ws_cnt_ints * 4);
+  return al(ws_o_floats * 4) + al(ws_lse_floats * 4) + al(ws_cnt_ints * 4) + al(ws_part_floats * 4) +
+         al(ws_part_lse_floats * 4) + al(ws_pair_ints * 4);
 }
 
 bool plan_partial(int mla, int fused, int P, int interleave, int page_size, int num_kv_heads, int num_q_heads, int head_dim,
@@ -255,15 +256,15 @@ bool plan_partial(int mla, int fused, int P, int interleave, int page_size, int 
   plan->chunk = chunk;
   plan->max_chunks = max_stripe > 0 ? (max_stripe + chunk - 1) / chunk : 1;
   if (fused) {
-    // the last CTA of a (token, KV head) merges in shared memory it no longer
-    // uses; the smallest such region: MLA's Q tile, the bf16 kernels' K/V
-    // rings (multi-token kernel at D 64), the fp32 kernel's ring (page runs
-    // of one row at D 64)
+    // the last partner of a (token, KV head) merges in shared memory it no
+    // longer uses; the smallest such region: MLA's Q tile, the bf16 kernels'
+    // K/V rings (multi-token kernel at D 64), the fp32 kernel's ring (page
+    // runs of one row at D 64)
     const int cap_floats = mla ? 36000 : (dtype_bytes == 2 ? 6000 : 3000);
-    if (merge_scratch_floats(G, P, plan->max_chunks) > cap_floats) return false;
+    if (merge_scratch_floats(G, P) > cap_floats) return false;
   }
   const size_t slots = static_cast<size_t>(num_tokens) * P * num_kv_heads;
-  if (plan->max_chunks > 1 || fused) {
+  if (plan->max_chunks > 1) {
     plan->ws_o_floats = slots * plan->max_chunks * G * Dv;
     plan->ws_lse_floats = slots * plan->max_chunks * G;
   } else {
@@ -271,6 +272,13 @@ bool plan_partial(int mla, int fused, int P, int interleave, int page_size, int 
     plan->ws_lse_floats = 0;
   }
   plan->ws_cnt_ints = slots;
+  if (fused) {
+    plan->ws_part_floats = slots * G * Dv;
+    plan->ws_part_lse_floats = slots * G;
+    plan->ws_pair_ints = static_cast<size_t>(num_tokens) * num_kv_heads;
+  } else {
+    plan->ws_part_floats = plan->ws_part_lse_floats = plan->ws_pair_ints = 0;
+  }
   return true;
 }
 

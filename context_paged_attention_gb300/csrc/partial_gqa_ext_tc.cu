@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
 
     // ---- row `tid`: normalised output and LSE, to o_part or the workspace.
     // Every lane runs the (warp-collective) TMEM loads; only valid rows store.
-    const bool single = !a.fused && nchunks == 1;
+    const bool single = (nchunks == 1);
     {
       const bool empty = (l == 0.f);
       const float inv = empty ? 0.f : 1.f / l;
@@ -366,24 +366,25 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
       if (my_ok) *ldst = lse;
     }
     tc05::fence_before_sync();
-    if (a.fused) {
-      // one ticket per (segment, KV head): every chunk of every partner
-      const int64_t pair0 = static_cast<int64_t>(s0) * a.num_kv_heads + h;
-      int arrivals = 0;
-      for (int pp = 0; pp < P; ++pp) arrivals += chunks_of(a, L, pp);
-      if (take_ticket(a.ws_cnt + pair0, arrivals)) {
-        for (int tok = s0; tok < s1; ++tok) merge_partners(a, tok, h, L, G, D, reinterpret_cast<float*>(sKV));
-        if (tid == 0) a.ws_cnt[pair0] = 0;
-      }
-    } else if (!single) {
+    bool done = true;  // this CTA holds the partner's complete partial of the segment
+    if (!single) {
       const int64_t slot0 = (static_cast<int64_t>(s0) * P + p) * a.num_kv_heads + h;
-      if (take_ticket(a.ws_cnt + slot0, nchunks)) {
+      done = take_ticket(a.ws_cnt + slot0, nchunks);
+      if (done) {
         for (int tok = s0; tok < s1; ++tok) {
           const int64_t slot = (static_cast<int64_t>(tok) * P + p) * a.num_kv_heads + h;
           const int64_t orow0 = (static_cast<int64_t>(p) * a.num_tokens + tok) * a.num_q_heads + h * G;
           merge_chunks(a, slot, nchunks, G, D, a.o_part + orow0 * D, a.lse_part + orow0);
         }
         if (tid == 0) a.ws_cnt[slot0] = 0;
+      }
+    }
+    if (a.fused && done) {
+      // fused: the last of the P partners of (segment, KV head) merges them
+      int32_t* pair = a.ws_pair + static_cast<int64_t>(s0) * a.num_kv_heads + h;
+      if (take_ticket(pair, P)) {
+        for (int tok = s0; tok < s1; ++tok) merge_partners(a, tok, h, G, D, reinterpret_cast<float*>(sKV));
+        if (tid == 0) *pair = 0;
       }
     }
     __syncthreads();  // Q, the ring and the page table are reused by the next row

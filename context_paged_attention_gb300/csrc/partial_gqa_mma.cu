@@ -81,7 +81,8 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(cons
   // token are handled here (rows of two or more tokens: partial_gqa_ext.cu,
   // which also writes the padding tokens past the last row); without a map
   // row b is token b
-  int b = blockIdx.z;
+  const int b = ordered_row(a.row_order, blockIdx.z, gridDim.z, a.dev_status);
+  if (b < 0) return;
   int t = b;
   if (a.qo_indptr != nullptr) {
     t = __ldg(a.qo_indptr + b);
@@ -376,7 +377,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(cons
 
   const int64_t orow0 = (static_cast<int64_t>(p) * a.num_tokens + t) * a.num_q_heads + h * G;
   const int64_t slot = (static_cast<int64_t>(t) * P + p) * a.num_kv_heads + h;
-  const bool single = !a.fused && nchunks == 1;
+  const bool single = (nchunks == 1);
   for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
     const int g = idx / D;
     const int d = idx - g * D;
@@ -391,14 +392,12 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(cons
       if (d == 0) a.ws_lse[wrow] = lse;
     }
   }
-  if (single) return;
-  if (a.fused) {
-    fused_finish(a, t, h, L, G, D, sm);
-    return;
+  if (!single) {
+    if (!take_ticket(a.ws_cnt + slot, nchunks)) return;
+    merge_chunks(a, slot, nchunks, G, D, a.o_part + orow0 * D, a.lse_part + orow0);
+    if (threadIdx.x == 0) a.ws_cnt[slot] = 0;  // ready for the next call
   }
-  if (!take_ticket(a.ws_cnt + slot, nchunks)) return;
-  merge_chunks(a, slot, nchunks, G, D, a.o_part + orow0 * D, a.lse_part + orow0);
-  if (threadIdx.x == 0) a.ws_cnt[slot] = 0;  // ready for the next call
+  if (a.fused) pair_finish(a, t, h, G, D, sm);
 }
 
 template <int D, int G, bool F8>

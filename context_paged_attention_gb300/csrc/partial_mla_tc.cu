@@ -82,7 +82,9 @@ __global__ void __launch_bounds__(128, 1)
 
   const int c = blockIdx.x;
   const int p = blockIdx.y;
-  const int t = blockIdx.z;
+  // token of this grid slot (a dispatch order applies when tokens are rows)
+  const int t = a.qo_indptr == nullptr ? ordered_row(a.row_order, blockIdx.z, gridDim.z, a.dev_status) : blockIdx.z;
+  if (t < 0) return;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -114,15 +116,10 @@ __global__ void __launch_bounds__(128, 1)
   const int64_t orow = (static_cast<int64_t>(p) * a.num_tokens + t) * a.num_q_heads + tid;  // head tid
   const int64_t slot = static_cast<int64_t>(t) * P + p;
   if (ntiles == 0) {  // empty stripe (or padding token): 0 / -inf
-    const int64_t wrow = (slot * a.max_chunks + c) * kHeads + tid;
-    float4* dst = reinterpret_cast<float4*>(a.fused ? a.ws_o + wrow * kDv : a.o_part + orow * kDv);
+    float4* dst = reinterpret_cast<float4*>(a.o_part + orow * kDv);
     for (int e = 0; e < kDv / 4; ++e) dst[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (a.fused) {
-      a.ws_lse[wrow] = -INFINITY;
-      fused_finish(a, t, 0, L, kHeads, kDv, reinterpret_cast<float*>(sQ));
-    } else {
-      a.lse_part[orow] = -INFINITY;
-    }
+    a.lse_part[orow] = -INFINITY;
+    if (a.fused) pair_finish(a, t, 0, kHeads, kDv, reinterpret_cast<float*>(sQ));
     return;
   }
 
@@ -397,7 +394,7 @@ __global__ void __launch_bounds__(128, 1)
     if (tid == 0) report(a.dev_status, CPATTN_DEV_TC_TIMEOUT);
   } else {
     // ---- normalised partial of head `tid`: to o_part directly, or to the workspace
-    const bool single = !a.fused && nchunks == 1;
+    const bool single = (nchunks == 1);
     const float inv = lr > 0.f ? 1.f / lr : 0.f;
     const float lse = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
     float* dst = single ? a.o_part + orow * kDv : a.ws_o + ((slot * a.max_chunks + c) * kHeads + tid) * kDv;
@@ -427,15 +424,13 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   if (warp == 0) tc05::tmem_dealloc(tbase, 512);
   if (!alive) return;
-  if (a.fused) {
-    fused_finish(a, t, 0, L, kHeads, kDv, reinterpret_cast<float*>(sQ));
-    return;
+  if (nchunks > 1) {
+    if (!take_ticket(a.ws_cnt + slot, nchunks)) return;
+    const int64_t orow0 = (static_cast<int64_t>(p) * a.num_tokens + t) * a.num_q_heads;
+    merge_chunks(a, slot, nchunks, kHeads, kDv, a.o_part + orow0 * kDv, a.lse_part + orow0);
+    if (tid == 0) a.ws_cnt[slot] = 0;
   }
-  if (nchunks == 1) return;
-  if (!take_ticket(a.ws_cnt + slot, nchunks)) return;
-  const int64_t orow0 = (static_cast<int64_t>(p) * a.num_tokens + t) * a.num_q_heads;
-  merge_chunks(a, slot, nchunks, kHeads, kDv, a.o_part + orow0 * kDv, a.lse_part + orow0);
-  if (tid == 0) a.ws_cnt[slot] = 0;
+  if (a.fused) pair_finish(a, t, 0, kHeads, kDv, reinterpret_cast<float*>(sQ));
 }
 
 int mla_tc_chunk(int ps_l) {

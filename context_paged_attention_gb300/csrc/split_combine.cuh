@@ -7,13 +7,13 @@
 // merge, as lse_merge does for partners) into o_part / lse_part.  No
 // spin-wait: the last arrival does the work, the others just exit.
 //
-// Fused calls (cp_paged_attn_fused) go one level further: every chunk CTA of
-// every partner of a (token, KV head) stores its partial in the workspace and
-// arrives on one ticket for the pair; the last one merges all of them (and an
-// optional precomputed partial, e.g. the own-token one) into the final
-// output.  The exact merge is associative, so this equals merging the
-// partners' partials (mstar PR #1124 "Context / Sequence Parallel 1/5",
-// description: the partials and their LSEs are combined exactly).
+// Fused calls (cp_paged_attn_fused) go one level further: the partner
+// partials live in the workspace, and the CTA that completes a partner's
+// partial of a (token, KV head) arrives on a second ticket for the pair; the
+// last of the P partners merges them (and an optional precomputed partial,
+// e.g. the own-token one) into the final output, as lse_merge would (mstar
+// PR #1124 "Context / Sequence Parallel 1/5", description: the partials and
+// their LSEs are combined exactly).
 #pragma once
 
 #include "common.cuh"
@@ -67,45 +67,26 @@ __device__ __forceinline__ void merge_chunks(const PartialArgs& a, int64_t slot,
   }
 }
 
-// Chunk CTAs of partner p's stripe of a row of L keys (an empty stripe still
-// has its chunk 0, which stores the empty partial).
-__device__ __forceinline__ int chunks_of(const PartialArgs& a, int L, int p) {
-  const int n = stripe_len(L, p, a.P, a.interleave);
-  return n > 0 ? (n + a.chunk - 1) / a.chunk : 1;
-}
+// Shared-memory floats merge_partners needs: the Hg x (P + 1) weight table
+// and one value per head.
+__host__ __device__ __forceinline__ int merge_scratch_floats(int Hg, int P) { return Hg * (P + 1) + Hg; }
 
-// Arrivals on the ticket of a fused (token, KV head) pair.
-__device__ __forceinline__ int fused_arrivals(const PartialArgs& a, int L) {
-  int n = 0;
-  for (int p = 0; p < a.P; ++p) n += chunks_of(a, L, p);
-  return n;
-}
-
-// Shared-memory floats merge_partners needs: the Hg x (P * max_chunks + 1)
-// weight table and two per-head values.
-__host__ __device__ __forceinline__ int merge_scratch_floats(int Hg, int P, int max_chunks) {
-  return Hg * (P * max_chunks + 1) + 2 * Hg;
-}
-
-// Final output of (token t, KV head h) from every partner's chunk partials in
-// the workspace (rows ((t * P + p) * Hkv + h) * max_chunks + c) and the
-// optional extra partial; written as bf16 (round to nearest even) or fp32.
-// Entry e = p * max_chunks + c (e = P * max_chunks: the extra partial).
-//   1. all threads load the entries' LSEs at once into a [Hg][E] table
-//      (-inf for chunks the partner does not have: their rows are stale);
+// Final output of (token t, KV head h) from the P partner partials (o_part /
+// lse_part rows, which fused calls keep in the workspace) and the optional
+// extra partial; written as bf16 (round to nearest even) or fp32.
+//   1. all threads load the entries' LSEs at once into a [Hg][P + 1] table;
 //   2. one warp per head turns them into weights exp(lse - max) and the
 //      head's LSE with shuffle reductions;
 //   3. each thread sums weight * row over the entries for a float4 group of
-//      value dims, the loads unrolled so several are in flight.
-// scratch: merge_scratch_floats(Hg, P, max_chunks) floats of shared memory
-// the CTA no longer uses.  Dv % 4 == 0.
-__device__ __forceinline__ void merge_partners(const PartialArgs& a, int t, int h, int L, int Hg, int Dv,
-                                               float* scratch) {
-  const int E = a.P * a.max_chunks + 1;
+//      value dims.
+// scratch: merge_scratch_floats(Hg, P) floats of shared memory the CTA no
+// longer uses.  Dv % 4 == 0.
+__device__ __forceinline__ void merge_partners(const PartialArgs& a, int t, int h, int Hg, int Dv, float* scratch) {
+  const int E = a.P + 1;
   float* wt = scratch;              // [Hg][E]
   float* s_inv = scratch + Hg * E;  // [Hg]
   const int64_t hq0 = static_cast<int64_t>(t) * a.num_q_heads + h * Hg;  // first query-head row of the pair
-  const int64_t wt0 = static_cast<int64_t>(t) * a.P * a.num_kv_heads + h;  // (t, p = 0, h)
+  const int64_t pstride = static_cast<int64_t>(a.num_tokens) * a.num_q_heads;  // rows between partners
   __syncthreads();  // the scratch may still be read from a previous token
   for (int idx = threadIdx.x; idx < Hg * E; idx += blockDim.x) {
     const int g = idx / E;
@@ -114,10 +95,7 @@ __device__ __forceinline__ void merge_partners(const PartialArgs& a, int t, int 
     if (e == E - 1) {
       if (a.extra_lse != nullptr) lse = __ldg(a.extra_lse + hq0 + g);
     } else {
-      const int p = e / a.max_chunks;
-      const int c = e - p * a.max_chunks;
-      if (c < chunks_of(a, L, p))
-        lse = __ldcg(a.ws_lse + ((wt0 + static_cast<int64_t>(p) * a.num_kv_heads) * a.max_chunks + c) * Hg + g);
+      lse = __ldcg(a.lse_part + e * pstride + hq0 + g);
     }
     wt[idx] = lse;
   }
@@ -153,11 +131,8 @@ __device__ __forceinline__ void merge_partners(const PartialArgs& a, int t, int 
 #pragma unroll 4
     for (int e = 0; e < E - 1; ++e) {
       const float w = wg[e];
-      if (w != 0.f) {  // rows of absent chunks are never read
-        const int p = e / a.max_chunks;
-        const int c = e - p * a.max_chunks;
-        const int64_t wrow = ((wt0 + static_cast<int64_t>(p) * a.num_kv_heads) * a.max_chunks + c) * Hg + g;
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(a.ws_o + wrow * Dv + d));
+      if (w != 0.f) {  // empty partials' rows are not read
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(a.o_part + (e * pstride + hq0 + g) * Dv + d));
         acc.x = fmaf(w, v.x, acc.x);
         acc.y = fmaf(w, v.y, acc.y);
         acc.z = fmaf(w, v.z, acc.z);
@@ -188,14 +163,14 @@ __device__ __forceinline__ void merge_partners(const PartialArgs& a, int t, int 
   }
 }
 
-// Fused finish of one CTA (all threads call, after their workspace stores):
-// arrive on the pair's ticket; the last arrival merges and re-arms the ticket.
-__device__ __forceinline__ void fused_finish(const PartialArgs& a, int t, int h, int L, int Hg, int Dv,
-                                             float* scratch) {
-  const int64_t pair = static_cast<int64_t>(t) * a.num_kv_heads + h;
-  if (!take_ticket(a.ws_cnt + pair, fused_arrivals(a, L))) return;
-  merge_partners(a, t, h, L, Hg, Dv, scratch);
-  if (threadIdx.x == 0) a.ws_cnt[pair] = 0;
+// Fused calls, after a partner's partial of (token t, KV head h) is complete
+// in o_part (written directly, or merged from its chunks by this CTA): arrive
+// on the pair's ticket; the last of the P partners merges (all threads call).
+__device__ __forceinline__ void pair_finish(const PartialArgs& a, int t, int h, int Hg, int Dv, float* scratch) {
+  int32_t* pair = a.ws_pair + static_cast<int64_t>(t) * a.num_kv_heads + h;
+  if (!take_ticket(pair, a.P)) return;
+  merge_partners(a, t, h, Hg, Dv, scratch);
+  if (threadIdx.x == 0) *pair = 0;
 }
 
 // Output rows of padding tokens (fused calls): 0 and -inf.

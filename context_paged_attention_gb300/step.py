@@ -77,6 +77,9 @@ class StripedAttention:
         self.workspace = torch.empty((max(ws, 256),), dtype=torch.uint8, device=self.device)
         self._fused_ws = None
         self.graph = None
+        # dispatch order of the rows: longest first (the host knows the lengths)
+        order = np.argsort(-w.kv_len.astype(np.int64), kind="stable").astype(np.int32)
+        self.row_order = _to_torch(order, self.device)
         if fill_history:
             self.fill_history()
 
@@ -139,6 +142,7 @@ class StripedAttention:
                               self.out if out is None else out, self._fused_ws,
                               lse_out=self.lse if lse is None else lse, extra_o=extra_o, extra_lse=extra_lse,
                               qo_indptr=None if one_per_row else self.qo_indptr, num_rows=self.w.num_rows,
+                              row_order=self.row_order if one_per_row else None,
                               dev_status=self.dev_status, stream=stream)
 
     def run_step_fused(self, stream=None, out=None, lse=None):

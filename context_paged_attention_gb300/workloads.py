@@ -120,8 +120,9 @@ class Workload:
         return (self.ctx_len + self.new_len).astype(np.int64)
 
     def kv_bytes_read(self) -> int:
-        """Algorithmic K/V bytes the pool partial reads: every visible key once."""
-        esz = 2 if self.dtype == "bf16" else 4
+        """Algorithmic K/V bytes the pool partial reads: every visible key once
+        (one byte a value for FP8 pools)."""
+        esz = 1 if self.kv_dtype == "fp8" else (2 if self.dtype == "bf16" else 4)
         keys = int(self.kv_len[: self.num_real_rows].astype(np.int64).sum())
         per_key = self.num_kv_heads * (self.head_dim + (0 if self.mla else self.head_dim_v)) * esz
         return keys * per_key

@@ -214,6 +214,13 @@ CPATTN_API size_t cp_paged_attn_workspace_bytes(const cpattn_pool_desc* desc, in
  * makes no host synchronisation and no allocation, so it can be captured.
  *
  * Arguments as cp_paged_attn_partial, except:
+ *   row_order   optional device [num_rows] permutation of the rows: the order
+ *               in which CTAs take rows when each row is one token (qo_indptr
+ *               NULL).  Longest rows first shortens the last wave; the
+ *               caller's host-side plan knows the lengths.  NULL: row order.
+ *               Entries outside [0, num_rows) are skipped and reported
+ *               (CPATTN_DEV_BAD_INDPTR); a non-permutation gives wrong rows.
+ *               Ignored when qo_indptr is given.
  *   extra_o, extra_lse  optional precomputed partial merged in too
  *               ([num_tokens][num_q_heads][head_dim_v] fp32 and
  *               [num_tokens][num_q_heads] fp32, e.g. own_token_attn's); both
@@ -232,7 +239,8 @@ CPATTN_API int cp_paged_attn_fused(const cpattn_pool_desc* desc, const void* poo
                                    int32_t num_rows, int32_t num_tokens, const int32_t* qo_indptr,
                                    const int32_t* kv_len, int32_t max_kv_len,
                                    const int32_t* kv_page_indptr, const int32_t* kv_page_indices,
-                                   float scale, const float* extra_o, const float* extra_lse,
+                                   const int32_t* row_order, float scale, const float* extra_o,
+                                   const float* extra_lse,
                                    int32_t out_dtype, void* out, float* lse_out, void* workspace,
                                    size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream);
 

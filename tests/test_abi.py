@@ -149,21 +149,21 @@ def test_fp8_descriptor_checks(lib):
 def test_fused_argument_checks(lib):
     d = _desc()
     args = lambda extra_o, extra_lse, odt, out: (ctypes.byref(d), FAKE, FAKE, FAKE, 32, 1, 1, None, FAKE, 100, FAKE,
-                                                 FAKE, 0.1, extra_o, extra_lse, odt, out, None, FAKE, 1 << 30,
+                                                 FAKE, None, 0.1, extra_o, extra_lse, odt, out, None, FAKE, 1 << 30,
                                                  None, None)
     assert lib.cp_paged_attn_fused(*args(None, None, 7, FAKE)) == -1           # unknown output type
     assert lib.cp_paged_attn_fused(*args(FAKE, None, 0, FAKE)) == -1           # extra partial half given
     assert lib.cp_paged_attn_fused(*args(None, None, 0, None)) == -1           # no output
     assert lib.cp_paged_attn_fused(*args(None, None, 0, FAKE + 8)) == -4       # misaligned output
     bad = _desc(P=3)
-    assert lib.cp_paged_attn_fused(ctypes.byref(bad), FAKE, FAKE, FAKE, 32, 1, 1, None, FAKE, 100, FAKE, FAKE, 0.1,
-                                   None, None, 0, FAKE, None, FAKE, 1 << 30, None, None) == -2
+    assert lib.cp_paged_attn_fused(ctypes.byref(bad), FAKE, FAKE, FAKE, 32, 1, 1, None, FAKE, 100, FAKE, FAKE, None,
+                                   0.1, None, None, 0, FAKE, None, FAKE, 1 << 30, None, None) == -2
     # workspace: always room for every chunk partial (the split path may need none)
     fused = lib.cp_paged_attn_fused_workspace_bytes(ctypes.byref(d), 32, 64, 256)
     plain = lib.cp_paged_attn_workspace_bytes(ctypes.byref(d), 32, 64, 256)
     assert fused >= 64 * 4 * 32 * 128 * 4 and fused > plain
-    assert lib.cp_paged_attn_fused(ctypes.byref(d), FAKE, FAKE, FAKE, 32, 64, 64, None, FAKE, 256, FAKE, FAKE, 0.1,
-                                   None, None, 0, FAKE, None, FAKE, fused - 1, None, None) == -5
+    assert lib.cp_paged_attn_fused(ctypes.byref(d), FAKE, FAKE, FAKE, 32, 64, 64, None, FAKE, 256, FAKE, FAKE, None,
+                                   0.1, None, None, 0, FAKE, None, FAKE, fused - 1, None, None) == -5
 
 
 def test_workspace_sizing(lib):

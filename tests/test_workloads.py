@@ -77,3 +77,9 @@ def test_full_size_geometry_cheap():
     rng = np.random.default_rng(2)
     L = rng.integers(512, 8192, size=64, endpoint=True)
     assert L.min() >= 512 and L.max() <= 8192
+
+
+def test_fp8_pool_bytes_halve():
+    w = W.gqa_decode(seed=5, batch=3, len_lo=10, len_hi=100)
+    f = W.fp8_pool(w, 0.01, 0.02)
+    assert f.kv_bytes_read() * 2 == w.kv_bytes_read() and f.kv_dtype == "fp8" and f.name.endswith("_fp8")
