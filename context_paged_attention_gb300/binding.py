@@ -19,6 +19,9 @@ DTYPE_BF16 = 0
 DTYPE_FP32 = 1
 DTYPE_FP8_E4M3 = 2  # pools only
 FP8_NAN_CODE = 0x7F
+LSE_TOKEN_MAJOR = 0
+LSE_HEAD_MAJOR = 1
+MAX_MERGE_VIEWS = 16
 
 _STATUS_NAMES = {
     0: "CPATTN_OK",
@@ -75,6 +78,19 @@ class PoolDesc(ctypes.Structure):
         return torch.uint8 if self.fp8 else self.torch_dtype()
 
 
+class PartialView(ctypes.Structure):
+    """Mirror of ``cpattn_partial_view``."""
+
+    _fields_ = [
+        ("o", ctypes.c_void_p),
+        ("lse", ctypes.c_void_p),
+        ("o_stride_token", ctypes.c_int64),
+        ("o_stride_head", ctypes.c_int64),
+        ("lse_stride_token", ctypes.c_int64),
+        ("lse_stride_head", ctypes.c_int64),
+    ]
+
+
 _lib = None
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -91,6 +107,10 @@ _SIGNATURES = {
     "cp_paged_attn_partial": (_i32, [_pdesc, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _i32, _vp, _vp, _f32,
                                      _vp, _vp, _vp, _sz, _vp, _vp]),
     "cp_paged_attn_workspace_bytes": (_sz, [_pdesc, _i32, _i32, _i32]),
+    "cp_paged_attn_partial_ex": (_i32, [_pdesc, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _i32, _vp, _vp, _f32,
+                                        _vp, _vp, _i32, _vp, _sz, _vp, _vp]),
+    "lse_merge_views": (_i32, [_i32, ctypes.POINTER(PartialView), _i32, _i32, _i32, _i32, _vp, _i64, _i64, _vp,
+                               _i64, _i64, _vp]),
     "cp_paged_attn_fused": (_i32, [_pdesc, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _f32,
                                    _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp, _vp]),
     "cp_paged_attn_fused_workspace_bytes": (_sz, [_pdesc, _i32, _i32, _i32]),
@@ -211,6 +231,45 @@ def cp_paged_attn_fused(desc: PoolDesc, pool_k, pool_v, q, kv_len, max_kv_len, k
                                  workspace.numel() * workspace.element_size(),
                                  _i32_tensor(dev_status, "dev_status"), _stream(stream))
     _check(st, "cp_paged_attn_fused")
+
+
+def cp_paged_attn_partial_ex(desc: PoolDesc, pool_k, pool_v, q, kv_len, max_kv_len, kv_page_indptr,
+                             kv_page_indices, scale, o_part, lse_part, workspace, lse_layout=LSE_TOKEN_MAJOR,
+                             qo_indptr=None, num_rows=None, dev_status=None, stream=None):
+    """cp_paged_attn_partial with the LSE layout chosen (see ``cp_paged_attn_partial_ex`` in cpattn.h)."""
+    lib = load_library()
+    T, Hq = q.shape[0], q.shape[1]
+    B = kv_len.numel() if num_rows is None else num_rows
+    st = lib.cp_paged_attn_partial_ex(ctypes.byref(desc), _ptr(pool_k), _ptr(pool_v), _ptr(q), Hq, B, T,
+                                      _i32_tensor(qo_indptr, "qo_indptr"), _i32_tensor(kv_len, "kv_len"),
+                                      int(max_kv_len), _i32_tensor(kv_page_indptr, "kv_page_indptr"),
+                                      _i32_tensor(kv_page_indices, "kv_page_indices"), float(scale), _ptr(o_part),
+                                      _ptr(lse_part), int(lse_layout), _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(),
+                                      _i32_tensor(dev_status, "dev_status"), _stream(stream))
+    _check(st, "cp_paged_attn_partial_ex")
+
+
+def view(o, lse, o_stride_token, o_stride_head, lse_stride_token, lse_stride_head, o_offset=0, lse_offset=0):
+    """A cpattn_partial_view of fp32 device tensors (offsets and strides in elements)."""
+    if o.dtype != torch.float32 or lse.dtype != torch.float32:
+        raise TypeError("partial views are fp32")
+    return PartialView(_ptr(o) + 4 * o_offset, _ptr(lse) + 4 * lse_offset, o_stride_token, o_stride_head,
+                       lse_stride_token, lse_stride_head)
+
+
+def lse_merge_views(views, num_tokens, num_heads, head_dim_v, out, out_stride_token, out_stride_head,
+                    lse_out=None, lse_out_stride_token=0, lse_out_stride_head=0, out_offset=0, lse_out_offset=0,
+                    stream=None):
+    """Exact merge of strided partial views (see ``lse_merge_views`` in cpattn.h)."""
+    lib = load_library()
+    arr = (PartialView * len(views))(*views)
+    dt = DTYPE_BF16 if out.dtype == torch.bfloat16 else DTYPE_FP32
+    lse_ptr = None if lse_out is None else _ptr(lse_out) + 4 * lse_out_offset
+    st = lib.lse_merge_views(len(views), arr, num_tokens, num_heads, head_dim_v, dt,
+                             _ptr(out) + out.element_size() * out_offset, out_stride_token, out_stride_head,
+                             lse_ptr, lse_out_stride_token, lse_out_stride_head, _stream(stream))
+    _check(st, "lse_merge_views")
 
 
 def own_token_attn(q, k_new, v_new, qo_indptr, num_real_rows, max_q_len, scale, o_own, lse_own, stream=None):

@@ -86,8 +86,9 @@ size_t partial_workspace(const cpattn_pool_desc* desc, int fused, int32_t num_q_
 int run_partial(const cpattn_pool_desc* desc, const void* pool_k, const void* pool_v, const void* q,
                 int32_t num_q_heads, int32_t num_rows, int32_t num_tokens, const int32_t* qo_indptr,
                 const int32_t* kv_len, int32_t max_kv_len, const int32_t* kv_page_indptr,
-                const int32_t* kv_page_indices, float scale, float* o_part, float* lse_part, const FusedOut& f,
-                void* workspace, size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream) {
+                const int32_t* kv_page_indices, float scale, float* o_part, float* lse_part, int lse_layout,
+                const FusedOut& f, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                cudaStream_t stream) {
   int st = check_desc(desc);
   if (st != CPATTN_OK) return st;
   if (num_q_heads < 1 || num_rows < 0 || num_tokens < 0 || max_kv_len < 0) return CPATTN_ERR_INVALID_ARG;
@@ -99,6 +100,7 @@ int run_partial(const cpattn_pool_desc* desc, const void* pool_k, const void* po
       kv_page_indices == nullptr)
     return CPATTN_ERR_INVALID_ARG;
   if (!f.fused && (o_part == nullptr || lse_part == nullptr)) return CPATTN_ERR_INVALID_ARG;
+  if (lse_layout != CPATTN_LSE_TOKEN_MAJOR && lse_layout != CPATTN_LSE_HEAD_MAJOR) return CPATTN_ERR_INVALID_ARG;
   if (!mla && pool_v == nullptr) return CPATTN_ERR_INVALID_ARG;
   if (mla && pool_v != nullptr && pool_v != pool_k) return CPATTN_ERR_INVALID_ARG;
   if (!aligned16(pool_k) || !aligned16(pool_v) || !aligned16(q) || !aligned16(o_part) || !aligned16(workspace))
@@ -141,6 +143,13 @@ int run_partial(const cpattn_pool_desc* desc, const void* pool_k, const void* po
   a.q = q;
   a.o_part = o_part;
   a.lse_part = lse_part;
+  // LSE of (partner, token, head): [P][T][Hq], or [P][Hq][T] (FlashAttention's [H, B] per partner);
+  // the partner partials of fused calls are internal and token-major
+  const int64_t TH = static_cast<int64_t>(num_tokens) * num_q_heads;
+  const bool head_major = !f.fused && lse_layout == CPATTN_LSE_HEAD_MAJOR;
+  a.lse_sp = TH;
+  a.lse_st = head_major ? 1 : num_q_heads;
+  a.lse_sh = head_major ? num_tokens : 1;
   a.qo_indptr = qo_indptr;
   a.kv_len = kv_len;
   a.page_indptr = kv_page_indptr;
@@ -269,8 +278,20 @@ int cp_paged_attn_partial(const cpattn_pool_desc* desc, const void* pool_k, cons
                           void* workspace, size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream) {
   FusedOut none;
   return run_partial(desc, pool_k, pool_v, q, num_q_heads, num_rows, num_tokens, qo_indptr, kv_len, max_kv_len,
-                     kv_page_indptr, kv_page_indices, scale, o_part, lse_part, none, workspace, workspace_bytes,
-                     dev_status, stream);
+                     kv_page_indptr, kv_page_indices, scale, o_part, lse_part, CPATTN_LSE_TOKEN_MAJOR, none,
+                     workspace, workspace_bytes, dev_status, stream);
+}
+
+int cp_paged_attn_partial_ex(const cpattn_pool_desc* desc, const void* pool_k, const void* pool_v, const void* q,
+                             int32_t num_q_heads, int32_t num_rows, int32_t num_tokens, const int32_t* qo_indptr,
+                             const int32_t* kv_len, int32_t max_kv_len, const int32_t* kv_page_indptr,
+                             const int32_t* kv_page_indices, float scale, float* o_part, float* lse_part,
+                             int32_t lse_layout, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                             cudaStream_t stream) {
+  FusedOut none;
+  return run_partial(desc, pool_k, pool_v, q, num_q_heads, num_rows, num_tokens, qo_indptr, kv_len, max_kv_len,
+                     kv_page_indptr, kv_page_indices, scale, o_part, lse_part, lse_layout, none, workspace,
+                     workspace_bytes, dev_status, stream);
 }
 
 int cp_paged_attn_fused(const cpattn_pool_desc* desc, const void* pool_k, const void* pool_v, const void* q,
@@ -296,8 +317,8 @@ int cp_paged_attn_fused(const cpattn_pool_desc* desc, const void* pool_k, const 
   f.lse_out = lse_out;
   f.row_order = qo_indptr == nullptr ? row_order : nullptr;
   return run_partial(desc, pool_k, pool_v, q, num_q_heads, num_rows, num_tokens, qo_indptr, kv_len, max_kv_len,
-                     kv_page_indptr, kv_page_indices, scale, nullptr, nullptr, f, workspace, workspace_bytes,
-                     dev_status, stream);
+                     kv_page_indptr, kv_page_indices, scale, nullptr, nullptr, CPATTN_LSE_TOKEN_MAJOR, f, workspace,
+                     workspace_bytes, dev_status, stream);
 }
 
 int own_token_attn(const void* q, const void* k_new, const void* v_new, int32_t num_q_heads, int32_t num_kv_heads,
@@ -359,6 +380,44 @@ int lse_merge(int32_t num_partials, const float* o_parts, const float* lse_parts
   a.out = out;
   a.lse_out = lse_out;
   return launch_lse_merge(a, stream) == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+}
+
+int lse_merge_views(int32_t num_views, const cpattn_partial_view* views, int32_t num_tokens, int32_t num_heads,
+                    int32_t head_dim_v, int32_t out_dtype, void* out, int64_t out_stride_token,
+                    int64_t out_stride_head, float* lse_out, int64_t lse_out_stride_token,
+                    int64_t lse_out_stride_head, cudaStream_t stream) {
+  if (num_views < 1 || num_views > CPATTN_MAX_MERGE_VIEWS || views == nullptr || num_tokens < 0 || num_heads < 1 ||
+      head_dim_v < 4 || head_dim_v % 4 != 0)
+    return CPATTN_ERR_INVALID_ARG;
+  if (out_dtype != CPATTN_DTYPE_BF16 && out_dtype != CPATTN_DTYPE_FP32) return CPATTN_ERR_INVALID_ARG;
+  if (num_tokens == 0) return CPATTN_OK;
+  if (out == nullptr) return CPATTN_ERR_INVALID_ARG;
+  // 16-byte row starts: every row pointer and row stride a multiple of 4 elements
+  if (!aligned16(out) || out_stride_token % 4 != 0 || out_stride_head % 4 != 0) return CPATTN_ERR_MISALIGNED;
+  MergeViewArgs a;
+  a.n = num_views;
+  for (int i = 0; i < num_views; ++i) {
+    const cpattn_partial_view& v = views[i];
+    if (v.o == nullptr || v.lse == nullptr) return CPATTN_ERR_INVALID_ARG;
+    if (!aligned16(v.o) || v.o_stride_token % 4 != 0 || v.o_stride_head % 4 != 0) return CPATTN_ERR_MISALIGNED;
+    a.v[i].o = v.o;
+    a.v[i].lse = v.lse;
+    a.v[i].o_st = v.o_stride_token;
+    a.v[i].o_sh = v.o_stride_head;
+    a.v[i].lse_st = v.lse_stride_token;
+    a.v[i].lse_sh = v.lse_stride_head;
+  }
+  a.num_tokens = num_tokens;
+  a.num_heads = num_heads;
+  a.head_dim_v = head_dim_v;
+  a.out_bf16 = out_dtype == CPATTN_DTYPE_BF16;
+  a.out = out;
+  a.out_st = out_stride_token;
+  a.out_sh = out_stride_head;
+  a.lse_out = lse_out;
+  a.lse_out_st = lse_out_stride_token;
+  a.lse_out_sh = lse_out_stride_head;
+  return launch_lse_merge_views(a, stream) == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
 }
 
 }  // extern "C"

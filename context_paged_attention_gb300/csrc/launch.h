@@ -54,6 +54,25 @@ struct MergeArgs {
 };
 cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t s);
 
+// lse_merge_views: partials given as strided views (any token / head layout).
+constexpr int kMaxMergeViews = 16;
+struct MergeView {
+  const float* o;
+  const float* lse;
+  int64_t o_st, o_sh, lse_st, lse_sh;
+};
+struct MergeViewArgs {
+  int n;
+  MergeView v[kMaxMergeViews];
+  int num_tokens, num_heads, head_dim_v;
+  int out_bf16;
+  void* out;
+  int64_t out_st, out_sh;
+  float* lse_out;
+  int64_t lse_out_st, lse_out_sh;
+};
+cudaError_t launch_lse_merge_views(const MergeViewArgs& a, cudaStream_t s);
+
 // Shared by every partial-attention kernel.
 struct PartialArgs {
   const void* pool_k;
@@ -61,6 +80,7 @@ struct PartialArgs {
   const void* q;
   float* o_part;
   float* lse_part;
+  int64_t lse_sp, lse_st, lse_sh;  // lse_part element of (partner, token, query head): strides
   const int32_t* qo_indptr;  // may be null: one token a row
   const int32_t* kv_len;
   const int32_t* page_indptr;

@@ -144,6 +144,7 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_partial_kernel(const Parti
   // ---- merge the warps through shared memory (the ring is free now)
   __syncthreads();
   float* sm = reinterpret_cast<float*>(smem);
+  const int scratch_cap = NW * NST * a.seg * C::ROWB * 2 / 4;  // the ring's floats (at most the dynamic smem)
   st.store(sm, NW, warp);
   __syncthreads();
 
@@ -157,7 +158,7 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_partial_kernel(const Parti
     merge_stored<D, G>(sm, NW, g, d, out, lse);
     if (single) {
       a.o_part[(orow0 + g) * D + d] = out;
-      if (d == 0) a.lse_part[orow0 + g] = lse;
+      if (d == 0) a.lse_part[lse_slot(a, p, t, h * G + g)] = lse;
     } else {
       const int64_t wrow = (slot * a.max_chunks + c) * G + g;
       a.ws_o[wrow * D + d] = out;
@@ -166,10 +167,10 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_partial_kernel(const Parti
   }
   if (!single) {
     if (!take_ticket(a.ws_cnt + slot, nchunks)) return;
-    merge_chunks(a, slot, nchunks, G, D, a.o_part + orow0 * D, a.lse_part + orow0);
+    merge_chunks(a, p, h, t, 1, slot, 0, nchunks, G, D, sm, scratch_cap);
     if (threadIdx.x == 0) a.ws_cnt[slot] = 0;  // ready for the next call
   }
-  if (a.fused) pair_finish(a, t, h, G, D, sm);
+  if (a.fused) pair_finish(a, t, h, G, D, sm, scratch_cap);
 }
 
 template <typename T, int D, int G>
@@ -255,14 +256,9 @@ bool plan_partial(int mla, int fused, int P, int interleave, int page_size, int 
   chunk = (chunk + unit - 1) / unit * unit;
   plan->chunk = chunk;
   plan->max_chunks = max_stripe > 0 ? (max_stripe + chunk - 1) / chunk : 1;
-  if (fused) {
-    // the last partner of a (token, KV head) merges in shared memory it no
-    // longer uses; the smallest such region: MLA's Q tile, the bf16 kernels'
-    // K/V rings (multi-token kernel at D 64), the fp32 kernel's ring (page
-    // runs of one row at D 64)
-    const int cap_floats = mla ? 36000 : (dtype_bytes == 2 ? 6000 : 3000);
-    if (merge_scratch_floats(G, P) > cap_floats) return false;
-  }
+  // the merges run in shared memory of at least 3000 floats (the fp32
+  // kernel's ring at page runs of one row, D 64) and need entries + 1
+  if (plan->max_chunks + 1 > 3000 || P + 2 > 3000) return false;
   const size_t slots = static_cast<size_t>(num_tokens) * P * num_kv_heads;
   if (plan->max_chunks > 1) {
     plan->ws_o_floats = slots * plan->max_chunks * G * Dv;

@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
     for (int tok = max(t_lo, t_real); tok < min(t_lo + QB, a.num_tokens); ++tok) {
       const int64_t orow0 = (static_cast<int64_t>(p) * a.num_tokens + tok) * a.num_q_heads + h * G;
       for (int x = tid; x < G * D; x += blockDim.x) a.o_part[orow0 * D + x] = 0.f;
-      if (tid < G) a.lse_part[orow0 + tid] = -INFINITY;
+      if (tid < G) a.lse_part[lse_slot(a, p, tok, h * G + tid)] = -INFINITY;
     }
   }
   if (t_lo >= t_hi) return;
@@ -338,7 +338,7 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
       if (single) {
         const int64_t orow = (static_cast<int64_t>(p) * a.num_tokens + my_tok) * a.num_q_heads + h * G + g;
         dst = a.o_part + orow * D;
-        ldst = a.lse_part + orow;
+        ldst = a.lse_part + lse_slot(a, p, my_tok, h * G + g);
       } else {
         const int64_t slot = (static_cast<int64_t>(my_tok) * P + p) * a.num_kv_heads + h;
         const int64_t wrow = (slot * a.max_chunks + c) * G + g;
@@ -371,11 +371,8 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
       const int64_t slot0 = (static_cast<int64_t>(s0) * P + p) * a.num_kv_heads + h;
       done = take_ticket(a.ws_cnt + slot0, nchunks);
       if (done) {
-        for (int tok = s0; tok < s1; ++tok) {
-          const int64_t slot = (static_cast<int64_t>(tok) * P + p) * a.num_kv_heads + h;
-          const int64_t orow0 = (static_cast<int64_t>(p) * a.num_tokens + tok) * a.num_q_heads + h * G;
-          merge_chunks(a, slot, nchunks, G, D, a.o_part + orow0 * D, a.lse_part + orow0);
-        }
+        merge_chunks(a, p, h, s0, s1 - s0, slot0, static_cast<int64_t>(P) * a.num_kv_heads, nchunks, G, D,
+                     reinterpret_cast<float*>(sKV), kXStages * Lt::STAGE / 4);
         if (tid == 0) a.ws_cnt[slot0] = 0;
       }
     }
@@ -383,7 +380,7 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
       // fused: the last of the P partners of (segment, KV head) merges them
       int32_t* pair = a.ws_pair + static_cast<int64_t>(s0) * a.num_kv_heads + h;
       if (take_ticket(pair, P)) {
-        for (int tok = s0; tok < s1; ++tok) merge_partners(a, tok, h, G, D, reinterpret_cast<float*>(sKV));
+        merge_partners(a, s0, s1 - s0, h, G, D, reinterpret_cast<float*>(sKV), kXStages * Lt::STAGE / 4);
         if (tid == 0) *pair = 0;
       }
     }

@@ -385,7 +385,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(cons
     merge_stored<D, G>(sm, NW, g, d, out, lse);
     if (single) {
       a.o_part[(orow0 + g) * D + d] = out;
-      if (d == 0) a.lse_part[orow0 + g] = lse;
+      if (d == 0) a.lse_part[lse_slot(a, p, t, h * G + g)] = lse;
     } else {
       const int64_t wrow = (slot * a.max_chunks + c) * G + g;
       a.ws_o[wrow * D + d] = out;
@@ -394,10 +394,10 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(cons
   }
   if (!single) {
     if (!take_ticket(a.ws_cnt + slot, nchunks)) return;
-    merge_chunks(a, slot, nchunks, G, D, a.o_part + orow0 * D, a.lse_part + orow0);
+    merge_chunks(a, p, h, t, 1, slot, 0, nchunks, G, D, sm, static_cast<int>(SM::MAIN / 4));
     if (threadIdx.x == 0) a.ws_cnt[slot] = 0;  // ready for the next call
   }
-  if (a.fused) pair_finish(a, t, h, G, D, sm);
+  if (a.fused) pair_finish(a, t, h, G, D, sm, static_cast<int>(SM::MAIN / 4));
 }
 
 template <int D, int G, bool F8>

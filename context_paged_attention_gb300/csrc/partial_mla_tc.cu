@@ -118,8 +118,8 @@ __global__ void __launch_bounds__(128, 1)
   if (ntiles == 0) {  // empty stripe (or padding token): 0 / -inf
     float4* dst = reinterpret_cast<float4*>(a.o_part + orow * kDv);
     for (int e = 0; e < kDv / 4; ++e) dst[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-    a.lse_part[orow] = -INFINITY;
-    if (a.fused) pair_finish(a, t, 0, kHeads, kDv, reinterpret_cast<float*>(sQ));
+    a.lse_part[lse_slot(a, p, t, tid)] = -INFINITY;
+    if (a.fused) pair_finish(a, t, 0, kHeads, kDv, reinterpret_cast<float*>(sQ), kQBytes / 4);
     return;
   }
 
@@ -415,7 +415,7 @@ __global__ void __launch_bounds__(128, 1)
         d4[e] = make_float4(tail[4 * e] * inv, tail[4 * e + 1] * inv, tail[4 * e + 2] * inv, tail[4 * e + 3] * inv);
     }
     if (single) {
-      a.lse_part[orow] = lse;
+      a.lse_part[lse_slot(a, p, t, tid)] = lse;
     } else {
       a.ws_lse[(slot * a.max_chunks + c) * kHeads + tid] = lse;
     }
@@ -427,10 +427,10 @@ __global__ void __launch_bounds__(128, 1)
   if (nchunks > 1) {
     if (!take_ticket(a.ws_cnt + slot, nchunks)) return;
     const int64_t orow0 = (static_cast<int64_t>(p) * a.num_tokens + t) * a.num_q_heads;
-    merge_chunks(a, slot, nchunks, kHeads, kDv, a.o_part + orow0 * kDv, a.lse_part + orow0);
+    merge_chunks(a, p, 0, t, 1, slot, 0, nchunks, kHeads, kDv, reinterpret_cast<float*>(sQ), kQBytes / 4);
     if (tid == 0) a.ws_cnt[slot] = 0;
   }
-  if (a.fused) pair_finish(a, t, 0, kHeads, kDv, reinterpret_cast<float*>(sQ));
+  if (a.fused) pair_finish(a, t, 0, kHeads, kDv, reinterpret_cast<float*>(sQ), kQBytes / 4);
 }
 
 int mla_tc_chunk(int ps_l) {

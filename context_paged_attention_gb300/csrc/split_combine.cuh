@@ -21,6 +21,11 @@
 
 namespace cpattn {
 
+// Index of the LSE of (partner p, token t, query head hq) in lse_part.
+__device__ __forceinline__ int64_t lse_slot(const PartialArgs& a, int p, int t, int hq) {
+  return p * a.lse_sp + t * a.lse_st + hq * a.lse_sh;
+}
+
 // Returns true in every thread of the CTA that must do the final merge.
 // Call after this CTA's workspace stores; all threads must call it.  The
 // barrier orders every thread's stores before thread 0's device-scope fence,
@@ -40,136 +45,151 @@ __device__ __forceinline__ bool take_ticket(int32_t* counter, int arrivals_neede
   return s_last != 0;
 }
 
-// Merge nchunks workspace partials of one (token, partner, KV head) slot.
-// ws rows: (slot * max_chunks + chunk) * Hg + head, each Dv floats.
-// Output rows: o_row0 + head (rows of Dv floats), lse at lse_row0 + head.
-__device__ __forceinline__ void merge_chunks(const PartialArgs& a, int64_t slot, int nchunks, int Hg,
-                                             int Dv, float* o_out, float* lse_out) {
-  for (int idx = threadIdx.x; idx < Hg * Dv; idx += blockDim.x) {
-    const int g = idx / Dv;
-    const int d = idx - g * Dv;
-    float mx = -INFINITY;
-    for (int c = 0; c < nchunks; ++c) mx = fmaxf(mx, __ldcg(a.ws_lse + (slot * a.max_chunks + c) * Hg + g));
-    float wsum = 0.f, acc = 0.f;
-    if (mx != -INFINITY) {
-      for (int c = 0; c < nchunks; ++c) {
-        const int64_t wrow = (slot * a.max_chunks + c) * Hg + g;
-        const float lc = __ldcg(a.ws_lse + wrow);
-        if (lc == -INFINITY) continue;  // empty chunk: its output row is not read
-        const float w = expf(lc - mx);
-        wsum += w;
-        acc = fmaf(w, __ldcg(a.ws_o + wrow * Dv + d), acc);
+// Exact merge of E partials for each of R rows of Dv values (the LSE merge
+// of lse_merge).  Row r, entry e: LSE lse_in(r, e) (-inf: empty, its values
+// are not read), values at o_in(r, e) (Dv floats, 16-byte aligned).  The
+// merged row goes to put(r, d, float4) for d = 0, 4, ..., its LSE to
+// put_lse(r, value).  In three phases, all threads busy in each:
+//   1. the R x E LSEs are loaded at once into a shared table;
+//   2. one warp per row turns them into weights exp(lse - max) / sum and the
+//      row's LSE with shuffle reductions;
+//   3. each thread sums weight * values over the entries for a float4 group
+//      of one row, the loads unrolled so several are in flight.
+// Rows go in batches that fit `scratch` (cap floats of shared memory the CTA
+// no longer uses; cap >= E + 1).  All threads of the CTA must call.
+template <class LseIn, class OIn, class Put, class PutLse>
+__device__ __forceinline__ void merge_rows(int R, int E, int Dv, LseIn lse_in, OIn o_in, Put put, PutLse put_lse,
+                                           float* scratch, int cap) {
+  const int RB = max(1, min(R, cap / (E + 1)));
+  const int D4 = Dv / 4;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  for (int r0 = 0; r0 < R; r0 += RB) {
+    const int nr = min(RB, R - r0);
+    float* wt = scratch;              // [nr][E]
+    float* s_ok = scratch + nr * E;   // [nr]: 1 if the row has keys
+    __syncthreads();  // the scratch may still be read from the previous batch or caller
+    for (int idx = threadIdx.x; idx < nr * E; idx += blockDim.x) wt[idx] = lse_in(r0 + idx / E, idx % E);
+    __syncthreads();
+    for (int r = warp; r < nr; r += nwarps) {
+      float mx = -INFINITY;
+      for (int e = lane; e < E; e += 32) mx = fmaxf(mx, wt[r * E + e]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      float sum = 0.f;
+      for (int e = lane; e < E; e += 32) {
+        const float l = wt[r * E + e];
+        sum += (mx == -INFINITY || l == -INFINITY) ? 0.f : expf(l - mx);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      const bool empty = (sum == 0.f);
+      const float inv = empty ? 0.f : 1.f / sum;
+      __syncwarp();
+      for (int e = lane; e < E; e += 32) {
+        const float l = wt[r * E + e];
+        wt[r * E + e] = (empty || l == -INFINITY) ? 0.f : expf(l - mx) * inv;
+      }
+      if (lane == 0) {
+        s_ok[r] = empty ? 0.f : 1.f;
+        put_lse(r0 + r, empty ? -INFINITY : mx + logf(sum));
       }
     }
-    const bool empty = (wsum == 0.f);
-    o_out[static_cast<int64_t>(g) * Dv + d] = empty ? 0.f : acc / wsum;
-    if (d == 0) lse_out[g] = empty ? -INFINITY : mx + logf(wsum);
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < nr * D4; idx += blockDim.x) {
+      const int r = idx / D4;
+      const int d = (idx - r * D4) * 4;
+      const float* wr = wt + r * E;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+      for (int e = 0; e < E; ++e) {
+        const float w = wr[e];
+        if (w != 0.f) {  // empty partials' rows are never read
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(o_in(r0 + r, e) + d));
+          acc.x = fmaf(w, v.x, acc.x);
+          acc.y = fmaf(w, v.y, acc.y);
+          acc.z = fmaf(w, v.z, acc.z);
+          acc.w = fmaf(w, v.w, acc.w);
+        }
+      }
+      put(r0 + r, d, acc);
+    }
   }
 }
 
-// Shared-memory floats merge_partners needs: the Hg x (P + 1) weight table
-// and one value per head.
-__host__ __device__ __forceinline__ int merge_scratch_floats(int Hg, int P) { return Hg * (P + 1) + Hg; }
+// Merge the nchunks workspace partials of ntok consecutive tokens of one
+// (partner p, KV head h): token i's slot is slot0 + i * slot_step; ws rows
+// (slot * max_chunks + chunk) * Hg + head, Dv floats each.  Results go to the
+// partner partial o_part / lse_part of tokens t0 .. t0 + ntok - 1.
+__device__ __forceinline__ void merge_chunks(const PartialArgs& a, int p, int h, int t0, int ntok, int64_t slot0,
+                                             int64_t slot_step, int nchunks, int Hg, int Dv, float* scratch,
+                                             int cap) {
+  auto wrow = [&](int r, int e) -> int64_t {
+    const int i = r / Hg;
+    return ((slot0 + i * slot_step) * a.max_chunks + e) * Hg + (r - i * Hg);
+  };
+  merge_rows(
+      ntok * Hg, nchunks, Dv, [&](int r, int e) { return __ldcg(a.ws_lse + wrow(r, e)); },
+      [&](int r, int e) { return a.ws_o + wrow(r, e) * Dv; },
+      [&](int r, int d, float4 v) {
+        const int i = r / Hg;
+        const int64_t orow = (static_cast<int64_t>(p) * a.num_tokens + t0 + i) * a.num_q_heads + h * Hg + (r - i * Hg);
+        *reinterpret_cast<float4*>(a.o_part + orow * Dv + d) = v;
+      },
+      [&](int r, float l) {
+        const int i = r / Hg;
+        a.lse_part[lse_slot(a, p, t0 + i, h * Hg + (r - i * Hg))] = l;
+      },
+      scratch, cap);
+}
 
-// Final output of (token t, KV head h) from the P partner partials (o_part /
-// lse_part rows, which fused calls keep in the workspace) and the optional
-// extra partial; written as bf16 (round to nearest even) or fp32.
-//   1. all threads load the entries' LSEs at once into a [Hg][P + 1] table;
-//   2. one warp per head turns them into weights exp(lse - max) and the
-//      head's LSE with shuffle reductions;
-//   3. each thread sums weight * row over the entries for a float4 group of
-//      value dims.
-// scratch: merge_scratch_floats(Hg, P) floats of shared memory the CTA no
-// longer uses.  Dv % 4 == 0.
-__device__ __forceinline__ void merge_partners(const PartialArgs& a, int t, int h, int Hg, int Dv, float* scratch) {
-  const int E = a.P + 1;
-  float* wt = scratch;              // [Hg][E]
-  float* s_inv = scratch + Hg * E;  // [Hg]
-  const int64_t hq0 = static_cast<int64_t>(t) * a.num_q_heads + h * Hg;  // first query-head row of the pair
+// Final output of tokens t0 .. t0 + ntok - 1 for KV head h from the P
+// partner partials (o_part / lse_part rows, which fused calls keep in the
+// workspace) and the optional extra partial (entry P); written as bf16
+// (round to nearest even) or fp32.  Row r = token t0 + r / Hg, head r % Hg.
+__device__ __forceinline__ void merge_partners(const PartialArgs& a, int t0, int ntok, int h, int Hg, int Dv,
+                                               float* scratch, int cap) {
   const int64_t pstride = static_cast<int64_t>(a.num_tokens) * a.num_q_heads;  // rows between partners
-  __syncthreads();  // the scratch may still be read from a previous token
-  for (int idx = threadIdx.x; idx < Hg * E; idx += blockDim.x) {
-    const int g = idx / E;
-    const int e = idx - g * E;
-    float lse = -INFINITY;
-    if (e == E - 1) {
-      if (a.extra_lse != nullptr) lse = __ldg(a.extra_lse + hq0 + g);
-    } else {
-      lse = __ldcg(a.lse_part + e * pstride + hq0 + g);
-    }
-    wt[idx] = lse;
-  }
-  __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-  for (int g = warp; g < Hg; g += nwarps) {
-    float mx = -INFINITY;
-    for (int e = lane; e < E; e += 32) mx = fmaxf(mx, wt[g * E + e]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    float sum = 0.f;
-    for (int e = lane; e < E; e += 32) {
-      const float l = wt[g * E + e];
-      const float w = (mx == -INFINITY || l == -INFINITY) ? 0.f : expf(l - mx);
-      wt[g * E + e] = w;
-      sum += w;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (lane == 0) {
-      const bool empty = (sum == 0.f);
-      s_inv[g] = empty ? 0.f : 1.f / sum;
-      if (a.lse_out != nullptr) a.lse_out[hq0 + g] = empty ? -INFINITY : mx + logf(sum);
-    }
-  }
-  __syncthreads();
-  const int D4 = Dv / 4;
-  for (int idx = threadIdx.x; idx < Hg * D4; idx += blockDim.x) {
-    const int g = idx / D4;
-    const int d = (idx - g * D4) * 4;
-    const float* wg = wt + g * E;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int e = 0; e < E - 1; ++e) {
-      const float w = wg[e];
-      if (w != 0.f) {  // empty partials' rows are not read
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(a.o_part + (e * pstride + hq0 + g) * Dv + d));
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
-      }
-    }
-    if (wg[E - 1] != 0.f) {
-      const float w = wg[E - 1];
-      const float4 v = __ldg(reinterpret_cast<const float4*>(a.extra_o + (hq0 + g) * Dv + d));
-      acc.x = fmaf(w, v.x, acc.x);
-      acc.y = fmaf(w, v.y, acc.y);
-      acc.z = fmaf(w, v.z, acc.z);
-      acc.w = fmaf(w, v.w, acc.w);
-    }
-    const float inv = s_inv[g];
-    const int64_t oi = (hq0 + g) * Dv + d;
-    if (a.out_bf16) {
-      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-      __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-      uint2 pk;
-      pk.x = *reinterpret_cast<uint32_t*>(&lo);
-      pk.y = *reinterpret_cast<uint32_t*>(&hi);
-      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + oi) = pk;
-    } else {
-      *reinterpret_cast<float4*>(static_cast<float*>(a.out) + oi) =
-          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-    }
-  }
+  const int E = a.P + (a.extra_lse != nullptr ? 1 : 0);
+  // query-head row (token * Hq + head) of merge row r
+  auto hq = [&](int r) -> int64_t {
+    const int i = r / Hg;
+    return static_cast<int64_t>(t0 + i) * a.num_q_heads + h * Hg + (r - i * Hg);
+  };
+  merge_rows(
+      ntok * Hg, E, Dv,
+      [&](int r, int e) {
+        const int i = r / Hg;
+        return e < a.P ? __ldcg(a.lse_part + lse_slot(a, e, t0 + i, h * Hg + (r - i * Hg)))
+                       : __ldg(a.extra_lse + hq(r));
+      },
+      [&](int r, int e) { return e < a.P ? a.o_part + (e * pstride + hq(r)) * Dv : a.extra_o + hq(r) * Dv; },
+      [&](int r, int d, float4 v) {
+        const int64_t oi = hq(r) * Dv + d;
+        if (a.out_bf16) {
+          __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+          __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+          uint2 pk;
+          pk.x = *reinterpret_cast<uint32_t*>(&lo);
+          pk.y = *reinterpret_cast<uint32_t*>(&hi);
+          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + oi) = pk;
+        } else {
+          *reinterpret_cast<float4*>(static_cast<float*>(a.out) + oi) = v;
+        }
+      },
+      [&](int r, float l) {
+        if (a.lse_out != nullptr) a.lse_out[hq(r)] = l;
+      },
+      scratch, cap);
 }
 
 // Fused calls, after a partner's partial of (token t, KV head h) is complete
 // in o_part (written directly, or merged from its chunks by this CTA): arrive
 // on the pair's ticket; the last of the P partners merges (all threads call).
-__device__ __forceinline__ void pair_finish(const PartialArgs& a, int t, int h, int Hg, int Dv, float* scratch) {
+__device__ __forceinline__ void pair_finish(const PartialArgs& a, int t, int h, int Hg, int Dv, float* scratch,
+                                            int cap) {
   int32_t* pair = a.ws_pair + static_cast<int64_t>(t) * a.num_kv_heads + h;
   if (!take_ticket(pair, a.P)) return;
-  merge_partners(a, t, h, Hg, Dv, scratch);
+  merge_partners(a, t, 1, h, Hg, Dv, scratch, cap);
   if (threadIdx.x == 0) *pair = 0;
 }
 

@@ -152,6 +152,51 @@ class StripedAttention:
         self.fused(stream, out, lse)
         return (self.out if out is None else out), (self.lse if lse is None else lse)
 
+    # -- TP-mode head layout (vLLM _forward_with_dcp): every partner attends the
+    # gathered query heads of all P ranks; its LSE comes head-major ([H, B]);
+    # rank r then combines the partners' partials of its own head slice and
+    # merges the result with its own-token partial.
+    def run_step_tp(self, stream=None, out=None, lse=None):
+        w = self.w
+        P, T, Hq, Dv = w.P, w.num_tokens, w.num_q_heads, w.head_dim_v
+        if Hq % P != 0:
+            raise ValueError("TP mode needs the query heads to split evenly over the P ranks")
+        Hl = Hq // P
+        out = self.out if out is None else out
+        lse = self.lse if lse is None else lse
+        if getattr(self, "_lse_hm", None) is None:
+            self._lse_hm = torch.empty((P, Hq, T), dtype=torch.float32, device=self.device)
+            self._cor = torch.empty((P, T, Hl, Dv), dtype=torch.float32, device=self.device)
+            self._lse_cor = torch.empty((P, Hl, T), dtype=torch.float32, device=self.device)
+        one_per_row = w.decode and w.num_tokens == w.num_rows
+        self.write_new(stream)
+        B.cp_paged_attn_partial_ex(self.desc, self.pool_k, self.pool_v, self.q, self.kv_len, self.max_kv_len,
+                                   self.page_indptr, self.page_indices, w.scale, self.o_parts[:P], self._lse_hm,
+                                   self.workspace, lse_layout=B.LSE_HEAD_MAJOR,
+                                   qo_indptr=None if one_per_row else self.qo_indptr, num_rows=w.num_rows,
+                                   dev_status=self.dev_status, stream=stream)
+        if not w.decode:
+            self.own(stream)
+        for r in range(P):
+            # dcp_combine for rank r: the P partners' rows of heads [r*Hl, (r+1)*Hl)
+            views = [B.view(self.o_parts, self._lse_hm, Hq * Dv, Dv, 1, T,
+                            o_offset=(p * T * Hq + r * Hl) * Dv, lse_offset=(p * Hq + r * Hl) * T)
+                     for p in range(P)]
+            if w.decode:  # no own-token partial: the combine is the rank's output
+                B.lse_merge_views(views, T, Hl, Dv, out, Hq * Dv, Dv, lse, Hq, 1, out_offset=r * Hl * Dv,
+                                  lse_out_offset=r * Hl, stream=stream)
+                continue
+            B.lse_merge_views(views, T, Hl, Dv, self._cor, Hl * Dv, Dv, self._lse_cor, 1, T,
+                              out_offset=r * T * Hl * Dv, lse_out_offset=r * Hl * T, stream=stream)
+            # merge_attn_states(context, own query partial) for the rank's heads
+            final = [B.view(self._cor, self._lse_cor, Hl * Dv, Dv, 1, T, o_offset=r * T * Hl * Dv,
+                            lse_offset=r * Hl * T),
+                     B.view(self.o_parts, self.lse_parts, Hq * Dv, Dv, Hq, 1, o_offset=(P * T * Hq + r * Hl) * Dv,
+                            lse_offset=P * T * Hq + r * Hl)]
+            B.lse_merge_views(final, T, Hl, Dv, out, Hq * Dv, Dv, lse, Hq, 1, out_offset=r * Hl * Dv,
+                              lse_out_offset=r * Hl, stream=stream)
+        return out, lse
+
     def capture(self):
         """Record the fused step into a CUDA graph over this object's buffers
         (a captured bucket: later steps refill the same inputs and replay)."""

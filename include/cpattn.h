@@ -196,6 +196,30 @@ CPATTN_API int cp_paged_attn_partial(const cpattn_pool_desc* desc, const void* p
 CPATTN_API size_t cp_paged_attn_workspace_bytes(const cpattn_pool_desc* desc, int32_t num_q_heads,
                                      int32_t num_tokens, int32_t max_kv_len);
 
+/* LSE layouts of cp_paged_attn_partial_ex's lse_part */
+#define CPATTN_LSE_TOKEN_MAJOR 0 /* [P][num_tokens][num_q_heads] (as cp_paged_attn_partial) */
+#define CPATTN_LSE_HEAD_MAJOR 1  /* [P][num_q_heads][num_tokens] */
+
+/*
+ * cp_paged_attn_partial_ex -- cp_paged_attn_partial with a choice of LSE
+ * layout.  In the vLLM page "[Core] Add explicit layer parallel plans"
+ * (_forward_with_dcp) the context attention returns its LSE head-major
+ * ("[H, B]") while the DCP combine takes it token-major ("[B, H]"); a TP-mode
+ * caller gathers the query heads of all partners (query_across_dcp), has each
+ * partner attend all of them, and combines per head.  lse_layout selects
+ * CPATTN_LSE_TOKEN_MAJOR or CPATTN_LSE_HEAD_MAJOR (anything else:
+ * CPATTN_ERR_INVALID_ARG); every other argument is as for
+ * cp_paged_attn_partial, and the values written are the same.
+ */
+CPATTN_API int cp_paged_attn_partial_ex(const cpattn_pool_desc* desc, const void* pool_k,
+                                        const void* pool_v, const void* q, int32_t num_q_heads,
+                                        int32_t num_rows, int32_t num_tokens, const int32_t* qo_indptr,
+                                        const int32_t* kv_len, int32_t max_kv_len,
+                                        const int32_t* kv_page_indptr, const int32_t* kv_page_indices,
+                                        float scale, float* o_part, float* lse_part, int32_t lse_layout,
+                                        void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                        cudaStream_t stream);
+
 /*
  * cp_paged_attn_fused -- the partials of all P partners and their exact merge
  * in one launch: the final attention output of every query token.
@@ -328,6 +352,41 @@ CPATTN_API int lse_merge(int32_t num_partials, const float* o_parts, const float
               int64_t stride_o, int64_t stride_lse, int32_t num_tokens, int32_t num_heads,
               int32_t head_dim_v, int32_t out_dtype, void* out, float* lse_out,
               cudaStream_t stream);
+
+/* One partial as a strided view: the output row of (token t, head h) is the
+ * head_dim_v fp32 values at o + t * o_stride_token + h * o_stride_head; its
+ * natural-log LSE is lse[t * lse_stride_token + h * lse_stride_head].  Strides
+ * count elements; o and its strides must keep rows 16-byte aligned. */
+typedef struct cpattn_partial_view {
+  const float* o;
+  const float* lse;
+  int64_t o_stride_token, o_stride_head;
+  int64_t lse_stride_token, lse_stride_head;
+} cpattn_partial_view;
+
+#define CPATTN_MAX_MERGE_VIEWS 16
+
+/*
+ * lse_merge_views -- lse_merge over partials of any layout.
+ *
+ * Same exact merge as lse_merge (mstar PR #1124 "Context / Sequence Parallel
+ * 1/5", description; vLLM _forward_with_dcp, merge_attn_states), but each of
+ * the num_views (1 .. CPATTN_MAX_MERGE_VIEWS) partials is a strided view (a
+ * HOST array of cpattn_partial_view read during the call; the pointers in it
+ * are device memory), and the output row of (t, h) goes to out + t *
+ * out_stride_token + h * out_stride_head (elements of out_dtype), its LSE to
+ * lse_out[t * lse_out_stride_token + h * lse_out_stride_head] (lse_out may be
+ * NULL).  With it a TP-mode caller combines the partners' partials of one
+ * rank's head slice from head-major LSEs, writes the rank's slice of the
+ * output, and merges the context result with the own-token partial without
+ * copies.  Views may not overlap the output.  Errors: bad counts or dims
+ * (CPATTN_ERR_INVALID_ARG), rows not 16-byte aligned (CPATTN_ERR_MISALIGNED).
+ */
+CPATTN_API int lse_merge_views(int32_t num_views, const cpattn_partial_view* views, int32_t num_tokens,
+                               int32_t num_heads, int32_t head_dim_v, int32_t out_dtype, void* out,
+                               int64_t out_stride_token, int64_t out_stride_head, float* lse_out,
+                               int64_t lse_out_stride_token, int64_t lse_out_stride_head,
+                               cudaStream_t stream);
 
 #ifdef __cplusplus
 }  /* extern "C" */

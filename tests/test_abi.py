@@ -166,6 +166,28 @@ def test_fused_argument_checks(lib):
                                    0.1, None, None, 0, FAKE, None, FAKE, fused - 1, None, None) == -5
 
 
+def test_partial_ex_and_view_checks(lib):
+    d = _desc()
+    # LSE layouts 0 (token-major) and 1 (head-major) only
+    assert lib.cp_paged_attn_partial_ex(ctypes.byref(d), FAKE, FAKE, FAKE, 32, 1, 1, None, FAKE, 100, FAKE, FAKE,
+                                        0.1, FAKE, FAKE, 2, FAKE, 1 << 30, None, None) == -1
+    V = B.PartialView
+    good = V(FAKE, FAKE, 512, 128, 4, 1)
+    arr = (V * 17)(*([good] * 17))
+    assert lib.lse_merge_views(0, arr, 4, 4, 128, 0, FAKE, 512, 128, None, 0, 0, None) == -1
+    assert lib.lse_merge_views(17, arr, 4, 4, 128, 0, FAKE, 512, 128, None, 0, 0, None) == -1  # > 16 views
+    assert lib.lse_merge_views(1, arr, 4, 4, 126, 0, FAKE, 512, 128, None, 0, 0, None) == -1  # dv % 4
+    assert lib.lse_merge_views(1, arr, 4, 4, 128, 5, FAKE, 512, 128, None, 0, 0, None) == -1  # out type
+    bad = (V * 1)(V(FAKE + 4, FAKE, 512, 128, 4, 1))
+    assert lib.lse_merge_views(1, bad, 4, 4, 128, 0, FAKE, 512, 128, None, 0, 0, None) == -4  # row not 16-B aligned
+    bad = (V * 1)(V(FAKE, FAKE, 514, 128, 4, 1))
+    assert lib.lse_merge_views(1, bad, 4, 4, 128, 0, FAKE, 512, 128, None, 0, 0, None) == -4  # stride
+    assert lib.lse_merge_views(1, arr, 4, 4, 128, 0, FAKE, 510, 128, None, 0, 0, None) == -4  # out stride
+    nul = (V * 1)(V(FAKE, None, 512, 128, 4, 1))
+    assert lib.lse_merge_views(1, nul, 4, 4, 128, 0, FAKE, 512, 128, None, 0, 0, None) == -1
+    assert lib.lse_merge_views(1, arr, 0, 4, 128, 0, FAKE, 512, 128, None, 0, 0, None) == 0  # nothing to do
+
+
 def test_workspace_sizing(lib):
     d = _desc()
     small = lib.cp_paged_attn_workspace_bytes(ctypes.byref(d), 32, 64, 256)

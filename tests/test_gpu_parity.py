@@ -189,6 +189,45 @@ def test_fused_step_matches_oracle(small):
     assert_close(got_o, f64(att.out), tol_o, "fused vs partial + merge")
 
 
+def test_head_major_lse_partial(small):
+    """cp_paged_attn_partial_ex with [P][H][T] LSEs writes the same values."""
+    w, att = small
+    from context_paged_attention_gb300 import binding as B
+    P, T, Hq = w.P, w.num_tokens, w.num_q_heads
+    o = torch.empty_like(att.o_parts[:P])
+    l_hm = torch.empty((P, Hq, T), dtype=torch.float32, device=att.device)
+    one_per_row = w.decode and w.num_tokens == w.num_rows
+    B.cp_paged_attn_partial_ex(att.desc, att.pool_k, att.pool_v, att.q, att.kv_len, att.max_kv_len, att.page_indptr,
+                               att.page_indices, w.scale, o, l_hm, att.workspace, lse_layout=B.LSE_HEAD_MAJOR,
+                               qo_indptr=None if one_per_row else att.qo_indptr, num_rows=w.num_rows,
+                               dev_status=att.dev_status)
+    torch.cuda.synchronize()
+    assert att.status() == 0
+    assert torch.equal(o, att.o_parts[:P])
+    assert torch.equal(l_hm.transpose(1, 2), att.lse_parts[:P])
+
+
+def test_tp_mode_step(small):
+    """TP-mode head layout: per-rank combine of head slices from head-major
+    LSEs, then the own-token merge, equals the plain attention."""
+    w, att = small
+    if w.num_q_heads % w.P != 0:
+        pytest.skip("query heads do not split over the P ranks")
+    out = torch.empty_like(att.out)
+    lse = torch.empty_like(att.lse)
+    att.run_step_tp(out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert att.status() == 0
+    O, L = OracleView(w).final()
+    tol_o, tol_l = tolerances(w)
+    got_o = f64(out)
+    got_l = lse.cpu().numpy().astype(np.float64)
+    assert_close(got_o, O, tol_o, "TP-mode output")
+    assert_close_lse(got_l, L, tol_l, "TP-mode LSE")
+    t0 = int(w.qo_indptr[w.num_real_rows])
+    assert np.all(got_o[t0:] == 0) and np.all(got_l[t0:] == -np.inf)
+
+
 def test_own_token_partial(small):
     w, att = small
     if w.decode:
@@ -227,6 +266,43 @@ FULL = {
     "mla_decode": (W.mla_decode, [0, 7, 19, 31]),
     "mixed_step": (W.mixed_step, [0, 17, 47, 48, 55, 63]),
 }
+
+
+@pytest.mark.parametrize("n,layout", [(1, "th"), (3, "ht"), (5, "mixed"), (16, "mixed")])
+def test_lse_merge_views(n, layout):
+    """Strided-view merge against the oracle merge on random partials (some
+    empty), LSEs token- or head-major, output into a head slice."""
+    from context_paged_attention_gb300 import binding as B
+    rng = np.random.default_rng(n)
+    T, H, Dv = 37, 6, 64
+    O = rng.standard_normal((n, T, H, Dv))
+    L = rng.standard_normal((n, T, H)) * 3
+    L[rng.random((n, T, H)) < 0.2] = -np.inf
+    L[:, 5, :] = -np.inf  # a token with every partial empty
+    dev = torch.device("cuda")
+    o_d = torch.tensor(O, dtype=torch.float32, device=dev)
+    views, keep = [], []
+    for i in range(n):
+        hm = layout == "ht" or (layout == "mixed" and i % 2 == 1)
+        lt = torch.tensor(L[i].T.copy() if hm else L[i], dtype=torch.float32, device=dev)
+        keep.append(lt)
+        views.append(B.view(o_d, lt, H * Dv, Dv, 1 if hm else H, T if hm else 1, o_offset=i * T * H * Dv))
+    Hout = H + 2  # write heads 1 .. H of a wider output
+    out = torch.zeros((T, Hout, Dv), dtype=torch.float32, device=dev)
+    lse = torch.zeros((Hout, T), dtype=torch.float32, device=dev)  # head-major LSE out
+    B.lse_merge_views(views, T, H, Dv, out, Hout * Dv, Dv, lse, 1, T, out_offset=Dv, lse_out_offset=T)
+    torch.cuda.synchronize()
+    O32 = o_d.cpu().numpy().astype(np.float64)
+    L32 = np.asarray(L, dtype=np.float32).astype(np.float64)
+    want_o = np.zeros((T, H, Dv))
+    want_l = np.zeros((T, H))
+    for t in range(T):
+        want_o[t], want_l[t] = oracle.merge(O32[:, t], L32[:, t])
+    got_o = out.cpu().numpy().astype(np.float64)
+    got_l = lse.cpu().numpy().astype(np.float64)
+    assert_close(got_o[:, 1:H + 1], want_o, 1e-5, "merged view output")
+    assert_close_lse(got_l[1:H + 1].T, want_l, 1e-5, "merged view LSE")
+    assert np.all(got_o[:, 0] == 0) and np.all(got_o[:, H + 1] == 0) and np.all(got_l[0] == 0)
 
 
 @pytest.mark.parametrize("name", ["gqa_decode", "mixed_step", "mla_decode"])
