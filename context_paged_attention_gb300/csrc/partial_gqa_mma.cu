@@ -32,21 +32,27 @@ namespace cpattn {
 
 constexpr int kMmaWarps = 4;
 constexpr int kMmaStages = 3;
-constexpr int kMmaStagesF8 = 4;  // E4M3 pools: half the bytes a stage, one stage deeper
+constexpr int kMmaStagesF8 = 5;  // E4M3 pools: half the bytes a stage, deeper ring
 constexpr int kMmaKeys = 16;  // keys per stage
 
-// Shared memory of one CTA: the warps' cp.async rings of pool rows, then (E4M3
-// pools) each warp's float16 copy of the stage it works on.
+// Shared memory of one CTA: the warps' cp.async rings of pool rows.
 template <int D, bool F8>
 struct MmaSmem {
   static constexpr int NST = F8 ? kMmaStagesF8 : kMmaStages;
   static constexpr int SRC_ROWB = F8 ? D : 2 * D;                    // bytes of a pool row
   static constexpr int RING_STAGE = kMmaKeys * SRC_ROWB;             // K (or V) bytes per ring stage
-  static constexpr int STAGE16 = kMmaKeys * 2 * D;                   // K (or V) bytes of a 16-bit stage
-  static constexpr size_t RING = static_cast<size_t>(kMmaWarps) * NST * RING_STAGE * 2;
-  static constexpr size_t STAGING = F8 ? static_cast<size_t>(kMmaWarps) * STAGE16 * 2 : 0;
-  static constexpr size_t MAIN = RING + STAGING;
+  static constexpr size_t MAIN = static_cast<size_t>(kMmaWarps) * NST * RING_STAGE * 2;
 };
+
+// 16-byte chunk c of row r of a stage sits at chunk position swz(c, r), so
+// the 8 rows an ldmatrix phase reads hit distinct banks: bf16 rows (2 D
+// bytes) and E4M3 rows of 128 bytes XOR with r & 7; E4M3 rows of 64 bytes
+// (4 chunks) XOR with (r >> 1) & 3.
+template <int CHR>
+__device__ __forceinline__ int swz(int c, int r) {
+  if constexpr (CHR >= 8) return c ^ (r & 7);
+  else return c ^ ((r >> 1) & (CHR - 1));
+}
 
 template <int D, int G, bool F8>
 __global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(const PartialArgs a) {
@@ -54,12 +60,10 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(cons
   constexpr int NW = kMmaWarps;
   constexpr int NST = SM::NST;
   constexpr int KT = kMmaKeys;
-  constexpr int ROWB = D * 2;            // bytes of a 16-bit row (the MMA operand layout)
-  constexpr int CH = ROWB / 16;          // 16-byte chunks per 16-bit row
+  constexpr int ROWB = D * 2;            // bytes of a bf16 row (query rows)
   constexpr int SRC_ROWB = SM::SRC_ROWB;
   constexpr int SRC_CH = SRC_ROWB / 16;  // 16-byte chunks per pool row
   constexpr int RING_STAGE = SM::RING_STAGE;
-  constexpr int STAGE_B = SM::STAGE16;   // K (or V) bytes per 16-bit stage
   constexpr int KSTEPS = D / 16;
   constexpr int NT = D / 8;              // n-tiles of the output
   constexpr int ITERS = KT * SRC_CH / 32;  // cp.async rounds per stage
@@ -114,12 +118,17 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(cons
     const bool r1ok = b >= 0 && quad + 8 < G;
 #pragma unroll
     for (int s = 0; s < KSTEPS; ++s) {
-      const int w0 = s * 8 + qi;  // word of dims (16s + 2qi, +1)
+      // bf16: MMA k index = dim (words of dims 16s + 2qi, +1 and +8, +9).
+      // E4M3: the K fragment comes from an ldmatrix of code bytes, whose k
+      // order is dims 16s + 4qi, +1 (k 2qi, 2qi+1) and +2, +3 (k 2qi+8, +9);
+      // the query takes the same order (float16 operands).
+      const int w0 = F8 ? s * 8 + 2 * qi : s * 8 + qi;
+      const int w1 = F8 ? w0 + 1 : w0 + 4;
       qa[s][0] = r0ok ? __ldg(qw + quad * (D / 2) + w0) : 0u;
       qa[s][1] = r1ok ? __ldg(qw + (quad + 8) * (D / 2) + w0) : 0u;
-      qa[s][2] = r0ok ? __ldg(qw + quad * (D / 2) + w0 + 4) : 0u;
-      qa[s][3] = r1ok ? __ldg(qw + (quad + 8) * (D / 2) + w0 + 4) : 0u;
-      if constexpr (F8) {  // E4M3 pools: the MMAs run on float16 operands
+      qa[s][2] = r0ok ? __ldg(qw + quad * (D / 2) + w1) : 0u;
+      qa[s][3] = r1ok ? __ldg(qw + (quad + 8) * (D / 2) + w1) : 0u;
+      if constexpr (F8) {
 #pragma unroll
         for (int r = 0; r < 4; ++r) qa[s][r] = bf16x2_to_f16x2(qa[s][r]);
       }
@@ -127,7 +136,6 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(cons
   }
 
   uint8_t* ring = smem + static_cast<size_t>(warp) * NST * RING_STAGE * 2;
-  uint8_t* stage16 = smem + SM::RING + static_cast<size_t>(warp) * STAGE_B * 2;  // E4M3 pools only
   const uint8_t* poolk = static_cast<const uint8_t*>(a.pool_k);
   const uint8_t* poolv = static_cast<const uint8_t*>(a.pool_v);
 
@@ -184,8 +192,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(cons
         const int key = idx / SRC_CH;
         const int ch = idx - key * SRC_CH;
         const int64_t row = __shfl_sync(0xffffffffu, myrow, key);
-        // bf16: the MMA layout directly; E4M3: plain rows, converted per stage
-        const int soff = F8 ? idx * 16 : (key * CH + (ch ^ (key & 7))) * 16;
+        const int soff = (key * SRC_CH + swz<SRC_CH>(ch, key)) * 16;
         if (row >= 0) {
           cp_async16(sk + soff, poolk + row * SRC_ROWB + ch * 16);
           cp_async16(sv + soff, poolv + row * SRC_ROWB + ch * 16);
@@ -213,32 +220,8 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(cons
     __syncwarp();
     issue(i + NST - 1);  // refills the stage consumed in step i - 1
 
-    uint32_t sk, sv;
-    if constexpr (F8) {
-      // the stage's E4M3 codes -> float16 rows in the MMA layout (exact)
-      const uint8_t* rk = ring + (i % NST) * RING_STAGE * 2;
-#pragma unroll
-      for (int it = 0; it < 2 * ITERS; ++it) {
-        const int x = it * 32 + lane;          // K chunks, then V chunks
-        const int kv = x / (KT * SRC_CH);
-        const int idx = x - kv * (KT * SRC_CH);
-        const int key = idx / SRC_CH;
-        const int c8 = idx - key * SRC_CH;     // 16 codes: dims 16 c8 .. 16 c8 + 15
-        const uint4 w = *reinterpret_cast<const uint4*>(rk + kv * RING_STAGE + idx * 16);
-        uint8_t* dst = stage16 + kv * STAGE_B + key * CH * 16;
-        const uint4 h0 = make_uint4(e4m3x2_to_f16x2(w.x), e4m3x2_to_f16x2(w.x >> 16), e4m3x2_to_f16x2(w.y),
-                                    e4m3x2_to_f16x2(w.y >> 16));
-        const uint4 h1 = make_uint4(e4m3x2_to_f16x2(w.z), e4m3x2_to_f16x2(w.z >> 16), e4m3x2_to_f16x2(w.w),
-                                    e4m3x2_to_f16x2(w.w >> 16));
-        *reinterpret_cast<uint4*>(dst + ((2 * c8) ^ (key & 7)) * 16) = h0;
-        *reinterpret_cast<uint4*>(dst + ((2 * c8 + 1) ^ (key & 7)) * 16) = h1;
-      }
-      __syncwarp();
-      sk = smem_u32(stage16);
-    } else {
-      sk = smem_u32(ring + (i % NST) * RING_STAGE * 2);
-    }
-    sv = sk + STAGE_B;
+    const uint32_t sk = smem_u32(ring + (i % NST) * RING_STAGE * 2);
+    const uint32_t sv = sk + RING_STAGE;
     const uint32_t vm = s_vmask[warp][i % NST];
 
     // S = Q K^T for the 16 keys (two n-tiles), even / odd k-steps in two MMA chains
@@ -247,16 +230,33 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(cons
     for (int j = 0; j < 2; ++j)
 #pragma unroll
       for (int e = 0; e < 4; ++e) s[j][e] = s_alt[j][e] = 0.f;
+    if constexpr (F8) {
+      // one ldmatrix.x4 of code bytes: keys 0-7 / 8-15 x chunks s2, s2 + 1
+      // (a 16-byte chunk of E4M3 codes is one 16-dim k-step); each register's
+      // 4 codes become the b0 / b1 float16 pairs of that k-step
+      const int key = (mi & 1) * 8 + mrow;
 #pragma unroll
-    for (int s2 = 0; s2 < KSTEPS; s2 += 2) {
+      for (int s2 = 0; s2 < KSTEPS; s2 += 2) {
+        const int ch = s2 + (mi >> 1);
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4(sk + (key * SRC_CH + swz<SRC_CH>(ch, key)) * 16, r0, r1, r2, r3);
+        mma_f16(s[0], qa[s2], e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r0 >> 16));
+        mma_f16(s[1], qa[s2], e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r1 >> 16));
+        mma_f16(s_alt[0], qa[s2 + 1], e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r2 >> 16));
+        mma_f16(s_alt[1], qa[s2 + 1], e4m3x2_to_f16x2(r3), e4m3x2_to_f16x2(r3 >> 16));
+      }
+    } else {
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int key = j * 8 + mrow;
-        const int ch = s2 * 2 + mi;  // chunks 2*s2 .. 2*s2+3 cover k-steps s2, s2+1
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(sk + (key * CH + (ch ^ (key & 7))) * 16, b0, b1, b2, b3);
-        mma16<F8>(s[j], qa[s2], b0, b1);
-        mma16<F8>(s_alt[j], qa[s2 + 1], b2, b3);
+      for (int s2 = 0; s2 < KSTEPS; s2 += 2) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int key = j * 8 + mrow;
+          const int ch = s2 * 2 + mi;  // chunks 2*s2 .. 2*s2+3 cover k-steps s2, s2+1
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(sk + (key * SRC_CH + swz<SRC_CH>(ch, key)) * 16, b0, b1, b2, b3);
+          mma_bf16(s[j], qa[s2], b0, b1);
+          mma_bf16(s_alt[j], qa[s2 + 1], b2, b3);
+        }
       }
     }
     // mask keys past the stripe end (or on a rejected page), scale into the log2 domain
@@ -306,26 +306,51 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(cons
       split16<F8>(p10, p11, pa[2], pl[2]);
       split16<F8>(p12, p13, pa[3], pl[3]);
     }
-    // O += P V  (V rows via ldmatrix.trans: two n-tiles of 8 dims per instruction)
-    {
-      const int key = (mi & 1) * 8 + mrow;
+    // O += P V  (V rows via ldmatrix.trans)
+    const int vkey = (mi & 1) * 8 + mrow;
+    if constexpr (F8) {
+      // ldmatrix.trans of code bytes: matrices keys 0-7 / 8-15 x chunks ch,
+      // ch + 1 (16 dims each); a register holds keys (2qi, 2qi+1) of the
+      // code pairs of dims 2n, 2n+1 (n = lane / 4), so its even bytes are
+      // the b pair of dim 2n and its odd bytes that of dim 2n + 1: n-tile
+      // 2 ch gathers a chunk's even dims, n-tile 2 ch + 1 its odd dims
+#pragma unroll
+      for (int ch0 = 0; ch0 < SRC_CH; ch0 += 2) {
+        const int ch = ch0 + (mi >> 1);
+        uint32_t r[4];
+        ldsm_x4_t(sv + (vkey * SRC_CH + swz<SRC_CH>(ch, vkey)) * 16, r[0], r[1], r[2], r[3]);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {  // chunk ch0 + hh: registers 2 hh (keys 0-7), 2 hh + 1 (keys 8-15)
+          const uint32_t lo = r[2 * hh], hi = r[2 * hh + 1];
+          const uint32_t ev0 = e4m3x2_to_f16x2(__byte_perm(lo, 0u, 0x4420u));
+          const uint32_t ev1 = e4m3x2_to_f16x2(__byte_perm(hi, 0u, 0x4420u));
+          const uint32_t od0 = e4m3x2_to_f16x2(__byte_perm(lo, 0u, 0x4431u));
+          const uint32_t od1 = e4m3x2_to_f16x2(__byte_perm(hi, 0u, 0x4431u));
+          const int u = 2 * (ch0 + hh);
+          mma_f16(o[u], pa, ev0, ev1);
+          mma_f16(o[u + 1], pa, od0, od1);
+          mma_f16(o[u], pl, ev0, ev1);
+          mma_f16(o[u + 1], pl, od0, od1);
+        }
+      }
+    } else {
 #pragma unroll
       for (int u = 0; u < NT; u += 4) {
         uint32_t bv[2][4];
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           const int ch = u + 2 * hh + (mi >> 1);  // 16-byte chunk = 8-dim group
-          ldsm_x4_t(sv + (key * CH + (ch ^ (key & 7))) * 16, bv[hh][0], bv[hh][1], bv[hh][2], bv[hh][3]);
+          ldsm_x4_t(sv + (vkey * SRC_CH + swz<SRC_CH>(ch, vkey)) * 16, bv[hh][0], bv[hh][1], bv[hh][2], bv[hh][3]);
         }
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          mma16<F8>(o[u + 2 * hh], pa, bv[hh][0], bv[hh][1]);
-          mma16<F8>(o[u + 2 * hh + 1], pa, bv[hh][2], bv[hh][3]);
+          mma_bf16(o[u + 2 * hh], pa, bv[hh][0], bv[hh][1]);
+          mma_bf16(o[u + 2 * hh + 1], pa, bv[hh][2], bv[hh][3]);
         }
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          mma16<F8>(o[u + 2 * hh], pl, bv[hh][0], bv[hh][1]);
-          mma16<F8>(o[u + 2 * hh + 1], pl, bv[hh][2], bv[hh][3]);
+          mma_bf16(o[u + 2 * hh], pl, bv[hh][0], bv[hh][1]);
+          mma_bf16(o[u + 2 * hh + 1], pl, bv[hh][2], bv[hh][3]);
         }
       }
     }
@@ -351,11 +376,14 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(cons
   float* sm_o = sm;                       // [NW][G][D]
   float* sm_m = sm_o + NW * G * D;        // [NW][G]
   float* sm_l = sm_m + NW * G;            // [NW][G]
+  // dim of accumulator column 2 qi + e of n-tile u: bf16 8 u + 2 qi + e;
+  // E4M3 (n-tiles of a chunk's even / odd dims) 16 (u / 2) + 4 qi + 2 e + u % 2
+  auto odim = [&](int u, int e) { return F8 ? 16 * (u >> 1) + 4 * qi + 2 * e + (u & 1) : u * 8 + 2 * qi + e; };
   if (quad < G) {
 #pragma unroll
     for (int u = 0; u < NT; ++u) {
-      sm_o[(warp * G + quad) * D + u * 8 + 2 * qi] = o[u][0];
-      sm_o[(warp * G + quad) * D + u * 8 + 2 * qi + 1] = o[u][1];
+      sm_o[(warp * G + quad) * D + odim(u, 0)] = o[u][0];
+      sm_o[(warp * G + quad) * D + odim(u, 1)] = o[u][1];
     }
     if (qi == 0) {
       sm_m[warp * G + quad] = m0;
@@ -365,8 +393,8 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 2) gqa_partial_mma_kernel(cons
   if (quad + 8 < G) {
 #pragma unroll
     for (int u = 0; u < NT; ++u) {
-      sm_o[(warp * G + quad + 8) * D + u * 8 + 2 * qi] = o[u][2];
-      sm_o[(warp * G + quad + 8) * D + u * 8 + 2 * qi + 1] = o[u][3];
+      sm_o[(warp * G + quad + 8) * D + odim(u, 0)] = o[u][2];
+      sm_o[(warp * G + quad + 8) * D + odim(u, 1)] = o[u][3];
     }
     if (qi == 0) {
       sm_m[warp * G + quad + 8] = m1;

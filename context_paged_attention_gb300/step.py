@@ -197,18 +197,20 @@ class StripedAttention:
                               lse_out_offset=r * Hl, stream=stream)
         return out, lse
 
-    def capture(self):
-        """Record the fused step into a CUDA graph over this object's buffers
-        (a captured bucket: later steps refill the same inputs and replay)."""
+    def capture(self, fused=True):
+        """Record the step (fused, or partial + merge) into a CUDA graph over
+        this object's buffers (a captured bucket: later steps refill the same
+        inputs and replay)."""
+        run = self.run_step_fused if fused else self.run_step
         side = torch.cuda.Stream(device=self.device)
         side.wait_stream(torch.cuda.current_stream(self.device))
         with torch.cuda.stream(side):
-            self.run_step_fused(side)  # first call outside capture: workspace and kernel attributes
+            run(side)  # first call outside capture: workspace and kernel attributes
         torch.cuda.current_stream(self.device).wait_stream(side)
         torch.cuda.synchronize(self.device)
         self.graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.graph):
-            self.run_step_fused(torch.cuda.current_stream(self.device))
+            run(torch.cuda.current_stream(self.device))
         return self.graph
 
     def replay(self):

@@ -305,15 +305,17 @@ def test_lse_merge_views(n, layout):
     assert np.all(got_o[:, 0] == 0) and np.all(got_o[:, H + 1] == 0) and np.all(got_l[0] == 0)
 
 
-@pytest.mark.parametrize("name", ["gqa_decode", "mixed_step", "mla_decode"])
-def test_graph_replay(name):
-    """The fused step captured as a CUDA graph: replays equal the eager call
-    bit for bit, and a replay after refilling the inputs gives the new step."""
+@pytest.mark.parametrize("name,fused", [("gqa_decode", True), ("mixed_step", True), ("mla_decode", True),
+                                        ("gqa_decode", False), ("mixed_step", False)])
+def test_graph_replay(name, fused):
+    """A step captured as a CUDA graph (fused, or partial + merge): replays
+    equal the eager call bit for bit, and a replay after refilling the inputs
+    gives the new step."""
     w = SMALL[name]()
     att = _att(w)
-    out0, lse0 = att.run_step_fused()
+    out0, lse0 = att.run_step_fused() if fused else att.run_step()
     ref_o, ref_l = out0.clone(), lse0.clone()
-    att.capture()
+    att.capture(fused)
     for _ in range(2):
         o, l_ = att.replay()
         torch.cuda.synchronize()
