@@ -143,5 +143,6 @@ struct OwnArgs {
   float scale;
 };
 int launch_own_token(const OwnArgs& a, int dtype_bf16, cudaStream_t s, cudaError_t* err);
+int launch_own_token_mma(const OwnArgs& a, cudaStream_t s, cudaError_t* err);  // bf16, tensor cores
 
 }  // namespace cpattn

@@ -86,8 +86,7 @@ int launch_own_token(const OwnArgs& a, int dtype_bf16, cudaStream_t s, cudaError
   const int G = a.num_q_heads / a.num_kv_heads;
   if (a.num_tokens == 0) return CPATTN_OK;
   if (dtype_bf16) {
-    if (a.head_dim == 128) return own_dispatch_g<__nv_bfloat16, 128>(a, G, s, err);
-    if (a.head_dim == 64) return own_dispatch_g<__nv_bfloat16, 64>(a, G, s, err);
+    return launch_own_token_mma(a, s, err);  // tensor cores (own_token_mma.cu)
   } else {
     if (a.head_dim == 128) return own_dispatch_g<float, 128>(a, G, s, err);
     if (a.head_dim == 64) return own_dispatch_g<float, 64>(a, G, s, err);

@@ -326,8 +326,11 @@ CPATTN_API size_t cp_paged_attn_noalloc_scratch_bytes(void);
  *   k_new  [num_tokens][num_kv_heads][head_dim]; v_new [..][head_dim_v]
  *          (v_new NULL: the value is the first head_dim_v values of k_new)
  *   qo_indptr [num_rows_bucket + 1]
+ *   max_q_len the most new tokens of any row (sizes the launch; an
+ *          underestimate only costs time)
  *   o_own  [num_tokens][num_q_heads][head_dim_v] fp32, lse_own [num_tokens][num_q_heads]
- * Supported: head_dim == head_dim_v in {64, 128}, group size in {1, 2, 4, 8, 16}.
+ * Supported: head_dim == head_dim_v in {64, 128}; group size in {1, 2, 4, 8,
+ * 16} (bf16, tensor cores) or {1, 2, 4, 8} (fp32).
  */
 CPATTN_API int own_token_attn(const void* q, const void* k_new, const void* v_new, int32_t num_q_heads,
                    int32_t num_kv_heads, int32_t head_dim, int32_t head_dim_v, int32_t dtype,

@@ -75,6 +75,13 @@ SMALL = {
                                                           num_q_heads=4, num_kv_heads=4, head_dim=64,
                                                           ctx_len=[3, 400, 1], new_len=[1] * 3, seed=40),
                                          0.0091, 0.0213),
+    # non-decode steps at other shapes: group 16 / D 64, group 1 / D 128, padded token count
+    "mixed_g16_d64": lambda: W.build_workload("mixed_g16_d64", dtype="bf16", P=2, page_size=8, num_q_heads=16,
+                                              num_kv_heads=1, head_dim=64, decode=False, ctx_len=[0, 5, 40, 300],
+                                              new_len=[3, 1, 17, 70], num_tokens=96, seed=41),
+    "mixed_g1": lambda: W.build_workload("mixed_g1", dtype="bf16", P=4, page_size=16, num_q_heads=4,
+                                         num_kv_heads=4, head_dim=128, decode=False, ctx_len=[100, 0, 2000],
+                                         new_len=[40, 9, 2], seed=42),
     "gqa_P16_ps16": lambda: W.build_workload("gqa_P16_ps16", dtype="bf16", P=16, page_size=16, num_q_heads=16,
                                              num_kv_heads=2, head_dim=128, ctx_len=[5, 40, 2000], new_len=[1] * 3,
                                              seed=29),
