@@ -41,7 +41,7 @@ FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
 # sources whose digest keys the recorded ncu traffic of each partial kernel
 KERNEL_SOURCES = {
-    "gqa_partial": ["partial_gqa.cu", "partial_gqa_mma.cu", "partial_gqa_ext_tc.cu", "gqa_core.cuh",
+    "gqa_partial": ["partial_gqa.cu", "partial_gqa_mma.cu", "partial_gqa_mmat.cu", "partial_gqa_ext_tc.cu", "gqa_core.cuh",
                     "split_combine.cuh", "common.cuh", "tc05.cuh", "mma_sync.cuh"],
     "mla_partial": ["partial_gqa.cu", "partial_mla_tc.cu", "tc05.cuh", "split_combine.cuh", "common.cuh"],
 }

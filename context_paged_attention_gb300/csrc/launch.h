@@ -144,5 +144,6 @@ struct OwnArgs {
 };
 int launch_own_token(const OwnArgs& a, int dtype_bf16, cudaStream_t s, cudaError_t* err);
 int launch_own_token_mma(const OwnArgs& a, cudaStream_t s, cudaError_t* err);  // bf16, tensor cores
+int launch_gqa_partial_mmat(const PartialArgs& a, cudaStream_t s, cudaError_t* err);  // decode rows, groups <= 8
 
 }  // namespace cpattn
