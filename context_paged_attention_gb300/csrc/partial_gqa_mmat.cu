@@ -11,7 +11,7 @@
 //   O^T += V^T P^T (A = V rows by ldmatrix.trans, one m-tile a 16 dims; B = P^T)
 // which takes half the MMAs of the head-rows form (a group of 4 fills half an
 // n-tile instead of a quarter of an m-tile) and half the accumulator
-// registers, so three CTAs fit an SM.  P^T is built from the S^T accumulators
+// registers.  P^T is built from the S^T accumulators
 // (key rows, head columns) with movmatrix.trans, as a 16-bit hi + lo pair so
 // P V keeps fp32-grade probabilities.  Softmax state (running max and sum) is
 // per head: each lane holds heads 2 (lane % 4) and 2 (lane % 4) + 1 for keys
@@ -36,11 +36,12 @@ constexpr int kTWarps = 4;
 constexpr int kTKeys = 16;  // keys a stage
 }  // namespace
 
-// Shared memory of one CTA: the warps' cp.async rings (2 stages of bf16 rows,
-// 4 of E4M3 rows: 64 KB either way at D 128).
+// Shared memory of one CTA: the warps' cp.async rings.  bf16: 3 stages (96 KB
+// at D 128, two CTAs an SM, 128 KB of K/V in flight an SM); E4M3: 4 stages of
+// half-size rows (64 KB, three CTAs an SM).
 template <int D, bool F8>
 struct TSmem {
-  static constexpr int NST = F8 ? 4 : 2;
+  static constexpr int NST = F8 ? 4 : 3;
   static constexpr int SRC_ROWB = F8 ? D : 2 * D;
   static constexpr int RING_STAGE = kTKeys * SRC_ROWB;
   static constexpr size_t MAIN = static_cast<size_t>(kTWarps) * NST * RING_STAGE * 2;
@@ -59,7 +60,7 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
 }
 
 template <int D, int G, bool F8>
-__global__ void __launch_bounds__(kTWarps * 32, 3) gqa_partial_mmat_kernel(const PartialArgs a) {
+__global__ void __launch_bounds__(kTWarps * 32, F8 ? 3 : 2) gqa_partial_mmat_kernel(const PartialArgs a) {
   using SM = TSmem<D, F8>;
   constexpr int NW = kTWarps;
   constexpr int NST = SM::NST;
