@@ -17,10 +17,9 @@
 // per head: each lane holds heads 2 (lane % 4) and 2 (lane % 4) + 1 for keys
 // lane / 4 and lane / 4 + 8, and reduces over keys with three xor shuffles.
 //
-// Loads: two lanes share a key of a stage: each resolves the key's pool row
-// once and issues its half of the row's 16-byte cp.async copies into an
-// XOR-swizzled ring (chunk c of key r at c ^ (r & 7); E4M3 rows of 64 bytes
-// at c ^ ((r >> 1) & 3)).  E4M3 pools: the fragments are ldmatrix-ed as code
+// Loads: 16-byte cp.async copies, each warp instruction covering whole rows,
+// into an XOR-swizzled ring (chunk c of key r at c ^ (r & 7); E4M3 rows of
+// 64 bytes at c ^ ((r >> 1) & 3)).  E4M3 pools: the fragments are ldmatrix-ed as code
 // bytes and converted in registers (float16 MMAs; the K fragment's k order is
 // dims 4 (lane % 4) .. + 3, which the query fragment follows; V's code bytes
 // split into even- and odd-dim rows of the m-tile).
@@ -67,13 +66,13 @@ __global__ void __launch_bounds__(kTWarps * 32, F8 ? 3 : 2) gqa_partial_mmat_ker
   constexpr int KT = kTKeys;
   constexpr int SRC_ROWB = SM::SRC_ROWB;
   constexpr int SRC_CH = SRC_ROWB / 16;  // 16-byte chunks of a pool row
-  constexpr int CPL = SRC_CH / 2;        // chunks a lane copies (two lanes a key)
+  constexpr int ITERS = KT * SRC_CH / 32;  // copy instructions a stage (K and V each)
   constexpr int RING_STAGE = SM::RING_STAGE;
   constexpr int KSTEPS = D / 16;         // k-steps of S^T
   constexpr int MT = D / 16;             // m-tiles of O^T (16 dims each)
   static_assert(G >= 1 && G <= 8, "group size");
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ uint32_t s_vmask[NW][NST];  // bit 2k: key k of the stage was copied
+  __shared__ uint32_t s_vmask[NW][NST];  // bit k: key k of the stage was copied
 
   const int c = blockIdx.x;
   const int p = blockIdx.y / a.num_kv_heads;
@@ -159,21 +158,24 @@ __global__ void __launch_bounds__(kTWarps * 32, F8 ? 3 : 2) gqa_partial_mmat_ker
     return (head_row0 + static_cast<int64_t>(pg) * a.num_kv_heads) * a.ps_l + (k - j * a.ps_l);
   };
 
-  // stage i of this warp: lanes 2k, 2k + 1 copy key k (halves of its row)
-  const int my_key = lane >> 1;
-  const int my_half = lane & 1;
+  // stage i of this warp: each copy instruction covers whole rows (32 lanes
+  // = 32 consecutive 16-byte chunks), the rows resolved once a stage by lanes
+  // 0-15 (and 16-31) and shared by shuffle
   auto issue = [&](int i) {
     if (i < my_n) {
       const int k0 = k_begin + (warp + i * NW) * KT;
-      const int64_t row = row_of(k0 + my_key);
-      const uint32_t vm = __ballot_sync(0xffffffffu, row >= 0);
+      const int64_t myrow = row_of(k0 + (lane & (KT - 1)));
+      const uint32_t vm = __ballot_sync(0xffffffffu, myrow >= 0) & 0xffffu;  // bit k: key k copied
       if (lane == 0) s_vmask[warp][i % NST] = vm;
       uint8_t* sk = ring + (i % NST) * RING_STAGE * 2;
       uint8_t* sv = sk + RING_STAGE;
 #pragma unroll
-      for (int j = 0; j < CPL; ++j) {
-        const int ch = my_half * CPL + j;
-        const int soff = (my_key * SRC_CH + swz_t<SRC_CH>(ch, my_key)) * 16;
+      for (int it = 0; it < ITERS; ++it) {
+        const int idx = it * 32 + lane;
+        const int key = idx / SRC_CH;
+        const int ch = idx - key * SRC_CH;
+        const int64_t row = __shfl_sync(0xffffffffu, myrow, key);
+        const int soff = (key * SRC_CH + swz_t<SRC_CH>(ch, key)) * 16;
         if (row >= 0) {
           cp_async16(sk + soff, poolk + row * SRC_ROWB + ch * 16);
           cp_async16(sv + soff, poolv + row * SRC_ROWB + ch * 16);
@@ -234,8 +236,8 @@ __global__ void __launch_bounds__(kTWarps * 32, F8 ? 3 : 2) gqa_partial_mmat_ker
       }
     }
     // ---- mask keys past the stripe end (or on a rejected page), per-head block max
-    const bool ka = (vm >> (2 * g8)) & 1u;        // key g8
-    const bool kb = (vm >> (2 * g8 + 16)) & 1u;   // key g8 + 8
+    const bool ka = (vm >> g8) & 1u;        // key g8
+    const bool kb = (vm >> (g8 + 8)) & 1u;  // key g8 + 8
     float v[4];
     v[0] = ka ? (st[0] + st2[0]) * sl : -INFINITY;  // key g8,     head 2 qi
     v[1] = ka ? (st[1] + st2[1]) * sl : -INFINITY;  // key g8,     head 2 qi + 1
