@@ -7,26 +7,23 @@
 // layer parallel plans", _forward_with_dcp: the context partial over the paged
 // cache).  The queries of 128 / G consecutive tokens of a row and the G heads
 // of KV head h form a dense 128-row tile against partner p's stripe of that
-// context (stripe slot k at physical slot k % (page_size / P) of the row's
-// page k / (page_size / P)):
-//   S = Q K^T  (M = 128 query rows, N = 64 keys, K = head_dim)
-//   O += P V   (N = head_dim, K = 64 keys)
+// context (stripe slot k = logical position k * P + p, at physical slot
+// k % (page_size / P) of page k / (page_size / P)):
+//   S = Q K^T  (M = 128 query rows, N = 32 keys, K = head_dim)
+//   O += P V   (N = head_dim, K = 32 keys)
 //
 // CTA = (chunk, partner p, KV head h, token block j), 4 warps; thread r owns
 // query row r = (token j * 128 / G + r / G, head h * G + r % G) and TMEM lane r,
 // so the online softmax is thread-local.  Shared memory: Q [128 x D] K-major
-// with the 128-byte swizzle, four stages of 64 keys (K and V, the same layout;
-// V is read M/N-major), P [128 x 64] bf16 K-major (128-byte swizzle).  Tensor
-// memory: two 64-column S buffers and D columns of O.  Schedule of tile i:
-// wait S(i); issue S(i + 1) into the other buffer (the tensor pipe computes it
-// while the threads do the softmax of tile i); softmax of S(i); wait P V of
-// tile i - 1 (then P, O and that stage are free); rescale O if the running max
-// rose; load tile i + 3; write P; issue P V of tile i.  P is bf16 and O is
-// normalised by the sum of the rounded probabilities (an exact convex
-// combination of the values; the LSE uses the fp32 sum).  A chunk split of a
-// stripe is merged by the last CTA to arrive.  Rows of one token are left to
-// the decode kernels; this kernel also writes the padding tokens past the last
-// row.  Waits are bounded (CPATTN_DEV_TC_TIMEOUT).
+// with the 128-byte swizzle, three stages of 32 keys (K and V, the same
+// layout; V is read M/N-major), P [128 x 32] bf16 K-major with the 64-byte
+// swizzle; O is normalised by the sum of the bf16-rounded probabilities (an
+// exact convex combination of the values; the LSE keeps the fp32 sum).
+// Tensor memory: 32 columns of S and D columns of O (256 allocated, two CTAs
+// per SM).  The S MMAs of a tile overlap the P V MMAs of the one before.  A
+// chunk split of a stripe is merged by the last CTA to arrive, per token.
+// Rows of one token are left to the decode kernel; this kernel also writes the
+// padding tokens past the last row.  Waits are bounded (CPATTN_DEV_TC_TIMEOUT).
 #include "common.cuh"
 #include "launch.h"
 #include "split_combine.cuh"
@@ -35,8 +32,8 @@
 namespace cpattn {
 
 namespace {
-constexpr int kXTile = 64;    // keys per tile
-constexpr int kXStages = 4;
+constexpr int kXTile = 32;    // keys per tile
+constexpr int kXStages = 3;
 constexpr int kXRows = 128;   // query rows per CTA
 }  // namespace
 
@@ -47,17 +44,17 @@ struct ExtTcLayout {
   static constexpr int BLK = kXTile * 128;            // one column block of a key tile
   static constexpr int TILE = KB * BLK;               // K (or V) tile
   static constexpr int STAGE = 2 * TILE;              // K + V
-  static constexpr int PBYTES = kXRows * 128;         // P tile (bf16, 64 keys)
+  static constexpr int PBYTES = kXRows * 64;          // one P tile (bf16, 32 keys)
   static constexpr int TMEM_COLS = 256;
-  static constexpr int S_COL = 0;                     // S buffers: columns 0..63 and 64..127
-  static constexpr int O_COL = 128;                   // O: columns 128..128+D
+  static constexpr int S_COL = 0;                     // S: columns 0..31
+  static constexpr int O_COL = 64;                    // O: columns 64..64+D
   static size_t smem_bytes(int page_slots) {
     return 1024 + QBYTES + kXStages * STAGE + PBYTES + 64 + static_cast<size_t>(page_slots) * 4;
   }
 };
 
 template <int D, int G>
-__global__ void __launch_bounds__(128, 1) gqa_partial_ext_tc_kernel(const PartialArgs a) {
+__global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const PartialArgs a) {
   using Lt = ExtTcLayout<D>;
   constexpr int QB = kXRows / G;  // tokens per block
   static_assert(G >= 1 && G <= 16 && (D == 64 || D == 128), "shape");
@@ -65,8 +62,8 @@ __global__ void __launch_bounds__(128, 1) gqa_partial_ext_tc_kernel(const Partia
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base;
   uint8_t* sKV = sQ + Lt::QBYTES;
-  uint8_t* sP = sKV + kXStages * Lt::STAGE;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + Lt::PBYTES);  // [0] S done, [1] P V done
+  uint8_t* sPh = sKV + kXStages * Lt::STAGE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sPh + Lt::PBYTES);  // [0] S done, [1] P V done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2);
   int* spg = reinterpret_cast<int*>(bars + 4);
 
@@ -122,7 +119,7 @@ __global__ void __launch_bounds__(128, 1) gqa_partial_ext_tc_kernel(const Partia
   const uint32_t mb_pv = tc05::smem_addr(&bars[1]);
   const uint32_t my_lane = tc05::taddr(tbase, warp * 32, 0);
   const uint32_t q0 = tc05::smem_addr(sQ);
-  const uint32_t p0 = tc05::smem_addr(sP);
+  const uint32_t ph0 = tc05::smem_addr(sPh);
   const uint32_t id_s = tc05::idesc_bf16(128, kXTile, false, false);
   const uint32_t id_o = tc05::idesc_bf16(128, D, false, true);
   const uint8_t* poolk = static_cast<const uint8_t*>(a.pool_k);
@@ -193,21 +190,17 @@ __global__ void __launch_bounds__(128, 1) gqa_partial_ext_tc_kernel(const Partia
       return (head_row0 + static_cast<int64_t>(pg) * a.num_kv_heads) * a.ps_l + (k - j * a.ps_l);
     };
     // copies of tile i (K and V rows) into stage i % kXStages; each warp
-    // resolves the 64 keys' rows once (lanes: keys lane, lane + 32) and shares
-    // them by shuffle
+    // resolves the 32 keys' rows once (lane = key) and shares them by shuffle
     auto load_tile = [&](int i) {
       if (i < ntiles) {
         uint8_t* sk = sKV + (i % kXStages) * Lt::STAGE;
         uint8_t* sv = sk + Lt::TILE;
-        const int64_t row_a = row_of(k_begin + i * kXTile + lane);
-        const int64_t row_b = row_of(k_begin + i * kXTile + 32 + lane);
+        const int64_t myrow = row_of(k_begin + i * kXTile + lane);
         constexpr int CH = D / 8;
         for (int x = tid; x < kXTile * CH; x += blockDim.x) {
           const int key = x / CH;
           const int cc = x - key * CH;
-          const int64_t ra = __shfl_sync(0xffffffffu, row_a, key & 31);
-          const int64_t rb = __shfl_sync(0xffffffffu, row_b, key & 31);
-          const int64_t row = key < 32 ? ra : rb;
+          const int64_t row = __shfl_sync(0xffffffffu, myrow, key);
           const int off = (cc >> 3) * Lt::BLK + tc05::sw128(key, cc & 7);
           if (row >= 0) {
             cp_async16(sk + off, poolk + row * (D * 2) + cc * 16);
@@ -219,122 +212,108 @@ __global__ void __launch_bounds__(128, 1) gqa_partial_ext_tc_kernel(const Partia
       }
       cp_async_commit();
     };
-    // S(i) = Q K^T into S buffer i % 2; P V of tile i into O (one thread issues)
-    auto issue_s = [&](int i) {
-      const uint32_t kv0 = tc05::smem_addr(sKV + (i % kXStages) * Lt::STAGE);
-      const uint32_t col = Lt::S_COL + (i & 1) * kXTile;
-#pragma unroll
-      for (int s = 0; s < D / 16; ++s) {
-        const uint32_t off = (s >> 2) * (kXRows * 128) + (s & 3) * 32;
-        const uint32_t koff = (s >> 2) * Lt::BLK + (s & 3) * 32;
-        tc05::mma_ss(tbase + col, tc05::desc_k128(q0 + off), tc05::desc_k128(kv0 + koff), id_s, s > 0);
-      }
-    };
-    auto issue_pv = [&](int i) {
-      const uint32_t kv0 = tc05::smem_addr(sKV + (i % kXStages) * Lt::STAGE);
-#pragma unroll
-      for (int k = 0; k < kXTile / 16; ++k) {
-        const uint64_t bd = tc05::desc_mn128(kv0 + Lt::TILE + k * 16 * 128, Lt::BLK);
-        tc05::mma_ss(tbase + Lt::O_COL, tc05::desc_k128(p0 + k * 32), bd, id_o, i > 0 || k > 0);
-      }
-    };
-    load_tile(0);  // with Q
+    load_tile(0);
     load_tile(1);
-    load_tile(2);
 
     float m = -INFINITY, l = 0.f, lr = 0.f;  // running max (log2), fp32 sum, sum of the bf16-rounded p
-    if (ntiles > 0) {
-      cp_async_wait<2>();  // Q and tile 0 landed for this thread
+    bool have_pv = false;  // a P V MMA of this segment is in flight (or done but unwaited)
+    for (int i = 0; i < ntiles; ++i) {
+      cp_async_wait<1>();  // tile i (and Q) landed for this thread
       tc05::fence_smem_to_async();
       __syncthreads();
+      const uint32_t kv0 = tc05::smem_addr(sKV + (i % kXStages) * Lt::STAGE);
+      uint32_t vmask;
+      {
+        const int k = k_begin + i * kXTile + lane;
+        vmask = __ballot_sync(0xffffffffu, row_of(k) >= 0);
+      }
       if (tid == 0) {
         tc05::fence_after_sync();
-        issue_s(0);
-        tc05::commit(mb_s);
+#pragma unroll
+        for (int s = 0; s < D / 16; ++s) {
+          const uint32_t off = (s >> 2) * (kXRows * 128) + (s & 3) * 32;
+          const uint32_t koff = (s >> 2) * Lt::BLK + (s & 3) * 32;
+          tc05::mma_ss(tbase + Lt::S_COL, tc05::desc_k128(q0 + off), tc05::desc_k128(kv0 + koff), id_s, s > 0);
+        }
+        tc05::commit(mb_s);  // also covers the previous tile's P V
       }
-    }
-    for (int i = 0; i < ntiles; ++i) {
-      alive = __syncthreads_and(tc05::mbar_wait(mb_s, s_phase & 1)) != 0;  // S(i) done
+      if (have_pv) {  // P V of tile i-1 done: its stage and P are free, O is stable
+        alive = __syncthreads_and(tc05::mbar_wait(mb_pv, pv_phase & 1)) != 0;
+        ++pv_phase;
+        have_pv = false;
+        if (!alive) break;
+      }
+      load_tile(i + 2);  // into the stage tile i-1 used
+      alive = __syncthreads_and(tc05::mbar_wait(mb_s, s_phase & 1)) != 0;
       ++s_phase;
       if (!alive) break;
-      cp_async_wait<1>();  // tile i + 1 landed for this thread
-      tc05::fence_smem_to_async();
-      __syncthreads();
-      if (tid == 0 && i + 1 < ntiles) {  // S(i + 1) runs during the softmax of tile i
-        tc05::fence_after_sync();
-        issue_s(i + 1);
-        tc05::commit(mb_s);
-      }
       tc05::fence_after_sync();
-      float sv[kXTile];
-#pragma unroll
-      for (int q4 = 0; q4 < kXTile / 16; ++q4) {
+      float sv[32];
+      {
         float v16[16];
-        tc05::ld_x16(my_lane + Lt::S_COL + (i & 1) * kXTile + 16 * q4, v16);
+        tc05::ld_x16(my_lane + Lt::S_COL, v16);
         tc05::ld_wait();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) sv[16 * q4 + e] = v16[e];
+        for (int e = 0; e < 16; ++e) sv[e] = v16[e];
+        tc05::ld_x16(my_lane + Lt::S_COL + 16, v16);
+        tc05::ld_wait();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) sv[16 + e] = v16[e];
       }
-      tc05::fence_before_sync();  // this buffer's loads are done before S(i + 2) reuses it
-      const int kt = k_begin + i * kXTile;
-      const uint32_t vm_a = __ballot_sync(0xffffffffu, row_of(kt + lane) >= 0);
-      const uint32_t vm_b = __ballot_sync(0xffffffffu, row_of(kt + 32 + lane) >= 0);
       float bm = -INFINITY;
 #pragma unroll
-      for (int e = 0; e < kXTile; ++e) {
-        const bool ok = ((e < 32 ? vm_a : vm_b) >> (e & 31)) & 1u;
-        sv[e] = ok ? sv[e] * sl : -INFINITY;
+      for (int e = 0; e < 32; ++e) {
+        sv[e] = ((vmask >> e) & 1u) ? sv[e] * sl : -INFINITY;
         bm = fmaxf(bm, sv[e]);
       }
       const bool up = bm > m + 8.f;
-      const float alpha = up ? exp2f(m - bm) : 1.f;
-      if (up) m = bm;
-      uint32_t pk[kXTile / 2];
-      float ps = 0.f, psr = 0.f;
+      if (__any_sync(0xffffffffu, up) && i > 0) {  // rescale O rows whose max rose (rare)
+        const float alpha = up ? exp2f(m - bm) : 1.f;
 #pragma unroll
-      for (int e = 0; e < kXTile / 2; ++e) {
-        const float pa = sv[2 * e] == -INFINITY ? 0.f : exp2f(sv[2 * e] - m);
-        const float pb = sv[2 * e + 1] == -INFINITY ? 0.f : exp2f(sv[2 * e + 1] - m);
-        ps += pa + pb;
-        __nv_bfloat162 h2 = __floats2bfloat162_rn(pa, pb);
-        psr += __low2float(h2) + __high2float(h2);
-        pk[e] = *reinterpret_cast<uint32_t*>(&h2);
-      }
-      l = l * alpha + ps;
-      lr = lr * alpha + psr;
-      if (i > 0) {  // P V of tile i - 1 done: P, O and that tile's stage are free
-        alive = __syncthreads_and(tc05::mbar_wait(mb_pv, pv_phase & 1)) != 0;
-        ++pv_phase;
-        if (!alive) break;
-        tc05::fence_after_sync();
-        if (__any_sync(0xffffffffu, up)) {  // rescale this warp's O rows whose max rose (rare)
+        for (int col = 0; col < D; col += 16) {
+          float v[16];
+          tc05::ld_x16(my_lane + Lt::O_COL + col, v);
+          tc05::ld_wait();
 #pragma unroll
-          for (int col = 0; col < D; col += 16) {
-            float v[16];
-            tc05::ld_x16(my_lane + Lt::O_COL + col, v);
-            tc05::ld_wait();
-#pragma unroll
-            for (int e = 0; e < 16; ++e) v[e] *= alpha;
-            tc05::st_x16(my_lane + Lt::O_COL + col, v);
-          }
-          tc05::st_wait();
+          for (int e = 0; e < 16; ++e) v[e] *= alpha;
+          tc05::st_x16(my_lane + Lt::O_COL + col, v);
         }
+        tc05::st_wait();
+        l *= alpha;
+        lr *= alpha;
       }
-      load_tile(i + 3);  // into the stage of tile i - 1
+      if (up) m = bm;
+      {
+        uint32_t hi[16];
 #pragma unroll
-      for (int q8 = 0; q8 < kXTile / 8; ++q8)
-        *reinterpret_cast<uint4*>(sP + tc05::sw128(tid, q8)) =
-            make_uint4(pk[4 * q8], pk[4 * q8 + 1], pk[4 * q8 + 2], pk[4 * q8 + 3]);
+        for (int e = 0; e < 16; ++e) {
+          const float pa = sv[2 * e] == -INFINITY ? 0.f : exp2f(sv[2 * e] - m);  // masked: 0, also while m is -inf
+          const float pb = sv[2 * e + 1] == -INFINITY ? 0.f : exp2f(sv[2 * e + 1] - m);
+          l += pa + pb;
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(pa, pb);
+          lr += __low2float(h2) + __high2float(h2);
+          hi[e] = *reinterpret_cast<uint32_t*>(&h2);
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          *reinterpret_cast<uint4*>(sPh + tc05::sw64(tid, q4)) =
+              make_uint4(hi[4 * q4], hi[4 * q4 + 1], hi[4 * q4 + 2], hi[4 * q4 + 3]);
+      }
       tc05::fence_smem_to_async();
       tc05::fence_before_sync();
       __syncthreads();
       if (tid == 0) {
         tc05::fence_after_sync();
-        issue_pv(i);
+#pragma unroll
+        for (int s = 0; s < kXTile / 16; ++s) {
+          const uint64_t bd = tc05::desc_mn128(kv0 + Lt::TILE + s * 16 * 128, Lt::BLK);
+          tc05::mma_ss(tbase + Lt::O_COL, tc05::desc_k64(ph0 + s * 32), bd, id_o, i > 0 || s > 0);
+        }
         tc05::commit(mb_pv);
       }
+      have_pv = true;
     }
-    if (alive && ntiles > 0) {
+    if (have_pv && alive) {
       alive = __syncthreads_and(tc05::mbar_wait(mb_pv, pv_phase & 1)) != 0;
       ++pv_phase;
     }
