@@ -106,8 +106,8 @@ int run_partial(const cpattn_pool_desc* desc, const void* pool_k, const void* po
   if (!aligned16(pool_k) || !aligned16(pool_v) || !aligned16(q) || !aligned16(o_part) || !aligned16(workspace))
     return CPATTN_ERR_MISALIGNED;
   if (mla && desc->dtype != CPATTN_DTYPE_BF16) return CPATTN_ERR_UNSUPPORTED_SHAPE;
-  // E4M3 pools: GQA rows of one token (the decode kernel); no MLA, no ragged rows
-  if (is_fp8(desc) && (mla || qo_indptr != nullptr)) return CPATTN_ERR_UNSUPPORTED_SHAPE;
+  // E4M3 pools: GQA (the MLA kernel reads bf16 latent rows only)
+  if (is_fp8(desc) && mla) return CPATTN_ERR_UNSUPPORTED_SHAPE;
 
   PartialPlan plan;
   if (!plan_partial(mla, f.fused, desc->P, interleave_of(desc), desc->page_size, desc->num_kv_heads, num_q_heads,

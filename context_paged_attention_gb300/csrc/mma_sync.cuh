@@ -93,4 +93,12 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes16) {
   return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
 }
 
+// Two E4M3 codes (low byte first) -> their exact bf16 values (every E4M3
+// value has at most 4 significant bits and a bf16 exponent).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t codes16) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(codes16 & 0xffffu), __NV_E4M3);
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+  return pack_bf16(f.x, f.y);
+}
+
 }  // namespace cpattn

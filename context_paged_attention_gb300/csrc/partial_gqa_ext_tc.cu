@@ -26,6 +26,7 @@
 // padding tokens past the last row.  Waits are bounded (CPATTN_DEV_TC_TIMEOUT).
 #include "common.cuh"
 #include "launch.h"
+#include "mma_sync.cuh"
 #include "split_combine.cuh"
 #include "tc05.cuh"
 
@@ -48,12 +49,17 @@ struct ExtTcLayout {
   static constexpr int TMEM_COLS = 256;
   static constexpr int S_COL = 0;                     // S: columns 0..31
   static constexpr int O_COL = 64;                    // O: columns 64..64+D
-  static size_t smem_bytes(int page_slots) {
-    return 1024 + QBYTES + kXStages * STAGE + PBYTES + 64 + static_cast<size_t>(page_slots) * 4;
+  // E4M3 pools: the code rows of a tile land in a ring of kXStages stages
+  // (K then V, [key][D] bytes) and are converted into one of two bf16 tiles
+  static constexpr int RING8 = 2 * kXTile * D;        // one E4M3 stage (K + V)
+  static size_t smem_bytes(int page_slots, bool f8) {
+    const size_t tiles = f8 ? 2 * static_cast<size_t>(STAGE) + kXStages * static_cast<size_t>(RING8)
+                            : kXStages * static_cast<size_t>(STAGE);
+    return 1024 + QBYTES + tiles + PBYTES + 64 + static_cast<size_t>(page_slots) * 4;
   }
 };
 
-template <int D, int G>
+template <int D, int G, bool F8>
 __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const PartialArgs a) {
   using Lt = ExtTcLayout<D>;
   constexpr int QB = kXRows / G;  // tokens per block
@@ -61,8 +67,9 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base;
-  uint8_t* sKV = sQ + Lt::QBYTES;
-  uint8_t* sPh = sKV + kXStages * Lt::STAGE;
+  uint8_t* sKV = sQ + Lt::QBYTES;  // bf16 tiles the MMAs read: kXStages stages, or (E4M3) two
+  uint8_t* sRing8 = sKV + (F8 ? 2 : kXStages) * Lt::STAGE;  // E4M3 code stages (unused for bf16)
+  uint8_t* sPh = sRing8 + (F8 ? kXStages * Lt::RING8 : 0);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sPh + Lt::PBYTES);  // [0] S done, [1] P V done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2);
   int* spg = reinterpret_cast<int*>(bars + 4);
@@ -124,7 +131,7 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
   const uint32_t id_o = tc05::idesc_bf16(128, D, false, true);
   const uint8_t* poolk = static_cast<const uint8_t*>(a.pool_k);
   const uint8_t* poolv = static_cast<const uint8_t*>(a.pool_v);
-  const float sl = a.scale * kLog2e;
+  const float sl = a.scale * kLog2e * (F8 ? a.k_descale : 1.f);
   uint32_t s_phase = 0, pv_phase = 0;  // completed phases of the two mbarriers
   bool alive = true;
 
@@ -193,24 +200,70 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
     // resolves the 32 keys' rows once (lane = key) and shares them by shuffle
     auto load_tile = [&](int i) {
       if (i < ntiles) {
-        uint8_t* sk = sKV + (i % kXStages) * Lt::STAGE;
-        uint8_t* sv = sk + Lt::TILE;
         const int64_t myrow = row_of(k_begin + i * kXTile + lane);
-        constexpr int CH = D / 8;
-        for (int x = tid; x < kXTile * CH; x += blockDim.x) {
-          const int key = x / CH;
-          const int cc = x - key * CH;
-          const int64_t row = __shfl_sync(0xffffffffu, myrow, key);
-          const int off = (cc >> 3) * Lt::BLK + tc05::sw128(key, cc & 7);
-          if (row >= 0) {
-            cp_async16(sk + off, poolk + row * (D * 2) + cc * 16);
-            cp_async16(sv + off, poolv + row * (D * 2) + cc * 16);
-          } else {
-            *reinterpret_cast<uint4*>(sv + off) = make_uint4(0u, 0u, 0u, 0u);  // masked keys: value 0
+        if constexpr (F8) {  // code rows, [key][D] bytes per K / V
+          uint8_t* rk = sRing8 + (i % kXStages) * Lt::RING8;
+          uint8_t* rv = rk + kXTile * D;
+          constexpr int CH8 = D / 16;
+          for (int x = tid; x < kXTile * CH8; x += blockDim.x) {
+            const int key = x / CH8;
+            const int cc = x - key * CH8;
+            const int64_t row = __shfl_sync(0xffffffffu, myrow, key);
+            if (row >= 0) {
+              cp_async16(rk + x * 16, poolk + row * D + cc * 16);
+              cp_async16(rv + x * 16, poolv + row * D + cc * 16);
+            } else {
+              *reinterpret_cast<uint4*>(rv + x * 16) = make_uint4(0u, 0u, 0u, 0u);  // masked keys: value 0
+            }
+          }
+        } else {
+          uint8_t* sk = sKV + (i % kXStages) * Lt::STAGE;
+          uint8_t* sv = sk + Lt::TILE;
+          constexpr int CH = D / 8;
+          for (int x = tid; x < kXTile * CH; x += blockDim.x) {
+            const int key = x / CH;
+            const int cc = x - key * CH;
+            const int64_t row = __shfl_sync(0xffffffffu, myrow, key);
+            const int off = (cc >> 3) * Lt::BLK + tc05::sw128(key, cc & 7);
+            if (row >= 0) {
+              cp_async16(sk + off, poolk + row * (D * 2) + cc * 16);
+              cp_async16(sv + off, poolv + row * (D * 2) + cc * 16);
+            } else {
+              *reinterpret_cast<uint4*>(sv + off) = make_uint4(0u, 0u, 0u, 0u);  // masked keys: value 0
+            }
           }
         }
       }
       cp_async_commit();
+    };
+    // E4M3: the codes of tile i -> bf16 tile i % 2 in the MMA layout (exact:
+    // every E4M3 value is a bf16 value); the tile it overwrites (i - 2) was
+    // last read by P V of tile i - 2, which has completed
+    auto convert_tile = [&](int i) {
+      const uint8_t* rk = sRing8 + (i % kXStages) * Lt::RING8;
+      uint8_t* wk = sKV + (i & 1) * Lt::STAGE;
+      constexpr int CH8 = D / 16;
+      for (int x = tid; x < 2 * kXTile * CH8; x += blockDim.x) {
+        const int kv = x / (kXTile * CH8);  // 0: K, 1: V
+        const int y = x - kv * (kXTile * CH8);
+        const int key = y / CH8;
+        const int c16 = y - key * CH8;  // codes of dims 16 c16 .. 16 c16 + 15
+        const uint4 w = *reinterpret_cast<const uint4*>(rk + kv * kXTile * D + y * 16);
+        const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+        uint32_t bf[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          bf[2 * q] = e4m3x2_to_bf16x2(wd[q]);
+          bf[2 * q + 1] = e4m3x2_to_bf16x2(wd[q] >> 16);
+        }
+        uint8_t* dst = wk + kv * Lt::TILE;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int cc = 2 * c16 + hh;  // 8-dim chunk of the bf16 row
+          *reinterpret_cast<uint4*>(dst + (cc >> 3) * Lt::BLK + tc05::sw128(key, cc & 7)) =
+              make_uint4(bf[4 * hh], bf[4 * hh + 1], bf[4 * hh + 2], bf[4 * hh + 3]);
+        }
+      }
     };
     load_tile(0);
     load_tile(1);
@@ -219,9 +272,13 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
     bool have_pv = false;  // a P V MMA of this segment is in flight (or done but unwaited)
     for (int i = 0; i < ntiles; ++i) {
       cp_async_wait<1>();  // tile i (and Q) landed for this thread
+      if constexpr (F8) {
+        __syncthreads();  // every thread's codes of tile i landed
+        convert_tile(i);
+      }
       tc05::fence_smem_to_async();
       __syncthreads();
-      const uint32_t kv0 = tc05::smem_addr(sKV + (i % kXStages) * Lt::STAGE);
+      const uint32_t kv0 = tc05::smem_addr(sKV + (F8 ? (i & 1) : (i % kXStages)) * Lt::STAGE);
       uint32_t vmask;
       {
         const int k = k_begin + i * kXTile + lane;
@@ -326,7 +383,7 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
     const bool single = (nchunks == 1);
     {
       const bool empty = (l == 0.f);
-      const float inv = lr > 0.f ? 1.f / lr : 0.f;
+      const float inv = lr > 0.f ? (F8 ? a.v_descale : 1.f) / lr : 0.f;  // E4M3: value = code * v_descale
       const float lse = empty ? -INFINITY : (m + log2f(l)) * kLn2;
       const int g = tid % G;
       float* dst = nullptr;
@@ -368,7 +425,7 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
       done = take_ticket(a.ws_cnt + slot0, nchunks);
       if (done) {
         merge_chunks(a, p, h, s0, s1 - s0, slot0, static_cast<int64_t>(P) * a.num_kv_heads, nchunks, G, D,
-                     reinterpret_cast<float*>(sKV), kXStages * Lt::STAGE / 4);
+                     reinterpret_cast<float*>(sKV), (F8 ? 2 : kXStages) * Lt::STAGE / 4);
         if (tid == 0) a.ws_cnt[slot0] = 0;
       }
     }
@@ -376,7 +433,7 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
       // fused: the last of the P partners of (segment, KV head) merges them
       int32_t* pair = a.ws_pair + static_cast<int64_t>(s0) * a.num_kv_heads + h;
       if (take_ticket(pair, P)) {
-        merge_partners(a, s0, s1 - s0, h, G, D, reinterpret_cast<float*>(sKV), kXStages * Lt::STAGE / 4);
+        merge_partners(a, s0, s1 - s0, h, G, D, reinterpret_cast<float*>(sKV), (F8 ? 2 : kXStages) * Lt::STAGE / 4);
         if (tid == 0) *pair = 0;
       }
     }
@@ -388,13 +445,13 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
   if (warp == 0) tc05::tmem_dealloc(tbase, Lt::TMEM_COLS);
 }
 
-template <int D, int G>
+template <int D, int G, bool F8>
 static int launch_ext_tc_t(const PartialArgs& a, cudaStream_t s, cudaError_t* err) {
   constexpr int QB = kXRows / G;
   const int page_slots = a.chunk / a.ps_l + 2;
-  const size_t smem = ExtTcLayout<D>::smem_bytes(page_slots);
+  const size_t smem = ExtTcLayout<D>::smem_bytes(page_slots, F8);
   if (smem > 227 * 1024) return CPATTN_ERR_UNSUPPORTED_SHAPE;
-  auto kern = gqa_partial_ext_tc_kernel<D, G>;
+  auto kern = gqa_partial_ext_tc_kernel<D, G, F8>;
   static std::atomic<int> smem_set[64];
   *err = ensure_smem(kern, smem, smem_set);
   if (*err != cudaSuccess) return CPATTN_ERR_CUDA;
@@ -404,22 +461,27 @@ static int launch_ext_tc_t(const PartialArgs& a, cudaStream_t s, cudaError_t* er
   return *err == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
 }
 
-template <int D>
+template <int D, bool F8>
 static int ext_tc_dispatch_g(const PartialArgs& a, int G, cudaStream_t s, cudaError_t* err) {
   switch (G) {
-    case 1: return launch_ext_tc_t<D, 1>(a, s, err);
-    case 2: return launch_ext_tc_t<D, 2>(a, s, err);
-    case 4: return launch_ext_tc_t<D, 4>(a, s, err);
-    case 8: return launch_ext_tc_t<D, 8>(a, s, err);
-    case 16: return launch_ext_tc_t<D, 16>(a, s, err);
+    case 1: return launch_ext_tc_t<D, 1, F8>(a, s, err);
+    case 2: return launch_ext_tc_t<D, 2, F8>(a, s, err);
+    case 4: return launch_ext_tc_t<D, 4, F8>(a, s, err);
+    case 8: return launch_ext_tc_t<D, 8, F8>(a, s, err);
+    case 16: return launch_ext_tc_t<D, 16, F8>(a, s, err);
     default: return CPATTN_ERR_UNSUPPORTED_SHAPE;
   }
 }
 
 int launch_gqa_partial_ext(const PartialArgs& a, cudaStream_t s, cudaError_t* err) {
   const int G = a.num_q_heads / a.num_kv_heads;
-  if (a.head_dim == 128) return ext_tc_dispatch_g<128>(a, G, s, err);
-  if (a.head_dim == 64) return ext_tc_dispatch_g<64>(a, G, s, err);
+  if (a.kv_fp8) {
+    if (a.head_dim == 128) return ext_tc_dispatch_g<128, true>(a, G, s, err);
+    if (a.head_dim == 64) return ext_tc_dispatch_g<64, true>(a, G, s, err);
+  } else {
+    if (a.head_dim == 128) return ext_tc_dispatch_g<128, false>(a, G, s, err);
+    if (a.head_dim == 64) return ext_tc_dispatch_g<64, false>(a, G, s, err);
+  }
   return CPATTN_ERR_UNSUPPORTED_SHAPE;
 }
 

@@ -463,14 +463,13 @@ int launch_gqa_partial_mma(const PartialArgs& a, cudaStream_t s, cudaError_t* er
   // groups of up to 8 heads: the transposed kernel (partial_gqa_mmat.cu);
   // groups of 16: the head-rows kernel above
   if (a.kv_fp8) {
-    // E4M3 pools: rows of one token only (the multi-token kernel reads bf16 pools)
-    if (a.qo_indptr != nullptr) return CPATTN_ERR_UNSUPPORTED_SHAPE;
-    if (G <= 8) return launch_gqa_partial_mmat(a, s, err);
-    if (a.head_dim == 128) st = mma_dispatch_g<128, true>(a, G, s, err);
-    if (a.head_dim == 64) st = mma_dispatch_g<64, true>(a, G, s, err);
-    return st;
-  }
-  if (G <= 8) {
+    if (G <= 8) {
+      st = launch_gqa_partial_mmat(a, s, err);
+    } else {
+      if (a.head_dim == 128) st = mma_dispatch_g<128, true>(a, G, s, err);
+      if (a.head_dim == 64) st = mma_dispatch_g<64, true>(a, G, s, err);
+    }
+  } else if (G <= 8) {
     st = launch_gqa_partial_mmat(a, s, err);
   } else {
     if (a.head_dim == 128) st = mma_dispatch_g<128, false>(a, G, s, err);

@@ -141,7 +141,7 @@ def fp8_pool(w: Workload, k_descale: float, v_descale: float) -> Workload:
     """The same step with the pool kept as FP8 E4M3 codes and per-tensor
     descales (inputs unchanged; a bf16 layer only)."""
     if w.dtype != "bf16" or w.mla:
-        raise ValueError("FP8 pools are for bf16 GQA layers")
+        raise ValueError("FP8 pools are for bf16 GQA layers")  # the library refuses the rest
     return dataclasses.replace(w, kv_dtype="fp8", k_descale=float(k_descale), v_descale=float(v_descale),
                                name=f"{w.name}_fp8")
 

@@ -69,9 +69,16 @@ class OracleView:
 
     def final(self, rows=None, heads=None):
         w = self.w
-        if w.kv_dtype == "fp8":  # keys and values as the pool returns them
+        if w.kv_dtype == "fp8":
+            # keys and values as the pool returns them; a non-decode step's own
+            # tokens are attended from the step's bf16 K / V, not the pool
             k = oracle.e4m3_dequantize(oracle.e4m3_quantize(w.k_seq, w.k_descale), w.k_descale)
             v = oracle.e4m3_dequantize(oracle.e4m3_quantize(w.v_seq, w.v_descale), w.v_descale)
+            if not w.decode:
+                for b in range(w.num_real_rows):
+                    s0, c, n = int(w.seq_indptr[b]), int(w.ctx_len[b]), int(w.new_len[b])
+                    k[s0 + c: s0 + c + n] = oracle.raw_to_f64(w.k_seq[s0 + c: s0 + c + n])
+                    v[s0 + c: s0 + c + n] = oracle.raw_to_f64(w.v_seq[s0 + c: s0 + c + n])
         else:
             k = oracle.raw_to_f64(w.k_seq)
             v = oracle.mla_kv(k, w.head_dim_v)[1] if w.mla else oracle.raw_to_f64(w.v_seq)

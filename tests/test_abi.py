@@ -141,9 +141,10 @@ def test_fp8_descriptor_checks(lib):
     # kv_dtype 0 and kv_dtype == dtype mean the same pool
     assert lib.cpattn_pool_bytes(ctypes.byref(_desc(kv_dtype=0)), 0) == \
         lib.cpattn_pool_bytes(ctypes.byref(_desc(kv_dtype=B.DTYPE_BF16)), 0)
-    # E4M3 pools with ragged multi-token rows are not supported (refused before any launch)
-    assert lib.cp_paged_attn_partial(ctypes.byref(d), FAKE, FAKE, FAKE, 32, 2, 3, FAKE, FAKE, 100, FAKE, FAKE, 0.1,
-                                     FAKE, FAKE, FAKE, 1 << 30, None, None) == -3
+    # E4M3 pools are for GQA layers: an MLA descriptor is refused before any launch
+    mla = _desc(num_kv_heads=1, head_dim=576, head_dim_v=512, page_size=64, **fp8)
+    assert lib.cp_paged_attn_partial(ctypes.byref(mla), FAKE, FAKE, FAKE, 128, 1, 1, None, FAKE, 100, FAKE, FAKE,
+                                     0.1, FAKE, FAKE, FAKE, 1 << 30, None, None) == -3
 
 
 def test_fused_argument_checks(lib):

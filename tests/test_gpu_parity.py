@@ -71,6 +71,8 @@ SMALL = {
     "gqa_decode_fp8": lambda: W.gqa_decode_fp8(seed=38, batch=6, len_lo=20, len_hi=5000),
     "gqa_decode_fp8_I2_pad": lambda: W.interleaved(W.gqa_decode_fp8(seed=39, batch=5, len_lo=1, len_hi=2000,
                                                                     padding_spans=[1, 1]), 2),
+    "mixed_fp8": lambda: W.fp8_pool(W.mixed_step(seed=43, n_decode=3, n_extend=3, dec_ctx=(1, 2000), ext_new=(2, 40),
+                                                  ext_ctx=(0, 1500), token_multiple=64), 0.0123, 0.0137),
     "gqa_fp8_g1_d64": lambda: W.fp8_pool(W.build_workload("gqa_fp8_g1_d64", dtype="bf16", P=2, page_size=8,
                                                           num_q_heads=4, num_kv_heads=4, head_dim=64,
                                                           ctx_len=[3, 400, 1], new_len=[1] * 3, seed=40),
