@@ -108,7 +108,7 @@ _SIGNATURES = {
                                      _vp, _vp, _vp, _sz, _vp, _vp]),
     "cp_paged_attn_workspace_bytes": (_sz, [_pdesc, _i32, _i32, _i32]),
     "cp_paged_attn_partial_ex": (_i32, [_pdesc, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _i32, _vp, _vp, _f32,
-                                        _vp, _vp, _i32, _vp, _sz, _vp, _vp]),
+                                        _vp, _vp, _i32, _vp, _vp, _sz, _vp, _vp]),
     "lse_merge_views": (_i32, [_i32, ctypes.POINTER(PartialView), _i32, _i32, _i32, _i32, _vp, _i64, _i64, _vp,
                                _i64, _i64, _vp]),
     "cp_paged_attn_fused": (_i32, [_pdesc, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _f32,
@@ -235,7 +235,7 @@ def cp_paged_attn_fused(desc: PoolDesc, pool_k, pool_v, q, kv_len, max_kv_len, k
 
 def cp_paged_attn_partial_ex(desc: PoolDesc, pool_k, pool_v, q, kv_len, max_kv_len, kv_page_indptr,
                              kv_page_indices, scale, o_part, lse_part, workspace, lse_layout=LSE_TOKEN_MAJOR,
-                             qo_indptr=None, num_rows=None, dev_status=None, stream=None):
+                             qo_indptr=None, num_rows=None, row_order=None, dev_status=None, stream=None):
     """cp_paged_attn_partial with the LSE layout chosen (see ``cp_paged_attn_partial_ex`` in cpattn.h)."""
     lib = load_library()
     T, Hq = q.shape[0], q.shape[1]
@@ -244,7 +244,8 @@ def cp_paged_attn_partial_ex(desc: PoolDesc, pool_k, pool_v, q, kv_len, max_kv_l
                                       _i32_tensor(qo_indptr, "qo_indptr"), _i32_tensor(kv_len, "kv_len"),
                                       int(max_kv_len), _i32_tensor(kv_page_indptr, "kv_page_indptr"),
                                       _i32_tensor(kv_page_indices, "kv_page_indices"), float(scale), _ptr(o_part),
-                                      _ptr(lse_part), int(lse_layout), _ptr(workspace),
+                                      _ptr(lse_part), int(lse_layout), _i32_tensor(row_order, "row_order"),
+                                      _ptr(workspace),
                                       workspace.numel() * workspace.element_size(),
                                       _i32_tensor(dev_status, "dev_status"), _stream(stream))
     _check(st, "cp_paged_attn_partial_ex")

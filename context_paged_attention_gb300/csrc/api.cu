@@ -286,9 +286,10 @@ int cp_paged_attn_partial_ex(const cpattn_pool_desc* desc, const void* pool_k, c
                              int32_t num_q_heads, int32_t num_rows, int32_t num_tokens, const int32_t* qo_indptr,
                              const int32_t* kv_len, int32_t max_kv_len, const int32_t* kv_page_indptr,
                              const int32_t* kv_page_indices, float scale, float* o_part, float* lse_part,
-                             int32_t lse_layout, void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                             cudaStream_t stream) {
+                             int32_t lse_layout, const int32_t* row_order, void* workspace, size_t workspace_bytes,
+                             int32_t* dev_status, cudaStream_t stream) {
   FusedOut none;
+  none.row_order = qo_indptr == nullptr ? row_order : nullptr;
   return run_partial(desc, pool_k, pool_v, q, num_q_heads, num_rows, num_tokens, qo_indptr, kv_len, max_kv_len,
                      kv_page_indptr, kv_page_indices, scale, o_part, lse_part, lse_layout, none, workspace,
                      workspace_bytes, dev_status, stream);

@@ -103,11 +103,12 @@ class StripedAttention:
         P = self.w.P
         # one token a row (a decode step): the call takes no token -> row map
         one_per_row = self.w.decode and self.w.num_tokens == self.w.num_rows
-        B.cp_paged_attn_partial(self.desc, self.pool_k, self.pool_v, self.q, self.kv_len, self.max_kv_len,
-                                self.page_indptr, self.page_indices, self.w.scale, self.o_parts[:P],
-                                self.lse_parts[:P], self.workspace,
-                                qo_indptr=None if one_per_row else self.qo_indptr,
-                                num_rows=self.w.num_rows, dev_status=self.dev_status, stream=stream)
+        B.cp_paged_attn_partial_ex(self.desc, self.pool_k, self.pool_v, self.q, self.kv_len, self.max_kv_len,
+                                   self.page_indptr, self.page_indices, self.w.scale, self.o_parts[:P],
+                                   self.lse_parts[:P], self.workspace,
+                                   qo_indptr=None if one_per_row else self.qo_indptr,
+                                   num_rows=self.w.num_rows, row_order=self.row_order if one_per_row else None,
+                                   dev_status=self.dev_status, stream=stream)
 
     def own(self, stream=None):
         P = self.w.P

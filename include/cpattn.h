@@ -202,14 +202,17 @@ CPATTN_API size_t cp_paged_attn_workspace_bytes(const cpattn_pool_desc* desc, in
 
 /*
  * cp_paged_attn_partial_ex -- cp_paged_attn_partial with a choice of LSE
- * layout.  In the vLLM page "[Core] Add explicit layer parallel plans"
- * (_forward_with_dcp) the context attention returns its LSE head-major
- * ("[H, B]") while the DCP combine takes it token-major ("[B, H]"); a TP-mode
- * caller gathers the query heads of all partners (query_across_dcp), has each
- * partner attend all of them, and combines per head.  lse_layout selects
- * CPATTN_LSE_TOKEN_MAJOR or CPATTN_LSE_HEAD_MAJOR (anything else:
- * CPATTN_ERR_INVALID_ARG); every other argument is as for
- * cp_paged_attn_partial, and the values written are the same.
+ * layout and of the rows' dispatch order.  In the vLLM page "[Core] Add
+ * explicit layer parallel plans" (_forward_with_dcp) the context attention
+ * returns its LSE head-major ("[H, B]") while the DCP combine takes it
+ * token-major ("[B, H]"); a TP-mode caller gathers the query heads of all
+ * partners (query_across_dcp), has each partner attend all of them, and
+ * combines per head.  lse_layout selects CPATTN_LSE_TOKEN_MAJOR or
+ * CPATTN_LSE_HEAD_MAJOR (anything else: CPATTN_ERR_INVALID_ARG).  row_order
+ * is as for cp_paged_attn_fused (a device permutation of the rows, used when
+ * qo_indptr is NULL; longest rows first shortens the last wave; NULL: row
+ * order).  Every other argument is as for cp_paged_attn_partial, and the
+ * values written are the same.
  */
 CPATTN_API int cp_paged_attn_partial_ex(const cpattn_pool_desc* desc, const void* pool_k,
                                         const void* pool_v, const void* q, int32_t num_q_heads,
@@ -217,8 +220,8 @@ CPATTN_API int cp_paged_attn_partial_ex(const cpattn_pool_desc* desc, const void
                                         const int32_t* kv_len, int32_t max_kv_len,
                                         const int32_t* kv_page_indptr, const int32_t* kv_page_indices,
                                         float scale, float* o_part, float* lse_part, int32_t lse_layout,
-                                        void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                                        cudaStream_t stream);
+                                        const int32_t* row_order, void* workspace, size_t workspace_bytes,
+                                        int32_t* dev_status, cudaStream_t stream);
 
 /*
  * cp_paged_attn_fused -- the partials of all P partners and their exact merge

@@ -171,7 +171,7 @@ def test_partial_ex_and_view_checks(lib):
     d = _desc()
     # LSE layouts 0 (token-major) and 1 (head-major) only
     assert lib.cp_paged_attn_partial_ex(ctypes.byref(d), FAKE, FAKE, FAKE, 32, 1, 1, None, FAKE, 100, FAKE, FAKE,
-                                        0.1, FAKE, FAKE, 2, FAKE, 1 << 30, None, None) == -1
+                                        0.1, FAKE, FAKE, 2, None, FAKE, 1 << 30, None, None) == -1
     V = B.PartialView
     good = V(FAKE, FAKE, 512, 128, 4, 1)
     arr = (V * 17)(*([good] * 17))

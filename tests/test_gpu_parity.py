@@ -84,6 +84,14 @@ SMALL = {
     "mixed_g1": lambda: W.build_workload("mixed_g1", dtype="bf16", P=4, page_size=16, num_q_heads=4,
                                          num_kv_heads=4, head_dim=128, decode=False, ctx_len=[100, 0, 2000],
                                          new_len=[40, 9, 2], seed=42),
+    # group 16 (the head-rows decode kernel), one partner with interleave 4; E4M3 at group 16, D 64
+    "gqa_g16_P1_I4": lambda: W.interleaved(W.build_workload("gqa_g16_P1", dtype="bf16", P=1, page_size=16,
+                                                            num_q_heads=32, num_kv_heads=2, head_dim=128,
+                                                            ctx_len=[0, 37, 900], new_len=[1] * 3, seed=44), 4),
+    "gqa_fp8_g16_d64": lambda: W.fp8_pool(W.build_workload("gqa_fp8_g16_d64", dtype="bf16", P=2, page_size=8,
+                                                           num_q_heads=16, num_kv_heads=1, head_dim=64,
+                                                           ctx_len=[5, 300, 1200], new_len=[1] * 3, seed=45),
+                                          0.0102, 0.0187),
     "gqa_P16_ps16": lambda: W.build_workload("gqa_P16_ps16", dtype="bf16", P=16, page_size=16, num_q_heads=16,
                                              num_kv_heads=2, head_dim=128, ctx_len=[5, 40, 2000], new_len=[1] * 3,
                                              seed=29),
@@ -215,6 +223,24 @@ def test_head_major_lse_partial(small):
     assert att.status() == 0
     assert torch.equal(o, att.o_parts[:P])
     assert torch.equal(l_hm.transpose(1, 2), att.lse_parts[:P])
+
+
+def test_plain_partial_entry(small):
+    """cp_paged_attn_partial (natural row order, token-major LSE) writes the
+    same partials as the step's cp_paged_attn_partial_ex (longest rows first)."""
+    w, att = small
+    from context_paged_attention_gb300 import binding as B
+    P = w.P
+    o = torch.empty_like(att.o_parts[:P])
+    lse = torch.empty_like(att.lse_parts[:P])
+    one_per_row = w.decode and w.num_tokens == w.num_rows
+    B.cp_paged_attn_partial(att.desc, att.pool_k, att.pool_v, att.q, att.kv_len, att.max_kv_len, att.page_indptr,
+                            att.page_indices, w.scale, o, lse, att.workspace,
+                            qo_indptr=None if one_per_row else att.qo_indptr, num_rows=w.num_rows,
+                            dev_status=att.dev_status)
+    torch.cuda.synchronize()
+    assert att.status() == 0
+    assert torch.equal(o, att.o_parts[:P]) and torch.equal(lse, att.lse_parts[:P])
 
 
 def test_tp_mode_step(small):
