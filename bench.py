@@ -278,6 +278,23 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(used), "window_samples": len(inside), "source": self.source}
 
 
+# ---------------------------------------------------------------- replicas (N ranks, one GPU each)
+
+def max_over_ranks(dist, values, device):
+    """Max of each timing over the ranks (the slowest replica sets the job's time)."""
+    import torch
+
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def job_throughput(world, bytes_per_rank, ms_per_step):
+    """Whole-job GB/s: every replica's bytes over the slowest replica's step time."""
+    return world * bytes_per_rank / (ms_per_step * 1e-3) / 1e9
+
+
 # ---------------------------------------------------------------- CPU oracle timing
 
 def _oracle_row_task(task):
@@ -463,14 +480,12 @@ def run_ours(args, rank, world, local_rank):
                  "unit": "GB/s", "note": "informational: the same step replayed from one captured CUDA graph"}
 
     if dist is not None:
-        t = torch.tensor([total_ms, e2e["ms_per_step"] if e2e else 0.0], device=f"cuda:{local_rank}")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, e2e_ms = float(t[0]), float(t[1])
+        total_ms, e2e_ms = max_over_ranks(dist, [total_ms, e2e["ms_per_step"] if e2e else 0.0], f"cuda:{local_rank}")
         if e2e:
             e2e["ms_per_step"] = e2e_ms
     ms = total_ms / K
     kv_bytes = alg["kv"]
-    value = world * kv_bytes / (ms * 1e-3) / 1e9
+    value = job_throughput(world, kv_bytes, ms)
     peak, peak_src = load_peaks()
 
     if rank != 0:

@@ -60,3 +60,33 @@ def test_launch_counts_and_bytes():
     # fused: merged output instead of P partials; the KV bytes are the same
     f, u = bench.algorithmic_bytes(dec, True), bench.algorithmic_bytes(dec, False)
     assert f["kv"] == u["kv"] == dec.kv_bytes_read() and f["partial"] < u["partial"]
+
+
+def _rank_main(rank, world, port, out):
+    import torch.distributed as dist
+
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+    try:
+        # each replica reports its own step time; the job takes the slowest
+        got = bench.max_over_ranks(dist, [1.0 + rank, 10.0 * rank], "cpu")
+        out[rank] = got
+    finally:
+        dist.destroy_process_group()
+
+
+def test_replica_timing_reduction_gloo():
+    """Two CPU ranks (gloo): the max over ranks, and the job throughput of
+    world x per-rank bytes over the slowest step."""
+    import socket
+
+    import torch.multiprocessing as mp
+
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    mgr = mp.Manager()
+    out = mgr.dict()
+    mp.spawn(_rank_main, args=(2, port, out), nprocs=2, join=True)
+    assert out[0] == [2.0, 10.0] and out[1] == [2.0, 10.0]
+    assert bench.job_throughput(2, 1e9, 2.0) == 2 * 1e9 / 2e-3 / 1e9
+    assert bench.max_over_ranks(None, [3.0], "cpu") == [3.0]
