@@ -41,8 +41,12 @@ FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
 # sources whose digest keys the recorded ncu traffic of each partial kernel
 KERNEL_SOURCES = {
-    "gqa_partial": ["partial_gqa.cu", "partial_gqa_mma.cu", "partial_gqa_mmat.cu", "partial_gqa_ext_tc.cu", "gqa_core.cuh",
-                    "split_combine.cuh", "common.cuh", "tc05.cuh", "mma_sync.cuh"],
+    # one-token rows (decode steps): the plan, the dispatch, the decode kernels, the merges
+    "gqa_partial": ["partial_gqa.cu", "partial_gqa_mma.cu", "partial_gqa_mmat.cu", "gqa_core.cuh",
+                    "split_combine.cuh", "common.cuh", "mma_sync.cuh"],
+    # non-decode steps add the multi-token kernel
+    "gqa_mixed_partial": ["partial_gqa.cu", "partial_gqa_mma.cu", "partial_gqa_mmat.cu", "partial_gqa_ext_tc.cu",
+                          "gqa_core.cuh", "split_combine.cuh", "common.cuh", "mma_sync.cuh", "tc05.cuh"],
     "mla_partial": ["partial_gqa.cu", "partial_mla_tc.cu", "tc05.cuh", "split_combine.cuh", "common.cuh"],
 }
 
@@ -491,7 +495,8 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return
     achieved = alg["partial"] / (partial_ms * 1e-3) / 1e9
-    traffic = recorded_traffic("gqa_partial" if not w.mla else "mla_partial", args.config)
+    traffic = recorded_traffic("mla_partial" if w.mla else ("gqa_partial" if w.decode else "gqa_mixed_partial"),
+                               args.config)
     line = {
         "metric": METRIC,
         "value": round(value, 2),

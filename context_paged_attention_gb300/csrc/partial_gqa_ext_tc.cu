@@ -15,8 +15,9 @@
 // CTA = (chunk, partner p, KV head h, token block j), 4 warps; thread r owns
 // query row r = (token j * 128 / G + r / G, head h * G + r % G) and TMEM lane r,
 // so the online softmax is thread-local.  Shared memory: Q [128 x D] K-major
-// with the 128-byte swizzle, three stages of 32 keys (K and V, the same
-// layout; V is read M/N-major), P [128 x 32] bf16 K-major with the 64-byte
+// with the 128-byte swizzle, four stages of 32 keys (K and V, the same
+// layout; V is read M/N-major; tile i + 2 is requested as soon as tile i has
+// landed, into the stage of tile i - 2), P [128 x 32] bf16 K-major with the 64-byte
 // swizzle; O is normalised by the sum of the bf16-rounded probabilities (an
 // exact convex combination of the values; the LSE keeps the fp32 sum).
 // Tensor memory: 32 columns of S and D columns of O (256 allocated, two CTAs
@@ -34,7 +35,7 @@ namespace cpattn {
 
 namespace {
 constexpr int kXTile = 32;    // keys per tile
-constexpr int kXStages = 3;
+constexpr int kXStages = 4;
 constexpr int kXRows = 128;   // query rows per CTA
 }  // namespace
 
@@ -279,6 +280,7 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
       tc05::fence_smem_to_async();
       __syncthreads();
       const uint32_t kv0 = tc05::smem_addr(sKV + (F8 ? (i & 1) : (i % kXStages)) * Lt::STAGE);
+      load_tile(i + 2);  // into the stage of tile i - 2, whose P V completed before this tile
       uint32_t vmask;
       {
         const int k = k_begin + i * kXTile + lane;
@@ -300,7 +302,6 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
         have_pv = false;
         if (!alive) break;
       }
-      load_tile(i + 2);  // into the stage tile i-1 used
       alive = __syncthreads_and(tc05::mbar_wait(mb_s, s_phase & 1)) != 0;
       ++s_phase;
       if (!alive) break;
