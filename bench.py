@@ -59,7 +59,7 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="gqa_decode",
                     choices=["tiny_fp32", "gqa_decode", "long_gqa_decode", "mla_decode", "mixed_step",
-                             "gqa_decode_fp8"])
+                             "gqa_decode_fp8", "mixed_step_fp8"])
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
     ap.add_argument("--no-clocks", action="store_true", help="do not sample nvidia-smi")
@@ -77,6 +77,8 @@ def make_workload(name):
 
     if name == "gqa_decode_fp8":
         return W.gqa_decode_fp8()
+    if name == "mixed_step_fp8":
+        return W.fp8_pool(W.mixed_step(), 0.0123, 0.0137)
     return W.WORKLOADS[{"tiny_fp32": 1, "gqa_decode": 2, "long_gqa_decode": 3, "mla_decode": 4,
                         "mixed_step": 5}[name]]()
 

@@ -16,16 +16,12 @@
 // query row r = (token j * 128 / G + r / G, head h * G + r % G) and TMEM lane r,
 // so the online softmax is thread-local.  Shared memory: Q [128 x D] K-major
 // with the 128-byte swizzle, four stages of 32 keys (K and V, the same
-// layout; V is read M/N-major), P [128 x 32] bf16 K-major with the 64-byte
+// layout; V is read M/N-major; tile i + 2 is requested as soon as tile i has
+// landed, into the stage of tile i - 2), P [128 x 32] bf16 K-major with the 64-byte
 // swizzle; O is normalised by the sum of the bf16-rounded probabilities (an
 // exact convex combination of the values; the LSE keeps the fp32 sum).
-// Tensor memory: two 32-column S buffers and D columns of O (256 allocated,
-// two CTAs per SM).  Schedule of tile i: wait S(i); issue S(i + 1) into the
-// other buffer (the tensor pipe runs it during the softmax of tile i);
-// softmax; wait P V of tile i - 1 (P, O and that tile's stage are free);
-// rescale O if the running max rose; request tile i + 3; write P; issue
-// P V of tile i.  E4M3 pools: code rows land in a 3-stage ring and each tile
-// is converted exactly into one of three bf16 tiles before its S.  A
+// Tensor memory: 32 columns of S and D columns of O (256 allocated, two CTAs
+// per SM).  The S MMAs of a tile overlap the P V MMAs of the one before.  A
 // chunk split of a stripe is merged by the last CTA to arrive, per token.
 // Rows of one token are left to the decode kernel; this kernel also writes the
 // padding tokens past the last row.  Waits are bounded (CPATTN_DEV_TC_TIMEOUT).
@@ -52,14 +48,14 @@ struct ExtTcLayout {
   static constexpr int STAGE = 2 * TILE;              // K + V
   static constexpr int PBYTES = kXRows * 64;          // one P tile (bf16, 32 keys)
   static constexpr int TMEM_COLS = 256;
-  static constexpr int S_COL = 0;                     // S buffers: columns 0..31 and 32..63
+  static constexpr int S_COL = 0;                     // S: columns 0..31
   static constexpr int O_COL = 64;                    // O: columns 64..64+D
-  // E4M3 pools: the code rows of a tile land in a ring of 3 stages (K then
-  // V, [key][D] bytes) and are converted into one of 3 bf16 tiles
+  // E4M3 pools: the code rows of a tile land in a ring of kXStages stages
+  // (K then V, [key][D] bytes) and are converted into one of two bf16 tiles
   static constexpr int RING8 = 2 * kXTile * D;        // one E4M3 stage (K + V)
-  static constexpr int NTILE = 3;                     // E4M3: bf16 tiles and code stages
   static size_t smem_bytes(int page_slots, bool f8) {
-    const size_t tiles = f8 ? NTILE * (static_cast<size_t>(STAGE) + RING8) : kXStages * static_cast<size_t>(STAGE);
+    const size_t tiles = f8 ? 2 * static_cast<size_t>(STAGE) + kXStages * static_cast<size_t>(RING8)
+                            : kXStages * static_cast<size_t>(STAGE);
     return 1024 + QBYTES + tiles + PBYTES + 64 + static_cast<size_t>(page_slots) * 4;
   }
 };
@@ -72,9 +68,9 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base;
-  uint8_t* sKV = sQ + Lt::QBYTES;  // bf16 tiles the MMAs read: kXStages stages, or (E4M3) three
-  uint8_t* sRing8 = sKV + (F8 ? Lt::NTILE : kXStages) * Lt::STAGE;  // E4M3 code stages (unused for bf16)
-  uint8_t* sPh = sRing8 + (F8 ? Lt::NTILE * Lt::RING8 : 0);
+  uint8_t* sKV = sQ + Lt::QBYTES;  // bf16 tiles the MMAs read: kXStages stages, or (E4M3) two
+  uint8_t* sRing8 = sKV + (F8 ? 2 : kXStages) * Lt::STAGE;  // E4M3 code stages (unused for bf16)
+  uint8_t* sPh = sRing8 + (F8 ? kXStages * Lt::RING8 : 0);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sPh + Lt::PBYTES);  // [0] S done, [1] P V done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2);
   int* spg = reinterpret_cast<int*>(bars + 4);
@@ -207,7 +203,7 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
       if (i < ntiles) {
         const int64_t myrow = row_of(k_begin + i * kXTile + lane);
         if constexpr (F8) {  // code rows, [key][D] bytes per K / V
-          uint8_t* rk = sRing8 + (i % Lt::NTILE) * Lt::RING8;
+          uint8_t* rk = sRing8 + (i % kXStages) * Lt::RING8;
           uint8_t* rv = rk + kXTile * D;
           constexpr int CH8 = D / 16;
           for (int x = tid; x < kXTile * CH8; x += blockDim.x) {
@@ -241,12 +237,12 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
       }
       cp_async_commit();
     };
-    // E4M3: the codes of tile i -> bf16 tile i % 3 in the MMA layout (exact:
-    // every E4M3 value is a bf16 value); the tile it overwrites (i - 3) was
-    // last read by P V of tile i - 3, which has completed
+    // E4M3: the codes of tile i -> bf16 tile i % 2 in the MMA layout (exact:
+    // every E4M3 value is a bf16 value); the tile it overwrites (i - 2) was
+    // last read by P V of tile i - 2, which has completed
     auto convert_tile = [&](int i) {
-      const uint8_t* rk = sRing8 + (i % Lt::NTILE) * Lt::RING8;
-      uint8_t* wk = sKV + (i % Lt::NTILE) * Lt::STAGE;
+      const uint8_t* rk = sRing8 + (i % kXStages) * Lt::RING8;
+      uint8_t* wk = sKV + (i & 1) * Lt::STAGE;
       constexpr int CH8 = D / 16;
       for (int x = tid; x < 2 * kXTile * CH8; x += blockDim.x) {
         const int kv = x / (kXTile * CH8);  // 0: K, 1: V
@@ -270,74 +266,58 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
         }
       }
     };
-    // bf16 / E4M3 tile of tile i that the MMAs read
-    auto tile_addr = [&](int i) { return tc05::smem_addr(sKV + (i % (F8 ? Lt::NTILE : kXStages)) * Lt::STAGE); };
-    auto issue_s = [&](int i) {  // S(i) into buffer i % 2 (one thread)
-      const uint32_t kv0 = tile_addr(i);
-#pragma unroll
-      for (int s = 0; s < D / 16; ++s) {
-        const uint32_t off = (s >> 2) * (kXRows * 128) + (s & 3) * 32;
-        const uint32_t koff = (s >> 2) * Lt::BLK + (s & 3) * 32;
-        tc05::mma_ss(tbase + Lt::S_COL + (i & 1) * kXTile, tc05::desc_k128(q0 + off), tc05::desc_k128(kv0 + koff),
-                     id_s, s > 0);
-      }
-    };
-    load_tile(0);  // with Q
+    load_tile(0);
     load_tile(1);
-    load_tile(2);
 
     float m = -INFINITY, l = 0.f, lr = 0.f;  // running max (log2), fp32 sum, sum of the bf16-rounded p
-    if (ntiles > 0) {
-      cp_async_wait<2>();  // Q and tile 0 landed for this thread
+    bool have_pv = false;  // a P V MMA of this segment is in flight (or done but unwaited)
+    for (int i = 0; i < ntiles; ++i) {
+      cp_async_wait<1>();  // tile i (and Q) landed for this thread
       if constexpr (F8) {
-        __syncthreads();
-        convert_tile(0);
+        __syncthreads();  // every thread's codes of tile i landed
+        convert_tile(i);
       }
       tc05::fence_smem_to_async();
       __syncthreads();
-      if (tid == 0) {
-        tc05::fence_after_sync();
-        issue_s(0);
-        tc05::commit(mb_s);
-      }
-    }
-    for (int i = 0; i < ntiles; ++i) {
-      alive = __syncthreads_and(tc05::mbar_wait(mb_s, s_phase & 1)) != 0;  // S(i) done
-      ++s_phase;
-      if (!alive) break;
-      if (i + 1 < ntiles) {  // S(i + 1) into the other buffer: the tensor pipe runs it during the softmax of tile i
-        cp_async_wait<1>();  // tile i + 1 landed for this thread
-        if constexpr (F8) {
-          __syncthreads();
-          convert_tile(i + 1);
-        }
-        tc05::fence_smem_to_async();
-        __syncthreads();
-        if (tid == 0) {
-          tc05::fence_after_sync();
-          issue_s(i + 1);
-          tc05::commit(mb_s);
-        }
-      }
-      tc05::fence_after_sync();
+      const uint32_t kv0 = tc05::smem_addr(sKV + (F8 ? (i & 1) : (i % kXStages)) * Lt::STAGE);
+      load_tile(i + 2);  // into the stage of tile i - 2, whose P V completed before this tile
       uint32_t vmask;
       {
         const int k = k_begin + i * kXTile + lane;
         vmask = __ballot_sync(0xffffffffu, row_of(k) >= 0);
       }
+      if (tid == 0) {
+        tc05::fence_after_sync();
+#pragma unroll
+        for (int s = 0; s < D / 16; ++s) {
+          const uint32_t off = (s >> 2) * (kXRows * 128) + (s & 3) * 32;
+          const uint32_t koff = (s >> 2) * Lt::BLK + (s & 3) * 32;
+          tc05::mma_ss(tbase + Lt::S_COL, tc05::desc_k128(q0 + off), tc05::desc_k128(kv0 + koff), id_s, s > 0);
+        }
+        tc05::commit(mb_s);  // also covers the previous tile's P V
+      }
+      if (have_pv) {  // P V of tile i-1 done: its stage and P are free, O is stable
+        alive = __syncthreads_and(tc05::mbar_wait(mb_pv, pv_phase & 1)) != 0;
+        ++pv_phase;
+        have_pv = false;
+        if (!alive) break;
+      }
+      alive = __syncthreads_and(tc05::mbar_wait(mb_s, s_phase & 1)) != 0;
+      ++s_phase;
+      if (!alive) break;
+      tc05::fence_after_sync();
       float sv[32];
       {
         float v16[16];
-        tc05::ld_x16(my_lane + Lt::S_COL + (i & 1) * kXTile, v16);
+        tc05::ld_x16(my_lane + Lt::S_COL, v16);
         tc05::ld_wait();
 #pragma unroll
         for (int e = 0; e < 16; ++e) sv[e] = v16[e];
-        tc05::ld_x16(my_lane + Lt::S_COL + (i & 1) * kXTile + 16, v16);
+        tc05::ld_x16(my_lane + Lt::S_COL + 16, v16);
         tc05::ld_wait();
 #pragma unroll
         for (int e = 0; e < 16; ++e) sv[16 + e] = v16[e];
       }
-      tc05::fence_before_sync();  // this S buffer is reused by S(i + 2) after a later barrier
       float bm = -INFINITY;
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
@@ -345,52 +325,43 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
         bm = fmaxf(bm, sv[e]);
       }
       const bool up = bm > m + 8.f;
-      const float alpha = up ? exp2f(m - bm) : 1.f;
-      if (up) m = bm;
-      uint32_t hi[16];
-      float ps = 0.f, psr = 0.f;
+      if (__any_sync(0xffffffffu, up) && i > 0) {  // rescale O rows whose max rose (rare)
+        const float alpha = up ? exp2f(m - bm) : 1.f;
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const float pa = sv[2 * e] == -INFINITY ? 0.f : exp2f(sv[2 * e] - m);  // masked: 0, also while m is -inf
-        const float pb = sv[2 * e + 1] == -INFINITY ? 0.f : exp2f(sv[2 * e + 1] - m);
-        ps += pa + pb;
-        __nv_bfloat162 h2 = __floats2bfloat162_rn(pa, pb);
-        psr += __low2float(h2) + __high2float(h2);
-        hi[e] = *reinterpret_cast<uint32_t*>(&h2);
-      }
-      l = l * alpha + ps;
-      lr = lr * alpha + psr;
-      if (i > 0) {  // P V of tile i - 1 done: P is free, O is stable, its tile is free
-        alive = __syncthreads_and(tc05::mbar_wait(mb_pv, pv_phase & 1)) != 0;
-        ++pv_phase;
-        if (!alive) break;
-        tc05::fence_after_sync();
-        if (__any_sync(0xffffffffu, up)) {  // rescale this warp's O rows whose max rose (rare)
+        for (int col = 0; col < D; col += 16) {
+          float v[16];
+          tc05::ld_x16(my_lane + Lt::O_COL + col, v);
+          tc05::ld_wait();
 #pragma unroll
-          for (int col = 0; col < D; col += 16) {
-            float v[16];
-            tc05::ld_x16(my_lane + Lt::O_COL + col, v);
-            tc05::ld_wait();
-#pragma unroll
-            for (int e = 0; e < 16; ++e) v[e] *= alpha;
-            tc05::st_x16(my_lane + Lt::O_COL + col, v);
-          }
-          tc05::st_wait();
+          for (int e = 0; e < 16; ++e) v[e] *= alpha;
+          tc05::st_x16(my_lane + Lt::O_COL + col, v);
         }
+        tc05::st_wait();
+        l *= alpha;
+        lr *= alpha;
       }
-      // tile i + 3: bf16 into the stage of tile i - 1 (its P V just completed);
-      // E4M3 into the code stage of tile i, converted at the start of this tile
-      load_tile(i + 3);
+      if (up) m = bm;
+      {
+        uint32_t hi[16];
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4)
-        *reinterpret_cast<uint4*>(sPh + tc05::sw64(tid, q4)) =
-            make_uint4(hi[4 * q4], hi[4 * q4 + 1], hi[4 * q4 + 2], hi[4 * q4 + 3]);
+        for (int e = 0; e < 16; ++e) {
+          const float pa = sv[2 * e] == -INFINITY ? 0.f : exp2f(sv[2 * e] - m);  // masked: 0, also while m is -inf
+          const float pb = sv[2 * e + 1] == -INFINITY ? 0.f : exp2f(sv[2 * e + 1] - m);
+          l += pa + pb;
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(pa, pb);
+          lr += __low2float(h2) + __high2float(h2);
+          hi[e] = *reinterpret_cast<uint32_t*>(&h2);
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          *reinterpret_cast<uint4*>(sPh + tc05::sw64(tid, q4)) =
+              make_uint4(hi[4 * q4], hi[4 * q4 + 1], hi[4 * q4 + 2], hi[4 * q4 + 3]);
+      }
       tc05::fence_smem_to_async();
       tc05::fence_before_sync();
       __syncthreads();
       if (tid == 0) {
         tc05::fence_after_sync();
-        const uint32_t kv0 = tile_addr(i);
 #pragma unroll
         for (int s = 0; s < kXTile / 16; ++s) {
           const uint64_t bd = tc05::desc_mn128(kv0 + Lt::TILE + s * 16 * 128, Lt::BLK);
@@ -398,8 +369,9 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
         }
         tc05::commit(mb_pv);
       }
+      have_pv = true;
     }
-    if (alive && ntiles > 0) {
+    if (have_pv && alive) {
       alive = __syncthreads_and(tc05::mbar_wait(mb_pv, pv_phase & 1)) != 0;
       ++pv_phase;
     }
@@ -454,7 +426,7 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
       done = take_ticket(a.ws_cnt + slot0, nchunks);
       if (done) {
         merge_chunks(a, p, h, s0, s1 - s0, slot0, static_cast<int64_t>(P) * a.num_kv_heads, nchunks, G, D,
-                     reinterpret_cast<float*>(sKV), (F8 ? Lt::NTILE : kXStages) * Lt::STAGE / 4);
+                     reinterpret_cast<float*>(sKV), (F8 ? 2 : kXStages) * Lt::STAGE / 4);
         if (tid == 0) a.ws_cnt[slot0] = 0;
       }
     }
@@ -462,7 +434,7 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
       // fused: the last of the P partners of (segment, KV head) merges them
       int32_t* pair = a.ws_pair + static_cast<int64_t>(s0) * a.num_kv_heads + h;
       if (take_ticket(pair, P)) {
-        merge_partners(a, s0, s1 - s0, h, G, D, reinterpret_cast<float*>(sKV), (F8 ? Lt::NTILE : kXStages) * Lt::STAGE / 4);
+        merge_partners(a, s0, s1 - s0, h, G, D, reinterpret_cast<float*>(sKV), (F8 ? 2 : kXStages) * Lt::STAGE / 4);
         if (tid == 0) *pair = 0;
       }
     }
