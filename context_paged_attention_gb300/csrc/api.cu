@@ -159,6 +159,9 @@ int run_partial(const cpattn_pool_desc* desc, const void* pool_k, const void* po
   a.interleave = interleave_of(desc);
   a.page_size = desc->page_size;
   a.ps_l = desc->page_size / desc->P;
+  a.ps_shift = -1;
+  for (int sh = 0; sh < 31; ++sh)
+    if ((1 << sh) == a.ps_l) a.ps_shift = sh;
   a.num_pages = desc->num_pages;
   a.num_kv_heads = desc->num_kv_heads;
   a.num_q_heads = num_q_heads;

@@ -67,6 +67,15 @@ __device__ __forceinline__ int find_row(const int32_t* __restrict__ indptr, int 
   return lo;
 }
 
+// 2^x by the hardware approximation (PTX ex2.approx.ftz.f32: relative error
+// about 2^-22, results below 2^-126 flushed to zero).  Used where the
+// probability is rounded to bf16 right after (relative step 2^-9).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Keys of a row of L positions that partner p holds when runs of I
 // consecutive positions go round the P partners (I = 1: positions p, p + P, ...).
 // Those keys fill the partner's physical slots 0 .. n - 1 in stripe order.

@@ -92,6 +92,7 @@ struct PartialArgs {
   int32_t* ws_cnt;   // [T * P * Hkv] chunk tickets
   int32_t* ws_pair;  // [T * Hkv] partner tickets (fused calls)
   int P, interleave, page_size, ps_l, num_pages, num_kv_heads, num_q_heads, head_dim, head_dim_v;
+  int ps_shift;  // log2(ps_l) when ps_l is a power of two, else -1
   int num_rows, num_tokens, max_kv_len;
   int seg;         // tokens per staged segment (divides ps_l)
   int chunk;       // stripe tokens per CTA (multiple of seg)

@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
     const int64_t head_row0 = static_cast<int64_t>(p) * a.num_pages * a.num_kv_heads + h;
     auto row_of = [&](int k) -> int64_t {
       if (k >= k_end) return -1;
-      const int j = k / a.ps_l;
+      const int j = page_of_slot(a, k);
       const int pg = spg[j - j0];
       if (pg < 0) return -1;
       return (head_row0 + static_cast<int64_t>(pg) * a.num_kv_heads) * a.ps_l + (k - j * a.ps_l);
@@ -345,8 +345,8 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
         uint32_t hi[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float pa = sv[2 * e] == -INFINITY ? 0.f : exp2f(sv[2 * e] - m);  // masked: 0, also while m is -inf
-          const float pb = sv[2 * e + 1] == -INFINITY ? 0.f : exp2f(sv[2 * e + 1] - m);
+          const float pa = sv[2 * e] == -INFINITY ? 0.f : ex2_approx(sv[2 * e] - m);  // masked: 0, also while m is -inf
+          const float pb = sv[2 * e + 1] == -INFINITY ? 0.f : ex2_approx(sv[2 * e + 1] - m);
           l += pa + pb;
           __nv_bfloat162 h2 = __floats2bfloat162_rn(pa, pb);
           lr += __low2float(h2) + __high2float(h2);

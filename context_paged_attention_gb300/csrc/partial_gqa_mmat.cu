@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(kTWarps * 32, F8 ? 4 : 2) gqa_partial_mmat_ker
   const int64_t head_row0 = static_cast<int64_t>(p) * a.num_pages * a.num_kv_heads + h;
   auto row_of = [&](int k) -> int64_t {
     if (k >= k_end) return -1;
-    const int j = k / a.ps_l;
+    const int j = page_of_slot(a, k);
     const int pg = spg[j - j0];
     if (pg < 0) return -1;
     return (head_row0 + static_cast<int64_t>(pg) * a.num_kv_heads) * a.ps_l + (k - j * a.ps_l);

@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(128, 1)
   }
   // pool row of stripe slot k (k < k_end), or -1 on a rejected page
   auto pool_row = [&](int k) -> int64_t {
-    const int jj = k / a.ps_l;
+    const int jj = page_of_slot(a, k);
     const int pg = spg[jj - j0];
     if (pg < 0) return -1;
     return (static_cast<int64_t>(p) * a.num_pages + pg) * a.ps_l + (k - jj * a.ps_l);
@@ -347,8 +347,8 @@ __global__ void __launch_bounds__(128, 1)
       uint32_t pk[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
-        const float p0f = exp2f(sv[2 * e] - m);
-        const float p1f = exp2f(sv[2 * e + 1] - m);
+        const float p0f = sv[2 * e] == -INFINITY ? 0.f : ex2_approx(sv[2 * e] - m);  // masked: 0
+        const float p1f = sv[2 * e + 1] == -INFINITY ? 0.f : ex2_approx(sv[2 * e + 1] - m);
         l += p0f + p1f;
         __nv_bfloat162 pb = __floats2bfloat162_rn(p0f, p1f);
         lr += __low2float(pb) + __high2float(pb);

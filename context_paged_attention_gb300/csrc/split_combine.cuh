@@ -21,6 +21,11 @@
 
 namespace cpattn {
 
+// Page index of stripe slot k (k / ps_l; a shift when ps_l is a power of two).
+__device__ __forceinline__ int page_of_slot(const PartialArgs& a, int k) {
+  return a.ps_shift >= 0 ? (k >> a.ps_shift) : k / a.ps_l;
+}
+
 // Index of the LSE of (partner p, token t, query head hq) in lse_part.
 __device__ __forceinline__ int64_t lse_slot(const PartialArgs& a, int p, int t, int hq) {
   return p * a.lse_sp + t * a.lse_st + hq * a.lse_sh;
