@@ -126,8 +126,8 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
   const uint32_t mb_s = tc05::smem_addr(&bars[0]);
   const uint32_t mb_pv = tc05::smem_addr(&bars[1]);
   const uint32_t my_lane = tc05::taddr(tbase, warp * 32, 0);
-  const uint32_t q0 = tc05::smem_addr(sQ);
-  const uint32_t ph0 = tc05::smem_addr(sPh);
+  const uint64_t dq = tc05::desc_k128(tc05::smem_addr(sQ));
+  const uint64_t dph = tc05::desc_k64(tc05::smem_addr(sPh));
   const uint32_t id_s = tc05::idesc_bf16(128, kXTile, false, false);
   const uint32_t id_o = tc05::idesc_bf16(128, D, false, true);
   const uint8_t* poolk = static_cast<const uint8_t*>(a.pool_k);
@@ -288,11 +288,12 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
       }
       if (tid == 0) {
         tc05::fence_after_sync();
+        const uint64_t dk = tc05::desc_k128(kv0);
 #pragma unroll
         for (int s = 0; s < D / 16; ++s) {
           const uint32_t off = (s >> 2) * (kXRows * 128) + (s & 3) * 32;
           const uint32_t koff = (s >> 2) * Lt::BLK + (s & 3) * 32;
-          tc05::mma_ss(tbase + Lt::S_COL, tc05::desc_k128(q0 + off), tc05::desc_k128(kv0 + koff), id_s, s > 0);
+          tc05::mma_ss(tbase + Lt::S_COL, tc05::desc_add(dq, off), tc05::desc_add(dk, koff), id_s, s > 0);
         }
         tc05::commit(mb_s);  // also covers the previous tile's P V
       }
@@ -362,11 +363,11 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
       __syncthreads();
       if (tid == 0) {
         tc05::fence_after_sync();
+        const uint64_t dv = tc05::desc_mn128(kv0 + Lt::TILE, Lt::BLK);
 #pragma unroll
-        for (int s = 0; s < kXTile / 16; ++s) {
-          const uint64_t bd = tc05::desc_mn128(kv0 + Lt::TILE + s * 16 * 128, Lt::BLK);
-          tc05::mma_ss(tbase + Lt::O_COL, tc05::desc_k64(ph0 + s * 32), bd, id_o, i > 0 || s > 0);
-        }
+        for (int s = 0; s < kXTile / 16; ++s)
+          tc05::mma_ss(tbase + Lt::O_COL, tc05::desc_add(dph, s * 32), tc05::desc_add(dv, s * 16 * 128), id_o,
+                       i > 0 || s > 0);
         tc05::commit(mb_pv);
       }
       have_pv = true;
@@ -425,7 +426,7 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
       const int64_t slot0 = (static_cast<int64_t>(s0) * P + p) * a.num_kv_heads + h;
       done = take_ticket(a.ws_cnt + slot0, nchunks);
       if (done) {
-        merge_chunks(a, p, h, s0, s1 - s0, slot0, static_cast<int64_t>(P) * a.num_kv_heads, nchunks, G, D,
+        merge_chunks<4>(a, p, h, s0, s1 - s0, slot0, static_cast<int64_t>(P) * a.num_kv_heads, nchunks, G, D,
                      reinterpret_cast<float*>(sKV), (F8 ? 2 : kXStages) * Lt::STAGE / 4);
         if (tid == 0) a.ws_cnt[slot0] = 0;
       }
@@ -434,7 +435,7 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
       // fused: the last of the P partners of (segment, KV head) merges them
       int32_t* pair = a.ws_pair + static_cast<int64_t>(s0) * a.num_kv_heads + h;
       if (take_ticket(pair, P)) {
-        merge_partners(a, s0, s1 - s0, h, G, D, reinterpret_cast<float*>(sKV), (F8 ? 2 : kXStages) * Lt::STAGE / 4);
+        merge_partners<4>(a, s0, s1 - s0, h, G, D, reinterpret_cast<float*>(sKV), (F8 ? 2 : kXStages) * Lt::STAGE / 4);
         if (tid == 0) *pair = 0;
       }
     }

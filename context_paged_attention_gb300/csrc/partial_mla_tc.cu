@@ -21,8 +21,8 @@
 // add into registers -- O (512 x 128 fp32) and S together would need more
 // than the 512 columns.
 //
-// Loads: with page runs that tile the 32-key tile evenly, one thread copies
-// each run of latent rows with TMA (tensor-map bulk copies, 128-byte swizzle,
+// Loads: with page runs that tile the 32-key tile evenly, thread 32 (while
+// thread 0 issues the S MMAs) copies each run of latent rows with TMA (tensor-map bulk copies, 128-byte swizzle,
 // completion counted in bytes on the stage's mbarrier) -- 9 copies of 64
 // columns per run -- and Q the same way.  Other page sizes use 16-byte
 // cp.async copies.  Rows of keys past the stripe end are zeroed before P V
@@ -64,6 +64,8 @@ constexpr int kMainCols = 448;              // O columns kept in TMEM
 constexpr int kTailCol = 448;               // S, then the P V tail
 constexpr int kPageSlots = 256;             // staged page ids per CTA
 constexpr int kBars = 5;                    // tile stage 0 / 1 full, Q full, S done, P V done
+constexpr int kMergeUnroll = 8;             // float4 loads in flight a thread in the chunk / partner merges
+constexpr int kTmaThread = 32;              // issues the TMA copies (warp 1), beside thread 0's MMAs
 constexpr size_t kSmemBytes = 1024 /*align*/ + kQBytes + 2 * kTileBytes + kPBytes + kPageSlots * 4 + kBars * 8 + 8;
 }  // namespace
 
@@ -119,7 +121,7 @@ __global__ void __launch_bounds__(128, 1)
     float4* dst = reinterpret_cast<float4*>(a.o_part + orow * kDv);
     for (int e = 0; e < kDv / 4; ++e) dst[e] = make_float4(0.f, 0.f, 0.f, 0.f);
     a.lse_part[lse_slot(a, p, t, tid)] = -INFINITY;
-    if (a.fused) pair_finish(a, t, 0, kHeads, kDv, reinterpret_cast<float*>(sQ), kQBytes / 4);
+    if (a.fused) pair_finish<kMergeUnroll>(a, t, 0, kHeads, kDv, reinterpret_cast<float*>(sQ), kQBytes / 4);
     return;
   }
 
@@ -173,7 +175,7 @@ __global__ void __launch_bounds__(128, 1)
     uint8_t* st = sKV + (i & 1) * kTileBytes;
     const int k0 = k_begin + i * kTile;
     if constexpr (kTma) {
-      if (tid == 0) {
+      if (tid == kTmaThread) {
         const int runs = kTile / box_rows;
         uint32_t bytes = 0;
         for (int r = 0; r < runs; ++r) {
@@ -243,8 +245,8 @@ __global__ void __launch_bounds__(128, 1)
   const uint32_t id_256 = tc05::idesc_bf16(128, 256, false, true);
   const uint32_t id_192 = tc05::idesc_bf16(128, 192, false, true);
   const uint32_t id_64 = tc05::idesc_bf16(128, 64, false, true);
-  const uint32_t q0 = tc05::smem_addr(sQ);
-  const uint32_t p0 = tc05::smem_addr(sP);
+  const uint64_t dq = tc05::desc_k128(tc05::smem_addr(sQ));
+  const uint64_t dp = tc05::desc_k64(tc05::smem_addr(sP));
   const float sl = a.scale * kLog2e;
 
   float m = -INFINITY, l = 0.f, lr = 0.f;  // running max (log2), fp32 sum, sum of bf16-rounded p
@@ -285,13 +287,15 @@ __global__ void __launch_bounds__(128, 1)
     // columns 448..479, 18..35 into 480..511), summed after the read-back
     if (tid == 0) {
       tc05::fence_after_sync();
+      const uint64_t dk = tc05::desc_k128(kv0);
+#pragma unroll
       for (int s = 0; s < kDqk / 32; ++s) {
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
           const int ks = h2 * (kDqk / 32) + s;
           const uint32_t off = (ks & 3) * 32;
-          tc05::mma_ss(tbase + kTailCol + 32 * h2, tc05::desc_k128(q0 + (ks >> 2) * (kHeads * 128) + off),
-                       tc05::desc_k128(kv0 + (ks >> 2) * kBlkB + off), id_s, s > 0);
+          tc05::mma_ss(tbase + kTailCol + 32 * h2, tc05::desc_add(dq, (ks >> 2) * (kHeads * 128) + off),
+                       tc05::desc_add(dk, (ks >> 2) * kBlkB + off), id_s, s > 0);
         }
       }
       tc05::commit(mb_s);
@@ -366,12 +370,14 @@ __global__ void __launch_bounds__(128, 1)
     // O[:, 0:448] += P V ; tail (columns 448..511) = P V[:, 448:512]
     if (tid == 0) {
       tc05::fence_after_sync();
+      const uint64_t dv = tc05::desc_mn128(kv0, kBlkB);
+#pragma unroll
       for (int s = 0; s < kTile / 16; ++s) {
-        const uint64_t ad = tc05::desc_k64(p0 + s * 32);
-        const uint32_t vrow = kv0 + s * 16 * 128;
-        tc05::mma_ss(tbase, ad, tc05::desc_mn128(vrow, kBlkB), id_256, i > 0 || s > 0);
-        tc05::mma_ss(tbase + 256, ad, tc05::desc_mn128(vrow + 4 * kBlkB, kBlkB), id_192, i > 0 || s > 0);
-        tc05::mma_ss(tbase + kTailCol, ad, tc05::desc_mn128(vrow + 7 * kBlkB, kBlkB), id_64, s > 0);
+        const uint64_t ad = tc05::desc_add(dp, s * 32);
+        const uint32_t vrow = s * 16 * 128;
+        tc05::mma_ss(tbase, ad, tc05::desc_add(dv, vrow), id_256, i > 0 || s > 0);
+        tc05::mma_ss(tbase + 256, ad, tc05::desc_add(dv, vrow + 4 * kBlkB), id_192, i > 0 || s > 0);
+        tc05::mma_ss(tbase + kTailCol, ad, tc05::desc_add(dv, vrow + 7 * kBlkB), id_64, s > 0);
       }
       tc05::commit(mb_pv);
     }
@@ -426,11 +432,11 @@ __global__ void __launch_bounds__(128, 1)
   if (!alive) return;
   if (nchunks > 1) {
     if (!take_ticket(a.ws_cnt + slot, nchunks)) return;
-    const int64_t orow0 = (static_cast<int64_t>(p) * a.num_tokens + t) * a.num_q_heads;
-    merge_chunks(a, p, 0, t, 1, slot, 0, nchunks, kHeads, kDv, reinterpret_cast<float*>(sQ), kQBytes / 4);
+    merge_chunks<kMergeUnroll>(a, p, 0, t, 1, slot, 0, nchunks, kHeads, kDv, reinterpret_cast<float*>(sQ),
+                               kQBytes / 4);
     if (tid == 0) a.ws_cnt[slot] = 0;
   }
-  if (a.fused) pair_finish(a, t, 0, kHeads, kDv, reinterpret_cast<float*>(sQ), kQBytes / 4);
+  if (a.fused) pair_finish<kMergeUnroll>(a, t, 0, kHeads, kDv, reinterpret_cast<float*>(sQ), kQBytes / 4);
 }
 
 int mla_tc_chunk(int ps_l) {

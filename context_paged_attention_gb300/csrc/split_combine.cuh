@@ -59,10 +59,14 @@ __device__ __forceinline__ bool take_ticket(int32_t* counter, int arrivals_neede
 //   2. one warp per row turns them into weights exp(lse - max) / sum and the
 //      row's LSE with shuffle reductions;
 //   3. each thread sums weight * values over the entries for a float4 group
-//      of one row, the loads unrolled so several are in flight.
+//      of one row, the loads unrolled so several are in flight; with UNR > 1
+//      a thread takes UNR float4 groups (blockDim apart, so a warp's loads
+//      stay coalesced) and issues all UNR loads of an entry before it uses
+//      them: UNR x 16 bytes in flight a thread, for the wide rows (MLA's 512
+//      values x 128 heads) where one CTA merges a megabyte.
 // Rows go in batches that fit `scratch` (cap floats of shared memory the CTA
 // no longer uses; cap >= E + 1).  All threads of the CTA must call.
-template <class LseIn, class OIn, class Put, class PutLse>
+template <int UNR = 1, class LseIn, class OIn, class Put, class PutLse>
 __device__ __forceinline__ void merge_rows(int R, int E, int Dv, LseIn lse_in, OIn o_in, Put put, PutLse put_lse,
                                            float* scratch, int cap) {
   const int RB = max(1, min(R, cap / (E + 1)));
@@ -100,23 +104,58 @@ __device__ __forceinline__ void merge_rows(int R, int E, int Dv, LseIn lse_in, O
       }
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < nr * D4; idx += blockDim.x) {
-      const int r = idx / D4;
-      const int d = (idx - r * D4) * 4;
-      const float* wr = wt + r * E;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if constexpr (UNR == 1) {
+      for (int idx = threadIdx.x; idx < nr * D4; idx += blockDim.x) {
+        const int r = idx / D4;
+        const int d = (idx - r * D4) * 4;
+        const float* wr = wt + r * E;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-      for (int e = 0; e < E; ++e) {
-        const float w = wr[e];
-        if (w != 0.f) {  // empty partials' rows are never read
-          const float4 v = __ldcg(reinterpret_cast<const float4*>(o_in(r0 + r, e) + d));
-          acc.x = fmaf(w, v.x, acc.x);
-          acc.y = fmaf(w, v.y, acc.y);
-          acc.z = fmaf(w, v.z, acc.z);
-          acc.w = fmaf(w, v.w, acc.w);
+        for (int e = 0; e < E; ++e) {
+          const float w = wr[e];
+          if (w != 0.f) {  // empty partials' rows are never read
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(o_in(r0 + r, e) + d));
+            acc.x = fmaf(w, v.x, acc.x);
+            acc.y = fmaf(w, v.y, acc.y);
+            acc.z = fmaf(w, v.z, acc.z);
+            acc.w = fmaf(w, v.w, acc.w);
+          }
         }
+        put(r0 + r, d, acc);
       }
-      put(r0 + r, d, acc);
+    } else {
+      const int n4 = nr * D4;
+      for (int i0 = threadIdx.x; i0 < n4; i0 += blockDim.x * UNR) {
+        int rr[UNR], dd[UNR];
+        float4 acc[UNR];
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) {
+          const int idx = i0 + u * blockDim.x;
+          rr[u] = idx < n4 ? idx / D4 : -1;
+          dd[u] = idx < n4 ? (idx - rr[u] * D4) * 4 : 0;
+          acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        for (int e = 0; e < E; ++e) {
+          float w[UNR];
+          float4 v[UNR];
+#pragma unroll
+          for (int u = 0; u < UNR; ++u) {
+            w[u] = rr[u] >= 0 ? wt[rr[u] * E + e] : 0.f;
+            v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (w[u] != 0.f) v[u] = __ldcg(reinterpret_cast<const float4*>(o_in(r0 + rr[u], e) + dd[u]));
+          }
+#pragma unroll
+          for (int u = 0; u < UNR; ++u) {
+            acc[u].x = fmaf(w[u], v[u].x, acc[u].x);
+            acc[u].y = fmaf(w[u], v[u].y, acc[u].y);
+            acc[u].z = fmaf(w[u], v[u].z, acc[u].z);
+            acc[u].w = fmaf(w[u], v[u].w, acc[u].w);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < UNR; ++u)
+          if (rr[u] >= 0) put(r0 + rr[u], dd[u], acc[u]);
+      }
     }
   }
 }
@@ -125,6 +164,7 @@ __device__ __forceinline__ void merge_rows(int R, int E, int Dv, LseIn lse_in, O
 // (partner p, KV head h): token i's slot is slot0 + i * slot_step; ws rows
 // (slot * max_chunks + chunk) * Hg + head, Dv floats each.  Results go to the
 // partner partial o_part / lse_part of tokens t0 .. t0 + ntok - 1.
+template <int UNR = 1>
 __device__ __forceinline__ void merge_chunks(const PartialArgs& a, int p, int h, int t0, int ntok, int64_t slot0,
                                              int64_t slot_step, int nchunks, int Hg, int Dv, float* scratch,
                                              int cap) {
@@ -132,7 +172,7 @@ __device__ __forceinline__ void merge_chunks(const PartialArgs& a, int p, int h,
     const int i = r / Hg;
     return ((slot0 + i * slot_step) * a.max_chunks + e) * Hg + (r - i * Hg);
   };
-  merge_rows(
+  merge_rows<UNR>(
       ntok * Hg, nchunks, Dv, [&](int r, int e) { return __ldcg(a.ws_lse + wrow(r, e)); },
       [&](int r, int e) { return a.ws_o + wrow(r, e) * Dv; },
       [&](int r, int d, float4 v) {
@@ -151,6 +191,7 @@ __device__ __forceinline__ void merge_chunks(const PartialArgs& a, int p, int h,
 // partner partials (o_part / lse_part rows, which fused calls keep in the
 // workspace) and the optional extra partial (entry P); written as bf16
 // (round to nearest even) or fp32.  Row r = token t0 + r / Hg, head r % Hg.
+template <int UNR = 1>
 __device__ __forceinline__ void merge_partners(const PartialArgs& a, int t0, int ntok, int h, int Hg, int Dv,
                                                float* scratch, int cap) {
   const int64_t pstride = static_cast<int64_t>(a.num_tokens) * a.num_q_heads;  // rows between partners
@@ -160,7 +201,7 @@ __device__ __forceinline__ void merge_partners(const PartialArgs& a, int t0, int
     const int i = r / Hg;
     return static_cast<int64_t>(t0 + i) * a.num_q_heads + h * Hg + (r - i * Hg);
   };
-  merge_rows(
+  merge_rows<UNR>(
       ntok * Hg, E, Dv,
       [&](int r, int e) {
         const int i = r / Hg;
@@ -190,11 +231,12 @@ __device__ __forceinline__ void merge_partners(const PartialArgs& a, int t0, int
 // Fused calls, after a partner's partial of (token t, KV head h) is complete
 // in o_part (written directly, or merged from its chunks by this CTA): arrive
 // on the pair's ticket; the last of the P partners merges (all threads call).
+template <int UNR = 1>
 __device__ __forceinline__ void pair_finish(const PartialArgs& a, int t, int h, int Hg, int Dv, float* scratch,
                                             int cap) {
   int32_t* pair = a.ws_pair + static_cast<int64_t>(t) * a.num_kv_heads + h;
   if (!take_ticket(pair, a.P)) return;
-  merge_partners(a, t, 1, h, Hg, Dv, scratch, cap);
+  merge_partners<UNR>(a, t, 1, h, Hg, Dv, scratch, cap);
   if (threadIdx.x == 0) *pair = 0;
 }
 

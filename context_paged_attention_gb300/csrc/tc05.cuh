@@ -55,6 +55,15 @@ __device__ __forceinline__ uint64_t desc_mn128(uint32_t saddr, uint32_t block_st
   return make_desc(saddr, block_stride, 1024, kSwizzle128);
 }
 
+// The descriptor of an operand `byte_off` bytes further on: the start field
+// holds (address >> 4) of a shared-memory address below 256 KB, so adding
+// byte_off >> 4 (byte_off a multiple of 16, the sum still inside shared
+// memory) never carries out of it.  Lets an issuing loop build each
+// descriptor once and step it with one add.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t byte_off) {
+  return desc + static_cast<uint64_t>(byte_off >> 4);
+}
+
 // --- instruction descriptor (kind::f16, bf16 x bf16 -> f32) ------------------
 // bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format,
 // 15 A major (1 = MN), 16 B major (1 = MN), 17-22 N >> 3, 24-28 M >> 4.
