@@ -63,10 +63,106 @@ constexpr int kPBytes = kHeads * 64;              // 8192
 constexpr int kMainCols = 448;              // O columns kept in TMEM
 constexpr int kTailCol = 448;               // S, then the P V tail
 constexpr int kPageSlots = 256;             // staged page ids per CTA
-constexpr int kBars = 5;                    // tile stage 0 / 1 full, Q full, S done, P V done
+constexpr int kBars = 7;                    // tile stage 0 / 1 full, Q full, S done, P V done, 2 merge buffers
 constexpr int kMergeUnroll = 8;             // float4 loads in flight a thread in the chunk / partner merges
 constexpr int kTmaThread = 32;              // issues the TMA copies (warp 1), beside thread 0's MMAs
 constexpr size_t kSmemBytes = 1024 /*align*/ + kQBytes + 2 * kTileBytes + kPBytes + kPageSlots * 4 + kBars * 8 + 8;
+constexpr int kScratchB = kQBytes + 2 * kTileBytes + kPBytes;  // contiguous shared memory free after the key loop
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(mbar)
+               : "memory");
+}
+
+// Split-KV merge of the E chunk partials of (token t, partner p) into the
+// partner partial: the LSE merge, as merge_chunks does, with the chunk rows
+// brought into shared memory by bulk asynchronous copies (one thread keeps
+// E x HB x 2 KB in flight; two buffers, batches of HB heads), so that one CTA
+// reads the E x 256 KB at copy speed.  Returns false when the shared memory
+// cannot hold two batches of one head (the caller falls back to merge_chunks)
+// or a copy did not land within the poll limit (reported).  All threads call.
+__device__ bool mla_merge_chunks_bulk(const PartialArgs& a, int p, int t, int64_t slot, int E, uint8_t* scratch,
+                                      uint64_t* mb2) {
+  int HB = 8;
+  while (HB > 0 && 2 * E * HB * (kDv * 4) + E * kHeads * 4 > kScratchB) HB >>= 1;
+  if (HB == 0) return false;
+  const int tid = threadIdx.x;
+  const uint32_t buf_bytes = static_cast<uint32_t>(E * HB * kDv * 4);
+  uint8_t* buf0 = scratch;
+  float* wt = reinterpret_cast<float*>(scratch + 2 * buf_bytes);  // [E][128] weights
+  const uint32_t mb0 = tc05::smem_addr(&mb2[0]);
+  if (tid == 0) {
+    tc05::mbar_init(mb0, 1);
+    tc05::mbar_init(mb0 + 8, 1);
+    tc05::mbar_init_fence();
+  }
+  // weights of head `tid` (128 threads, one head each) and its merged LSE
+  {
+    const int h = tid;
+    const float* lp = a.ws_lse + (slot * a.max_chunks) * kHeads + h;
+    float mx = -INFINITY;
+    for (int e = 0; e < E; ++e) mx = fmaxf(mx, __ldcg(lp + e * kHeads));
+    float sum = 0.f;
+    for (int e = 0; e < E; ++e) {
+      const float l = __ldcg(lp + e * kHeads);
+      sum += (mx == -INFINITY || l == -INFINITY) ? 0.f : expf(l - mx);
+    }
+    const float inv = sum == 0.f ? 0.f : 1.f / sum;
+    for (int e = 0; e < E; ++e) {
+      const float l = __ldcg(lp + e * kHeads);
+      wt[e * kHeads + h] = (sum == 0.f || l == -INFINITY) ? 0.f : expf(l - mx) * inv;
+    }
+    a.lse_part[lse_slot(a, p, t, h)] = sum == 0.f ? -INFINITY : mx + logf(sum);
+  }
+  __syncthreads();
+  const int nbatch = kHeads / HB;
+  auto issue = [&](int k) {
+    const uint32_t mb = mb0 + (k & 1) * 8;
+    const uint32_t dst = tc05::smem_addr(buf0 + (k & 1) * buf_bytes);
+    tc05::mbar_arrive_expect_tx(mb, buf_bytes);
+    for (int e = 0; e < E; ++e)
+      bulk_g2s(dst + e * HB * kDv * 4, a.ws_o + ((slot * a.max_chunks + e) * kHeads + k * HB) * kDv, HB * kDv * 4, mb);
+  };
+  if (tid == 0) {
+    // the chunk rows were written by other CTAs' plain stores, published by
+    // the ticket; the copies read them through the async proxy
+    asm volatile("fence.proxy.async;\n" ::: "memory");
+    issue(0);
+    if (nbatch > 1) issue(1);
+  }
+  const int64_t orow0 = (static_cast<int64_t>(p) * a.num_tokens + t) * a.num_q_heads;
+  bool ok = true;
+  for (int k = 0; k < nbatch; ++k) {
+    ok = __syncthreads_and(tc05::mbar_wait(mb0 + (k & 1) * 8, (k >> 1) & 1)) != 0;
+    if (!ok) break;
+    const float4* bf = reinterpret_cast<const float4*>(buf0 + (k & 1) * buf_bytes);
+    for (int idx = tid; idx < HB * (kDv / 4); idx += blockDim.x) {
+      const int hl = idx / (kDv / 4);
+      const int h = k * HB + hl;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int e = 0; e < E; ++e) {
+        const float w = wt[e * kHeads + h];
+        const float4 v = bf[e * HB * (kDv / 4) + idx];
+        if (w != 0.f) {  // empty chunks' rows never enter the sum
+          acc.x = fmaf(w, v.x, acc.x);
+          acc.y = fmaf(w, v.y, acc.y);
+          acc.z = fmaf(w, v.z, acc.z);
+          acc.w = fmaf(w, v.w, acc.w);
+        }
+      }
+      reinterpret_cast<float4*>(a.o_part + (orow0 + h) * kDv)[idx - hl * (kDv / 4)] = acc;
+    }
+    __syncthreads();  // buffer k & 1 consumed
+    if (tid == 0 && k + 2 < nbatch) issue(k + 2);
+  }
+  if (!ok) {
+    if (tid == 0) report(a.dev_status, CPATTN_DEV_TC_TIMEOUT);
+    // nothing may land after the CTA exits: wait (bounded) for both buffers' copies
+    for (int k = 0; k < 2 && k < nbatch; ++k) tc05::mbar_wait(mb0 + k * 8, 0, 1u << 20);
+  }
+  return true;
+}
 }  // namespace
 
 template <bool kTma>
@@ -432,8 +528,9 @@ __global__ void __launch_bounds__(128, 1)
   if (!alive) return;
   if (nchunks > 1) {
     if (!take_ticket(a.ws_cnt + slot, nchunks)) return;
-    merge_chunks<kMergeUnroll>(a, p, 0, t, 1, slot, 0, nchunks, kHeads, kDv, reinterpret_cast<float*>(sQ),
-                               kQBytes / 4);
+    if (!mla_merge_chunks_bulk(a, p, t, slot, nchunks, sQ, bars + 5))
+      merge_chunks<kMergeUnroll>(a, p, 0, t, 1, slot, 0, nchunks, kHeads, kDv, reinterpret_cast<float*>(sQ),
+                                 kQBytes / 4);
     if (tid == 0) a.ws_cnt[slot] = 0;
   }
   if (a.fused) pair_finish<kMergeUnroll>(a, t, 0, kHeads, kDv, reinterpret_cast<float*>(sQ), kQBytes / 4);
