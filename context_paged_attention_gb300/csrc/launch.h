@@ -130,6 +130,7 @@ bool plan_partial(int mla, int fused, int P, int interleave, int page_size, int 
 int launch_gqa_partial(const PartialArgs& a, int dtype_bf16, cudaStream_t s, cudaError_t* err);
 int launch_gqa_partial_mma(const PartialArgs& a, cudaStream_t s, cudaError_t* err);
 int launch_gqa_partial_ext(const PartialArgs& a, cudaStream_t s, cudaError_t* err);
+int launch_gqa_partial_ext_ws(const PartialArgs& a, cudaStream_t s, cudaError_t* err);  // bf16 pools
 int launch_mla_partial(const PartialArgs& a, cudaStream_t s, cudaError_t* err);
 int mla_tc_chunk(int ps_l);  // keys per CTA of the MLA tensor-core kernel
 

@@ -1,5 +1,6 @@
 // cp_paged_attn_partial, GQA rows with several query tokens on the tcgen05
-// tensor cores (bf16 pools).
+// tensor cores, E4M3 pools (bf16 pools take the warp-specialised kernel of
+// partial_gqa_ext_ws.cu).
 //
 // A non-decode step attends the pool for its context only, and every new
 // token of a row sees the same context (mstar PR #1124 "Context / Sequence
@@ -476,14 +477,12 @@ static int ext_tc_dispatch_g(const PartialArgs& a, int G, cudaStream_t s, cudaEr
 }
 
 int launch_gqa_partial_ext(const PartialArgs& a, cudaStream_t s, cudaError_t* err) {
+  // bf16 pools: the warp-specialised kernel (partial_gqa_ext_ws.cu); E4M3
+  // pools: this kernel, which converts each tile of codes before its MMAs
+  if (!a.kv_fp8) return launch_gqa_partial_ext_ws(a, s, err);
   const int G = a.num_q_heads / a.num_kv_heads;
-  if (a.kv_fp8) {
-    if (a.head_dim == 128) return ext_tc_dispatch_g<128, true>(a, G, s, err);
-    if (a.head_dim == 64) return ext_tc_dispatch_g<64, true>(a, G, s, err);
-  } else {
-    if (a.head_dim == 128) return ext_tc_dispatch_g<128, false>(a, G, s, err);
-    if (a.head_dim == 64) return ext_tc_dispatch_g<64, false>(a, G, s, err);
-  }
+  if (a.head_dim == 128) return ext_tc_dispatch_g<128, true>(a, G, s, err);
+  if (a.head_dim == 64) return ext_tc_dispatch_g<64, true>(a, G, s, err);
   return CPATTN_ERR_UNSUPPORTED_SHAPE;
 }
 
