@@ -63,7 +63,8 @@ constexpr int W_PFULL = 18;   // [4 softmax warps] x2: P buffer written
 constexpr int W_PVDONE = 20;  // [commit] x2: P V of the buffer's tile done
 constexpr int W_Q = 22;       // [64 loader lanes]
 constexpr int W_FIN = 23;     // [commit]
-constexpr int W_BARS = 24;
+constexpr int W_MERGE = 24;   // [1 + bytes] x2: chunk rows landed (split-KV merge)
+constexpr int W_BARS = 26;
 
 template <int D>
 struct WsLayout {
@@ -83,6 +84,7 @@ struct WsLayout {
   static constexpr size_t OFF_MASK = OFF_BAR + W_BARS * 8;
   static constexpr size_t OFF_MISC = OFF_MASK + kMaskSlots * 4;  // TMEM base, abort flag
   static constexpr int SCRATCH_FLOATS = static_cast<int>((OFF_P - OFF_K) / 4);  // K + V rings, free after the loop
+  static constexpr int MERGE_BYTES = static_cast<int>(OFF_BAR);  // Q, rings and P: contiguous, free after the loop
   static constexpr size_t OFF_PG = OFF_MISC + 16;
   static size_t smem_bytes(int page_slots) { return 1024 + OFF_PG + static_cast<size_t>(page_slots) * 4; }
 };
@@ -101,6 +103,11 @@ __device__ __forceinline__ void ws_cp16(uint32_t dst, const void* src) {
 __device__ __forceinline__ void ws_cp16_zero(uint32_t dst, const void* any_gmem) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, 0;\n" ::"r"(dst), "l"(any_gmem) : "memory");
 }
+__device__ __forceinline__ void ws_bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(mbar)
+               : "memory");
+}
 // bounded wait on a phase; gives up when the abort flag is raised
 __device__ __forceinline__ bool ws_wait(uint32_t mbar, uint32_t parity, const volatile int* abort_flag) {
   for (uint32_t it = 0; it < (1u << 22); ++it) {
@@ -116,6 +123,102 @@ __device__ __forceinline__ bool ws_wait(uint32_t mbar, uint32_t parity, const vo
   return false;
 }
 }  // namespace
+
+// Split-KV merge of the E chunk partials of tokens s0 .. s1-1 (KV head h,
+// partner p) into the partner partial: the LSE merge of merge_chunks, with
+// each token's G x D chunk rows (2 KB at G 4, D 128) brought into shared
+// memory by bulk asynchronous copies, one thread keeping a batch of TB tokens
+// x E chunks in flight while the CTA combines the previous batch.  Returns
+// false (nothing done) when a batch of one token does not fit; a copy that
+// does not land within the poll limit is reported.  All threads call.
+template <int D, int G>
+__device__ bool ws_merge_chunks_bulk(const PartialArgs& a, int p, int h, int s0, int s1, int E, uint8_t* scratch,
+                                     int scratch_bytes, uint32_t mb0) {
+  constexpr int ROW = G * D;  // floats of one (token, chunk) block
+  const int ntok = s1 - s0;
+  const int wt_bytes = ((ntok * G * E * 4) + 15) & ~15;
+  int TB = (scratch_bytes - wt_bytes) / (2 * E * ROW * 4);
+  if (TB < 1) return false;
+  TB = min(TB, ntok);
+  const int tid = threadIdx.x;
+  const uint32_t buf_bytes = static_cast<uint32_t>(TB * E * ROW * 4);
+  float* wt = reinterpret_cast<float*>(scratch + 2 * buf_bytes);  // [ntok][G][E] weights
+  const int64_t sstep = static_cast<int64_t>(a.P) * a.num_kv_heads;
+  const int64_t slot0 = (static_cast<int64_t>(s0) * a.P + p) * a.num_kv_heads + h;
+  if (tid == 0) {
+    tc05::mbar_init(mb0, 1);
+    tc05::mbar_init(mb0 + 8, 1);
+    tc05::mbar_init_fence();
+  }
+  // weights and merged LSE of each (token, head) row
+  for (int r = tid; r < ntok * G; r += blockDim.x) {
+    const int i = r / G, g = r - i * G;
+    const float* lp = a.ws_lse + ((slot0 + i * sstep) * a.max_chunks) * G + g;
+    float mx = -INFINITY;
+    for (int e = 0; e < E; ++e) mx = fmaxf(mx, __ldcg(lp + e * G));
+    float sum = 0.f;
+    for (int e = 0; e < E; ++e) {
+      const float l = __ldcg(lp + e * G);
+      sum += (mx == -INFINITY || l == -INFINITY) ? 0.f : expf(l - mx);
+    }
+    const float inv = sum == 0.f ? 0.f : 1.f / sum;
+    for (int e = 0; e < E; ++e) {
+      const float l = __ldcg(lp + e * G);
+      wt[r * E + e] = (sum == 0.f || l == -INFINITY) ? 0.f : expf(l - mx) * inv;
+    }
+    a.lse_part[lse_slot(a, p, s0 + i, h * G + g)] = sum == 0.f ? -INFINITY : mx + logf(sum);
+  }
+  __syncthreads();
+  const int nbatch = (ntok + TB - 1) / TB;
+  auto issue = [&](int k) {
+    const uint32_t mb = mb0 + (k & 1) * 8;
+    const uint32_t dst = tc05::smem_addr(scratch + (k & 1) * buf_bytes);
+    const int t0 = k * TB, nt = min(TB, ntok - t0);
+    tc05::mbar_arrive_expect_tx(mb, static_cast<uint32_t>(nt * E * ROW * 4));
+    for (int i = 0; i < nt; ++i)
+      for (int e = 0; e < E; ++e)
+        ws_bulk_g2s(dst + (i * E + e) * ROW * 4, a.ws_o + ((slot0 + (t0 + i) * sstep) * a.max_chunks + e) * ROW,
+                    ROW * 4, mb);
+  };
+  if (tid == 0) {
+    // the chunk rows were written by other CTAs' plain stores, published by
+    // the ticket; the copies read them through the async proxy
+    asm volatile("fence.proxy.async;\n" ::: "memory");
+    issue(0);
+    if (nbatch > 1) issue(1);
+  }
+  bool ok = true;
+  for (int k = 0; k < nbatch; ++k) {
+    ok = __syncthreads_and(tc05::mbar_wait(mb0 + (k & 1) * 8, (k >> 1) & 1)) != 0;
+    if (!ok) break;
+    const float4* bf = reinterpret_cast<const float4*>(scratch + (k & 1) * buf_bytes);
+    const int t0 = k * TB, nt = min(TB, ntok - t0);
+    for (int idx = tid; idx < nt * (ROW / 4); idx += blockDim.x) {
+      const int i = idx / (ROW / 4), f = idx - i * (ROW / 4);  // token in batch, float4 of its G x D block
+      const int g = f / (D / 4);
+      const float* w = wt + ((t0 + i) * G + g) * E;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int e = 0; e < E; ++e) {
+        const float4 v = bf[(i * E + e) * (ROW / 4) + f];
+        if (w[e] != 0.f) {  // empty chunks' rows never enter the sum
+          acc.x = fmaf(w[e], v.x, acc.x);
+          acc.y = fmaf(w[e], v.y, acc.y);
+          acc.z = fmaf(w[e], v.z, acc.z);
+          acc.w = fmaf(w[e], v.w, acc.w);
+        }
+      }
+      const int64_t orow0 = (static_cast<int64_t>(p) * a.num_tokens + s0 + t0 + i) * a.num_q_heads + h * G;
+      reinterpret_cast<float4*>(a.o_part + orow0 * D)[f] = acc;
+    }
+    __syncthreads();  // buffer k & 1 consumed
+    if (tid == 0 && k + 2 < nbatch) issue(k + 2);
+  }
+  if (!ok) {
+    if (tid == 0) report(a.dev_status, CPATTN_DEV_TC_TIMEOUT);
+    for (int k = 0; k < 2 && k < nbatch; ++k) tc05::mbar_wait(mb0 + k * 8, 0, 1u << 20);  // nothing lands later
+  }
+  return true;
+}
 
 template <int D, int G>
 __global__ void __launch_bounds__(kWThreads, 2) gqa_partial_ext_ws_kernel(const PartialArgs a) {
@@ -251,7 +354,7 @@ __global__ void __launch_bounds__(kWThreads, 2) gqa_partial_ext_ws_kernel(const 
     }
     auto bar = [&](int i) { return tc05::smem_addr(&bars[i]); };
     if (tid == 0) {
-      for (int i = 0; i < W_BARS; ++i) {
+      for (int i = 0; i < W_MERGE; ++i) {  // the merge initialises its own two
         uint32_t cnt = 1;
         if (i < W_KFREE || (i >= W_VFULL && i < W_VFREE)) cnt = 32;  // one loader warp's lanes
         if (i == W_Q) cnt = 64;
@@ -318,6 +421,9 @@ __global__ void __launch_bounds__(kWThreads, 2) gqa_partial_ext_ws_kernel(const 
           }
         }
         const uint32_t dst0 = ring + st * Lt::TILE;
+        // unrolled: the shuffles and addresses of all the warp's rows are
+        // formed before the copies issue (one chain a row is latency-bound)
+#pragma unroll
         for (int key = ro; key < kWTile; key += RPI) {
           const int64_t row = __shfl_sync(0xffffffffu, myrow, key);
           const uint32_t dst = dst0 + coff + tc05::sw128(key, cc & 7);
@@ -509,8 +615,10 @@ __global__ void __launch_bounds__(kWThreads, 2) gqa_partial_ext_ws_kernel(const 
       const int64_t slot0 = (static_cast<int64_t>(s0) * P + p) * a.num_kv_heads + h;
       done = take_ticket(a.ws_cnt + slot0, nchunks);
       if (done) {
-        merge_chunks<kWMergeUnroll>(a, p, h, s0, s1 - s0, slot0, static_cast<int64_t>(P) * a.num_kv_heads, nchunks,
-                                    G, D, reinterpret_cast<float*>(sK), Lt::SCRATCH_FLOATS);
+        if (!ws_merge_chunks_bulk<D, G>(a, p, h, s0, s1, nchunks, base, Lt::MERGE_BYTES,
+                                        tc05::smem_addr(&bars[W_MERGE])))
+          merge_chunks<kWMergeUnroll>(a, p, h, s0, s1 - s0, slot0, static_cast<int64_t>(P) * a.num_kv_heads,
+                                      nchunks, G, D, reinterpret_cast<float*>(sK), Lt::SCRATCH_FLOATS);
         if (tid == 0) a.ws_cnt[slot0] = 0;
       }
     }
