@@ -21,18 +21,21 @@
 //   * warp 4, lane 0 (MMA): S of tile j+2 as soon as its keys landed and S of
 //     tile j was read, then P V of tile j once P(j) is written: the tensor
 //     core computes the next scores while the softmax warps work.
-//   * warps 5-6 (copies): Q once, then key tiles into a 3-stage ring with
-//     16-byte cp.async (keys past the stripe end or on a rejected page are
-//     zero-filled, and the stage's valid-key mask is published for the
-//     softmax); a stage is refilled once P V of its previous tile completed.
+//   * warps 5-7 (copies): Q once, then K tiles (warps 5 and 7, half the keys
+//     each) into a 4-stage ring refilled as soon as S of a stage's tile is
+//     done, and V tiles (warp 6) into a 3-stage ring refilled once P V of a
+//     stage's tile is done; 16-byte cp.async, a warp instruction covering
+//     whole 128-byte blocks of rows.  Keys past the stripe end or on a
+//     rejected page are zero-filled, and each tile's valid-key mask is
+//     published for the softmax.
 // Tensor memory (256 columns, two CTAs an SM): S in two 32-column buffers,
 // O at column 64.  O is normalised by the sum of the bf16-rounded
 // probabilities (an exact convex combination of the values); the LSE keeps
 // the fp32 sum.  A chunk split of a stripe is merged by the last chunk CTA of
-// the segment.  CTAs past the last row block write the padding tokens'
-// 0 / -inf.  Every wait is bounded; one that runs out raises the CTA's abort
-// flag, which ends every other wait, and the call reports
-// CPATTN_DEV_TC_TIMEOUT.
+// the segment, its chunk rows brought in by bulk asynchronous copies.  The
+// CTAs of chunk 0 also write the padding tokens' 0 / -inf.  Every wait is
+// bounded; one that runs out raises the CTA's abort flag, which ends every
+// other wait, and the call reports CPATTN_DEV_TC_TIMEOUT.
 #include "common.cuh"
 #include "launch.h"
 #include "split_combine.cuh"
@@ -47,13 +50,14 @@ constexpr int kVStages = 3;     // V ring: a stage is refilled once P V of its t
 constexpr int kMaskSlots = 8;   // valid-key masks of the tiles in flight
 constexpr int kWRows = 128;     // query rows per CTA
 constexpr int kWMma = 128;      // lane 0 of warp 4 issues the MMAs
-constexpr int kWLoadK = 5;      // warp 5 copies K tiles, warp 6 V tiles (both: Q)
-constexpr int kWLoadV = 6;
-constexpr int kWThreads = 32 * 7;
+constexpr int kWLoadK = 5;      // warps 5 and 7 copy K tiles (half the keys each), warp 6
+constexpr int kWLoadV = 6;      // V tiles; all three copy Q
+constexpr int kWLoadK2 = 7;
+constexpr int kWThreads = 32 * 8;
 constexpr int kWMergeUnroll = 4;
 
 // barrier indices (arrival counts in brackets)
-constexpr int W_KFULL = 0;    // [32 K-loader lanes] x4: K tile landed
+constexpr int W_KFULL = 0;    // [64 K-loader lanes] x4: K tile landed
 constexpr int W_KFREE = 4;    // [commit] x4: S of the stage's tile done
 constexpr int W_VFULL = 8;    // [32 V-loader lanes] x3: V tile landed
 constexpr int W_VFREE = 11;   // [commit] x3: P V of the stage's tile done
@@ -61,7 +65,7 @@ constexpr int W_SDONE = 14;   // [commit] x2: S of the buffer's tile done
 constexpr int W_SFREE = 16;   // [4 softmax warps] x2: S buffer read
 constexpr int W_PFULL = 18;   // [4 softmax warps] x2: P buffer written
 constexpr int W_PVDONE = 20;  // [commit] x2: P V of the buffer's tile done
-constexpr int W_Q = 22;       // [64 loader lanes]
+constexpr int W_Q = 22;       // [96 loader lanes]
 constexpr int W_FIN = 23;     // [commit]
 constexpr int W_MERGE = 24;   // [1 + bytes] x2: chunk rows landed (split-KV merge)
 constexpr int W_BARS = 26;
@@ -228,7 +232,7 @@ __global__ void __launch_bounds__(kWThreads, 2) gqa_partial_ext_ws_kernel(const 
   constexpr int RPI = 32 / CH;    // rows a warp instruction copies
   static_assert(G >= 1 && G <= 16 && (D == 64 || D == 128), "shape");
   extern __shared__ uint8_t smem_raw[];
-  __shared__ int s_scan[8];
+  __shared__ int s_scan[kWThreads / 32];  // one partial sum a warp
   __shared__ int s_row[3];  // row, first token, end token of this CTA's block
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base;
@@ -289,7 +293,7 @@ __global__ void __launch_bounds__(kWThreads, 2) gqa_partial_ext_ws_kernel(const 
       if (lane == 31) s_scan[warp] = incl;
       __syncthreads();
       int before = done_blocks, total = done_blocks;
-      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+      for (int w = 0; w < kWThreads / 32; ++w) {
         if (w < warp) before += s_scan[w];
         total += s_scan[w];
       }
@@ -356,8 +360,9 @@ __global__ void __launch_bounds__(kWThreads, 2) gqa_partial_ext_ws_kernel(const 
     if (tid == 0) {
       for (int i = 0; i < W_MERGE; ++i) {  // the merge initialises its own two
         uint32_t cnt = 1;
-        if (i < W_KFREE || (i >= W_VFULL && i < W_VFREE)) cnt = 32;  // one loader warp's lanes
-        if (i == W_Q) cnt = 64;
+        if (i < W_KFREE) cnt = 64;                    // the two K warps' lanes
+        if (i >= W_VFULL && i < W_VFREE) cnt = 32;    // the V warp's lanes
+        if (i == W_Q) cnt = 96;
         if (i >= W_SFREE && i < W_SFREE + 4) cnt = 4;  // sfree, pfull: one arrival a softmax warp
         tc05::mbar_init(bar(i), cnt);
       }
@@ -371,13 +376,14 @@ __global__ void __launch_bounds__(kWThreads, 2) gqa_partial_ext_ws_kernel(const 
     const uint32_t tbase = *tmem_slot;
 
     bool alive = true;
-    if (warp == kWLoadK || warp == kWLoadV) {
-      // ================= copies: Q (both warps), then K tiles (warp 5) or V tiles (warp 6) =================
-      const bool is_k = (warp == kWLoadK);
+    if (warp >= kWLoadK) {
+      // ================= copies: Q (all three), then K tiles (warps 5, 7) or V tiles (warp 6) =================
+      const bool is_k = (warp != kWLoadV);
+      const int khalf = (warp == kWLoadK2) ? 1 : 0;  // K warps: which half of each tile's keys
       {
         const uint8_t* q = static_cast<const uint8_t*>(a.q);
         const uint32_t q0 = tc05::smem_addr(sQ);
-        for (int x = (is_k ? 0 : 32) + lane; x < kWRows * CH; x += 64) {
+        for (int x = (warp - kWLoadK) * 32 + lane; x < kWRows * CH; x += 96) {
           const int r = x / CH, cc = x - r * CH;
           const int tok = s0 + r / G;
           const uint32_t dst = q0 + (cc >> 3) * Lt::QBLK + tc05::sw128(r, cc & 7);
@@ -401,16 +407,17 @@ __global__ void __launch_bounds__(kWThreads, 2) gqa_partial_ext_ws_kernel(const 
           const bool ok = ws_wait(bar(b_free + st), ((i - nst) / nst) & 1, s_abort);
           if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
         }
-        int64_t myrow = -1;  // lane k: pool row of key k of the tile
+        int myrow = -1;  // lane k: pool row of key k of the tile (the launch checks rows fit 31 bits)
         {
           const int k = k_begin + i * kWTile + lane;
           if (k < k_end) {
             const int j = page_of_slot(a, k);
             const int pg = spg[j - j0];
-            if (pg >= 0) myrow = (head_row0 + static_cast<int64_t>(pg) * a.num_kv_heads) * a.ps_l + (k - j * a.ps_l);
+            if (pg >= 0)
+              myrow = static_cast<int>((head_row0 + static_cast<int64_t>(pg) * a.num_kv_heads) * a.ps_l + (k - j * a.ps_l));
           }
         }
-        if (is_k) {
+        if (is_k && khalf == 0) {
           // keys of the tile that hold data, for the softmax mask: written
           // before the tile's copies; its slot is rewritten kMaskSlots tiles
           // later, when the softmax has long read it
@@ -423,11 +430,12 @@ __global__ void __launch_bounds__(kWThreads, 2) gqa_partial_ext_ws_kernel(const 
         const uint32_t dst0 = ring + st * Lt::TILE;
         // unrolled: the shuffles and addresses of all the warp's rows are
         // formed before the copies issue (one chain a row is latency-bound)
-#pragma unroll
-        for (int key = ro; key < kWTile; key += RPI) {
-          const int64_t row = __shfl_sync(0xffffffffu, myrow, key);
+        const int kstep = is_k ? 2 * RPI : RPI;  // the K warps split the keys
+#pragma unroll 8
+        for (int key = ro + khalf * RPI; key < kWTile; key += kstep) {
+          const int row = __shfl_sync(0xffffffffu, myrow, key);
           const uint32_t dst = dst0 + coff + tc05::sw128(key, cc & 7);
-          if (row >= 0) ws_cp16(dst, pool + (row * D + cc * 8) * 2);
+          if (row >= 0) ws_cp16(dst, pool + (static_cast<int64_t>(row) * D + cc * 8) * 2);
           else ws_cp16_zero(dst, pool);  // masked key: zero row (finite scores, zero values)
         }
         ws_cp_arrive(bar(b_full + st));
@@ -639,6 +647,9 @@ static int launch_ext_ws_t(const PartialArgs& a, cudaStream_t s, cudaError_t* er
   const int page_slots = a.chunk / a.ps_l + 2;
   const size_t smem = WsLayout<D>::smem_bytes(page_slots);
   if (smem > 227 * 1024) return CPATTN_ERR_UNSUPPORTED_SHAPE;
+  // the copy warps exchange pool row indices as 32-bit values
+  if (static_cast<int64_t>(a.P) * a.num_pages * a.num_kv_heads * a.ps_l >= (int64_t{1} << 31))
+    return CPATTN_ERR_UNSUPPORTED_SHAPE;
   auto kern = gqa_partial_ext_ws_kernel<D, G>;
   static std::atomic<int> smem_set[64];
   *err = ensure_smem(kern, smem, smem_set);
