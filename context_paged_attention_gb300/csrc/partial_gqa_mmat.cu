@@ -35,12 +35,15 @@ constexpr int kTWarps = 4;
 constexpr int kTKeys = 16;  // keys a stage
 }  // namespace
 
-// Shared memory of one CTA: the warps' cp.async rings.  bf16: 3 stages (96 KB
-// at D 128, two CTAs an SM, 128 KB of K/V in flight an SM); E4M3: 3 stages of
+// Shared memory of one CTA: the warps' cp.async rings.  bf16: 2 stages (64 KB
+// at D 128, three CTAs an SM at <= 170 registers: 96 KB of K/V in flight an
+// SM, and while one CTA starts or finishes -- page table and first copies;
+// cross-warp merge, partial write, split-KV ticket -- two keep streaming;
+// 3 stages at two CTAs an SM ran 3% slower on short rows); E4M3: 3 stages of
 // half-size rows (48 KB, four CTAs an SM at <= 128 registers, 16 warps).
 template <int D, bool F8>
 struct TSmem {
-  static constexpr int NST = 3;
+  static constexpr int NST = F8 ? 3 : 2;
   static constexpr int SRC_ROWB = F8 ? D : 2 * D;
   static constexpr int RING_STAGE = kTKeys * SRC_ROWB;
   static constexpr size_t MAIN = static_cast<size_t>(kTWarps) * NST * RING_STAGE * 2;
@@ -59,7 +62,7 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
 }
 
 template <int D, int G, bool F8>
-__global__ void __launch_bounds__(kTWarps * 32, F8 ? 4 : 2) gqa_partial_mmat_kernel(const PartialArgs a) {
+__global__ void __launch_bounds__(kTWarps * 32, F8 ? 4 : 3) gqa_partial_mmat_kernel(const PartialArgs a) {
   using SM = TSmem<D, F8>;
   constexpr int NW = kTWarps;
   constexpr int NST = SM::NST;
