@@ -241,11 +241,13 @@ bool plan_partial(int mla, int fused, int P, int interleave, int page_size, int 
     chunk = mla_tc_chunk(ps_l);
     unit = 32;
   } else if (dtype_bytes == 2) {
-    // tensor-core path: 16-key stages, 4 warps; about four chunks on the
-    // longest stripe, within [1024, 2048] keys (long enough to amortise a CTA's
-    // start and merge, short enough to balance rows of unequal length)
-    chunk = (max_stripe + 3) / 4;
-    chunk = chunk < 1024 ? 1024 : (chunk > 2048 ? 2048 : chunk);
+    // tensor-core paths: 2048-key chunks.  Splitting shorter stripes costs
+    // more (a device-scope ticket and a merge of the chunk partials at the end
+    // of each CTA) than the balance it buys, now that three decode CTAs share
+    // an SM; measured on decode rows of 512-8192 keys (P 4) and on the mixed
+    // step, 1024- and 512-key chunks were 2-9% and 14% slower; longer stripes
+    // (the 64k-128k rows) lose 0.5% at 4096.
+    chunk = 2048;
     unit = 64;
   } else {
     // CUDA-core path: about eight chunks on the longest stripe, within [256, 2048] keys

@@ -192,12 +192,16 @@ def test_partial_ex_and_view_checks(lib):
 def test_workspace_sizing(lib):
     d = _desc()
     small = lib.cp_paged_attn_workspace_bytes(ctypes.byref(d), 32, 64, 256)
-    big = lib.cp_paged_attn_workspace_bytes(ctypes.byref(d), 32, 64, 8192)
-    assert small > 0 and big > small
+    mid = lib.cp_paged_attn_workspace_bytes(ctypes.byref(d), 32, 64, 8192)
+    # stripes past one split-KV chunk need room for the chunk partials
+    big = lib.cp_paged_attn_workspace_bytes(ctypes.byref(d), 32, 64, 1 << 16)
+    assert small > 0 and mid >= small and big > mid
     assert lib.cp_paged_attn_workspace_bytes(ctypes.byref(d), 30, 64, 8192) == 0
     # too-small workspace is refused before any launch
     assert lib.cp_paged_attn_partial(ctypes.byref(d), FAKE, FAKE, FAKE, 32, 64, 64, None, FAKE, 8192, FAKE, FAKE,
-                                     0.1, FAKE, FAKE, FAKE, big - 1, None, None) == -5
+                                     0.1, FAKE, FAKE, FAKE, mid - 1, None, None) == -5
+    assert lib.cp_paged_attn_partial(ctypes.byref(d), FAKE, FAKE, FAKE, 32, 64, 64, None, FAKE, 1 << 16, FAKE,
+                                     FAKE, 0.1, FAKE, FAKE, FAKE, big - 1, None, None) == -5
 
 
 def test_binding_refuses_cpu_tensors(lib):

@@ -73,6 +73,16 @@ SMALL = {
                                                                     padding_spans=[1, 1]), 2),
     "mixed_fp8": lambda: W.fp8_pool(W.mixed_step(seed=43, n_decode=3, n_extend=3, dec_ctx=(1, 2000), ext_new=(2, 40),
                                                   ext_ctx=(0, 1500), token_multiple=64), 0.0123, 0.0137),
+    # stripes longer than the 2048-key split-KV chunk: the chunk merges of the
+    # decode kernel, of the multi-token kernel (bulk-copy merge, batches of
+    # token rows) and of the E4M3 kernels
+    "gqa_decode_split": lambda: W.gqa_decode(seed=44, batch=4, len_lo=8300, len_hi=13000),
+    "gqa_decode_fp8_split": lambda: W.gqa_decode_fp8(seed=45, batch=3, len_lo=8300, len_hi=12000),
+    "mixed_split": lambda: W.mixed_step(seed=46, n_decode=2, n_extend=3, dec_ctx=(8300, 9000), ext_new=(20, 70),
+                                        ext_ctx=(8300, 10000), token_multiple=64),
+    "mixed_fp8_split": lambda: W.fp8_pool(W.mixed_step(seed=47, n_decode=1, n_extend=2, dec_ctx=(100, 900),
+                                                       ext_new=(5, 40), ext_ctx=(8300, 9500), token_multiple=64),
+                                          0.0123, 0.0137),
     "gqa_fp8_g1_d64": lambda: W.fp8_pool(W.build_workload("gqa_fp8_g1_d64", dtype="bf16", P=2, page_size=8,
                                                           num_q_heads=4, num_kv_heads=4, head_dim=64,
                                                           ctx_len=[3, 400, 1], new_len=[1] * 3, seed=40),
