@@ -534,7 +534,8 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": K * launches_per_step(w, fused),
         "launch_note": "per step: " + ("kv_write, the fused partial+merge" if fused else "kv_write, partial, lse_merge") +
                        (" (+ own_token and the multi-token-row partial kernel for non-decode steps)" if not w.decode
-                        else "") + "; plus one cudaMemsetAsync of the split tickets",
+                        else "") + "; plus one cudaMemsetAsync of the split-KV tickets when a stripe splits "
+                                   "or the call is fused",
         "path": args.path,
     }
     if graph is not None:

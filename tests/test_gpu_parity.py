@@ -78,10 +78,10 @@ SMALL = {
     # token rows) and of the E4M3 kernels
     "gqa_decode_split": lambda: W.gqa_decode(seed=44, batch=4, len_lo=8300, len_hi=13000),
     "gqa_decode_fp8_split": lambda: W.gqa_decode_fp8(seed=45, batch=3, len_lo=8300, len_hi=12000),
-    "mixed_split": lambda: W.mixed_step(seed=46, n_decode=2, n_extend=3, dec_ctx=(8300, 9000), ext_new=(20, 70),
-                                        ext_ctx=(8300, 10000), token_multiple=64),
-    "mixed_fp8_split": lambda: W.fp8_pool(W.mixed_step(seed=47, n_decode=1, n_extend=2, dec_ctx=(100, 900),
-                                                       ext_new=(5, 40), ext_ctx=(8300, 9500), token_multiple=64),
+    "mixed_split": lambda: W.mixed_step(seed=46, n_decode=1, n_extend=2, dec_ctx=(8300, 8600), ext_new=(33, 40),
+                                        ext_ctx=(8300, 8700), token_multiple=64),
+    "mixed_fp8_split": lambda: W.fp8_pool(W.mixed_step(seed=47, n_decode=1, n_extend=1, dec_ctx=(100, 900),
+                                                       ext_new=(33, 36), ext_ctx=(8300, 8600), token_multiple=64),
                                           0.0123, 0.0137),
     "gqa_fp8_g1_d64": lambda: W.fp8_pool(W.build_workload("gqa_fp8_g1_d64", dtype="bf16", P=2, page_size=8,
                                                           num_q_heads=4, num_kv_heads=4, head_dim=64,
