@@ -18,12 +18,55 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const MergeArgs a) {
   const int64_t items = static_cast<int64_t>(a.num_tokens) * a.num_heads;
   if (item >= items) return;
 
+  const int nvec = a.head_dim_v / 4;
+  if (a.num_partials <= 32) {
+    // lane i holds partial i's LSE and weight; the value loop takes the
+    // weights by shuffle (the same arithmetic and summation order as below)
+    const float li = lane < a.num_partials ? __ldg(a.lse_parts + lane * a.stride_lse + item) : -INFINITY;
+    float mx = li;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (mx != -INFINITY) {
+      const float wi = (li == -INFINITY) ? 0.f : expf(li - mx);
+      float wsum = wi;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
+      const float inv = 1.f / wsum;
+      for (int v = lane; v < nvec; v += 32) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int i = 0; i < a.num_partials; ++i) {
+          const float w = __shfl_sync(0xffffffffu, wi, i) * inv;
+          if (w != 0.f) {  // an empty partial contributes nothing (its output is not read)
+            const float4 o =
+                __ldg(reinterpret_cast<const float4*>(a.o_parts + i * a.stride_o + item * a.head_dim_v) + v);
+            acc.x = fmaf(w, o.x, acc.x);
+            acc.y = fmaf(w, o.y, acc.y);
+            acc.z = fmaf(w, o.z, acc.z);
+            acc.w = fmaf(w, o.w, acc.w);
+          }
+        }
+        if (a.out_bf16) {
+          __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+          __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+          uint2 packed;
+          packed.x = *reinterpret_cast<uint32_t*>(&lo);
+          packed.y = *reinterpret_cast<uint32_t*>(&hi);
+          reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + item * a.head_dim_v)[v] = packed;
+        } else {
+          reinterpret_cast<float4*>(static_cast<float*>(a.out) + item * a.head_dim_v)[v] = acc;
+        }
+      }
+      if (a.lse_out != nullptr && lane == 0) a.lse_out[item] = mx + logf(wsum);
+      return;
+    }
+  }
+
   float mx = -INFINITY;
   for (int i = lane; i < a.num_partials; i += 32) mx = fmaxf(mx, __ldg(a.lse_parts + i * a.stride_lse + item));
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
 
-  const int nvec = a.head_dim_v / 4;
   if (mx == -INFINITY) {  // every partial empty: padding merges to zero
     if (a.out_bf16) {
       uint2* o = reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + item * a.head_dim_v);

@@ -314,6 +314,41 @@ FULL = {
 }
 
 
+@pytest.mark.parametrize("n", [1, 5, 32, 33, 40])
+@pytest.mark.parametrize("out_bf16", [False, True])
+def test_lse_merge_partial_counts(n, out_bf16):
+    """Contiguous-partial merge against the oracle merge for partial counts on
+    both sides of the warp width (weights held one a lane up to 32), with
+    empty partials and a token whose partials are all empty."""
+    from context_paged_attention_gb300 import binding as B
+    rng = np.random.default_rng(100 + n)
+    T, H, Dv = 29, 3, 128
+    O = rng.standard_normal((n, T, H, Dv))
+    L = rng.standard_normal((n, T, H)) * 3
+    L[rng.random((n, T, H)) < 0.25] = -np.inf
+    L[:, 4, :] = -np.inf
+    dev = torch.device("cuda")
+    o_d = torch.tensor(O, dtype=torch.float32, device=dev)
+    l_d = torch.tensor(L, dtype=torch.float32, device=dev)
+    out = torch.zeros((T, H, Dv), dtype=torch.bfloat16 if out_bf16 else torch.float32, device=dev)
+    lse = torch.zeros((T, H), dtype=torch.float32, device=dev)
+    B.lse_merge(o_d, l_d, out, lse)
+    torch.cuda.synchronize()
+    O32 = o_d.cpu().numpy().astype(np.float64)
+    L32 = l_d.cpu().numpy().astype(np.float64)
+    want_o = np.zeros((T, H, Dv))
+    want_l = np.zeros((T, H))
+    for t in range(T):
+        want_o[t], want_l[t] = oracle.merge(O32[:, t], L32[:, t])
+    got_o = out.float().cpu().numpy().astype(np.float64)
+    got_l = lse.cpu().numpy().astype(np.float64)
+    assert np.all(got_o[4] == 0.0) and np.all(np.isneginf(got_l[4]))
+    assert_close(got_o, want_o, 1e-2 if out_bf16 else 1e-5, "merged O")
+    fin = np.isfinite(want_l)
+    assert np.array_equal(fin, np.isfinite(got_l))
+    assert_close(got_l[fin], want_l[fin], 1e-5, "merged LSE")
+
+
 @pytest.mark.parametrize("n,layout", [(1, "th"), (3, "ht"), (5, "mixed"), (16, "mixed")])
 def test_lse_merge_views(n, layout):
     """Strided-view merge against the oracle merge on random partials (some
