@@ -559,32 +559,24 @@ def run_ours(args, rank, world, local_rank):
 
 
 def time_e2e(att, w, args, stream, fused=True):
-    """Same step through the public API, inputs copied from pinned host buffers each step."""
+    """Same step through the public API, its inputs copied each step from one
+    pinned host buffer (the step's packed inputs) and its output and LSE read
+    back into another."""
     import torch
 
-    names = ["q", "k_new", "v_new", "positions", "qo_indptr", "kv_len", "page_indptr", "page_indices"]
-    host = {}
-    h2d = 0
-    for n in names:
-        t = getattr(att, n)
-        if t is None:
-            continue
-        host[n] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-        host[n].copy_(t)
-        h2d += t.numel() * t.element_size()
-    out_h = torch.empty(att.out.shape, dtype=att.out.dtype, pin_memory=True)
-    lse_h = torch.empty(att.lse.shape, dtype=att.lse.dtype, pin_memory=True)
-    d2h = att.out.numel() * att.out.element_size() + att.lse.numel() * att.lse.element_size()
+    host_in = torch.empty(att.packed_inputs.shape, dtype=torch.uint8, pin_memory=True)
+    host_in.copy_(att.packed_inputs)
+    host_out = torch.empty(att.packed_outputs.shape, dtype=torch.uint8, pin_memory=True)
+    h2d = att.packed_inputs.numel()
+    d2h = att.packed_outputs.numel()
 
     def e2e_step():
-        for n, h in host.items():
-            getattr(att, n).copy_(h, non_blocking=True)
+        att.packed_inputs.copy_(host_in, non_blocking=True)
         if fused:
             att.run_step_fused()
         else:
             att.run_step()
-        out_h.copy_(att.out, non_blocking=True)
-        lse_h.copy_(att.lse, non_blocking=True)
+        host_out.copy_(att.packed_outputs, non_blocking=True)
 
     for _ in range(args.warmup):
         e2e_step()

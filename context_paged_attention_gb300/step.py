@@ -80,8 +80,32 @@ class StripedAttention:
         # dispatch order of the rows: longest first (the host knows the lengths)
         order = np.argsort(-w.kv_len.astype(np.int64), kind="stable").astype(np.int32)
         self.row_order = _to_torch(order, self.device)
+        # the step's inputs and outputs as views into one buffer each, so that
+        # a caller feeding the step from host memory makes one copy in and one
+        # copy out a step (``packed_inputs`` / ``packed_outputs``)
+        self.packed_inputs = self._pack(self.INPUTS)
+        self.packed_outputs = self._pack(("out", "lse"))
         if fill_history:
             self.fill_history()
+
+    # per-step inputs, in the order they are packed
+    INPUTS = ("q", "k_new", "v_new", "positions", "qo_indptr", "kv_len", "page_indptr", "page_indices", "row_order")
+
+    def _pack(self, names):
+        """Move the named tensors into one device buffer (256-byte aligned
+        offsets) and rebind them to views of it; returns the buffer."""
+        items = [(n, getattr(self, n)) for n in names if getattr(self, n) is not None]
+        offs, end = [], 0
+        for _, t in items:
+            end = (end + 255) // 256 * 256
+            offs.append(end)
+            end += t.numel() * t.element_size()
+        buf = torch.empty((max(end, 256),), dtype=torch.uint8, device=self.device)
+        for (n, t), o in zip(items, offs):
+            v = buf[o: o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+            v.copy_(t)
+            setattr(self, n, v)
+        return buf
 
     def fill_history(self):
         """Write every real row's context (positions 0 .. ctx-1) through cp_kv_write."""
