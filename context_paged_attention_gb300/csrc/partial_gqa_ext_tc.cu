@@ -16,11 +16,14 @@
 // CTA = (chunk, partner p, KV head h, token block j), 4 warps; thread r owns
 // query row r = (token j * 128 / G + r / G, head h * G + r % G) and TMEM lane r,
 // so the online softmax is thread-local.  Shared memory: Q [128 x D] K-major
-// with the 128-byte swizzle, four stages of 32 keys (K and V, the same
-// layout; V is read M/N-major; tile i + 2 is requested as soon as tile i has
-// landed, into the stage of tile i - 2), P [128 x 32] bf16 K-major with the 64-byte
-// swizzle; O is normalised by the sum of the bf16-rounded probabilities (an
-// exact convex combination of the values; the LSE keeps the fp32 sum).
+// with the 128-byte swizzle; a ring of four stages of E4M3 code rows of 32
+// keys (K then V, [key][D] bytes; tile i + 2 is requested as soon as tile i
+// has landed); each landed tile is converted exactly (every E4M3 value is a
+// bf16 value) into one of two bf16 tiles in the MMA layout (the same bytes
+// serve K-major for S and M/N-major for P V); the scores take k_descale and
+// the output v_descale.  P [128 x 32] bf16 K-major with the 64-byte swizzle;
+// O is normalised by the sum of the bf16-rounded probabilities (an exact
+// convex combination of the values; the LSE keeps the fp32 sum).
 // Tensor memory: 32 columns of S and D columns of O (256 allocated, two CTAs
 // per SM).  The S MMAs of a tile overlap the P V MMAs of the one before.  A
 // chunk split of a stripe is merged by the last CTA to arrive, per token.
@@ -51,17 +54,16 @@ struct ExtTcLayout {
   static constexpr int TMEM_COLS = 256;
   static constexpr int S_COL = 0;                     // S: columns 0..31
   static constexpr int O_COL = 64;                    // O: columns 64..64+D
-  // E4M3 pools: the code rows of a tile land in a ring of kXStages stages
-  // (K then V, [key][D] bytes) and are converted into one of two bf16 tiles
+  // the code rows of a tile land in a ring of kXStages stages (K then V,
+  // [key][D] bytes) and are converted into one of two bf16 tiles
   static constexpr int RING8 = 2 * kXTile * D;        // one E4M3 stage (K + V)
-  static size_t smem_bytes(int page_slots, bool f8) {
-    const size_t tiles = f8 ? 2 * static_cast<size_t>(STAGE) + kXStages * static_cast<size_t>(RING8)
-                            : kXStages * static_cast<size_t>(STAGE);
+  static size_t smem_bytes(int page_slots) {
+    const size_t tiles = 2 * static_cast<size_t>(STAGE) + kXStages * static_cast<size_t>(RING8);
     return 1024 + QBYTES + tiles + PBYTES + 64 + static_cast<size_t>(page_slots) * 4;
   }
 };
 
-template <int D, int G, bool F8>
+template <int D, int G>
 __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const PartialArgs a) {
   using Lt = ExtTcLayout<D>;
   constexpr int QB = kXRows / G;  // tokens per block
@@ -70,8 +72,8 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base;
   uint8_t* sKV = sQ + Lt::QBYTES;  // bf16 tiles the MMAs read: kXStages stages, or (E4M3) two
-  uint8_t* sRing8 = sKV + (F8 ? 2 : kXStages) * Lt::STAGE;  // E4M3 code stages (unused for bf16)
-  uint8_t* sPh = sRing8 + (F8 ? kXStages * Lt::RING8 : 0);
+  uint8_t* sRing8 = sKV + 2 * Lt::STAGE;  // E4M3 code stages
+  uint8_t* sPh = sRing8 + kXStages * Lt::RING8;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sPh + Lt::PBYTES);  // [0] S done, [1] P V done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2);
   int* spg = reinterpret_cast<int*>(bars + 4);
@@ -133,7 +135,7 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
   const uint32_t id_o = tc05::idesc_bf16(128, D, false, true);
   const uint8_t* poolk = static_cast<const uint8_t*>(a.pool_k);
   const uint8_t* poolv = static_cast<const uint8_t*>(a.pool_v);
-  const float sl = a.scale * kLog2e * (F8 ? a.k_descale : 1.f);
+  const float sl = a.scale * kLog2e * a.k_descale;
   uint32_t s_phase = 0, pv_phase = 0;  // completed phases of the two mbarriers
   bool alive = true;
 
@@ -203,36 +205,19 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
     auto load_tile = [&](int i) {
       if (i < ntiles) {
         const int64_t myrow = row_of(k_begin + i * kXTile + lane);
-        if constexpr (F8) {  // code rows, [key][D] bytes per K / V
-          uint8_t* rk = sRing8 + (i % kXStages) * Lt::RING8;
-          uint8_t* rv = rk + kXTile * D;
-          constexpr int CH8 = D / 16;
-          for (int x = tid; x < kXTile * CH8; x += blockDim.x) {
-            const int key = x / CH8;
-            const int cc = x - key * CH8;
-            const int64_t row = __shfl_sync(0xffffffffu, myrow, key);
-            if (row >= 0) {
-              cp_async16(rk + x * 16, poolk + row * D + cc * 16);
-              cp_async16(rv + x * 16, poolv + row * D + cc * 16);
-            } else {
-              *reinterpret_cast<uint4*>(rv + x * 16) = make_uint4(0u, 0u, 0u, 0u);  // masked keys: value 0
-            }
-          }
-        } else {
-          uint8_t* sk = sKV + (i % kXStages) * Lt::STAGE;
-          uint8_t* sv = sk + Lt::TILE;
-          constexpr int CH = D / 8;
-          for (int x = tid; x < kXTile * CH; x += blockDim.x) {
-            const int key = x / CH;
-            const int cc = x - key * CH;
-            const int64_t row = __shfl_sync(0xffffffffu, myrow, key);
-            const int off = (cc >> 3) * Lt::BLK + tc05::sw128(key, cc & 7);
-            if (row >= 0) {
-              cp_async16(sk + off, poolk + row * (D * 2) + cc * 16);
-              cp_async16(sv + off, poolv + row * (D * 2) + cc * 16);
-            } else {
-              *reinterpret_cast<uint4*>(sv + off) = make_uint4(0u, 0u, 0u, 0u);  // masked keys: value 0
-            }
+        // code rows, [key][D] bytes per K / V
+        uint8_t* rk = sRing8 + (i % kXStages) * Lt::RING8;
+        uint8_t* rv = rk + kXTile * D;
+        constexpr int CH8 = D / 16;
+        for (int x = tid; x < kXTile * CH8; x += blockDim.x) {
+          const int key = x / CH8;
+          const int cc = x - key * CH8;
+          const int64_t row = __shfl_sync(0xffffffffu, myrow, key);
+          if (row >= 0) {
+            cp_async16(rk + x * 16, poolk + row * D + cc * 16);
+            cp_async16(rv + x * 16, poolv + row * D + cc * 16);
+          } else {
+            *reinterpret_cast<uint4*>(rv + x * 16) = make_uint4(0u, 0u, 0u, 0u);  // masked keys: value 0
           }
         }
       }
@@ -274,13 +259,11 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
     bool have_pv = false;  // a P V MMA of this segment is in flight (or done but unwaited)
     for (int i = 0; i < ntiles; ++i) {
       cp_async_wait<1>();  // tile i (and Q) landed for this thread
-      if constexpr (F8) {
-        __syncthreads();  // every thread's codes of tile i landed
-        convert_tile(i);
-      }
+      __syncthreads();  // every thread's codes of tile i landed
+      convert_tile(i);
       tc05::fence_smem_to_async();
       __syncthreads();
-      const uint32_t kv0 = tc05::smem_addr(sKV + (F8 ? (i & 1) : (i % kXStages)) * Lt::STAGE);
+      const uint32_t kv0 = tc05::smem_addr(sKV + (i & 1) * Lt::STAGE);
       load_tile(i + 2);  // into the stage of tile i - 2, whose P V completed before this tile
       uint32_t vmask;
       {
@@ -386,7 +369,7 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
     const bool single = (nchunks == 1);
     {
       const bool empty = (l == 0.f);
-      const float inv = lr > 0.f ? (F8 ? a.v_descale : 1.f) / lr : 0.f;  // E4M3: value = code * v_descale
+      const float inv = lr > 0.f ? a.v_descale / lr : 0.f;  // E4M3: value = code * v_descale
       const float lse = empty ? -INFINITY : (m + log2f(l)) * kLn2;
       const int g = tid % G;
       float* dst = nullptr;
@@ -428,7 +411,7 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
       done = take_ticket(a.ws_cnt + slot0, nchunks);
       if (done) {
         merge_chunks<4>(a, p, h, s0, s1 - s0, slot0, static_cast<int64_t>(P) * a.num_kv_heads, nchunks, G, D,
-                     reinterpret_cast<float*>(sKV), (F8 ? 2 : kXStages) * Lt::STAGE / 4);
+                     reinterpret_cast<float*>(sKV), 2 * Lt::STAGE / 4);
         if (tid == 0) a.ws_cnt[slot0] = 0;
       }
     }
@@ -436,7 +419,7 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
       // fused: the last of the P partners of (segment, KV head) merges them
       int32_t* pair = a.ws_pair + static_cast<int64_t>(s0) * a.num_kv_heads + h;
       if (take_ticket(pair, P)) {
-        merge_partners<4>(a, s0, s1 - s0, h, G, D, reinterpret_cast<float*>(sKV), (F8 ? 2 : kXStages) * Lt::STAGE / 4);
+        merge_partners<4>(a, s0, s1 - s0, h, G, D, reinterpret_cast<float*>(sKV), 2 * Lt::STAGE / 4);
         if (tid == 0) *pair = 0;
       }
     }
@@ -448,13 +431,13 @@ __global__ void __launch_bounds__(128, 2) gqa_partial_ext_tc_kernel(const Partia
   if (warp == 0) tc05::tmem_dealloc(tbase, Lt::TMEM_COLS);
 }
 
-template <int D, int G, bool F8>
+template <int D, int G>
 static int launch_ext_tc_t(const PartialArgs& a, cudaStream_t s, cudaError_t* err) {
   constexpr int QB = kXRows / G;
   const int page_slots = a.chunk / a.ps_l + 2;
-  const size_t smem = ExtTcLayout<D>::smem_bytes(page_slots, F8);
+  const size_t smem = ExtTcLayout<D>::smem_bytes(page_slots);
   if (smem > 227 * 1024) return CPATTN_ERR_UNSUPPORTED_SHAPE;
-  auto kern = gqa_partial_ext_tc_kernel<D, G, F8>;
+  auto kern = gqa_partial_ext_tc_kernel<D, G>;
   static std::atomic<int> smem_set[64];
   *err = ensure_smem(kern, smem, smem_set);
   if (*err != cudaSuccess) return CPATTN_ERR_CUDA;
@@ -464,14 +447,14 @@ static int launch_ext_tc_t(const PartialArgs& a, cudaStream_t s, cudaError_t* er
   return *err == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
 }
 
-template <int D, bool F8>
+template <int D>
 static int ext_tc_dispatch_g(const PartialArgs& a, int G, cudaStream_t s, cudaError_t* err) {
   switch (G) {
-    case 1: return launch_ext_tc_t<D, 1, F8>(a, s, err);
-    case 2: return launch_ext_tc_t<D, 2, F8>(a, s, err);
-    case 4: return launch_ext_tc_t<D, 4, F8>(a, s, err);
-    case 8: return launch_ext_tc_t<D, 8, F8>(a, s, err);
-    case 16: return launch_ext_tc_t<D, 16, F8>(a, s, err);
+    case 1: return launch_ext_tc_t<D, 1>(a, s, err);
+    case 2: return launch_ext_tc_t<D, 2>(a, s, err);
+    case 4: return launch_ext_tc_t<D, 4>(a, s, err);
+    case 8: return launch_ext_tc_t<D, 8>(a, s, err);
+    case 16: return launch_ext_tc_t<D, 16>(a, s, err);
     default: return CPATTN_ERR_UNSUPPORTED_SHAPE;
   }
 }
@@ -481,8 +464,8 @@ int launch_gqa_partial_ext(const PartialArgs& a, cudaStream_t s, cudaError_t* er
   // pools: this kernel, which converts each tile of codes before its MMAs
   if (!a.kv_fp8) return launch_gqa_partial_ext_ws(a, s, err);
   const int G = a.num_q_heads / a.num_kv_heads;
-  if (a.head_dim == 128) return ext_tc_dispatch_g<128, true>(a, G, s, err);
-  if (a.head_dim == 64) return ext_tc_dispatch_g<64, true>(a, G, s, err);
+  if (a.head_dim == 128) return ext_tc_dispatch_g<128>(a, G, s, err);
+  if (a.head_dim == 64) return ext_tc_dispatch_g<64>(a, G, s, err);
   return CPATTN_ERR_UNSUPPORTED_SHAPE;
 }
 
