@@ -36,6 +36,24 @@ def desc_for(w) -> B.PoolDesc:
                       k_descale=w.k_descale if fp8 else 0.0, v_descale=w.v_descale if fp8 else 0.0)
 
 
+def pack_tensors(tensors, device, align=256):
+    """One uint8 buffer on ``device`` holding copies of ``tensors`` at
+    ``align``-byte offsets, and views of it with each tensor's dtype and shape
+    (in order).  Empty tensors get empty views."""
+    offs, end = [], 0
+    for t in tensors:
+        end = (end + align - 1) // align * align
+        offs.append(end)
+        end += t.numel() * t.element_size()
+    buf = torch.empty((max(end, align),), dtype=torch.uint8, device=device)
+    views = []
+    for t, o in zip(tensors, offs):
+        v = buf[o: o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+        v.copy_(t)
+        views.append(v)
+    return buf, views
+
+
 class StripedAttention:
     """Device state of one workload: the striped pool, the step's inputs and outputs.
 
@@ -92,18 +110,11 @@ class StripedAttention:
     INPUTS = ("q", "k_new", "v_new", "positions", "qo_indptr", "kv_len", "page_indptr", "page_indices", "row_order")
 
     def _pack(self, names):
-        """Move the named tensors into one device buffer (256-byte aligned
-        offsets) and rebind them to views of it; returns the buffer."""
+        """Move the named tensors into one device buffer and rebind them to
+        views of it; returns the buffer."""
         items = [(n, getattr(self, n)) for n in names if getattr(self, n) is not None]
-        offs, end = [], 0
-        for _, t in items:
-            end = (end + 255) // 256 * 256
-            offs.append(end)
-            end += t.numel() * t.element_size()
-        buf = torch.empty((max(end, 256),), dtype=torch.uint8, device=self.device)
-        for (n, t), o in zip(items, offs):
-            v = buf[o: o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
-            v.copy_(t)
+        buf, views = pack_tensors([t for _, t in items], self.device)
+        for (n, _), v in zip(items, views):
             setattr(self, n, v)
         return buf
 
