@@ -41,7 +41,8 @@ __global__ void __launch_bounds__(128) umma_selftest_kernel(int variant, const _
       *reinterpret_cast<uint4*>(sB + (c / 8) * (N * 128) + tc05::sw128(r, c % 8)) = gB[i];
     }
   } else {
-    // A [128][32] K-major SW64; B [K][N] MN-major SW128 in 64-element N blocks
+    // A [128][32] K-major SW64 (variant 3: A goes to tensor memory below);
+    // B [K][N] MN-major SW128 in 64-element N blocks
     sB = sA + 128 * 64;
     for (int i = tid; i < 128 * 4; i += blockDim.x) {
       const int r = i / 4, c = i % 4;
@@ -55,7 +56,8 @@ __global__ void __launch_bounds__(128) umma_selftest_kernel(int variant, const _
   }
   tc05::fence_smem_to_async();
   __syncthreads();  // operands complete before the allocation and the MMAs
-  if (warp == 0) tc05::tmem_alloc(tc05::smem_addr(&tmem_base_sh), 256);
+  const uint32_t ncols = variant == 3 ? 512 : 256;  // variant 3: A at column 256
+  if (warp == 0) tc05::tmem_alloc(tc05::smem_addr(&tmem_base_sh), ncols);
   if (tid == 0) {
     tc05::mbar_init(tc05::smem_addr(&mbar), 1);
     tc05::mbar_init_fence();
@@ -65,6 +67,24 @@ __global__ void __launch_bounds__(128) umma_selftest_kernel(int variant, const _
   tc05::fence_after_sync();
   const uint32_t tbase = tmem_base_sh;
   const uint32_t mb = tc05::smem_addr(&mbar);
+  if (variant == 3) {
+    // row tid of A (32 bf16 = 16 words, element 2j in the low half of word j) -> lane tid, columns 256..271
+    uint32_t w[16];
+    const uint4* row = gA + tid * 4;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 u = row[q];
+      w[4 * q] = u.x;
+      w[4 * q + 1] = u.y;
+      w[4 * q + 2] = u.z;
+      w[4 * q + 3] = u.w;
+    }
+    tc05::st_x16_u32(tc05::taddr(tbase, warp * 32, 256), w);
+    asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+    tc05::fence_before_sync();
+    __syncthreads();
+    tc05::fence_after_sync();
+  }
 
   if (tid == 0) {
     const uint32_t a0 = tc05::smem_addr(sA), b0 = tc05::smem_addr(sB);
@@ -76,6 +96,10 @@ __global__ void __launch_bounds__(128) umma_selftest_kernel(int variant, const _
         const uint64_t bd = tc05::desc_k128(b0 + (s / 4) * (N * 128) + off);
         tc05::mma_ss(tbase, ad, bd, id, s > 0);
       }
+    } else if (variant == 3) {
+      const uint32_t id = tc05::idesc_bf16(128, N, false, true);
+      for (int s = 0; s < K / 16; ++s)
+        tc05::mma_ts(tbase, tbase + 256 + s * 8, tc05::desc_mn128(b0 + s * 16 * 128, K * 128), id, s > 0);
     } else {
       const uint32_t id = tc05::idesc_bf16(128, N, false, true);
       for (int s = 0; s < K / 16; ++s) {
@@ -104,7 +128,7 @@ __global__ void __launch_bounds__(128) umma_selftest_kernel(int variant, const _
   }
   tc05::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc05::tmem_dealloc(tbase, 256);
+  if (warp == 0) tc05::tmem_dealloc(tbase, ncols);
 }
 
 }  // namespace cpattn
@@ -115,7 +139,7 @@ extern "C" int cpattn_umma_selftest(int variant, const void* A, const void* B, f
   if (A == nullptr || B == nullptr || D == nullptr) return CPATTN_ERR_INVALID_ARG;
   if (variant == 0) {
     if (N < 16 || N > 256 || N % 16 != 0 || K < 64 || K > 256 || K % 64 != 0) return CPATTN_ERR_UNSUPPORTED_SHAPE;
-  } else if (variant == 1 || variant == 2) {
+  } else if (variant == 1 || variant == 2 || variant == 3) {
     if (N < 64 || N > 256 || N % 64 != 0 || K != 32) return CPATTN_ERR_UNSUPPORTED_SHAPE;
   } else {
     return CPATTN_ERR_INVALID_ARG;

@@ -29,6 +29,8 @@ extern "C" {
  *              N in {64, 128, 192, 256}.
  *   variant 2: variant 1 with the two descriptor strides exchanged (a check
  *              of which field carries which stride).
+ *   variant 3: variant 1 with A read from tensor memory (row m in lane m, two
+ *              bf16 K elements a 32-bit column), written there by tcgen05.st.
  * A completion wait that times out stores 4 in *dev_status (if not NULL).
  */
 CPATTN_API int cpattn_umma_selftest(int variant, const void* A, const void* B, float* D, int N, int K,

@@ -67,3 +67,10 @@ def test_shapes_beyond_the_tile_are_refused(selftest):
     x = torch.zeros(16, device="cuda")
     assert selftest(0, x.data_ptr(), x.data_ptr(), x.data_ptr(), 272, 64, None, None) == -3
     assert selftest(1, x.data_ptr(), x.data_ptr(), x.data_ptr(), 256, 64, None, None) == -3
+
+
+@pytest.mark.parametrize("N", [64, 128, 256])
+def test_pv_pattern_a_in_tmem(selftest, N):
+    # P V with P in tensor memory (row m in lane m, bf16 pairs a column): the
+    # layout a kernel keeping P in TMEM relies on
+    assert _run(selftest, 3, N, 32, seed=N + 7) <= 1e-3
