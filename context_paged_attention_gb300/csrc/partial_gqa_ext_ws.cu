@@ -17,7 +17,8 @@
 //     head h * G + r % G) and TMEM lane r; it reads S, keeps the online
 //     softmax state (running max raised only when it grows by more than 8,
 //     so a rescale of O is rare and every probability stays <= 2^8), and
-//     writes its row of P (bf16, 64-byte swizzle).
+//     writes its row of P as bf16 pairs into tensor memory, where P V reads
+//     it as the MMA's A operand (no shared-memory copy, no proxy fence).
 //   * warp 4, lane 0 (MMA): S of tile j+2 as soon as its keys landed and S of
 //     tile j was read, then P V of tile j once P(j) is written: the tensor
 //     core computes the next scores while the softmax warps work.
@@ -29,7 +30,7 @@
 //     rejected page are zero-filled, and each tile's valid-key mask is
 //     published for the softmax.
 // Tensor memory (256 columns, two CTAs an SM): S in two 32-column buffers,
-// O at column 64.  O is normalised by the sum of the bf16-rounded
+// O at column 64, P in two 16-column buffers after O.  O is normalised by the sum of the bf16-rounded
 // probabilities (an exact convex combination of the values); the LSE keeps
 // the fp32 sum.  A chunk split of a stripe is merged by the last chunk CTA of
 // the segment, its chunk rows brought in by bulk asynchronous copies.  The
@@ -77,18 +78,17 @@ struct WsLayout {
   static constexpr int QBYTES = KB * QBLK;
   static constexpr int BLK = kWTile * 128;            // one column block of a key tile
   static constexpr int TILE = KB * BLK;               // K (or V) tile
-  static constexpr int PBUF = kWRows * 64;            // P tile (bf16, 32 keys)
   static constexpr int TMEM_COLS = 256;
   static constexpr uint32_t S_COL = 0;                // S buffers at columns 0 and 32
-  static constexpr uint32_t O_COL = 64;
+  static constexpr uint32_t O_COL = 64;               // O: D columns
+  static constexpr uint32_t P_COL = 64 + D;           // P buffers: 16 columns each (bf16 pairs)
   static constexpr size_t OFF_K = QBYTES;
   static constexpr size_t OFF_V = OFF_K + static_cast<size_t>(kKStages) * TILE;
-  static constexpr size_t OFF_P = OFF_V + static_cast<size_t>(kVStages) * TILE;
-  static constexpr size_t OFF_BAR = OFF_P + 2 * PBUF;
+  static constexpr size_t OFF_BAR = OFF_V + static_cast<size_t>(kVStages) * TILE;
   static constexpr size_t OFF_MASK = OFF_BAR + W_BARS * 8;
   static constexpr size_t OFF_MISC = OFF_MASK + kMaskSlots * 4;  // TMEM base, abort flag
-  static constexpr int SCRATCH_FLOATS = static_cast<int>((OFF_P - OFF_K) / 4);  // K + V rings, free after the loop
-  static constexpr int MERGE_BYTES = static_cast<int>(OFF_BAR);  // Q, rings and P: contiguous, free after the loop
+  static constexpr int SCRATCH_FLOATS = static_cast<int>((OFF_BAR - OFF_K) / 4);  // K + V rings, free after the loop
+  static constexpr int MERGE_BYTES = static_cast<int>(OFF_BAR);  // Q and the rings: contiguous, free after the loop
   static constexpr size_t OFF_PG = OFF_MISC + 16;
   static size_t smem_bytes(int page_slots) { return 1024 + OFF_PG + static_cast<size_t>(page_slots) * 4; }
 };
@@ -238,7 +238,6 @@ __global__ void __launch_bounds__(kWThreads, 2) gqa_partial_ext_ws_kernel(const 
   uint8_t* sQ = base;
   uint8_t* sK = base + Lt::OFF_K;
   uint8_t* sV = base + Lt::OFF_V;
-  uint8_t* sP = base + Lt::OFF_P;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + Lt::OFF_BAR);
   uint32_t* smask = reinterpret_cast<uint32_t*>(base + Lt::OFF_MASK);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + Lt::OFF_MISC);
@@ -475,12 +474,11 @@ __global__ void __launch_bounds__(kWThreads, 2) gqa_partial_ext_ws_kernel(const 
         if (!ws_wait(bar(W_VFULL + st), (j / kVStages) & 1, s_abort)) { alive = false; break; }
         tc05::fence_smem_to_async();
         tc05::fence_after_sync();
-        const uint64_t dp = tc05::desc_k64(tc05::smem_addr(sP + bb * Lt::PBUF));
         const uint64_t dv = tc05::desc_mn128(tc05::smem_addr(sV + st * Lt::TILE), Lt::BLK);
 #pragma unroll
-        for (int s = 0; s < kWTile / 16; ++s)
-          tc05::mma_ss(tbase + Lt::O_COL, tc05::desc_add(dp, s * 32), tc05::desc_add(dv, s * 16 * 128), id_o,
-                       j > 0 || s > 0);
+        for (int s = 0; s < kWTile / 16; ++s)  // P from tensor memory: 8 columns a 16-key step
+          tc05::mma_ts(tbase + Lt::O_COL, tbase + Lt::P_COL + 16 * bb + 8 * s, tc05::desc_add(dv, s * 16 * 128),
+                       id_o, j > 0 || s > 0);
         tc05::commit(bar(W_PVDONE + bb));
         tc05::commit(bar(W_VFREE + st));
         ++batches;
@@ -551,8 +549,7 @@ __global__ void __launch_bounds__(kWThreads, 2) gqa_partial_ext_ws_kernel(const 
           if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
         }
         {
-          uint8_t* pbuf = sP + bb * Lt::PBUF;
-          uint32_t pk[16];
+          uint32_t pk[16];  // bf16 pairs of keys 2e, 2e+1: row `tid` of P, as the MMA reads it from TMEM
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const float pa = sv[2 * e] == -INFINITY ? 0.f : ex2_approx(sv[2 * e] - m);
@@ -562,12 +559,9 @@ __global__ void __launch_bounds__(kWThreads, 2) gqa_partial_ext_ws_kernel(const 
             lr += __low2float(h2) + __high2float(h2);
             pk[e] = *reinterpret_cast<uint32_t*>(&h2);
           }
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-            *reinterpret_cast<uint4*>(pbuf + tc05::sw64(tid, q4)) =
-                make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+          tc05::st_x16_u32(my_lane + Lt::P_COL + 16 * bb, pk);
+          asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
         }
-        tc05::fence_smem_to_async();
         tc05::fence_before_sync();
         __syncwarp();
         if (lane == 0) ws_arrive(bar(W_PFULL + bb));
