@@ -183,6 +183,9 @@ CPATTN_API int cp_kv_write(const cpattn_pool_desc* desc, void* pool_k, void* poo
  *              more; its contents need no initialisation and are clobbered.
  * Supported: GQA with head_dim in {64, 128}, group size in {1, 2, 4, 8, 16};
  * MLA (num_kv_heads 1, head_dim 576, head_dim_v 512, bf16, 128 query heads).
+ * Other shapes, and multi-token rows over a bf16 pool of 2^31 or more K rows
+ * (P * num_pages * num_kv_heads * page_size / P), return
+ * CPATTN_ERR_UNSUPPORTED_SHAPE before any launch.
  */
 CPATTN_API int cp_paged_attn_partial(const cpattn_pool_desc* desc, const void* pool_k,
                           const void* pool_v, const void* q, int32_t num_q_heads,
