@@ -108,6 +108,11 @@ int run_partial(const cpattn_pool_desc* desc, const void* pool_k, const void* po
   if (mla && desc->dtype != CPATTN_DTYPE_BF16) return CPATTN_ERR_UNSUPPORTED_SHAPE;
   // E4M3 pools: GQA (the MLA kernel reads bf16 latent rows only)
   if (is_fp8(desc) && mla) return CPATTN_ERR_UNSUPPORTED_SHAPE;
+  // multi-token rows over a bf16 pool: the kernel's copy warps pass pool row
+  // indices as 32-bit values (checked here, before the one-token rows' launch)
+  if (!mla && qo_indptr != nullptr && !is_fp8(desc) &&
+      static_cast<int64_t>(desc->num_pages) * desc->num_kv_heads * desc->page_size >= (int64_t{1} << 31))
+    return CPATTN_ERR_UNSUPPORTED_SHAPE;
 
   PartialPlan plan;
   if (!plan_partial(mla, f.fused, desc->P, interleave_of(desc), desc->page_size, desc->num_kv_heads, num_q_heads,

@@ -115,6 +115,10 @@ def test_invalid_and_misaligned(lib):
                                      100, FAKE, FAKE, 0.1, FAKE, FAKE, FAKE, 1 << 30, None, None) == -3
     assert lib.cp_paged_attn_partial(ctypes.byref(_desc(head_dim=4, head_dim_v=4)), FAKE, FAKE, FAKE, 32, 1, 1,
                                      None, FAKE, 100, FAKE, FAKE, 0.1, FAKE, FAKE, FAKE, 1 << 30, None, None) == -3
+    # multi-token rows over a bf16 pool of 2^31 or more K rows: refused before any launch
+    huge = _desc(num_pages=1 << 26)  # 2^26 pages x 8 heads x 16 slots = 2^33 rows
+    assert lib.cp_paged_attn_partial(ctypes.byref(huge), FAKE, FAKE, FAKE, 32, 2, 8, FAKE, FAKE, 100, FAKE, FAKE,
+                                     0.1, FAKE, FAKE, FAKE, 1 << 30, None, None) == -3
     # merge: bad counts / dims
     assert lib.lse_merge(0, FAKE, FAKE, 0, 0, 1, 1, 128, 0, FAKE, None, None) == -1
     assert lib.lse_merge(2, FAKE, FAKE, 10, 1, 1, 1, 128, 0, FAKE, None, None) == -1
