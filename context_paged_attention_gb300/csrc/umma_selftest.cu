@@ -28,8 +28,9 @@ __global__ void __launch_bounds__(128) umma_selftest_kernel(int variant, const _
   uint8_t* sB;
   const uint4* gA = reinterpret_cast<const uint4*>(A);
   const uint4* gB = reinterpret_cast<const uint4*>(B);
-  if (variant == 0) {
+  if (variant == 0 || variant == 4) {
     // A [128][K], B [N][K], both K-major SW128 in 64-element column blocks
+    // (variant 4 reads A from tensor memory instead, written below)
     sB = sA + 128 * K * 2;
     const int kc = K / 8;
     for (int i = tid; i < 128 * kc; i += blockDim.x) {
@@ -56,7 +57,7 @@ __global__ void __launch_bounds__(128) umma_selftest_kernel(int variant, const _
   }
   tc05::fence_smem_to_async();
   __syncthreads();  // operands complete before the allocation and the MMAs
-  const uint32_t ncols = variant == 3 ? 512 : 256;  // variant 3: A at column 256
+  const uint32_t ncols = variant >= 3 ? 512 : 256;  // variants 3, 4: A at column 256
   if (warp == 0) tc05::tmem_alloc(tc05::smem_addr(&tmem_base_sh), ncols);
   if (tid == 0) {
     tc05::mbar_init(tc05::smem_addr(&mbar), 1);
@@ -67,6 +68,26 @@ __global__ void __launch_bounds__(128) umma_selftest_kernel(int variant, const _
   tc05::fence_after_sync();
   const uint32_t tbase = tmem_base_sh;
   const uint32_t mb = tc05::smem_addr(&mbar);
+  if (variant == 4) {
+    // row tid of A (K bf16 = K/2 words) -> lane tid, columns 256 .. 256 + K/2
+    const uint4* row = gA + tid * (K / 8);
+    for (int c0 = 0; c0 < K / 2; c0 += 16) {
+      uint32_t w[16];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 u = row[c0 / 4 + q];
+        w[4 * q] = u.x;
+        w[4 * q + 1] = u.y;
+        w[4 * q + 2] = u.z;
+        w[4 * q + 3] = u.w;
+      }
+      tc05::st_x16_u32(tc05::taddr(tbase, warp * 32, 256 + c0), w);
+    }
+    asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+    tc05::fence_before_sync();
+    __syncthreads();
+    tc05::fence_after_sync();
+  }
   if (variant == 3) {
     // row tid of A (32 bf16 = 16 words, element 2j in the low half of word j) -> lane tid, columns 256..271
     uint32_t w[16];
@@ -95,6 +116,12 @@ __global__ void __launch_bounds__(128) umma_selftest_kernel(int variant, const _
         const uint64_t ad = tc05::desc_k128(a0 + (s / 4) * (128 * 128) + off);
         const uint64_t bd = tc05::desc_k128(b0 + (s / 4) * (N * 128) + off);
         tc05::mma_ss(tbase, ad, bd, id, s > 0);
+      }
+    } else if (variant == 4) {
+      const uint32_t id = tc05::idesc_bf16(128, N, false, false);
+      for (int s = 0; s < K / 16; ++s) {
+        const uint64_t bd = tc05::desc_k128(b0 + (s / 4) * (N * 128) + (s % 4) * 32);
+        tc05::mma_ts(tbase, tbase + 256 + s * 8, bd, id, s > 0);
       }
     } else if (variant == 3) {
       const uint32_t id = tc05::idesc_bf16(128, N, false, true);
@@ -137,7 +164,7 @@ extern "C" int cpattn_umma_selftest(int variant, const void* A, const void* B, f
                                     int32_t* dev_status, cudaStream_t stream) {
   using namespace cpattn;
   if (A == nullptr || B == nullptr || D == nullptr) return CPATTN_ERR_INVALID_ARG;
-  if (variant == 0) {
+  if (variant == 0 || variant == 4) {
     if (N < 16 || N > 256 || N % 16 != 0 || K < 64 || K > 256 || K % 64 != 0) return CPATTN_ERR_UNSUPPORTED_SHAPE;
   } else if (variant == 1 || variant == 2 || variant == 3) {
     if (N < 64 || N > 256 || N % 64 != 0 || K != 32) return CPATTN_ERR_UNSUPPORTED_SHAPE;
@@ -145,7 +172,7 @@ extern "C" int cpattn_umma_selftest(int variant, const void* A, const void* B, f
     return CPATTN_ERR_INVALID_ARG;
   }
   // both operand tiles plus the 1 KB alignment slack must fit the shared-memory allocation
-  const size_t need = (variant == 0 ? static_cast<size_t>(128 + N) * K * 2 : 128 * 64 + static_cast<size_t>(K) * N * 2) + 1024;
+  const size_t need = (variant == 0 || variant == 4 ? static_cast<size_t>(128 + N) * K * 2 : 128 * 64 + static_cast<size_t>(K) * N * 2) + 1024;
   if (need > static_cast<size_t>(kSelfTestSmem)) return CPATTN_ERR_UNSUPPORTED_SHAPE;
   if (cudaFuncSetAttribute(umma_selftest_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelfTestSmem) !=
       cudaSuccess)

@@ -31,6 +31,8 @@ extern "C" {
  *              of which field carries which stride).
  *   variant 3: variant 1 with A read from tensor memory (row m in lane m, two
  *              bf16 K elements a 32-bit column), written there by tcgen05.st.
+ *   variant 4: variant 0 with A read from tensor memory the same way (the
+ *              Q K^T pattern with Q held in TMEM, K/16 k-steps of 8 columns).
  * A completion wait that times out stores 4 in *dev_status (if not NULL).
  */
 CPATTN_API int cpattn_umma_selftest(int variant, const void* A, const void* B, float* D, int N, int K,

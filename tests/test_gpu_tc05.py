@@ -33,8 +33,9 @@ def selftest():
 
 def _run(f, variant, N, K, seed):
     g = torch.Generator(device="cuda").manual_seed(seed)
-    A = torch.randn(128, K if variant == 0 else 32, device="cuda", generator=g).bfloat16()
-    if variant == 0:
+    qk = variant in (0, 4)  # D = A B^T with B [N][K]; else D = A B with A [128][32]
+    A = torch.randn(128, K if qk else 32, device="cuda", generator=g).bfloat16()
+    if qk:
         Bm = torch.randn(N, K, device="cuda", generator=g).bfloat16()
     else:
         Bm = torch.randn(32, N, device="cuda", generator=g).bfloat16()
@@ -44,7 +45,7 @@ def _run(f, variant, N, K, seed):
            torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     assert rc == 0 and int(st.item()) == 0
-    ref = A.double() @ (Bm.double().t() if variant == 0 else Bm.double())
+    ref = A.double() @ (Bm.double().t() if qk else Bm.double())
     return float((D.double() - ref).abs().max())
 
 
@@ -74,3 +75,9 @@ def test_pv_pattern_a_in_tmem(selftest, N):
     # P V with P in tensor memory (row m in lane m, bf16 pairs a column): the
     # layout a kernel keeping P in TMEM relies on
     assert _run(selftest, 3, N, 32, seed=N + 7) <= 1e-3
+
+
+@pytest.mark.parametrize("N,K", [(32, 128), (128, 192), (256, 256)])
+def test_qk_pattern_a_in_tmem(selftest, N, K):
+    # Q K^T with Q in tensor memory over several k-steps
+    assert _run(selftest, 4, N, K, seed=N + K + 11) <= 1e-3
