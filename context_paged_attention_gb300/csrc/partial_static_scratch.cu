@@ -17,13 +17,16 @@
 //   kScratchBytes are refused with CPATTN_ERR_WORKSPACE_TOO_SMALL, nothing
 //   launched.
 // * All calls share the one array.  The array keeps whatever the previous call
-//   left; the parts that must start at zero (the split tickets) are cleared on
-//   the caller's stream by every call.  Two calls whose kernels can overlap on
-//   the GPU (different streams, or different host threads) race on the array:
+//   left; the only part that must start at zero, the split tickets, is
+//   cleared on the caller's stream whenever the call splits a stripe (the only
+//   time the tickets are read).  Two calls whose kernels can overlap on the
+//   GPU (different streams, or different host threads) race on the array:
 //   order them on one stream.
 // * The first call on each device looks up the array's device address
 //   (cudaGetSymbolAddress, with that device current) and remembers it; make
-//   that first call before any stream capture begins.
+//   that first call before any stream capture begins.  The address belongs to
+//   the device's primary context: after cudaDeviceReset it is stale, so this
+//   entry point is not to be called again in that process.
 #include <cuda_runtime.h>
 
 #include <mutex>

@@ -21,8 +21,11 @@
  * ---------------------------------------
  * - Every pointer argument is DEVICE memory owned by the caller, except the
  *   cpattn_pool_desc pointer, which is HOST memory read during the call.  The
- *   library allocates nothing, keeps no state between calls, never
- *   synchronises, and launches only on the given stream (0 = legacy default).
+ *   library allocates nothing, never synchronises, and launches only on the
+ *   given stream (0 = legacy default).  It keeps no state between calls,
+ *   except cp_paged_attn_partial_noalloc: that entry point owns a fixed
+ *   device array inside the library and caches its address per device (see
+ *   its own block below).
  * - Return value: CPATTN_OK (0) or a negative CPATTN_ERR_* code.  Argument
  *   checks happen on the host before any launch; a failed check launches
  *   nothing.  CPATTN_ERR_CUDA means a launch failed (cudaGetLastError);
@@ -294,12 +297,17 @@ CPATTN_API size_t cp_paged_attn_fused_workspace_bytes(const cpattn_pool_desc* de
  *     cp_paged_attn_workspace_bytes(desc, num_q_heads, num_tokens, max_kv_len)
  *     exceeds that size.
  *   - Allocates nothing; all calls share the one array, which keeps the last
- *     call's contents.  Each call clears what must start at zero on `stream`.
- *     Calls whose kernels can overlap on the GPU (other streams, other host
- *     threads) race on the array: order them on one stream.
+ *     call's contents.  The split tickets, the only part that must start at
+ *     zero, are cleared on `stream` whenever the call splits a stripe (the
+ *     only time they are read).  Calls whose kernels can overlap on the GPU
+ *     (other streams, other host threads) race on the array: order them on
+ *     one stream.
  *   - The first call on each device looks up the array's device address with
  *     that device current and caches it; make that first call before any
- *     stream capture begins.
+ *     stream capture begins.  The cached address belongs to the device's
+ *     primary context: after cudaDeviceReset (or any teardown of that
+ *     context) it is stale, and this entry point must not be called again in
+ *     the same process.
  * Results equal those of cp_paged_attn_partial with a caller workspace.
  */
 CPATTN_API int cp_paged_attn_partial_noalloc(const cpattn_pool_desc* desc, const void* pool_k,
