@@ -132,7 +132,8 @@ int launch_gqa_partial_mma(const PartialArgs& a, cudaStream_t s, cudaError_t* er
 int launch_gqa_partial_ext(const PartialArgs& a, cudaStream_t s, cudaError_t* err);
 int launch_gqa_partial_ext_ws(const PartialArgs& a, cudaStream_t s, cudaError_t* err);  // bf16 pools
 int launch_mla_partial(const PartialArgs& a, cudaStream_t s, cudaError_t* err);
-int mla_tc_chunk(int ps_l);  // keys per CTA of the MLA tensor-core kernel
+// MLA kernel: workspace slots for the pieces of cut stripes (0: no stripe can be cut)
+int mla_ws_slots(int P, int interleave, int num_tokens, int max_kv_len);
 
 struct OwnArgs {
   const void* q;

@@ -235,12 +235,29 @@ bool plan_partial(int mla, int fused, int P, int interleave, int page_size, int 
   const int Dv = mla ? 512 : head_dim;
   plan->seg = pick_seg(ps_l, mla ? 16 : kSegMax);
   const int max_stripe = max_stripe_len(max_kv_len, P, interleave);
+  if (mla) {
+    // the MLA kernel plans on the device (stripes longest first, long ones cut
+    // into pieces); the workspace holds the pieces' partials, max_chunks of
+    // them at most (0: no stripe can be cut)
+    const int slots = mla_ws_slots(P, interleave, num_tokens, max_kv_len);
+    const size_t stripes = static_cast<size_t>(num_tokens) * P;
+    plan->chunk = 64;
+    plan->max_chunks = slots;
+    plan->ws_o_floats = static_cast<size_t>(slots) * num_q_heads * Dv;
+    plan->ws_lse_floats = static_cast<size_t>(slots) * num_q_heads;
+    plan->ws_cnt_ints = stripes;
+    if (fused) {
+      plan->ws_part_floats = stripes * num_q_heads * Dv;
+      plan->ws_part_lse_floats = stripes * num_q_heads;
+      plan->ws_pair_ints = static_cast<size_t>(num_tokens);
+    } else {
+      plan->ws_part_floats = plan->ws_part_lse_floats = plan->ws_pair_ints = 0;
+    }
+    return true;
+  }
   int chunk;
   int unit;
-  if (mla) {
-    chunk = mla_tc_chunk(ps_l);
-    unit = 32;
-  } else if (dtype_bytes == 2) {
+  if (dtype_bytes == 2) {
     // tensor-core paths: 2048-key chunks.  Splitting shorter stripes costs
     // more (a device-scope ticket and a merge of the chunk partials at the end
     // of each CTA) than the balance it buys, now that three decode CTAs share

@@ -1,0 +1,1000 @@
+// cp_paged_attn_partial, MLA path: one work item per two-CTA cluster, the two
+// CTAs split by role, on the tcgen05 tensor cores.
+//
+// MLA's one latent KV head is striped like a GQA head (mstar PR #1124
+// "Context / Sequence Parallel 1/5", description: MLA's one latent head
+// included; copy_slots indexes the token axis): partner p's stripe slot k is
+// logical position k * P + p at physical slot k % (page_size / P) of page
+// k / (page_size / P).  All 128 query heads of a token share the latent
+// rows, so a partner's partial is a dense contraction with M = 128 heads:
+//   S = Q K^T   (K = the 576 latent + rope values of each key row)
+//   O += P V    (V = the first 512 values of the same rows)
+//
+// Why two CTAs: O alone (128 x 512 fp32) fills all 512 columns of an SM's
+// tensor memory, so one CTA can neither keep Q there nor double-buffer S.
+// The cluster therefore splits the work by role, with the same key tiles:
+//   * CTA 0 (scores) holds Q in tensor memory as the A operand of S (columns
+//     128..415, two bf16 a column) and two 64-column S buffers (0 and 64).
+//     Warp 5 streams 64-key tiles of whole latent rows (9 column blocks of
+//     64 values, 128-byte swizzle) into a 2-stage ring by TMA; warp 4 issues
+//     the 36 S MMAs of a tile (N = 64 keys, A from tensor memory, so only K
+//     is read from shared memory) as soon as the tile landed and the S
+//     buffer is free; warps 0-3 (thread = head = TMEM lane) read S, run the
+//     online softmax (running max raised only when it grows by more than 8
+//     in log2 units, so a rescale is rare and every probability stays
+//     <= 2^8) and store their row of P as bf16 (with the row's rescale
+//     factor) straight into CTA 1's shared memory with asynchronous stores
+//     counted in bytes on CTA 1's barrier.
+//   * CTA 1 (values) holds O in all 512 columns.  Warp 5 streams the value
+//     part of the same tiles (8 column blocks) into a 2-stage ring, each
+//     tile once CTA 0 reports that its rows landed there (so CTA 1's copies
+//     find them in L2 instead of racing CTA 0's to HBM); warps 0-3 rescale
+//     their O row when CTA 0 raised the max, zero the value rows of keys
+//     outside the stripe, and at the end of an item normalise O and write it
+//     out; warp 4 issues P V (two N = 256 MMAs per 16 keys) and, through a
+//     multicast commit, tells CTA 0 when a P buffer may be overwritten.
+// O is normalised by the sum of the bf16-rounded probabilities (an exact
+// convex combination of the values); the LSE keeps the fp32 sum.
+//
+// Work: every (token, partner) stripe is an item; the grid is persistent
+// (one cluster per two SMs).  Each CTA plans the same way: the stripes are
+// ranked longest first, stripes longer than max(total / clusters, 16 tiles)
+// are cut into near-equal pieces, and item i goes to cluster i mod C in a
+// snake order (C-1 .. 0 on odd rounds), which balances about as well as a
+// greedy longest-first queue without any shared counter.  Pieces of a cut
+// stripe write normalised partials to workspace slots; the last to finish
+// (a ticket) merges them.  Too many stripes to rank in shared memory: items
+// are whole stripes in dispatch order.
+//
+// Every wait is bounded; one that runs out raises the abort flag of both
+// CTAs, which ends their other waits, and the call reports
+// CPATTN_DEV_TC_TIMEOUT (that item's output is not written).
+#include <cuda.h>
+
+#include <atomic>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "launch.h"
+#include "split_combine.cuh"
+#include "tc05.cuh"
+
+namespace cpattn {
+
+namespace {
+
+constexpr int kHeads = 128;
+constexpr int kDqk = 576;
+constexpr int kDv = 512;
+constexpr int kKB = kDqk / 64;       // 9 column blocks of a latent row
+constexpr int kVB = kDv / 64;        // 8 column blocks of its value part
+constexpr int kTile = 64;            // keys per tile
+constexpr int kBlk = kTile * 128;    // one column block of a tile (8 KB)
+constexpr int kKStage = kKB * kBlk;  // 72 KB
+constexpr int kVStage = kVB * kBlk;  // 64 KB
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;
+constexpr int kLandRing = 16;        // CTA 1's "K tile landed on CTA 0" barriers
+constexpr int kPBuf = kHeads * 128;  // P of one tile: 128 rows x 64 bf16
+constexpr int kThreads = 192;
+constexpr int kWMma = 4;
+constexpr int kWLoad = 5;
+constexpr int kMinChunkTiles = 16;   // cut pieces hold at least 1024 keys
+constexpr int kSortMax = 512;        // stripes ranked in shared memory
+constexpr int kMaxOwn = 64;          // items one cluster keeps in its list
+constexpr uint32_t kQCol = 128;      // CTA 0: S buffers at columns 0 and 64, Q at 128..415
+constexpr int kMergeUnroll = 8;
+
+// shared-memory map (offsets from a 1024-byte aligned base), the same in both CTAs
+constexpr uint32_t OFF_P = kVStages * kVStage;                   // CTA 1: P buffers [2]
+constexpr uint32_t OFF_ALPHA = OFF_P + 2 * kPBuf;                // CTA 1: [2][128] rescale factors
+constexpr uint32_t OFF_FIN = OFF_ALPHA + 2 * kHeads * 4;         // CTA 1: [128] (1 / sum, LSE)
+constexpr uint32_t OFF_SCR = OFF_FIN + kHeads * 8;               // CTA 1: merge scratch
+constexpr uint32_t kStageArea = kKStages * kKStage;              // CTA 0: K stages
+constexpr int kScrFloats = static_cast<int>((kStageArea - OFF_SCR) / 4);
+// barriers (arrival counts in brackets)
+enum : int {
+  B_KFULL = 0,      // x3 CTA 0 [1 + bytes (TMA) | 32 copy lanes]: K tile landed
+  B_KEMPTY = 3,     // x3 CTA 0 [commit]: S of the stage's tile done
+
+  B_SFULL = 6,      // x2 CTA 0 [commit]: S written
+  B_SEMPTY = 8,     // x2 CTA 0 [4 softmax warps]: S read
+  B_QFULL = 10,     // CTA 0 [4 softmax warps]: the item's Q in tensor memory
+  B_QEMPTY = 11,    // CTA 0 [commit]: the item's last S done
+  B_PEMPTY = 12,    // x2 CTA 0 [multicast commit from CTA 1]: P V of the buffer done
+  B_FINEMPTY = 14,  // CTA 0 [4 remote arrivals]: CTA 1 read the item's row scales
+  B_VFULL = 15,     // x2 CTA 1 [1 + bytes | 32]: V tile landed
+  B_VEMPTY = 17,    // x2 CTA 1 [commit]: P V of the stage's tile done
+  B_PFULL = 19,     // x2 CTA 1 [1 + bytes of CTA 0's bulk copies]: P and rescale factors landed
+  B_READY = 21,     // x2 CTA 1 [4 epilogue warps]: O rescaled, V rows fixed
+  B_PVDONE = 23,    // x2 CTA 1 [commit]: P V done
+  B_FINFULL = 25,   // CTA 1 [128 remote arrivals]: the item's row scales and LSEs
+  B_DRAIN = 26,     // both [commit]: the MMA thread's last MMAs done
+  B_EPSYNC = 27,    // CTA 1 [128 epilogue threads]: their group barrier (merges)
+  B_KLAND = 28,     // x16 CTA 1 [1 remote arrival]: the tile's rows reached CTA 0 (so they sit in L2)
+  kBars = 44
+};
+constexpr uint32_t OFF_BAR = kStageArea;
+constexpr uint32_t OFF_MISC = OFF_BAR + kBars * 8;  // [0] TMEM base, [1] abort, [2] items (-1: on the fly), [3] sum
+struct MlaItem {
+  int t, p, b;           // token, partner, row (-1: no row)
+  int k_begin, k_end;    // stripe slots of this item
+  int slot;              // workspace slot of a cut stripe's piece, or -1
+  int slot_base, npieces;
+};
+constexpr uint32_t OFF_ITEMS = OFF_MISC + 16;
+constexpr size_t kSmemBytes = 1024 + OFF_ITEMS + kMaxOwn * sizeof(MlaItem);
+static_assert(OFF_SCR + 1024 <= kStageArea, "CTA 1 map exceeds the stage area");
+static_assert(kSmemBytes + 64 <= 232448, "shared memory per CTA");
+
+// The epilogue warps of CTA 1 (threads 0..127) as a merge group.  Their
+// barrier is an mbarrier with a bounded wait rather than bar.sync, so that a
+// warp that gave up after a timeout cannot leave the others waiting forever.
+struct EpGroup {
+  __device__ static int tid() { return threadIdx.x; }
+  __device__ static int size() { return kHeads; }
+  __device__ static void sync() {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t mb = tc05::smem_addr(reinterpret_cast<uint8_t*>(
+                            (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023))) +
+                        OFF_BAR + B_EPSYNC * 8;
+    uint64_t state;
+    asm volatile("mbarrier.arrive.shared::cta.b64 %0, [%1];\n" : "=l"(state) : "r"(mb) : "memory");
+    for (uint32_t it = 0; it < (1u << 22); ++it) {
+      uint32_t done;
+      asm volatile(
+          "{\n .reg .pred p;\n mbarrier.try_wait.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+          : "=r"(done)
+          : "r"(mb), "l"(state)
+          : "memory");
+      if (done) return;
+    }
+  }
+};
+
+__device__ __forceinline__ void arrive_local(uint32_t mbar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(mbar) : "memory");
+}
+__device__ __forceinline__ void cp_arrive_noinc(uint32_t mbar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(mbar) : "memory");
+}
+__device__ __forceinline__ void cp16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp16_zero(uint32_t dst, const void* any_gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, 0;\n" ::"r"(dst), "l"(any_gmem) : "memory");
+}
+
+// Bounded wait for the phase of parity `parity`; gives up when the abort
+// flag is raised.  kCluster: the phase is completed by another CTA's release
+// (acquire at cluster scope).
+template <bool kCluster>
+__device__ __forceinline__ bool pwait(uint32_t mbar, uint32_t parity, const volatile int* abort_flag) {
+  for (uint32_t it = 0; it < (1u << 22); ++it) {
+    uint32_t done;
+    if constexpr (kCluster) {
+      asm volatile(
+          "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+          " selp.u32 %0, 1, 0, p;\n}\n"
+          : "=r"(done)
+          : "r"(mbar), "r"(parity)
+          : "memory");
+    } else {
+      asm volatile(
+          "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+          : "=r"(done)
+          : "r"(mbar), "r"(parity)
+          : "memory");
+    }
+    if (done) return true;
+    if ((it & 63u) == 63u && *abort_flag) return false;
+  }
+  return false;
+}
+
+// pwait by every lane of a warp, with one verdict for the whole warp (so no
+// lane leaves a loop that its warp-mates stay in).
+template <bool kCluster>
+__device__ __forceinline__ bool wwait(uint32_t mbar, uint32_t parity, const volatile int* abort_flag) {
+  return __all_sync(0xffffffffu, pwait<kCluster>(mbar, parity, abort_flag)) != 0;
+}
+
+// Token, partner, row and stripe length of stripe s = token * P + partner.
+struct StripeGeo {
+  int t, p, b, n;
+};
+__device__ __forceinline__ StripeGeo stripe_geo(const PartialArgs& a, int t, int p, bool may_report) {
+  StripeGeo g{t, p, -1, 0};
+  if (t < 0) return g;
+  if (a.qo_indptr != nullptr) {
+    if (t < __ldg(a.qo_indptr + a.num_rows)) g.b = find_row(a.qo_indptr, a.num_rows, t);
+  } else if (t < a.num_rows) {
+    g.b = t;
+  }
+  if (g.b >= 0) {
+    int L = __ldg(a.kv_len + g.b);
+    if (L > a.max_kv_len) {
+      if (may_report && p == 0) report(a.dev_status, CPATTN_DEV_POS_PAST_TABLE);
+      L = a.max_kv_len;
+    }
+    g.n = stripe_len(max(L, 0), p, a.P, a.interleave);
+  }
+  return g;
+}
+
+// The plan (all threads of the CTA; both CTAs of a cluster compute the same
+// one).  `tmp` is shared memory free until the first tile lands.
+__device__ void mla_plan(const PartialArgs& a, int C, int c, int* tmp, int* misc, MlaItem* items) {
+  const int S = a.num_tokens * a.P;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int* tiles = tmp;            // [S] tiles of each stripe
+  int* ns = tiles + S;         // [S] stripe lengths
+  int* order = ns + S;         // [S] stripes, longest first
+  int* pre = order + S;        // [S + 1] first item of each ranked stripe
+  int* sbase = pre + S + 1;    // [S] first workspace slot of each ranked stripe (cut stripes only)
+  int part = 0;
+  for (int s = tid; s < S; s += blockDim.x) {
+    const StripeGeo g = stripe_geo(a, s / a.P, s % a.P, true);
+    ns[s] = g.n;
+    tiles[s] = (g.n + kTile - 1) / kTile;
+    part += tiles[s];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+  if (lane == 0) atomicAdd(misc + 3, part);
+  __syncthreads();
+  const int W = misc[3];
+  const int chunk = max((W + C - 1) / C, kMinChunkTiles);
+  for (int s = tid; s < S; s += blockDim.x) {
+    const int ts = tiles[s];
+    int r = 0;
+    for (int s2 = 0; s2 < S; ++s2) {
+      const int t2 = tiles[s2];
+      r += (t2 > ts) || (t2 == ts && s2 < s);
+    }
+    order[r] = s;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int per = (S + 31) / 32;
+    const int i0 = min(S, lane * per), i1 = min(S, i0 + per);
+    int sp = 0, ss = 0;
+    for (int i = i0; i < i1; ++i) {
+      const int pc = max(1, (tiles[order[i]] + chunk - 1) / chunk);
+      sp += pc;
+      ss += pc > 1 ? pc : 0;
+    }
+    int ip = sp, is = ss;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, ip, o), v = __shfl_up_sync(0xffffffffu, is, o);
+      if (lane >= o) {
+        ip += u;
+        is += v;
+      }
+    }
+    int ep = ip - sp, es = is - ss;
+    for (int i = i0; i < i1; ++i) {
+      const int pc = max(1, (tiles[order[i]] + chunk - 1) / chunk);
+      pre[i] = ep;
+      sbase[i] = es;
+      ep += pc;
+      es += pc > 1 ? pc : 0;
+    }
+    if (lane == 31) pre[S] = ip;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const int N = pre[S];
+    int n = 0;
+    for (int k = 0; n < kMaxOwn; ++k) {
+      const int idx = k * C + ((k & 1) ? C - 1 - c : c);
+      if (idx >= N) break;
+      int lo = 0, hi = S - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pre[mid] <= idx) lo = mid; else hi = mid - 1;
+      }
+      const int s = order[lo];
+      const int pc = pre[lo + 1] - pre[lo];
+      const int piece = idx - pre[lo];
+      const StripeGeo g = stripe_geo(a, s / a.P, s % a.P, false);
+      const int tl = tiles[s];
+      const int base = tl / pc, rem = tl % pc;
+      const int st = piece * base + min(piece, rem);
+      const int cnt = base + (piece < rem ? 1 : 0);
+      MlaItem it;
+      it.t = g.t;
+      it.p = g.p;
+      it.b = g.b;
+      it.k_begin = st * kTile;
+      it.k_end = min(ns[s], (st + cnt) * kTile);
+      it.slot = pc > 1 ? sbase[lo] + piece : -1;
+      it.slot_base = sbase[lo];
+      it.npieces = pc;
+      if (it.slot >= a.max_chunks) {  // the workspace bound makes this impossible; never write past it
+        report(a.dev_status, CPATTN_DEV_BAD_INDPTR);
+        it.t = -1;
+      }
+      items[n++] = it;
+    }
+    misc[2] = n;
+  }
+  __syncthreads();
+}
+
+// Item k of cluster c: from the plan's list, or (too many stripes to rank)
+// stripe k * C + (snake c) in dispatch order, whole.
+__device__ __forceinline__ bool get_item(const PartialArgs& a, int k, int C, int c, int n_items, const MlaItem* items,
+                                         MlaItem& it) {
+  if (n_items >= 0) {
+    if (k >= n_items) return false;
+    it = items[k];
+    return true;
+  }
+  const int S = a.num_tokens * a.P;
+  const int idx = k * C + ((k & 1) ? C - 1 - c : c);
+  if (idx >= S) return false;
+  const int z = idx / a.P, p = idx - z * a.P;
+  int t = z;
+  if (a.qo_indptr == nullptr && a.row_order != nullptr) {
+    t = __ldg(a.row_order + z);
+    if (t < 0 || t >= a.num_rows) {
+      if (p == 0) report(a.dev_status, CPATTN_DEV_BAD_INDPTR);
+      t = -1;
+    }
+  }
+  const StripeGeo g = stripe_geo(a, t, p, true);
+  it.t = g.t;
+  it.p = g.p;
+  it.b = g.b;
+  it.k_begin = 0;
+  it.k_end = g.n;
+  it.slot = -1;
+  it.slot_base = -1;
+  it.npieces = 1;
+  return true;
+}
+
+// Pool row of stripe slot k of the item (-1 if its page is rejected; reported when `rep`).
+__device__ __forceinline__ int64_t pool_row(const PartialArgs& a, const MlaItem& it, int k, int pb0, int npg,
+                                            bool rep) {
+  const int jj = page_of_slot(a, k);
+  if (jj >= npg) {
+    if (rep) report(a.dev_status, CPATTN_DEV_POS_PAST_TABLE);
+    return -1;
+  }
+  const int pg = __ldg(a.page_indices + pb0 + jj);
+  if (pg < 0 || pg >= a.num_pages) {
+    if (rep) report(a.dev_status, CPATTN_DEV_PAGE_OUT_OF_RANGE);
+    return -1;
+  }
+  return (static_cast<int64_t>(it.p) * a.num_pages + pg) * a.ps_l + (k - jj * a.ps_l);
+}
+
+// Keys of tile j of the item that hold data (inside the item, page accepted),
+// one bit a key; every lane of the warp gets the mask.
+__device__ __forceinline__ uint64_t tile_mask(const PartialArgs& a, const MlaItem& it, int j, int pb0, int npg,
+                                              int lane) {
+  const int k0 = it.k_begin + j * kTile;
+  const int ka = k0 + lane, kb = k0 + 32 + lane;
+  const bool va = ka < it.k_end && pool_row(a, it, ka, pb0, npg, false) >= 0;
+  const bool vb = kb < it.k_end && pool_row(a, it, kb, pb0, npg, false) >= 0;
+  const uint32_t lo = __ballot_sync(0xffffffffu, va), hi = __ballot_sync(0xffffffffu, vb);
+  return static_cast<uint64_t>(lo) | (static_cast<uint64_t>(hi) << 32);
+}
+
+// Copies of tile j of the item into a stage (nblk column blocks of 64 values):
+// TMA boxes of `box_rows` rows (lane 0), or 16-byte cp.async copies by the
+// whole warp with zero fill for keys without data.  Completion is counted on
+// `full`.
+// Pool rows of the page runs of tile j (TMA path): lane r < kTile / box_rows
+// looks up run r (-1: past the item or a rejected page, reported), so a tile
+// costs one round trip to the page table.
+__device__ __forceinline__ int tile_run_row(const PartialArgs& a, const MlaItem& it, int j, int pb0, int npg,
+                                            int box_rows, int lane) {
+  const int kr = it.k_begin + j * kTile + lane * box_rows;
+  if (lane >= kTile / box_rows || kr >= it.k_end) return -1;
+  return static_cast<int>(pool_row(a, it, kr, pb0, npg, true));
+}
+
+template <bool kTma>
+__device__ __forceinline__ void load_tile(const PartialArgs& a, const CUtensorMap* tmap, const MlaItem& it, int j,
+                                          int pb0, int npg, uint32_t dst, int nblk, uint32_t full, int box_rows,
+                                          int lane, int run_row) {
+  const int k0 = it.k_begin + j * kTile;
+  if constexpr (kTma) {
+    // run_row: this lane's run of the tile (tile_run_row), gathered by lane 0
+    const int nr = kTile / box_rows;
+    int rows[kTile / 8];
+    uint32_t bytes = 0;
+#pragma unroll
+    for (int r = 0; r < kTile / 8; ++r) {
+      rows[r] = __shfl_sync(0xffffffffu, run_row, r);
+      if (r < nr && rows[r] >= 0) bytes += nblk * box_rows * 128;
+    }
+    if (lane == 0) {
+      tc05::mbar_arrive_expect_tx(full, bytes);
+      for (int r = 0; r < nr; ++r) {
+        if (rows[r] < 0) continue;
+        for (int kb = 0; kb < nblk; ++kb)
+          tc05::tma_load_2d(dst + kb * kBlk + r * box_rows * 128, tmap, kb * 64, rows[r], full);
+      }
+    }
+  } else {
+    const uint8_t* pool = static_cast<const uint8_t*>(a.pool_k);
+    const uint8_t* r0 = nullptr;
+    const uint8_t* r1 = nullptr;
+    {
+      const int ka = k0 + lane, kb = k0 + 32 + lane;
+      if (ka < it.k_end) {
+        const int64_t row = pool_row(a, it, ka, pb0, npg, true);
+        if (row >= 0) r0 = pool + row * (kDqk * 2);
+      }
+      if (kb < it.k_end) {
+        const int64_t row = pool_row(a, it, kb, pb0, npg, true);
+        if (row >= 0) r1 = pool + row * (kDqk * 2);
+      }
+    }
+    const int nch = nblk * 8;
+    for (int key = 0; key < kTile; ++key) {
+      const uint8_t* src = reinterpret_cast<const uint8_t*>(
+          __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(key < 32 ? r0 : r1), key & 31));
+      for (int ch = lane; ch < nch; ch += 32) {
+        const uint32_t d = dst + (ch >> 3) * kBlk + tc05::sw128(key, ch & 7);
+        if (src != nullptr) cp16(d, src + ch * 16);
+        else cp16_zero(d, pool);
+      }
+    }
+    cp_arrive_noinc(full);
+  }
+}
+
+}  // namespace
+
+template <bool kTma>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    mla_pair_kernel(const PartialArgs a, const __grid_constant__ CUtensorMap tmap, int box_rows) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = tc05::smem_addr(base);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = tc05::cluster_rank();  // 0: scores, 1: values
+  const uint32_t peer = rank ^ 1u;
+  const int C = gridDim.x / 2, c = blockIdx.x / 2;
+  int* misc = reinterpret_cast<int*>(base + OFF_MISC);
+  volatile int* abort_flag = misc + 1;
+  MlaItem* items = reinterpret_cast<MlaItem*>(base + OFF_ITEMS);
+  auto bar = [&](int i) -> uint32_t { return sb + OFF_BAR + static_cast<uint32_t>(i) * 8u; };
+  auto raise_abort = [&]() {
+    *abort_flag = 1;
+    tc05::st_cluster_u32(tc05::mapa(sb + OFF_MISC + 4, peer), 1u);
+    report(a.dev_status, CPATTN_DEV_TC_TIMEOUT);
+  };
+
+  // ---- plan, barriers, tensor memory
+  if (tid == 0) {
+    misc[1] = 0;
+    misc[2] = -1;
+    misc[3] = 0;
+  }
+  __syncthreads();
+  const int S = a.num_tokens * a.P;
+  if (S <= kSortMax && S + 2 * C <= kMaxOwn * C) mla_plan(a, C, c, reinterpret_cast<int*>(base), misc, items);
+  if (tid == 0) {
+    const uint32_t load_arrivals = kTma ? 1u : 32u;
+    for (int i = 0; i < kKStages; ++i) {
+      tc05::mbar_init(bar(B_KFULL + i), load_arrivals);
+      tc05::mbar_init(bar(B_KEMPTY + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc05::mbar_init(bar(B_SFULL + i), 1);
+      tc05::mbar_init(bar(B_SEMPTY + i), 4);
+      tc05::mbar_init(bar(B_PEMPTY + i), 1);
+      tc05::mbar_init(bar(B_PFULL + i), 1);
+      tc05::mbar_init(bar(B_READY + i), 4);
+      tc05::mbar_init(bar(B_PVDONE + i), 1);
+    }
+    for (int i = 0; i < kVStages; ++i) {
+      tc05::mbar_init(bar(B_VFULL + i), load_arrivals);
+      tc05::mbar_init(bar(B_VEMPTY + i), 1);
+    }
+    tc05::mbar_init(bar(B_QFULL), 4);
+    tc05::mbar_init(bar(B_QEMPTY), 1);
+    tc05::mbar_init(bar(B_FINEMPTY), 4);
+    tc05::mbar_init(bar(B_FINFULL), kHeads);
+    tc05::mbar_init(bar(B_DRAIN), 1);
+    tc05::mbar_init(bar(B_EPSYNC), kHeads);
+    for (int i = 0; i < kLandRing; ++i) tc05::mbar_init(bar(B_KLAND + i), 1);
+    tc05::mbar_init_fence();
+  }
+  if (warp == 0) tc05::tmem_alloc(tc05::smem_addr(misc), 512);
+  tc05::fence_before_sync();
+  __syncthreads();
+  tc05::fence_after_sync();
+  tc05::cluster_sync();  // the peer's barriers exist before any remote arrival
+  const uint32_t tbase = static_cast<uint32_t>(misc[0]);
+  const int n_items = misc[2];
+  auto item = [&](int k, MlaItem& it) { return get_item(a, k, C, c, n_items, items, it); };
+  auto ntiles = [](const MlaItem& it) {
+    return it.t >= 0 && it.k_end > it.k_begin ? (it.k_end - it.k_begin + kTile - 1) / kTile : 0;
+  };
+  bool ok = true;
+
+  if (warp == kWLoad) {
+    // ---- loader (both CTAs): whole latent rows into the K ring (CTA 0), the value part into the V ring (CTA 1)
+    const int nstages = rank == 0 ? kKStages : kVStages;
+    const uint32_t stage_bytes = rank == 0 ? kKStage : kVStage;
+    const int nblk = rank == 0 ? kKB : kVB;
+    const int b_full = rank == 0 ? B_KFULL : B_VFULL, b_empty = rank == 0 ? B_KEMPTY : B_VEMPTY;
+    int g = 0, issued = 0;
+    for (int k = 0; ok; ++k) {
+      MlaItem it;
+      if (!item(k, it)) break;
+      const int nt = ntiles(it);
+      if (nt == 0) continue;
+      const int pb0 = __ldg(a.page_indptr + it.b), npg = __ldg(a.page_indptr + it.b + 1) - pb0;
+      // page rows of the next tile are looked up while the stage it goes to is still busy
+      int run_row = kTma ? tile_run_row(a, it, 0, pb0, npg, box_rows, lane) : -1;
+      for (int j = 0; j < nt; ++j, ++g) {
+        const int st = g % nstages;
+        ok = wwait<false>(bar(b_empty + st), ((g / nstages) & 1) ^ 1, abort_flag);
+        // CTA 1 copies a tile's value rows once CTA 0 has the whole rows:
+        // they are in L2 by then, and CTA 1's copies do not race CTA 0's to HBM
+        if (ok && rank == 1) ok = wwait<true>(bar(B_KLAND + g % kLandRing), (g / kLandRing) & 1, abort_flag);
+        if (!ok) break;
+        load_tile<kTma>(a, &tmap, it, j, pb0, npg, sb + st * stage_bytes, nblk, bar(b_full + st), box_rows, lane,
+                        run_row);
+        issued = g + 1;
+        if (kTma && j + 1 < nt) run_row = tile_run_row(a, it, j + 1, pb0, npg, box_rows, lane);
+      }
+    }
+    if (!ok) raise_abort();
+    if (*abort_flag) {
+      // nothing may land after the CTA exits: wait (bounded) for the last copies issued into each stage
+      for (int g2 = max(0, issued - nstages); g2 < issued; ++g2) {
+        const uint32_t mb = bar(b_full + g2 % nstages), par = (g2 / nstages) & 1;
+        for (uint32_t i = 0; i < (1u << 20); ++i) {
+          uint32_t done;
+          asm volatile(
+              "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+              : "=r"(done)
+              : "r"(mb), "r"(par)
+              : "memory");
+          if (done) break;
+        }
+      }
+    }
+  } else if (rank == 0 && warp == kWMma) {
+    // ---- CTA 0, MMA warp (one elected lane issues): S = Q K^T of each tile, Q from tensor memory
+    const uint32_t id_s = tc05::idesc_bf16(128, kTile, false, false);
+    const uint32_t r_kland = tc05::mapa(bar(B_KLAND), 1);
+    int g = 0, qi = 0;
+    for (int k = 0; ok; ++k) {
+      MlaItem it;
+      if (!item(k, it)) break;
+      const int nt = ntiles(it);
+      if (nt == 0) continue;
+      ok = wwait<false>(bar(B_QFULL), qi & 1, abort_flag);
+      for (int j = 0; j < nt && ok; ++j, ++g) {
+        const int st = g % kKStages, sbuf = g & 1;
+        ok = wwait<false>(bar(B_KFULL + st), (g / kKStages) & 1, abort_flag);
+        if (ok && lane == 0) tc05::mbar_arrive_remote(r_kland + (g % kLandRing) * 8);
+        ok = ok && wwait<false>(bar(B_SEMPTY + sbuf), ((g >> 1) & 1) ^ 1, abort_flag);
+        if (!ok) break;
+        if (tc05::elect_one()) {
+          if constexpr (!kTma) tc05::fence_smem_to_async();  // the tile came through cp.async
+          tc05::fence_after_sync();
+          const uint64_t dk = tc05::desc_k128(sb + st * kKStage);
+          const uint32_t dcol = tbase + sbuf * kTile;
+#pragma unroll
+          for (int ks = 0; ks < kDqk / 16; ++ks)
+            tc05::mma_ts(dcol, tbase + kQCol + ks * 8, tc05::desc_add(dk, (ks >> 2) * kBlk + (ks & 3) * 32), id_s,
+                         ks > 0);
+          tc05::commit(bar(B_SFULL + sbuf));
+          tc05::commit(bar(B_KEMPTY + st));
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (tc05::elect_one()) tc05::commit(bar(B_QEMPTY));
+      __syncwarp();
+      ++qi;
+    }
+    if (!ok) raise_abort();
+    if (tc05::elect_one()) {
+      tc05::commit(bar(B_DRAIN));
+      tc05::mbar_wait(bar(B_DRAIN), 0, 1u << 20);
+    }
+    __syncwarp();
+  } else if (rank == 0) {
+    // ---- CTA 0, warps 0-3: Q into tensor memory, online softmax, P to CTA 1
+    const float sl = a.scale * kLog2e;
+    const uint32_t my_lane = tc05::taddr(tbase, warp * 32, 0);
+    const uint32_t r_p = tc05::mapa(sb + OFF_P, 1), r_alpha = tc05::mapa(sb + OFF_ALPHA, 1);
+    const uint32_t r_fin = tc05::mapa(sb + OFF_FIN, 1);
+    const uint32_t r_pfull = tc05::mapa(bar(B_PFULL), 1), r_finfull = tc05::mapa(bar(B_FINFULL), 1);
+    int g = 0, qi = 0, prev_t = -1;
+    for (int k = 0; ok; ++k) {
+      MlaItem it;
+      if (!item(k, it)) break;
+      const int nt = ntiles(it);
+      if (nt == 0) continue;
+      const int pb0 = __ldg(a.page_indptr + it.b), npg = __ldg(a.page_indptr + it.b + 1) - pb0;
+      // Q row (token it.t, head tid) -> columns 128..415 of lane tid, once the previous item's S is done
+      ok = wwait<false>(bar(B_QEMPTY), (qi & 1) ^ 1, abort_flag);
+      if (!ok) break;
+      tc05::fence_after_sync();
+      if (it.t != prev_t) {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            static_cast<const uint8_t*>(a.q) + (static_cast<int64_t>(it.t) * a.num_q_heads + tid) * (kDqk * 2));
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {  // 36 loads in flight a thread, two rounds
+          uint4 u[kDqk / 16];
+#pragma unroll
+          for (int i = 0; i < kDqk / 16; ++i) u[i] = __ldg(src + half * (kDqk / 16) + i);
+#pragma unroll
+          for (int cb = 0; cb < kDqk / 64; ++cb) {
+            const uint32_t w[16] = {u[4 * cb].x,     u[4 * cb].y,     u[4 * cb].z,     u[4 * cb].w,
+                                    u[4 * cb + 1].x, u[4 * cb + 1].y, u[4 * cb + 1].z, u[4 * cb + 1].w,
+                                    u[4 * cb + 2].x, u[4 * cb + 2].y, u[4 * cb + 2].z, u[4 * cb + 2].w,
+                                    u[4 * cb + 3].x, u[4 * cb + 3].y, u[4 * cb + 3].z, u[4 * cb + 3].w};
+            tc05::st_x16_u32(my_lane + kQCol + half * (kDqk / 4) + cb * 16, w);
+          }
+        }
+        tc05::st_wait();
+        prev_t = it.t;
+      }
+      tc05::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) arrive_local(bar(B_QFULL));
+      {
+        // the next item's Q row into L2 while this one runs
+        MlaItem nx;
+        if (item(k + 1, nx) && nx.t >= 0 && nx.t != it.t) {
+          const char* q2 = static_cast<const char*>(a.q) + (static_cast<int64_t>(nx.t) * a.num_q_heads + tid) * (kDqk * 2);
+#pragma unroll
+          for (int ln = 0; ln < (kDqk * 2) / 128; ++ln) asm volatile("prefetch.global.L2 [%0];\n" ::"l"(q2 + ln * 128));
+        }
+      }
+      float m = -INFINITY, l = 0.f, lr = 0.f;
+      for (int j = 0; j < nt; ++j, ++g) {
+        const int sbuf = g & 1;
+        const uint64_t vmask = tile_mask(a, it, j, pb0, npg, lane);
+        ok = wwait<false>(bar(B_SFULL + sbuf), (g >> 1) & 1, abort_flag);
+        if (!ok) break;
+        tc05::fence_after_sync();
+        float sv[kTile];
+        {
+          float v0[16], v1[16], v2[16], v3[16];
+          tc05::ld_x16(my_lane + sbuf * kTile, v0);
+          tc05::ld_x16(my_lane + sbuf * kTile + 16, v1);
+          tc05::ld_x16(my_lane + sbuf * kTile + 32, v2);
+          tc05::ld_x16(my_lane + sbuf * kTile + 48, v3);
+          tc05::ld_wait();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            sv[e] = v0[e];
+            sv[16 + e] = v1[e];
+            sv[32 + e] = v2[e];
+            sv[48 + e] = v3[e];
+          }
+        }
+        tc05::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) arrive_local(bar(B_SEMPTY + sbuf));
+        float bm = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < kTile; ++e) {
+          sv[e] = ((vmask >> e) & 1ull) ? sv[e] * sl : -INFINITY;
+          bm = fmaxf(bm, sv[e]);
+        }
+        float alpha = 1.f;
+        if (bm > m + 8.f) {
+          alpha = m == -INFINITY ? 0.f : exp2f(m - bm);
+          l *= alpha;
+          lr *= alpha;
+          m = bm;
+        }
+        // P buffer `sbuf` of CTA 1 is free once its P V two tiles back is done;
+        // the row of P (bf16, 128-byte swizzle) and the rescale factor go there
+        // by asynchronous stores counted in bytes on CTA 1's barrier
+        ok = wwait<true>(bar(B_PEMPTY + sbuf), ((g >> 1) & 1) ^ 1, abort_flag);
+        if (!ok) break;
+        const uint32_t prow = r_p + sbuf * kPBuf + tid * 128, pfull = r_pfull + sbuf * 8;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int e2 = 0; e2 < 4; ++e2) {
+            const int e = 8 * cc + 2 * e2;
+            const float p0 = sv[e] == -INFINITY ? 0.f : ex2_approx(sv[e] - m);
+            const float p1 = sv[e + 1] == -INFINITY ? 0.f : ex2_approx(sv[e + 1] - m);
+            l += p0 + p1;
+            __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+            lr += __low2float(pb) + __high2float(pb);
+            pk[e2] = *reinterpret_cast<uint32_t*>(&pb);
+          }
+          tc05::st_async_v4(prow + ((cc ^ (tid & 7)) << 4), pk[0], pk[1], pk[2], pk[3], pfull);
+        }
+        tc05::st_async_b32(r_alpha + (sbuf * kHeads + tid) * 4, __float_as_uint(alpha), pfull);
+      }
+      if (!ok) break;
+      // the item's row scale and LSE to CTA 1, once it read the previous item's
+      ok = wwait<true>(bar(B_FINEMPTY), (qi & 1) ^ 1, abort_flag);
+      if (!ok) break;
+      const float inv = lr > 0.f ? 1.f / lr : 0.f;
+      const float lse = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+      tc05::st_cluster_v2f32(r_fin + tid * 8, inv, lse);
+      tc05::mbar_arrive_remote(r_finfull);
+      ++qi;
+    }
+    if (!ok) raise_abort();
+  } else if (warp == kWMma) {
+    // ---- CTA 1, MMA warp (one elected lane issues): O += P V
+    const uint32_t id_pv = tc05::idesc_bf16(128, 256, false, true);
+    int g = 0;
+    for (int k = 0; ok; ++k) {
+      MlaItem it;
+      if (!item(k, it)) break;
+      const int nt = ntiles(it);
+      for (int j = 0; j < nt; ++j, ++g) {
+        const int pbuf = g & 1, vs = g % kVStages;
+        ok = wwait<false>(bar(B_READY + pbuf), (g >> 1) & 1, abort_flag);
+        if (!ok) break;
+        if (tc05::elect_one()) {
+          if constexpr (!kTma) tc05::fence_smem_to_async();
+          tc05::fence_after_sync();
+          const uint64_t dp = tc05::desc_k128(sb + OFF_P + pbuf * kPBuf);
+          const uint64_t dv = tc05::desc_mn128(sb + vs * kVStage, kBlk);
+#pragma unroll
+          for (int ks = 0; ks < kTile / 16; ++ks) {
+            const uint64_t ad = tc05::desc_add(dp, ks * 32);
+            const uint64_t bd = tc05::desc_add(dv, ks * 16 * 128);
+            tc05::mma_ss(tbase, ad, bd, id_pv, j > 0 || ks > 0);
+            tc05::mma_ss(tbase + 256, ad, tc05::desc_add(bd, 4 * kBlk), id_pv, j > 0 || ks > 0);
+          }
+          tc05::commit(bar(B_PVDONE + pbuf));
+          tc05::commit(bar(B_VEMPTY + vs));
+          tc05::commit_multicast(bar(B_PEMPTY + pbuf), 0x1);
+        }
+        __syncwarp();
+      }
+    }
+    if (!ok) raise_abort();
+    if (tc05::elect_one()) {
+      tc05::commit(bar(B_DRAIN));
+      tc05::mbar_wait(bar(B_DRAIN), 0, 1u << 20);
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ---- CTA 1, warps 0-3: value-row fixes, O rescales, the normalised output
+    const uint32_t my_lane = tc05::taddr(tbase, warp * 32, 0);
+    const uint32_t r_finempty = tc05::mapa(bar(B_FINEMPTY), 0);
+    const float* alpha_s = reinterpret_cast<const float*>(base + OFF_ALPHA);
+    const float2* fin_s = reinterpret_cast<const float2*>(base + OFF_FIN);
+    float* scratch = reinterpret_cast<float*>(base + OFF_SCR);
+    int g = 0, fi = 0;
+    for (int k = 0; ok; ++k) {
+      MlaItem it;
+      if (!item(k, it)) break;
+      if (it.t < 0) continue;
+      const int nt = ntiles(it);
+      const int64_t orow = (static_cast<int64_t>(it.p) * a.num_tokens + it.t) * a.num_q_heads + tid;
+      if (nt == 0) {  // empty stripe (or a token of no row): 0 / -inf
+        float4* d4 = reinterpret_cast<float4*>(a.o_part + orow * kDv);
+        for (int e = 0; e < kDv / 4; ++e) d4[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+        a.lse_part[lse_slot(a, it.p, it.t, tid)] = -INFINITY;
+        if (a.fused) pair_finish<kMergeUnroll, EpGroup>(a, it.t, 0, kHeads, kDv, scratch, kScrFloats);
+        continue;
+      }
+      const int pb0 = __ldg(a.page_indptr + it.b), npg = __ldg(a.page_indptr + it.b + 1) - pb0;
+      for (int j = 0; j < nt; ++j, ++g) {
+        const int pbuf = g & 1, vs = g % kVStages;
+        const uint64_t vmask = tile_mask(a, it, j, pb0, npg, lane);
+        // P and the rescale factors arrive by bulk copies from CTA 0 (bytes counted)
+        if (tid == 0) tc05::mbar_arrive_expect_tx(bar(B_PFULL + pbuf), kPBuf + kHeads * 4);
+        ok = wwait<true>(bar(B_PFULL + pbuf), (g >> 1) & 1, abort_flag);
+        if (!ok) break;
+        tc05::fence_smem_to_async();  // P was written by CTA 0's stores; the tensor core reads it
+        const float alpha = alpha_s[pbuf * kHeads + tid];
+        ok = wwait<false>(bar(B_VFULL + vs), (g / kVStages) & 1, abort_flag);
+        if (!ok) break;
+        if (kTma && vmask != ~0ull) {
+          // value rows of keys without data (past the item, rejected pages, runs not copied): zero
+          uint8_t* st = base + vs * kVStage;
+          for (int idx = tid; idx < kTile * kVB * 8; idx += 128) {
+            const int key = idx / (kVB * 8);
+            if ((vmask >> key) & 1ull) continue;
+            const int ch = idx - key * (kVB * 8);
+            *reinterpret_cast<uint4*>(st + (ch >> 3) * kBlk + tc05::sw128(key, ch & 7)) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          tc05::fence_smem_to_async();
+        }
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          // O (all 512 columns) of the rows whose max rose, after the previous P V
+          ok = wwait<false>(bar(B_PVDONE + ((g - 1) & 1)), ((g - 1) >> 1) & 1, abort_flag);
+          if (!ok) break;
+          tc05::fence_after_sync();
+#pragma unroll 1
+          for (int col = 0; col < kDv; col += 32) {
+            float v[16], w[16];
+            tc05::ld_x16(my_lane + col, v);
+            tc05::ld_x16(my_lane + col + 16, w);
+            tc05::ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              v[e] *= alpha;
+              w[e] *= alpha;
+            }
+            tc05::st_x16(my_lane + col, v);
+            tc05::st_x16(my_lane + col + 16, w);
+          }
+          tc05::st_wait();
+        }
+        tc05::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) arrive_local(bar(B_READY + pbuf));
+      }
+      if (!ok) break;
+      // ---- epilogue of the item: O / sum -> o_part (whole stripe) or the piece's workspace slot
+      ok = wwait<true>(bar(B_FINFULL), fi & 1, abort_flag);
+      if (!ok) break;
+      const float2 f = fin_s[tid];
+      __syncwarp();
+      if (lane == 0) tc05::mbar_arrive_remote(r_finempty);
+      ok = wwait<false>(bar(B_PVDONE + ((g - 1) & 1)), ((g - 1) >> 1) & 1, abort_flag);
+      if (!ok) break;
+      tc05::fence_after_sync();
+      float* dst = it.slot < 0 ? a.o_part + orow * kDv : a.ws_o + (static_cast<int64_t>(it.slot) * kHeads + tid) * kDv;
+#pragma unroll 1
+      for (int col = 0; col < kDv; col += 64) {
+        float v0[16], v1[16], v2[16], v3[16];
+        tc05::ld_x16(my_lane + col, v0);
+        tc05::ld_x16(my_lane + col + 16, v1);
+        tc05::ld_x16(my_lane + col + 32, v2);
+        tc05::ld_x16(my_lane + col + 48, v3);
+        tc05::ld_wait();
+        float4* d4 = reinterpret_cast<float4*>(dst + col);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          d4[e] = make_float4(v0[4 * e] * f.x, v0[4 * e + 1] * f.x, v0[4 * e + 2] * f.x, v0[4 * e + 3] * f.x);
+          d4[4 + e] = make_float4(v1[4 * e] * f.x, v1[4 * e + 1] * f.x, v1[4 * e + 2] * f.x, v1[4 * e + 3] * f.x);
+          d4[8 + e] = make_float4(v2[4 * e] * f.x, v2[4 * e + 1] * f.x, v2[4 * e + 2] * f.x, v2[4 * e + 3] * f.x);
+          d4[12 + e] = make_float4(v3[4 * e] * f.x, v3[4 * e + 1] * f.x, v3[4 * e + 2] * f.x, v3[4 * e + 3] * f.x);
+        }
+      }
+      tc05::fence_before_sync();
+      ++fi;
+      if (it.slot < 0) {
+        a.lse_part[lse_slot(a, it.p, it.t, tid)] = f.y;
+      } else {
+        a.ws_lse[static_cast<int64_t>(it.slot) * kHeads + tid] = f.y;
+        // the last piece of the stripe to finish merges the pieces into o_part
+        const int64_t s_idx = static_cast<int64_t>(it.t) * a.P + it.p;
+        if (!take_ticket<EpGroup>(a.ws_cnt + s_idx, it.npieces)) continue;
+        const int64_t sl0 = it.slot_base;
+        merge_rows<kMergeUnroll, EpGroup>(
+            kHeads, it.npieces, kDv, [&](int r, int e) { return __ldcg(a.ws_lse + (sl0 + e) * kHeads + r); },
+            [&](int r, int e) { return a.ws_o + ((sl0 + e) * kHeads + r) * kDv; },
+            [&](int r, int d, float4 v) {
+              const int64_t o = (static_cast<int64_t>(it.p) * a.num_tokens + it.t) * a.num_q_heads + r;
+              *reinterpret_cast<float4*>(a.o_part + o * kDv + d) = v;
+            },
+            [&](int r, float lv) { a.lse_part[lse_slot(a, it.p, it.t, r)] = lv; }, scratch, kScrFloats);
+        if (tid == 0) a.ws_cnt[s_idx] = 0;
+      }
+      if (a.fused) pair_finish<kMergeUnroll, EpGroup>(a, it.t, 0, kHeads, kDv, scratch, kScrFloats);
+    }
+    if (!ok) raise_abort();
+  }
+
+  // ---- teardown: every MMA done, tensor memory freed, and neither CTA exits
+  // while the other may still write into it
+  tc05::fence_before_sync();
+  __syncthreads();
+  tc05::fence_after_sync();
+  if (warp == 0) tc05::tmem_dealloc(tbase, 512);
+  tc05::cluster_sync();
+}
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// 2-D bf16 view [rows][576] with 1152-byte rows, 64-column boxes of `box_rows` rows, 128-byte swizzle.
+bool encode_rows(CUtensorMap* map, const void* ptr, uint64_t rows, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr || rows == 0) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDqk), rows};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDqk * 2)};
+  const cuuint32_t box[2] = {64u, box_rows};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// SMs of the current device (0 if unknown).
+int device_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return sms;
+}
+
+}  // namespace
+
+int mla_max_clusters() {
+  const int sms = device_sms();
+  return sms >= 2 ? sms / 2 : 76;
+}
+
+int mla_ws_slots(int P, int interleave, int num_tokens, int max_kv_len) {
+  // Pieces of cut stripes: a stripe of n tiles is cut only when n exceeds the
+  // chunk max(total / C, 16 tiles), into at most 2 n / chunk pieces, so all
+  // pieces together number at most 2 C; and at most ceil(n / 16) per stripe.
+  const int max_tiles = (max_stripe_len(max_kv_len, P, interleave) + kTile - 1) / kTile;
+  if (max_tiles <= kMinChunkTiles) return 0;
+  const int64_t per = (max_tiles + kMinChunkTiles - 1) / kMinChunkTiles;
+  const int64_t by_stripes = static_cast<int64_t>(num_tokens) * P * per;
+  const int64_t by_clusters = 2LL * mla_max_clusters();
+  return static_cast<int>(by_stripes < by_clusters ? by_stripes : by_clusters);
+}
+
+int launch_mla_partial(const PartialArgs& a, cudaStream_t s, cudaError_t* err) {
+  if (a.num_q_heads != kHeads || a.head_dim != kDqk || a.head_dim_v != kDv || a.num_kv_heads != 1)
+    return CPATTN_ERR_UNSUPPORTED_SHAPE;
+  const int64_t pool_rows = static_cast<int64_t>(a.P) * a.num_pages * a.ps_l;
+  if (pool_rows >= (int64_t{1} << 31)) return CPATTN_ERR_UNSUPPORTED_SHAPE;
+  // TMA when every 64-key tile is a whole number of page runs of >= 8 rows (so
+  // each box lands on a 1024-byte boundary of the 128-byte swizzle pattern),
+  // or lies inside one page run
+  int box_rows = 0;
+  if (a.ps_l >= 8 && a.ps_l <= kTile && kTile % a.ps_l == 0) box_rows = a.ps_l;
+  else if (a.ps_l % kTile == 0) box_rows = kTile;
+  CUtensorMap map;
+  std::memset(&map, 0, sizeof(map));
+  const bool tma = box_rows > 0 && encode_rows(&map, a.pool_k, static_cast<uint64_t>(pool_rows), box_rows);
+  auto kern = tma ? mla_pair_kernel<true> : mla_pair_kernel<false>;
+  static std::atomic<int> smem_set[2][64];
+  *err = ensure_smem(kern, kSmemBytes, smem_set[tma ? 1 : 0]);
+  if (*err != cudaSuccess) return CPATTN_ERR_CUDA;
+  // persistent grid: as many clusters as fit (one CTA per SM), at most one per item
+  static std::atomic<int> fit[2][64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int C = fit[tma ? 1 : 0][dev & 63].load(std::memory_order_relaxed);
+  if (C <= 0) {
+    C = mla_max_clusters();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * C, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0 && n < C) C = n;
+    cudaGetLastError();  // a failed query leaves no error behind
+    fit[tma ? 1 : 0][dev & 63].store(C, std::memory_order_relaxed);
+  }
+  kern<<<dim3(2 * C, 1, 1), kThreads, kSmemBytes, s>>>(a, map, box_rows);
+  *err = cudaGetLastError();
+  return *err == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+}
+
+}  // namespace cpattn

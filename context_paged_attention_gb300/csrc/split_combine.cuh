@@ -21,6 +21,21 @@
 
 namespace cpattn {
 
+// The threads that run a merge together: the whole CTA (CtaGroup), or the
+// first kThreads threads of a warp-specialised CTA synchronised by named
+// barrier kBarId (WarpsGroup), while its other warps keep working.
+struct CtaGroup {
+  __device__ static int tid() { return threadIdx.x; }
+  __device__ static int size() { return blockDim.x; }
+  __device__ static void sync() { __syncthreads(); }
+};
+template <int kBarId, int kThreads>
+struct WarpsGroup {
+  __device__ static int tid() { return threadIdx.x; }
+  __device__ static int size() { return kThreads; }
+  __device__ static void sync() { asm volatile("bar.sync %0, %1;\n" ::"n"(kBarId), "n"(kThreads) : "memory"); }
+};
+
 // Page index of stripe slot k (k / ps_l; a shift when ps_l is a power of two).
 __device__ __forceinline__ int page_of_slot(const PartialArgs& a, int k) {
   return a.ps_shift >= 0 ? (k >> a.ps_shift) : k / a.ps_l;
@@ -36,17 +51,18 @@ __device__ __forceinline__ int64_t lse_slot(const PartialArgs& a, int p, int t, 
 // barrier orders every thread's stores before thread 0's device-scope fence,
 // which (being cumulative) publishes them before the ticket; the last CTA's
 // thread 0 fences again before the barrier that releases its readers.
+template <class Grp = CtaGroup>
 __device__ __forceinline__ bool take_ticket(int32_t* counter, int arrivals_needed) {
   __shared__ int s_last;
-  __syncthreads();
-  if (threadIdx.x == 0) {
+  Grp::sync();
+  if (Grp::tid() == 0) {
     __threadfence();
     const int ticket = atomicAdd(counter, 1);
     const bool last = (ticket == arrivals_needed - 1);
     if (last) __threadfence();
     s_last = last;
   }
-  __syncthreads();
+  Grp::sync();
   return s_last != 0;
 }
 
@@ -64,21 +80,22 @@ __device__ __forceinline__ bool take_ticket(int32_t* counter, int arrivals_neede
 //      stay coalesced) and issues all UNR loads of an entry before it uses
 //      them: UNR x 16 bytes in flight a thread, for the wide rows (MLA's 512
 //      values x 128 heads) where one CTA merges a megabyte.
-// Rows go in batches that fit `scratch` (cap floats of shared memory the CTA
-// no longer uses; cap >= E + 1).  All threads of the CTA must call.
-template <int UNR = 1, class LseIn, class OIn, class Put, class PutLse>
+// Rows go in batches that fit `scratch` (cap floats of shared memory the
+// group no longer uses; cap >= E + 1).  All threads of the group must call.
+template <int UNR = 1, class Grp = CtaGroup, class LseIn, class OIn, class Put, class PutLse>
 __device__ __forceinline__ void merge_rows(int R, int E, int Dv, LseIn lse_in, OIn o_in, Put put, PutLse put_lse,
                                            float* scratch, int cap) {
   const int RB = max(1, min(R, cap / (E + 1)));
   const int D4 = Dv / 4;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  const int gtid = Grp::tid(), gsize = Grp::size();
+  const int warp = gtid >> 5, lane = gtid & 31, nwarps = gsize >> 5;
   for (int r0 = 0; r0 < R; r0 += RB) {
     const int nr = min(RB, R - r0);
     float* wt = scratch;              // [nr][E]
     float* s_ok = scratch + nr * E;   // [nr]: 1 if the row has keys
-    __syncthreads();  // the scratch may still be read from the previous batch or caller
-    for (int idx = threadIdx.x; idx < nr * E; idx += blockDim.x) wt[idx] = lse_in(r0 + idx / E, idx % E);
-    __syncthreads();
+    Grp::sync();  // the scratch may still be read from the previous batch or caller
+    for (int idx = gtid; idx < nr * E; idx += gsize) wt[idx] = lse_in(r0 + idx / E, idx % E);
+    Grp::sync();
     for (int r = warp; r < nr; r += nwarps) {
       float mx = -INFINITY;
       for (int e = lane; e < E; e += 32) mx = fmaxf(mx, wt[r * E + e]);
@@ -103,9 +120,9 @@ __device__ __forceinline__ void merge_rows(int R, int E, int Dv, LseIn lse_in, O
         put_lse(r0 + r, empty ? -INFINITY : mx + logf(sum));
       }
     }
-    __syncthreads();
+    Grp::sync();
     if constexpr (UNR == 1) {
-      for (int idx = threadIdx.x; idx < nr * D4; idx += blockDim.x) {
+      for (int idx = gtid; idx < nr * D4; idx += gsize) {
         const int r = idx / D4;
         const int d = (idx - r * D4) * 4;
         const float* wr = wt + r * E;
@@ -125,12 +142,12 @@ __device__ __forceinline__ void merge_rows(int R, int E, int Dv, LseIn lse_in, O
       }
     } else {
       const int n4 = nr * D4;
-      for (int i0 = threadIdx.x; i0 < n4; i0 += blockDim.x * UNR) {
+      for (int i0 = gtid; i0 < n4; i0 += gsize * UNR) {
         int rr[UNR], dd[UNR];
         float4 acc[UNR];
 #pragma unroll
         for (int u = 0; u < UNR; ++u) {
-          const int idx = i0 + u * blockDim.x;
+          const int idx = i0 + u * gsize;
           rr[u] = idx < n4 ? idx / D4 : -1;
           dd[u] = idx < n4 ? (idx - rr[u] * D4) * 4 : 0;
           acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -191,7 +208,7 @@ __device__ __forceinline__ void merge_chunks(const PartialArgs& a, int p, int h,
 // partner partials (o_part / lse_part rows, which fused calls keep in the
 // workspace) and the optional extra partial (entry P); written as bf16
 // (round to nearest even) or fp32.  Row r = token t0 + r / Hg, head r % Hg.
-template <int UNR = 1>
+template <int UNR = 1, class Grp = CtaGroup>
 __device__ __forceinline__ void merge_partners(const PartialArgs& a, int t0, int ntok, int h, int Hg, int Dv,
                                                float* scratch, int cap) {
   const int64_t pstride = static_cast<int64_t>(a.num_tokens) * a.num_q_heads;  // rows between partners
@@ -201,7 +218,7 @@ __device__ __forceinline__ void merge_partners(const PartialArgs& a, int t0, int
     const int i = r / Hg;
     return static_cast<int64_t>(t0 + i) * a.num_q_heads + h * Hg + (r - i * Hg);
   };
-  merge_rows<UNR>(
+  merge_rows<UNR, Grp>(
       ntok * Hg, E, Dv,
       [&](int r, int e) {
         const int i = r / Hg;
@@ -231,13 +248,13 @@ __device__ __forceinline__ void merge_partners(const PartialArgs& a, int t0, int
 // Fused calls, after a partner's partial of (token t, KV head h) is complete
 // in o_part (written directly, or merged from its chunks by this CTA): arrive
 // on the pair's ticket; the last of the P partners merges (all threads call).
-template <int UNR = 1>
+template <int UNR = 1, class Grp = CtaGroup>
 __device__ __forceinline__ void pair_finish(const PartialArgs& a, int t, int h, int Hg, int Dv, float* scratch,
                                             int cap) {
   int32_t* pair = a.ws_pair + static_cast<int64_t>(t) * a.num_kv_heads + h;
-  if (!take_ticket(pair, a.P)) return;
-  merge_partners<UNR>(a, t, 1, h, Hg, Dv, scratch, cap);
-  if (threadIdx.x == 0) *pair = 0;
+  if (!take_ticket<Grp>(pair, a.P)) return;
+  merge_partners<UNR, Grp>(a, t, 1, h, Hg, Dv, scratch, cap);
+  if (Grp::tid() == 0) *pair = 0;
 }
 
 // Output rows of padding tokens (fused calls): 0 and -inf.
