@@ -132,8 +132,10 @@ int launch_gqa_partial_mma(const PartialArgs& a, cudaStream_t s, cudaError_t* er
 int launch_gqa_partial_ext(const PartialArgs& a, cudaStream_t s, cudaError_t* err);
 int launch_gqa_partial_ext_ws(const PartialArgs& a, cudaStream_t s, cudaError_t* err);  // bf16 pools
 int launch_mla_partial(const PartialArgs& a, cudaStream_t s, cudaError_t* err);
-// MLA kernel: workspace slots for the pieces of cut stripes (0: no stripe can be cut)
-int mla_ws_slots(int P, int interleave, int num_tokens, int max_kv_len);
+// MLA kernel: workspace slots for the pieces of cut stripes (0: no stripe can be
+// cut); `grouped`: fused calls whose tiles are logical pages (cut tokens)
+int mla_ws_slots(int P, int interleave, int num_tokens, int max_kv_len, int grouped);
+constexpr int kMlaGroupMaxTokens = 511;  // grouped MLA plans keep two tables of this many tokens
 
 struct OwnArgs {
   const void* q;

@@ -239,7 +239,8 @@ bool plan_partial(int mla, int fused, int P, int interleave, int page_size, int 
     // the MLA kernel plans on the device (stripes longest first, long ones cut
     // into pieces); the workspace holds the pieces' partials, max_chunks of
     // them at most (0: no stripe can be cut)
-    const int slots = mla_ws_slots(P, interleave, num_tokens, max_kv_len);
+    const int grouped = fused && page_size == 64 && num_tokens <= kMlaGroupMaxTokens;  // the kernel's own test
+    const int slots = mla_ws_slots(P, interleave, num_tokens, max_kv_len, grouped);
     const size_t stripes = static_cast<size_t>(num_tokens) * P;
     plan->chunk = 64;
     plan->max_chunks = slots;

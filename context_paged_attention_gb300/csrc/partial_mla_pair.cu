@@ -46,6 +46,22 @@
 // (a ticket) merges them.  Too many stripes to rank in shared memory: items
 // are whole stripes in dispatch order.
 //
+// Fused calls over pages of 64 slots (P * page_size / P = 64) take another
+// grouping.  The P partners hold the 64 slots of a logical page as P runs of
+// page_size / P rows at the same page id of their pools, so one 3-D TMA box
+// per column block -- 64 values x page_size / P rows x P partners, 8 KB --
+// brings the whole logical page into a 64-key tile (row r = partner r /
+// (page_size / P), slot r % (page_size / P); the placement, interleave
+// included, says which position each row holds).  An item is then a token,
+// its tiles are its logical pages, and the online softmax runs over every
+// partner's keys at once: the exact merge of the partner partials happens
+// tile by tile inside it, and the kernel writes the token's final output.
+// With page runs of 16 rows this needs a quarter of the TMA boxes of the
+// per-partner tiles, and the copy engines, not the boxes, set the pace.  The
+// clusters split the sequence of all tiles into equal contiguous ranges; a
+// token that straddles a boundary is cut, its pieces go to workspace slots
+// and the last to finish merges them (with the optional extra partial).
+//
 // Every wait is bounded; one that runs out raises the abort flag of both
 // CTAs, which ends their other waits, and the call reports
 // CPATTN_DEV_TC_TIMEOUT (that item's output is not written).
@@ -82,7 +98,9 @@ constexpr int kWMma = 4;
 constexpr int kWLoad = 5;
 constexpr int kMinChunkTiles = 16;   // cut pieces hold at least 1024 keys
 constexpr int kSortMax = 512;        // stripes ranked in shared memory
-constexpr int kMaxOwn = 64;          // items one cluster keeps in its list
+constexpr int kItemsBytes = 4096;    // per-cluster item list (stripes), or the token tables (grouped)
+constexpr int kGroupMaxTokens = kItemsBytes / 8 - 1;  // grouped plans: pre[T + 1] and sbase[T] ints
+static_assert(kGroupMaxTokens == kMlaGroupMaxTokens, "grouped token limit shared with the planner");
 constexpr uint32_t kQCol = 128;      // CTA 0: S buffers at columns 0 and 64, Q at 128..415
 constexpr int kMergeUnroll = 8;
 
@@ -113,18 +131,20 @@ enum : int {
   B_DRAIN = 26,     // both [commit]: the MMA thread's last MMAs done
   B_EPSYNC = 27,    // CTA 1 [128 epilogue threads]: their group barrier (merges)
   B_KLAND = 28,     // x16 CTA 1 [1 remote arrival]: the tile's rows reached CTA 0 (so they sit in L2)
-  kBars = 44
+  B_MERGE = 44,     // x2 CTA 1 [1 + bytes]: a batch of partial rows landed (merges of cut items)
+  kBars = 46
 };
 constexpr uint32_t OFF_BAR = kStageArea;
-constexpr uint32_t OFF_MISC = OFF_BAR + kBars * 8;  // [0] TMEM base, [1] abort, [2] items (-1: on the fly), [3] sum
+constexpr uint32_t OFF_MISC = OFF_BAR + kBars * 8;  // [0] TMEM base, [1] abort, [2] items (-1: on the fly) / first token, [3] tiles
 struct MlaItem {
   int t, p, b;           // token, partner, row (-1: no row)
   int k_begin, k_end;    // stripe slots of this item
   int slot;              // workspace slot of a cut stripe's piece, or -1
   int slot_base, npieces;
 };
-constexpr uint32_t OFF_ITEMS = OFF_MISC + 16;
-constexpr size_t kSmemBytes = 1024 + OFF_ITEMS + kMaxOwn * sizeof(MlaItem);
+constexpr int kMaxOwn = kItemsBytes / static_cast<int>(sizeof(MlaItem));  // items one cluster keeps in its list
+constexpr uint32_t OFF_ITEMS = OFF_MISC + 32;
+constexpr size_t kSmemBytes = 1024 + OFF_ITEMS + kItemsBytes;
 static_assert(OFF_SCR + 1024 <= kStageArea, "CTA 1 map exceeds the stage area");
 static_assert(kSmemBytes + 64 <= 232448, "shared memory per CTA");
 
@@ -193,11 +213,17 @@ __device__ __forceinline__ bool pwait(uint32_t mbar, uint32_t parity, const vola
   return false;
 }
 
-// pwait by every lane of a warp, with one verdict for the whole warp (so no
-// lane leaves a loop that its warp-mates stay in).
+// A whole warp waits: lane 0 polls (one shared-memory probe at a time, not
+// 32), the verdict goes to every lane, and __syncwarp orders the other lanes'
+// later accesses after lane 0's acquire.  One verdict for the warp, so no lane
+// leaves a loop that its warp-mates stay in.
 template <bool kCluster>
 __device__ __forceinline__ bool wwait(uint32_t mbar, uint32_t parity, const volatile int* abort_flag) {
-  return __all_sync(0xffffffffu, pwait<kCluster>(mbar, parity, abort_flag)) != 0;
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = pwait<kCluster>(mbar, parity, abort_flag) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
 }
 
 // Token, partner, row and stripe length of stripe s = token * P + partner.
@@ -385,6 +411,184 @@ __device__ __forceinline__ uint64_t tile_mask(const PartialArgs& a, const MlaIte
   return static_cast<uint64_t>(lo) | (static_cast<uint64_t>(hi) << 32);
 }
 
+// ---- grouped tiles (fused calls, logical pages of 64 slots) ----------------
+
+// Keys of token t's row (clamped to max_kv_len; 0 for tokens of no row).
+__device__ __forceinline__ int token_len(const PartialArgs& a, int t, int* b_out, bool may_report) {
+  const StripeGeo g = stripe_geo(a, t, 0, may_report);
+  *b_out = g.b;
+  if (g.b < 0) return 0;
+  int L = __ldg(a.kv_len + g.b);
+  if (L > a.max_kv_len) L = a.max_kv_len;
+  return max(L, 0);
+}
+
+// Cluster whose range of the W tiles holds tile x (ranges [c W / C, (c + 1) W / C)).
+__device__ __forceinline__ int tile_cluster(int64_t x, int64_t W, int C) {
+  return static_cast<int>(((x + 1) * C + W - 1) / W) - 1;
+}
+
+// The grouped plan (all threads; both CTAs compute the same one): pre[t] =
+// first tile of token t in the sequence of all tokens' pages, pre[T] = W;
+// sbase[t] = first workspace slot of a cut token (the pieces of cut tokens
+// numbered in token order).  The W tiles go to Ce = min(C, ceil(W / 16))
+// clusters in equal contiguous ranges, so no range is shorter than 16 tiles
+// (clusters from Ce on get none).  misc[3] = W, misc[4] = Ce, misc[2] = first
+// token of cluster c.
+__device__ void mla_plan_group(const PartialArgs& a, int C, int c, int* pre, int* sbase, int* misc) {
+  const int T = a.num_tokens;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (warp == 0) {
+    const int per = (T + 31) / 32;
+    const int i0 = min(T, lane * per), i1 = min(T, i0 + per);
+    int sp = 0;
+    for (int t = i0; t < i1; ++t) {
+      int b;
+      sp += (token_len(a, t, &b, true) + kTile - 1) / kTile;
+    }
+    int ip = sp;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, ip, o);
+      if (lane >= o) ip += u;
+    }
+    int ep = ip - sp;
+    for (int t = i0; t < i1; ++t) {
+      int b;
+      pre[t] = ep;
+      ep += (token_len(a, t, &b, false) + kTile - 1) / kTile;
+    }
+    if (lane == 31) pre[T] = ip;
+    __syncwarp();
+    // workspace slots of cut tokens (pieces in token order)
+    const int64_t W = pre[T];
+    {
+      const int64_t cap = (W + kMinChunkTiles - 1) / kMinChunkTiles;
+      if (cap < C) C = static_cast<int>(cap);
+    }
+    if (C < 1) C = 1;
+    int ss = 0;
+    for (int t = i0; t < i1; ++t) {
+      const int n = pre[t + 1] - pre[t];
+      const int pcs = n > 0 && W > 0 ? tile_cluster(pre[t + 1] - 1, W, C) - tile_cluster(pre[t], W, C) + 1 : 1;
+      ss += pcs > 1 ? pcs : 0;
+    }
+    int is = ss;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, is, o);
+      if (lane >= o) is += u;
+    }
+    int es = is - ss;
+    for (int t = i0; t < i1; ++t) {
+      const int n = pre[t + 1] - pre[t];
+      const int pcs = n > 0 && W > 0 ? tile_cluster(pre[t + 1] - 1, W, C) - tile_cluster(pre[t], W, C) + 1 : 1;
+      sbase[t] = es;
+      es += pcs > 1 ? pcs : 0;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      misc[3] = pre[T];
+      misc[4] = C;
+      // first token whose tiles reach into this cluster's range
+      const int64_t s0 = static_cast<int64_t>(c) * W / C;
+      int lo = 0, hi = T;  // first t with pre[t + 1] > s0
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (pre[mid + 1] > s0) hi = mid; else lo = mid + 1;
+      }
+      misc[2] = lo;
+    }
+  }
+  __syncthreads();
+}
+
+// Item k of cluster c in the grouped plan: token t_first + k, the part of its
+// pages inside the cluster's range (k_begin / k_end in positions of the row).
+__device__ __forceinline__ bool get_item_group(const PartialArgs& a, int k, int C, int c, const int* pre,
+                                               const int* sbase, int64_t W, int t_first, MlaItem& it) {
+  const int t = t_first + k;
+  if (t >= a.num_tokens || W == 0 || c >= C) return false;
+  const int64_t s0 = static_cast<int64_t>(c) * W / C, s1 = static_cast<int64_t>(c + 1) * W / C;
+  if (pre[t] >= s1) return false;
+  int b;
+  const int L = token_len(a, t, &b, false);
+  const int64_t pt0 = pre[t], pt1 = pre[t + 1];
+  const int64_t lo = pt0 > s0 ? pt0 : s0, hi = pt1 < s1 ? pt1 : s1;
+  it.t = t;
+  it.p = 0;
+  it.b = b;
+  it.k_begin = static_cast<int>(lo - pre[t]) * kTile;
+  it.k_end = min(L, static_cast<int>(hi - pre[t]) * kTile);
+  if (hi <= lo) it.k_end = it.k_begin;  // a token of no pages: nothing here (written by the zero pass)
+  const int n = pre[t + 1] - pre[t];
+  const int c0 = n > 0 ? tile_cluster(pre[t], W, C) : c;
+  const int pcs = n > 0 ? tile_cluster(pre[t + 1] - 1, W, C) - c0 + 1 : 1;
+  it.npieces = pcs;
+  it.slot_base = sbase[t];
+  it.slot = pcs > 1 ? sbase[t] + (c - c0) : -1;
+  if (it.slot >= a.max_chunks) {  // the workspace bound makes this impossible; never write past it
+    if (threadIdx.x == 0) report(a.dev_status, CPATTN_DEV_BAD_INDPTR);
+    it.t = -1;
+  }
+  return true;
+}
+
+// Row of the page pool where logical page (k_begin / 64 + j) of the item
+// starts in every partner's pool (page id * page_size / P), or -1 (past the
+// table, rejected page; reported when `rep`).
+__device__ __forceinline__ int group_page_row(const PartialArgs& a, const MlaItem& it, int j, int pb0, int npg,
+                                              bool rep) {
+  const int jj = it.k_begin / kTile + j;
+  if (jj >= npg) {
+    if (rep) report(a.dev_status, CPATTN_DEV_POS_PAST_TABLE);
+    return -1;
+  }
+  const int pg = __ldg(a.page_indices + pb0 + jj);
+  if (pg < 0 || pg >= a.num_pages) {
+    if (rep) report(a.dev_status, CPATTN_DEV_PAGE_OUT_OF_RANGE);
+    return -1;
+  }
+  return pg * a.ps_l;
+}
+
+// Keys of grouped tile j that hold data: tile row r is partner r / ps_l's
+// physical slot l = r % ps_l of the page, i.e. in-page offset
+// (l / I) * I * P + p * I + l % I (I = 1: l * P + p), a key of the row when
+// its position is below the item's end and the page is accepted.
+__device__ __forceinline__ uint64_t tile_mask_group(const PartialArgs& a, const MlaItem& it, int j, int pb0, int npg,
+                                                    int lane) {
+  const bool page_ok = group_page_row(a, it, j, pb0, npg, false) >= 0;
+  const int base = it.k_begin + j * kTile;
+  const int I = a.interleave;
+  auto pos_of = [&](int r) {
+    const int p = r / a.ps_l, l = r - (r / a.ps_l) * a.ps_l;
+    return base + (l / I) * I * a.P + p * I + (l % I);
+  };
+  const bool va = page_ok && pos_of(lane) < it.k_end;
+  const bool vb = page_ok && pos_of(lane + 32) < it.k_end;
+  const uint32_t lo = __ballot_sync(0xffffffffu, va), hi = __ballot_sync(0xffffffffu, vb);
+  return static_cast<uint64_t>(lo) | (static_cast<uint64_t>(hi) << 32);
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int x, int y, int z, uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(
+          dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(mbar)
+      : "memory");
+}
+
+// Copies of grouped tile j: one 3-D box (64 values x ps_l rows x P partners)
+// per column block, lane 0; page_row from group_page_row (-1: nothing copied).
+__device__ __forceinline__ void load_tile_group(const CUtensorMap* tmap, uint32_t dst, int nblk, uint32_t full,
+                                                int page_row, int lane) {
+  if (lane != 0) return;
+  tc05::mbar_arrive_expect_tx(full, page_row >= 0 ? nblk * kBlk : 0);
+  if (page_row < 0) return;
+  for (int kb = 0; kb < nblk; ++kb) tma_load_3d(dst + kb * kBlk, tmap, kb * 64, page_row, 0, full);
+}
+
 // Copies of tile j of the item into a stage (nblk column blocks of 64 values):
 // TMA boxes of `box_rows` rows (lane 0), or 16-byte cp.async copies by the
 // whole warp with zero fill for keys without data.  Completion is counted on
@@ -453,7 +657,7 @@ __device__ __forceinline__ void load_tile(const PartialArgs& a, const CUtensorMa
 
 }  // namespace
 
-template <bool kTma>
+template <bool kTma, bool kGroup>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_pair_kernel(const PartialArgs a, const __grid_constant__ CUtensorMap tmap, int box_rows) {
   extern __shared__ uint8_t smem_raw[];
@@ -478,10 +682,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     misc[1] = 0;
     misc[2] = -1;
     misc[3] = 0;
+    misc[4] = C;
   }
   __syncthreads();
-  const int S = a.num_tokens * a.P;
-  if (S <= kSortMax && S + 2 * C <= kMaxOwn * C) mla_plan(a, C, c, reinterpret_cast<int*>(base), misc, items);
+  int* g_pre = reinterpret_cast<int*>(base + OFF_ITEMS);  // grouped plans: [kGroupMaxTokens + 1]
+  int* g_sbase = g_pre + (kGroupMaxTokens + 1);            //                [kGroupMaxTokens]
+  if constexpr (kGroup) {
+    mla_plan_group(a, C, c, g_pre, g_sbase, misc);
+  } else {
+    const int S = a.num_tokens * a.P;
+    if (S <= kSortMax && S + 2 * C <= kMaxOwn * C) mla_plan(a, C, c, reinterpret_cast<int*>(base), misc, items);
+  }
   if (tid == 0) {
     const uint32_t load_arrivals = kTma ? 1u : 32u;
     for (int i = 0; i < kKStages; ++i) {
@@ -506,6 +717,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc05::mbar_init(bar(B_FINFULL), kHeads);
     tc05::mbar_init(bar(B_DRAIN), 1);
     tc05::mbar_init(bar(B_EPSYNC), kHeads);
+    tc05::mbar_init(bar(B_MERGE), 1);
+    tc05::mbar_init(bar(B_MERGE + 1), 1);
     for (int i = 0; i < kLandRing; ++i) tc05::mbar_init(bar(B_KLAND + i), 1);
     tc05::mbar_init_fence();
   }
@@ -516,7 +729,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc05::cluster_sync();  // the peer's barriers exist before any remote arrival
   const uint32_t tbase = static_cast<uint32_t>(misc[0]);
   const int n_items = misc[2];
-  auto item = [&](int k, MlaItem& it) { return get_item(a, k, C, c, n_items, items, it); };
+  const int64_t g_W = misc[3];
+  const int g_C = misc[4];  // grouped plans: clusters with a range
+  auto item = [&](int k, MlaItem& it) {
+    if constexpr (kGroup) return get_item_group(a, k, g_C, c, g_pre, g_sbase, g_W, n_items, it);
+    else return get_item(a, k, C, c, n_items, items, it);
+  };
+  auto mask_of = [&](const MlaItem& it, int j, int pb0, int npg) {
+    if constexpr (kGroup) return tile_mask_group(a, it, j, pb0, npg, lane);
+    else return tile_mask(a, it, j, pb0, npg, lane);
+  };
   auto ntiles = [](const MlaItem& it) {
     return it.t >= 0 && it.k_end > it.k_begin ? (it.k_end - it.k_begin + kTile - 1) / kTile : 0;
   };
@@ -536,7 +758,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (nt == 0) continue;
       const int pb0 = __ldg(a.page_indptr + it.b), npg = __ldg(a.page_indptr + it.b + 1) - pb0;
       // page rows of the next tile are looked up while the stage it goes to is still busy
-      int run_row = kTma ? tile_run_row(a, it, 0, pb0, npg, box_rows, lane) : -1;
+      auto rows_of = [&](int jt) {
+        if constexpr (kGroup) return lane == 0 ? group_page_row(a, it, jt, pb0, npg, true) : -1;
+        else return kTma ? tile_run_row(a, it, jt, pb0, npg, box_rows, lane) : -1;
+      };
+      int run_row = rows_of(0);
       for (int j = 0; j < nt; ++j, ++g) {
         const int st = g % nstages;
         ok = wwait<false>(bar(b_empty + st), ((g / nstages) & 1) ^ 1, abort_flag);
@@ -544,10 +770,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // they are in L2 by then, and CTA 1's copies do not race CTA 0's to HBM
         if (ok && rank == 1) ok = wwait<true>(bar(B_KLAND + g % kLandRing), (g / kLandRing) & 1, abort_flag);
         if (!ok) break;
-        load_tile<kTma>(a, &tmap, it, j, pb0, npg, sb + st * stage_bytes, nblk, bar(b_full + st), box_rows, lane,
-                        run_row);
+        if constexpr (kGroup) load_tile_group(&tmap, sb + st * stage_bytes, nblk, bar(b_full + st), run_row, lane);
+        else load_tile<kTma>(a, &tmap, it, j, pb0, npg, sb + st * stage_bytes, nblk, bar(b_full + st), box_rows, lane,
+                             run_row);
         issued = g + 1;
-        if (kTma && j + 1 < nt) run_row = tile_run_row(a, it, j + 1, pb0, npg, box_rows, lane);
+        if (j + 1 < nt) run_row = rows_of(j + 1);
       }
     }
     if (!ok) raise_abort();
@@ -661,7 +888,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       float m = -INFINITY, l = 0.f, lr = 0.f;
       for (int j = 0; j < nt; ++j, ++g) {
         const int sbuf = g & 1;
-        const uint64_t vmask = tile_mask(a, it, j, pb0, npg, lane);
+        const uint64_t vmask = mask_of(it, j, pb0, npg);
         ok = wwait<false>(bar(B_SFULL + sbuf), (g >> 1) & 1, abort_flag);
         if (!ok) break;
         tc05::fence_after_sync();
@@ -775,13 +1002,210 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const float* alpha_s = reinterpret_cast<const float*>(base + OFF_ALPHA);
     const float2* fin_s = reinterpret_cast<const float2*>(base + OFF_FIN);
     float* scratch = reinterpret_cast<float*>(base + OFF_SCR);
+    // O (tensor memory, this thread's row = head tid) times wo, plus we times
+    // row tid of ext when given, into the 128 rows at dst0 (a row every 512
+    // elements; fp32, or bf16 rounded to nearest even).  Staged through shared
+    // memory in 128-byte chunks of every row, so that eight threads store each
+    // line.  All epilogue threads call.
+    auto store_rows = [&](void* dst0, bool to_bf16, float wo, float we, const float* ext) {
+      const int cols = to_bf16 ? 64 : 32;
+#pragma unroll 1
+      for (int ch = 0; ch < kDv / cols; ++ch) {
+        uint8_t* buf = base + OFF_SCR + (ch & 1) * (kHeads * 128);
+        const int c0 = ch * cols;
+        uint32_t wds[32];
+        if (!to_bf16) {
+          float v[32];
+          tc05::ld_x16(my_lane + c0, *reinterpret_cast<float(*)[16]>(v));
+          tc05::ld_x16(my_lane + c0 + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+          tc05::ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] *= wo;
+          if (ext != nullptr) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+              const float4 x = __ldg(reinterpret_cast<const float4*>(ext + static_cast<int64_t>(tid) * kDv + c0 + e));
+              v[e] = fmaf(we, x.x, v[e]);
+              v[e + 1] = fmaf(we, x.y, v[e + 1]);
+              v[e + 2] = fmaf(we, x.z, v[e + 2]);
+              v[e + 3] = fmaf(we, x.w, v[e + 3]);
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 32; ++e) wds[e] = __float_as_uint(v[e]);
+        } else {
+          float v[64];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) tc05::ld_x16(my_lane + c0 + 16 * q, *reinterpret_cast<float(*)[16]>(v + 16 * q));
+          tc05::ld_wait();
+#pragma unroll
+          for (int e = 0; e < 64; ++e) v[e] *= wo;
+          if (ext != nullptr) {
+#pragma unroll
+            for (int e = 0; e < 64; e += 4) {
+              const float4 x = __ldg(reinterpret_cast<const float4*>(ext + static_cast<int64_t>(tid) * kDv + c0 + e));
+              v[e] = fmaf(we, x.x, v[e]);
+              v[e + 1] = fmaf(we, x.y, v[e + 1]);
+              v[e + 2] = fmaf(we, x.z, v[e + 2]);
+              v[e + 3] = fmaf(we, x.w, v[e + 3]);
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+            wds[e] = *reinterpret_cast<uint32_t*>(&h);
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<uint4*>(buf + tc05::sw128(tid, q)) =
+              make_uint4(wds[4 * q], wds[4 * q + 1], wds[4 * q + 2], wds[4 * q + 3]);
+        EpGroup::sync();
+        const int esz = to_bf16 ? 2 : 4;
+#pragma unroll
+        for (int i2 = 0; i2 < 8; ++i2) {
+          const int x = i2 * kHeads + tid, row = x >> 3, q = x & 7;
+          const uint4 val = *reinterpret_cast<const uint4*>(buf + tc05::sw128(row, q));
+          *reinterpret_cast<uint4*>(static_cast<char*>(dst0) + static_cast<int64_t>(row) * kDv * esz + ch * 128 + q * 16) =
+              val;
+        }
+      }
+    };
+    // Exact merge of E partials of all 128 rows (the LSE merge of lse_merge):
+    // entry e < E0 is workspace slot sl0 + e (rows contiguous), entry E0 (when
+    // ext_o is given) the extra partial.  Each thread forms its row's weights;
+    // then batches of R rows of every entry come into shared memory by bulk
+    // copies (two batches in flight) and the weighted rows go to row r of
+    // dst0 (a row every 512 elements, fp32 or bf16) with coalesced stores; the
+    // row's LSE to put_lse.  Returns false (nothing done) when the entries do
+    // not fit the staging buffers.  All epilogue threads call.
+    int merge_phase = 0;  // batches issued on B_MERGE so far (parity tracking)
+    auto merge_bulk = [&](int E0, int64_t sl0, const float* ext_o, const float* ext_lse, void* dst0, bool to_bf16,
+                          auto put_lse) -> bool {
+      const int E = E0 + (ext_o != nullptr ? 1 : 0);
+      float* wt = scratch;  // [E][128]
+      const uint32_t wt_bytes = static_cast<uint32_t>((E * kHeads * 4 + 1023) & ~1023);
+      const uint32_t avail = static_cast<uint32_t>(kScrFloats) * 4u - wt_bytes;
+      const int R = static_cast<int>(avail / 2 / (static_cast<uint32_t>(E) * kDv * 4));
+      if (R < 1) return false;
+      {
+        // weights of row tid
+        float mx = -INFINITY;
+        for (int e = 0; e < E; ++e) {
+          const float l = e < E0 ? __ldcg(a.ws_lse + (sl0 + e) * kHeads + tid) : __ldg(ext_lse + tid);
+          wt[e * kHeads + tid] = l;
+          mx = fmaxf(mx, l);
+        }
+        float sum = 0.f;
+        for (int e = 0; e < E; ++e) {
+          const float l = wt[e * kHeads + tid];
+          sum += (mx == -INFINITY || l == -INFINITY) ? 0.f : expf(l - mx);
+        }
+        const float inv = sum == 0.f ? 0.f : 1.f / sum;
+        for (int e = 0; e < E; ++e) {
+          const float l = wt[e * kHeads + tid];
+          wt[e * kHeads + tid] = (sum == 0.f || l == -INFINITY) ? 0.f : expf(l - mx) * inv;
+        }
+        put_lse(tid, sum == 0.f ? -INFINITY : mx + logf(sum));
+      }
+      uint8_t* buf0 = base + OFF_SCR + wt_bytes;
+      const uint32_t buf_bytes = static_cast<uint32_t>(E) * R * kDv * 4;
+      const int nbatch = (kHeads + R - 1) / R;
+      auto issue = [&](int k) {
+        const uint32_t mb = bar(B_MERGE + ((merge_phase + k) & 1));  // batch k's barrier (as waited below)
+        const int r0 = k * R, nr = min(R, kHeads - r0);
+        const uint32_t dst = tc05::smem_addr(buf0 + (k & 1) * buf_bytes);
+        tc05::mbar_arrive_expect_tx(mb, static_cast<uint32_t>(E * nr) * kDv * 4);
+        for (int e = 0; e < E; ++e) {
+          const float* src = e < E0 ? a.ws_o + ((sl0 + e) * kHeads + r0) * kDv : ext_o + static_cast<int64_t>(r0) * kDv;
+          asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                           dst + e * nr * kDv * 4),
+                       "l"(src), "r"(nr * kDv * 4), "r"(mb)
+                       : "memory");
+        }
+      };
+      EpGroup::sync();  // weights in place; the staging area is free
+      if (tid == 0) {
+        // the partial rows were written by other CTAs' plain stores, published
+        // by the ticket; the copies read them through the async proxy
+        asm volatile("fence.proxy.async;\n" ::: "memory");
+        issue(0);
+        if (nbatch > 1) issue(1);
+      }
+      bool okm = true;
+      for (int k = 0; k < nbatch; ++k) {
+        const int ph = merge_phase + k;  // batch k is phase (ph >> 1) of barrier ph & 1
+        okm = okm && wwait<false>(bar(B_MERGE + (ph & 1)), (ph >> 1) & 1, abort_flag);
+        const int r0 = k * R, nr = min(R, kHeads - r0);
+        const float4* bf = reinterpret_cast<const float4*>(buf0 + (k & 1) * buf_bytes);
+        if (okm) {
+          for (int idx = tid; idx < nr * (kDv / 4); idx += kHeads) {
+            const int rr = idx / (kDv / 4), c4 = idx - rr * (kDv / 4);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int e = 0; e < E; ++e) {
+              const float w = wt[e * kHeads + r0 + rr];
+              if (w == 0.f) continue;  // empty entries' rows never enter the sum
+              const float4 v = bf[(e * nr + rr) * (kDv / 4) + c4];
+              acc.x = fmaf(w, v.x, acc.x);
+              acc.y = fmaf(w, v.y, acc.y);
+              acc.z = fmaf(w, v.z, acc.z);
+              acc.w = fmaf(w, v.w, acc.w);
+            }
+            const int64_t oi = static_cast<int64_t>(r0 + rr) * kDv + c4 * 4;
+            if (to_bf16) {
+              __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+              *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(dst0) + oi) =
+                  make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+            } else {
+              *reinterpret_cast<float4*>(static_cast<float*>(dst0) + oi) = acc;
+            }
+          }
+        }
+        EpGroup::sync();  // buffer k & 1 consumed
+        if (tid == 0 && okm && k + 2 < nbatch) issue(k + 2);
+      }
+      merge_phase += nbatch;
+      if (!okm) {
+        ok = false;
+        // nothing may land after the CTA exits: wait (bounded) for the batches in flight
+        if (tid == 0)
+          for (int k = max(0, nbatch - 2); k < nbatch; ++k) {
+            const int ph = merge_phase - nbatch + k;
+            tc05::mbar_wait(bar(B_MERGE + (ph & 1)), (ph >> 1) & 1, 1u << 20);
+          }
+      }
+      return true;
+    };
     int g = 0, fi = 0;
+    if constexpr (kGroup) {
+      // tokens without pages (padding tokens, rows of no keys): the extra
+      // partial alone, or 0 / -inf; cluster c takes tokens c, c + C, ...
+      for (int t = c; t < a.num_tokens; t += C) {
+        if (g_pre[t + 1] != g_pre[t]) continue;
+        const int64_t row = static_cast<int64_t>(t) * kHeads + tid;
+        const bool has_e = a.extra_lse != nullptr;
+        const float le = has_e ? __ldg(a.extra_lse + row) : -INFINITY;
+        for (int e = 0; e < kDv; e += 4) {
+          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (has_e && le != -INFINITY) v = __ldg(reinterpret_cast<const float4*>(a.extra_o + row * kDv + e));
+          if (a.out_bf16) {
+            __nv_bfloat162 h0 = __floats2bfloat162_rn(v.x, v.y), h1 = __floats2bfloat162_rn(v.z, v.w);
+            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + row * kDv + e) =
+                make_uint2(*reinterpret_cast<uint32_t*>(&h0), *reinterpret_cast<uint32_t*>(&h1));
+          } else {
+            *reinterpret_cast<float4*>(static_cast<float*>(a.out) + row * kDv + e) = v;
+          }
+        }
+        if (a.lse_out != nullptr) a.lse_out[row] = le;
+      }
+    }
     for (int k = 0; ok; ++k) {
       MlaItem it;
       if (!item(k, it)) break;
       if (it.t < 0) continue;
       const int nt = ntiles(it);
       const int64_t orow = (static_cast<int64_t>(it.p) * a.num_tokens + it.t) * a.num_q_heads + tid;
+      if (kGroup && nt == 0) continue;  // the zero pass wrote it
       if (nt == 0) {  // empty stripe (or a token of no row): 0 / -inf
         float4* d4 = reinterpret_cast<float4*>(a.o_part + orow * kDv);
         for (int e = 0; e < kDv / 4; ++e) d4[e] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -792,7 +1216,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int pb0 = __ldg(a.page_indptr + it.b), npg = __ldg(a.page_indptr + it.b + 1) - pb0;
       for (int j = 0; j < nt; ++j, ++g) {
         const int pbuf = g & 1, vs = g % kVStages;
-        const uint64_t vmask = tile_mask(a, it, j, pb0, npg, lane);
+        const uint64_t vmask = mask_of(it, j, pb0, npg);
         // P and the rescale factors arrive by bulk copies from CTA 0 (bytes counted)
         if (tid == 0) tc05::mbar_arrive_expect_tx(bar(B_PFULL + pbuf), kPBuf + kHeads * 4);
         ok = wwait<true>(bar(B_PFULL + pbuf), (g >> 1) & 1, abort_flag);
@@ -847,26 +1271,72 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ok = wwait<false>(bar(B_PVDONE + ((g - 1) & 1)), ((g - 1) >> 1) & 1, abort_flag);
       if (!ok) break;
       tc05::fence_after_sync();
-      float* dst = it.slot < 0 ? a.o_part + orow * kDv : a.ws_o + (static_cast<int64_t>(it.slot) * kHeads + tid) * kDv;
-#pragma unroll 1
-      for (int col = 0; col < kDv; col += 64) {
-        float v0[16], v1[16], v2[16], v3[16];
-        tc05::ld_x16(my_lane + col, v0);
-        tc05::ld_x16(my_lane + col + 16, v1);
-        tc05::ld_x16(my_lane + col + 32, v2);
-        tc05::ld_x16(my_lane + col + 48, v3);
-        tc05::ld_wait();
-        float4* d4 = reinterpret_cast<float4*>(dst + col);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          d4[e] = make_float4(v0[4 * e] * f.x, v0[4 * e + 1] * f.x, v0[4 * e + 2] * f.x, v0[4 * e + 3] * f.x);
-          d4[4 + e] = make_float4(v1[4 * e] * f.x, v1[4 * e + 1] * f.x, v1[4 * e + 2] * f.x, v1[4 * e + 3] * f.x);
-          d4[8 + e] = make_float4(v2[4 * e] * f.x, v2[4 * e + 1] * f.x, v2[4 * e + 2] * f.x, v2[4 * e + 3] * f.x);
-          d4[12 + e] = make_float4(v3[4 * e] * f.x, v3[4 * e + 1] * f.x, v3[4 * e + 2] * f.x, v3[4 * e + 3] * f.x);
-        }
-      }
-      tc05::fence_before_sync();
       ++fi;
+      if (kGroup && it.slot < 0) {
+        // a whole token: its final output, merged with the extra partial if given
+        const int64_t row = static_cast<int64_t>(it.t) * kHeads + tid;
+        float wo = f.x, we = 0.f, lse = f.y;
+        if (a.extra_lse != nullptr) {
+          const float le = __ldg(a.extra_lse + row);
+          const float M = fmaxf(f.y, le);
+          const float w1 = f.y == -INFINITY ? 0.f : expf(f.y - M), w2 = le == -INFINITY ? 0.f : expf(le - M);
+          const float sum = w1 + w2;
+          wo = sum > 0.f ? f.x * (w1 / sum) : 0.f;
+          we = sum > 0.f ? w2 / sum : 0.f;
+          lse = sum > 0.f ? M + logf(sum) : -INFINITY;
+        }
+        const int esz = a.out_bf16 ? 2 : 4;
+        store_rows(static_cast<char*>(a.out) + static_cast<int64_t>(it.t) * kHeads * kDv * esz, a.out_bf16 != 0, wo,
+                   we, a.extra_lse != nullptr ? a.extra_o + static_cast<int64_t>(it.t) * kHeads * kDv : nullptr);
+        tc05::fence_before_sync();
+        if (a.lse_out != nullptr) a.lse_out[row] = lse;
+        continue;
+      }
+      float* dst0 = it.slot < 0 ? a.o_part + (orow - tid) * kDv : a.ws_o + static_cast<int64_t>(it.slot) * kHeads * kDv;
+      store_rows(dst0, false, f.x, 0.f, nullptr);
+      tc05::fence_before_sync();
+      if (kGroup) {
+        // a piece of a cut token: the last piece to finish merges the pieces
+        // (and the extra partial) into the token's final output
+        a.ws_lse[static_cast<int64_t>(it.slot) * kHeads + tid] = f.y;
+        if (!take_ticket<EpGroup>(a.ws_cnt + it.t, it.npieces)) continue;
+        const int64_t sl0 = it.slot_base, trow = static_cast<int64_t>(it.t) * kHeads;
+        const int esz = a.out_bf16 ? 2 : 4;
+        const bool has_e = a.extra_lse != nullptr;
+        if (merge_bulk(it.npieces, sl0, has_e ? a.extra_o + trow * kDv : nullptr,
+                       has_e ? a.extra_lse + trow : nullptr, static_cast<char*>(a.out) + trow * kDv * esz,
+                       a.out_bf16 != 0, [&](int r, float lv) {
+                         if (a.lse_out != nullptr) a.lse_out[trow + r] = lv;
+                       })) {
+          if (tid == 0) a.ws_cnt[it.t] = 0;
+          continue;
+        }
+        const int E = it.npieces + (a.extra_lse != nullptr ? 1 : 0);
+        merge_rows<kMergeUnroll, EpGroup>(
+            kHeads, E, kDv,
+            [&](int r, int e) {
+              return e < it.npieces ? __ldcg(a.ws_lse + (sl0 + e) * kHeads + r) : __ldg(a.extra_lse + trow + r);
+            },
+            [&](int r, int e) {
+              return e < it.npieces ? a.ws_o + ((sl0 + e) * kHeads + r) * kDv : a.extra_o + (trow + r) * kDv;
+            },
+            [&](int r, int d, float4 v) {
+              const int64_t oi = (trow + r) * kDv + d;
+              if (a.out_bf16) {
+                __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+                *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + oi) =
+                    make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+              } else {
+                *reinterpret_cast<float4*>(static_cast<float*>(a.out) + oi) = v;
+              }
+            },
+            [&](int r, float lv) {
+              if (a.lse_out != nullptr) a.lse_out[trow + r] = lv;
+            },
+            scratch, kScrFloats);
+        if (tid == 0) a.ws_cnt[it.t] = 0;
+        continue;
+      }
       if (it.slot < 0) {
         a.lse_part[lse_slot(a, it.p, it.t, tid)] = f.y;
       } else {
@@ -875,6 +1345,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int64_t s_idx = static_cast<int64_t>(it.t) * a.P + it.p;
         if (!take_ticket<EpGroup>(a.ws_cnt + s_idx, it.npieces)) continue;
         const int64_t sl0 = it.slot_base;
+        const int64_t prow0 = (static_cast<int64_t>(it.p) * a.num_tokens + it.t) * a.num_q_heads;
+        if (!merge_bulk(it.npieces, sl0, nullptr, nullptr, a.o_part + prow0 * kDv, false,
+                        [&](int r, float lv) { a.lse_part[lse_slot(a, it.p, it.t, r)] = lv; }))
         merge_rows<kMergeUnroll, EpGroup>(
             kHeads, it.npieces, kDv, [&](int r, int e) { return __ldcg(a.ws_lse + (sl0 + e) * kHeads + r); },
             [&](int r, int e) { return a.ws_o + ((sl0 + e) * kHeads + r) * kDv; },
@@ -931,6 +1404,20 @@ bool encode_rows(CUtensorMap* map, const void* ptr, uint64_t rows, uint32_t box_
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D bf16 view [P][num_pages * ps_l][576] of an MLA pool: boxes of 64
+// values x ps_l rows x P partners (a logical page of every partner), 128-byte swizzle.
+bool encode_pages(CUtensorMap* map, const void* ptr, int P, uint64_t rows_per_partner, uint32_t ps_l) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr || rows_per_partner == 0) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDqk), rows_per_partner, static_cast<cuuint64_t>(P)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kDqk * 2), rows_per_partner * kDqk * 2};
+  const cuuint32_t box[3] = {64u, ps_l, static_cast<cuuint32_t>(P)};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // SMs of the current device (0 if unknown).
 int device_sms() {
   int dev = 0, sms = 0;
@@ -946,16 +1433,29 @@ int mla_max_clusters() {
   return sms >= 2 ? sms / 2 : 76;
 }
 
-int mla_ws_slots(int P, int interleave, int num_tokens, int max_kv_len) {
+int mla_ws_slots(int P, int interleave, int num_tokens, int max_kv_len, int grouped) {
+  const int64_t by_clusters = 2LL * mla_max_clusters();
   // Pieces of cut stripes: a stripe of n tiles is cut only when n exceeds the
   // chunk max(total / C, 16 tiles), into at most 2 n / chunk pieces, so all
   // pieces together number at most 2 C; and at most ceil(n / 16) per stripe.
-  const int max_tiles = (max_stripe_len(max_kv_len, P, interleave) + kTile - 1) / kTile;
-  if (max_tiles <= kMinChunkTiles) return 0;
-  const int64_t per = (max_tiles + kMinChunkTiles - 1) / kMinChunkTiles;
-  const int64_t by_stripes = static_cast<int64_t>(num_tokens) * P * per;
-  const int64_t by_clusters = 2LL * mla_max_clusters();
-  return static_cast<int>(by_stripes < by_clusters ? by_stripes : by_clusters);
+  int64_t n = 0;
+  const int max_stripe_tiles = (max_stripe_len(max_kv_len, P, interleave) + kTile - 1) / kTile;
+  if (max_stripe_tiles > kMinChunkTiles) {
+    const int64_t per = (max_stripe_tiles + kMinChunkTiles - 1) / kMinChunkTiles;
+    const int64_t by_stripes = static_cast<int64_t>(num_tokens) * P * per;
+    n = by_stripes < by_clusters ? by_stripes : by_clusters;
+  }
+  if (grouped) {
+    // Pieces of cut tokens: Ce - 1 range boundaries, each cutting at most one
+    // token, so at most 2 (Ce - 1) <= 2 C pieces; and Ce <= W / 16, W <= T x
+    // the tiles of the longest row.  (The per-stripe bound stays covered: the
+    // kernel falls back to per-partner tiles if it cannot describe the pool.)
+    const int64_t max_tiles = (static_cast<int64_t>(max_kv_len) + kTile - 1) / kTile;
+    const int64_t by_tiles = 2 * ((static_cast<int64_t>(num_tokens) * max_tiles + kMinChunkTiles - 1) / kMinChunkTiles);
+    const int64_t g = by_tiles < by_clusters ? by_tiles : by_clusters;
+    if (g >= 2 && g > n) n = g;
+  }
+  return static_cast<int>(n);
 }
 
 int launch_mla_partial(const PartialArgs& a, cudaStream_t s, cudaError_t* err) {
@@ -963,24 +1463,30 @@ int launch_mla_partial(const PartialArgs& a, cudaStream_t s, cudaError_t* err) {
     return CPATTN_ERR_UNSUPPORTED_SHAPE;
   const int64_t pool_rows = static_cast<int64_t>(a.P) * a.num_pages * a.ps_l;
   if (pool_rows >= (int64_t{1} << 31)) return CPATTN_ERR_UNSUPPORTED_SHAPE;
-  // TMA when every 64-key tile is a whole number of page runs of >= 8 rows (so
-  // each box lands on a 1024-byte boundary of the 128-byte swizzle pattern),
-  // or lies inside one page run
+  CUtensorMap map;
+  std::memset(&map, 0, sizeof(map));
+  // fused calls over logical pages of 64 slots: tiles are whole logical
+  // pages, one 3-D box per column block (the per-partner partials are merged
+  // inside the online softmax)
+  const bool group = a.fused && a.page_size == kTile && a.num_tokens <= kGroupMaxTokens &&
+                     encode_pages(&map, a.pool_k, a.P, static_cast<uint64_t>(a.num_pages) * a.ps_l, a.ps_l);
+  // per-partner tiles: TMA when every 64-key tile is a whole number of page
+  // runs of >= 8 rows (so each box lands on a 1024-byte boundary of the
+  // 128-byte swizzle pattern), or lies inside one page run
   int box_rows = 0;
   if (a.ps_l >= 8 && a.ps_l <= kTile && kTile % a.ps_l == 0) box_rows = a.ps_l;
   else if (a.ps_l % kTile == 0) box_rows = kTile;
-  CUtensorMap map;
-  std::memset(&map, 0, sizeof(map));
-  const bool tma = box_rows > 0 && encode_rows(&map, a.pool_k, static_cast<uint64_t>(pool_rows), box_rows);
-  auto kern = tma ? mla_pair_kernel<true> : mla_pair_kernel<false>;
-  static std::atomic<int> smem_set[2][64];
-  *err = ensure_smem(kern, kSmemBytes, smem_set[tma ? 1 : 0]);
+  const bool tma = group || (box_rows > 0 && encode_rows(&map, a.pool_k, static_cast<uint64_t>(pool_rows), box_rows));
+  auto kern = group ? mla_pair_kernel<true, true> : (tma ? mla_pair_kernel<true, false> : mla_pair_kernel<false, false>);
+  const int variant = group ? 2 : (tma ? 1 : 0);
+  static std::atomic<int> smem_set[3][64];
+  *err = ensure_smem(kern, kSmemBytes, smem_set[variant]);
   if (*err != cudaSuccess) return CPATTN_ERR_CUDA;
-  // persistent grid: as many clusters as fit (one CTA per SM), at most one per item
-  static std::atomic<int> fit[2][64];
+  // persistent grid: as many clusters as fit (one CTA per SM)
+  static std::atomic<int> fit[3][64];
   int dev = 0;
   cudaGetDevice(&dev);
-  int C = fit[tma ? 1 : 0][dev & 63].load(std::memory_order_relaxed);
+  int C = fit[variant][dev & 63].load(std::memory_order_relaxed);
   if (C <= 0) {
     C = mla_max_clusters();
     cudaLaunchConfig_t cfg = {};
@@ -990,7 +1496,7 @@ int launch_mla_partial(const PartialArgs& a, cudaStream_t s, cudaError_t* err) {
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0 && n < C) C = n;
     cudaGetLastError();  // a failed query leaves no error behind
-    fit[tma ? 1 : 0][dev & 63].store(C, std::memory_order_relaxed);
+    fit[variant][dev & 63].store(C, std::memory_order_relaxed);
   }
   kern<<<dim3(2 * C, 1, 1), kThreads, kSmemBytes, s>>>(a, map, box_rows);
   *err = cudaGetLastError();

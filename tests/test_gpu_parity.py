@@ -213,8 +213,12 @@ def test_fused_step_matches_oracle(small):
     assert_close_lse(got_l, L, tol_l, "fused LSE")
     t0 = int(w.qo_indptr[w.num_real_rows])
     assert np.all(got_o[t0:] == 0) and np.all(got_l[t0:] == -np.inf)
-    # and against the two-launch path on the device (same partials, another merge order)
-    assert_close(got_o, f64(att.out), tol_o, "fused vs partial + merge")
+    # and against the two-launch path on the device: both are within tol_o of
+    # the oracle, and they sum in different orders (the fused MLA kernel over
+    # pages merges the partners inside its softmax), so two independent
+    # round-to-nearest bf16 outputs may sit one unit apart (2^-6 near 2.5):
+    # within 2 tol_o of each other
+    assert_close(got_o, f64(att.out), 2 * tol_o, "fused vs partial + merge")
 
 
 def test_head_major_lse_partial(small):
