@@ -70,6 +70,7 @@
 #include <atomic>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "launch.h"
@@ -87,12 +88,16 @@ constexpr int kKB = kDqk / 64;       // 9 column blocks of a latent row
 constexpr int kVB = kDv / 64;        // 8 column blocks of its value part
 constexpr int kTile = 64;            // keys per tile
 constexpr int kBlk = kTile * 128;    // one column block of a tile (8 KB)
-constexpr int kKStage = kKB * kBlk;  // 72 KB
 constexpr int kVStage = kVB * kBlk;  // 64 KB
-constexpr int kKStages = 3;
+constexpr int kUBlk = 3;             // CTA 0: column blocks of a ring unit (24 KB, one TMA box)
+constexpr int kUnitsK = kKB / kUBlk;  // units of a tile
+constexpr int kKUnits = 8;            // CTA 0: ring of units (2.7 tiles)
+constexpr uint32_t kKUnit = kUBlk * kBlk;
+static_assert(kKB % kUBlk == 0, "whole units a tile");
 constexpr int kVStages = 2;
 constexpr int kLandRing = 16;        // CTA 1's "K tile landed on CTA 0" barriers
 constexpr int kPBuf = kHeads * 128;  // P of one tile: 128 rows x 64 bf16
+constexpr int kPBufs = 3;            // CTA 1: P buffers (the softmax runs up to 3 tiles ahead of P V)
 constexpr int kThreads = 192;
 constexpr int kWMma = 4;
 constexpr int kWLoad = 5;
@@ -105,34 +110,38 @@ constexpr uint32_t kQCol = 128;      // CTA 0: S buffers at columns 0 and 64, Q 
 constexpr int kMergeUnroll = 8;
 
 // shared-memory map (offsets from a 1024-byte aligned base), the same in both CTAs
-constexpr uint32_t OFF_P = kVStages * kVStage;                   // CTA 1: P buffers [2]
-constexpr uint32_t OFF_ALPHA = OFF_P + 2 * kPBuf;                // CTA 1: [2][128] rescale factors
-constexpr uint32_t OFF_FIN = OFF_ALPHA + 2 * kHeads * 4;         // CTA 1: [128] (1 / sum, LSE)
+constexpr uint32_t OFF_P = kVStages * kVStage;                   // CTA 1: P buffers [kPBufs]
+constexpr uint32_t OFF_ALPHA = OFF_P + kPBufs * kPBuf;           // CTA 1: [kPBufs][128] rescale factors
+constexpr uint32_t OFF_FIN = OFF_ALPHA + kPBufs * kHeads * 4;    // CTA 1: [128] (1 / sum, LSE)
 constexpr uint32_t OFF_SCR = OFF_FIN + kHeads * 8;               // CTA 1: merge scratch
-constexpr uint32_t kStageArea = kKStages * kKStage;              // CTA 0: K stages
+constexpr uint32_t OFF_PSTAGE = kKUnits * kKUnit;               // CTA 0: P rows of the 4 softmax warps
+constexpr uint32_t kPSlot = 32 * 128;                            //   (4 KB each) on their way to CTA 1
+constexpr uint32_t kAreaK = OFF_PSTAGE + 4 * kPSlot;              // CTA 0's part of the map
+constexpr uint32_t kScrMin = 2 * kHeads * 128;                    // CTA 1: store_rows' two staging chunks
+constexpr uint32_t kAreaV = OFF_SCR + kScrMin;                     // CTA 1's part, with the least scratch
+constexpr uint32_t kStageArea = ((kAreaK > kAreaV ? kAreaK : kAreaV) + 1023u) & ~1023u;
 constexpr int kScrFloats = static_cast<int>((kStageArea - OFF_SCR) / 4);
 // barriers (arrival counts in brackets)
 enum : int {
-  B_KFULL = 0,      // x3 CTA 0 [1 + bytes (TMA) | 32 copy lanes]: K tile landed
-  B_KEMPTY = 3,     // x3 CTA 0 [commit]: S of the stage's tile done
-
-  B_SFULL = 6,      // x2 CTA 0 [commit]: S written
-  B_SEMPTY = 8,     // x2 CTA 0 [4 softmax warps]: S read
-  B_QFULL = 10,     // CTA 0 [4 softmax warps]: the item's Q in tensor memory
-  B_QEMPTY = 11,    // CTA 0 [commit]: the item's last S done
-  B_PEMPTY = 12,    // x2 CTA 0 [multicast commit from CTA 1]: P V of the buffer done
-  B_FINEMPTY = 14,  // CTA 0 [4 remote arrivals]: CTA 1 read the item's row scales
-  B_VFULL = 15,     // x2 CTA 1 [1 + bytes | 32]: V tile landed
-  B_VEMPTY = 17,    // x2 CTA 1 [commit]: P V of the stage's tile done
-  B_PFULL = 19,     // x2 CTA 1 [1 + bytes of CTA 0's bulk copies]: P and rescale factors landed
-  B_READY = 21,     // x2 CTA 1 [4 epilogue warps]: O rescaled, V rows fixed
-  B_PVDONE = 23,    // x2 CTA 1 [commit]: P V done
-  B_FINFULL = 25,   // CTA 1 [128 remote arrivals]: the item's row scales and LSEs
-  B_DRAIN = 26,     // both [commit]: the MMA thread's last MMAs done
-  B_EPSYNC = 27,    // CTA 1 [128 epilogue threads]: their group barrier (merges)
-  B_KLAND = 28,     // x16 CTA 1 [1 remote arrival]: the tile's rows reached CTA 0 (so they sit in L2)
-  B_MERGE = 44,     // x2 CTA 1 [1 + bytes]: a batch of partial rows landed (merges of cut items)
-  kBars = 46
+  B_KFULL = 0,                      // x8 CTA 0 [1 + bytes (TMA) | 32 copy lanes]: unit landed
+  B_KEMPTY = B_KFULL + kKUnits,     // x8 CTA 0 [commit]: the S MMAs that read the unit done
+  B_SFULL = B_KEMPTY + kKUnits,     // x2 CTA 0 [commit]: S written
+  B_SEMPTY = B_SFULL + 2,           // x2 CTA 0 [4 softmax warps]: S read
+  B_QFULL = B_SEMPTY + 2,           // CTA 0 [4 softmax warps]: the item's Q in tensor memory
+  B_QEMPTY = B_QFULL + 1,           // CTA 0 [commit]: the item's last S done
+  B_PEMPTY = B_QEMPTY + 1,          // x3 CTA 0 [multicast commit from CTA 1]: P V of the buffer done
+  B_FINEMPTY = B_PEMPTY + kPBufs,   // CTA 0 [4 remote arrivals]: CTA 1 read the item's row scales
+  B_VFULL = B_FINEMPTY + 1,         // x2 CTA 1 [1 + bytes | 32]: V tile landed
+  B_VEMPTY = B_VFULL + kVStages,    // x2 CTA 1 [commit]: P V of the stage's tile done
+  B_PFULL = B_VEMPTY + kVStages,    // x3 CTA 1 [1 + bytes of CTA 0's copies]: P and rescale factors landed
+  B_READY = B_PFULL + kPBufs,       // x2 CTA 1 [4 epilogue warps]: O rescaled, V rows fixed
+  B_PVDONE = B_READY + 2,           // x2 CTA 1 [commit]: P V done
+  B_FINFULL = B_PVDONE + 2,         // CTA 1 [128 remote arrivals]: the item's row scales and LSEs
+  B_DRAIN = B_FINFULL + 1,          // both [commit]: the MMA thread's last MMAs done
+  B_EPSYNC = B_DRAIN + 1,           // CTA 1 [128 epilogue threads]: their group barrier (merges)
+  B_KLAND = B_EPSYNC + 1,           // x16 CTA 1 [1 remote arrival]: the tile's rows reached CTA 0 (so they sit in L2)
+  B_MERGE = B_KLAND + kLandRing,    // x2 CTA 1 [1 + bytes]: a batch of partial rows landed (merges of cut items)
+  kBars = B_MERGE + 2
 };
 constexpr uint32_t OFF_BAR = kStageArea;
 constexpr uint32_t OFF_MISC = OFF_BAR + kBars * 8;  // [0] TMEM base, [1] abort, [2] items (-1: on the fly) / first token, [3] tiles
@@ -145,7 +154,8 @@ struct MlaItem {
 constexpr int kMaxOwn = kItemsBytes / static_cast<int>(sizeof(MlaItem));  // items one cluster keeps in its list
 constexpr uint32_t OFF_ITEMS = OFF_MISC + 32;
 constexpr size_t kSmemBytes = 1024 + OFF_ITEMS + kItemsBytes;
-static_assert(OFF_SCR + 1024 <= kStageArea, "CTA 1 map exceeds the stage area");
+static_assert(OFF_SCR + kScrMin <= kStageArea && kScrFloats * 4 >= static_cast<int>(kScrMin),
+              "CTA 1 map exceeds the stage area");
 static_assert(kSmemBytes + 64 <= 232448, "shared memory per CTA");
 
 // The epilogue warps of CTA 1 (threads 0..127) as a merge group.  Their
@@ -399,18 +409,6 @@ __device__ __forceinline__ int64_t pool_row(const PartialArgs& a, const MlaItem&
   return (static_cast<int64_t>(it.p) * a.num_pages + pg) * a.ps_l + (k - jj * a.ps_l);
 }
 
-// Keys of tile j of the item that hold data (inside the item, page accepted),
-// one bit a key; every lane of the warp gets the mask.
-__device__ __forceinline__ uint64_t tile_mask(const PartialArgs& a, const MlaItem& it, int j, int pb0, int npg,
-                                              int lane) {
-  const int k0 = it.k_begin + j * kTile;
-  const int ka = k0 + lane, kb = k0 + 32 + lane;
-  const bool va = ka < it.k_end && pool_row(a, it, ka, pb0, npg, false) >= 0;
-  const bool vb = kb < it.k_end && pool_row(a, it, kb, pb0, npg, false) >= 0;
-  const uint32_t lo = __ballot_sync(0xffffffffu, va), hi = __ballot_sync(0xffffffffu, vb);
-  return static_cast<uint64_t>(lo) | (static_cast<uint64_t>(hi) << 32);
-}
-
 // ---- grouped tiles (fused calls, logical pages of 64 slots) ----------------
 
 // Keys of token t's row (clamped to max_kv_len; 0 for tokens of no row).
@@ -552,47 +550,79 @@ __device__ __forceinline__ int group_page_row(const PartialArgs& a, const MlaIte
   return pg * a.ps_l;
 }
 
-// Keys of grouped tile j that hold data: tile row r is partner r / ps_l's
-// physical slot l = r % ps_l of the page, i.e. in-page offset
-// (l / I) * I * P + p * I + l % I (I = 1: l * P + p), a key of the row when
-// its position is below the item's end and the page is accepted.
-__device__ __forceinline__ uint64_t tile_mask_group(const PartialArgs& a, const MlaItem& it, int j, int pb0, int npg,
-                                                    int lane) {
-  const bool page_ok = group_page_row(a, it, j, pb0, npg, false) >= 0;
-  const int base = it.k_begin + j * kTile;
-  const int I = a.interleave;
-  auto pos_of = [&](int r) {
-    const int p = r / a.ps_l, l = r - (r / a.ps_l) * a.ps_l;
-    return base + (l / I) * I * a.P + p * I + (l % I);
-  };
-  const bool va = page_ok && pos_of(lane) < it.k_end;
-  const bool vb = page_ok && pos_of(lane + 32) < it.k_end;
-  const uint32_t lo = __ballot_sync(0xffffffffu, va), hi = __ballot_sync(0xffffffffu, vb);
-  return static_cast<uint64_t>(lo) | (static_cast<uint64_t>(hi) << 32);
+// Page-table words behind the key mask of tile j, read a tile before the
+// mask is needed (tile_mask_from takes the decision then), so the table's
+// latency hides behind the previous tile.  Grouped tiles: the logical page
+// (same word in every lane); per-partner tiles: the pages of keys lane and
+// 32 + lane.  -2: no word (past the item or the table).
+struct MaskWords {
+  int pa, pb;
+};
+template <bool kGroup>
+__device__ __forceinline__ MaskWords tile_mask_words(const PartialArgs& a, const MlaItem& it, int j, int pb0, int npg,
+                                                     int lane) {
+  MaskWords w{-2, -2};
+  if constexpr (kGroup) {
+    const int jj = it.k_begin / kTile + j;
+    if (jj < npg) w.pa = __ldg(a.page_indices + pb0 + jj);
+  } else {
+    const int ka = it.k_begin + j * kTile + lane, kb = ka + 32;
+    if (ka < it.k_end) {
+      const int jj = page_of_slot(a, ka);
+      if (jj < npg) w.pa = __ldg(a.page_indices + pb0 + jj);
+    }
+    if (kb < it.k_end) {
+      const int jj = page_of_slot(a, kb);
+      if (jj < npg) w.pb = __ldg(a.page_indices + pb0 + jj);
+    }
+  }
+  return w;
+}
+// Key mask of tile j (one bit a key, every lane gets it) from the words read
+// before: a key holds data when its page is accepted and its position lies
+// inside the item.  Grouped tile row r is partner p = r / ps_l's physical
+// slot l = r % ps_l of the logical page, at in-page offset
+// (l / I) * I * P + p * I + l % I (I = 1: l * P + p).
+template <bool kGroup>
+__device__ __forceinline__ uint64_t tile_mask_from(const PartialArgs& a, const MlaItem& it, int j, MaskWords w,
+                                                   int lane) {
+  auto page_ok = [&](int pg) { return pg >= 0 && pg < a.num_pages; };
+  if constexpr (kGroup) {
+    if (!page_ok(w.pa)) return 0ull;
+    const int base = it.k_begin + j * kTile;
+    if (base + kTile <= it.k_end) return ~0ull;  // the rows hold positions base .. base + 63
+    const int I = a.interleave;
+    auto pos_of = [&](int r) {
+      const int p = r / a.ps_l, l = r - (r / a.ps_l) * a.ps_l;
+      return base + (l / I) * I * a.P + p * I + (l % I);
+    };
+    const uint32_t lo = __ballot_sync(0xffffffffu, pos_of(lane) < it.k_end);
+    const uint32_t hi = __ballot_sync(0xffffffffu, pos_of(lane + 32) < it.k_end);
+    return static_cast<uint64_t>(lo) | (static_cast<uint64_t>(hi) << 32);
+  } else {
+    const uint32_t lo = __ballot_sync(0xffffffffu, page_ok(w.pa)), hi = __ballot_sync(0xffffffffu, page_ok(w.pb));
+    return static_cast<uint64_t>(lo) | (static_cast<uint64_t>(hi) << 32);
+  }
 }
 
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int x, int y, int z, uint32_t mbar) {
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, int x, int y, int z, int w, uint32_t mbar) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(
-          dst),
-      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(mbar)
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];\n" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(w), "r"(mbar)
       : "memory");
 }
 
-// Copies of grouped tile j: one 3-D box (64 values x ps_l rows x P partners)
-// per column block, lane 0; page_row from group_page_row (-1: nothing copied).
-__device__ __forceinline__ void load_tile_group(const CUtensorMap* tmap, uint32_t dst, int nblk, uint32_t full,
-                                                int page_row, int lane) {
-  if (lane != 0) return;
-  tc05::mbar_arrive_expect_tx(full, page_row >= 0 ? nblk * kBlk : 0);
-  if (page_row < 0) return;
-  for (int kb = 0; kb < nblk; ++kb) tma_load_3d(dst + kb * kBlk, tmap, kb * 64, page_row, 0, full);
+// Copies of column blocks kb0 .. kb0 + nb - 1 of grouped tile j into dst
+// (8 KB a block), by the calling lane: one 4-D box (64 values x ps_l rows x
+// P partners x nb blocks; the map's box holds nb blocks); page_row from
+// group_page_row (-1: nothing copied).
+__device__ __forceinline__ void load_unit_group(const CUtensorMap* tmap, uint32_t dst, int kb0, int nb, uint32_t full,
+                                                int page_row) {
+  tc05::mbar_arrive_expect_tx(full, page_row >= 0 ? nb * kBlk : 0);
+  if (page_row >= 0) tma_load_4d(dst, tmap, 0, page_row, 0, kb0, full);
 }
 
-// Copies of tile j of the item into a stage (nblk column blocks of 64 values):
-// TMA boxes of `box_rows` rows (lane 0), or 16-byte cp.async copies by the
-// whole warp with zero fill for keys without data.  Completion is counted on
-// `full`.
 // Pool rows of the page runs of tile j (TMA path): lane r < kTile / box_rows
 // looks up run r (-1: past the item or a rejected page, reported), so a tile
 // costs one round trip to the page table.
@@ -603,63 +633,60 @@ __device__ __forceinline__ int tile_run_row(const PartialArgs& a, const MlaItem&
   return static_cast<int>(pool_row(a, it, kr, pb0, npg, true));
 }
 
-template <bool kTma>
-__device__ __forceinline__ void load_tile(const PartialArgs& a, const CUtensorMap* tmap, const MlaItem& it, int j,
-                                          int pb0, int npg, uint32_t dst, int nblk, uint32_t full, int box_rows,
-                                          int lane, int run_row) {
-  const int k0 = it.k_begin + j * kTile;
-  if constexpr (kTma) {
-    // run_row: this lane's run of the tile (tile_run_row), gathered by lane 0
-    const int nr = kTile / box_rows;
-    int rows[kTile / 8];
-    uint32_t bytes = 0;
-#pragma unroll
-    for (int r = 0; r < kTile / 8; ++r) {
-      rows[r] = __shfl_sync(0xffffffffu, run_row, r);
-      if (r < nr && rows[r] >= 0) bytes += nblk * box_rows * 128;
-    }
-    if (lane == 0) {
-      tc05::mbar_arrive_expect_tx(full, bytes);
-      for (int r = 0; r < nr; ++r) {
-        if (rows[r] < 0) continue;
-        for (int kb = 0; kb < nblk; ++kb)
-          tc05::tma_load_2d(dst + kb * kBlk + r * box_rows * 128, tmap, kb * 64, rows[r], full);
-      }
-    }
-  } else {
-    const uint8_t* pool = static_cast<const uint8_t*>(a.pool_k);
-    const uint8_t* r0 = nullptr;
-    const uint8_t* r1 = nullptr;
-    {
-      const int ka = k0 + lane, kb = k0 + 32 + lane;
-      if (ka < it.k_end) {
-        const int64_t row = pool_row(a, it, ka, pb0, npg, true);
-        if (row >= 0) r0 = pool + row * (kDqk * 2);
-      }
-      if (kb < it.k_end) {
-        const int64_t row = pool_row(a, it, kb, pb0, npg, true);
-        if (row >= 0) r1 = pool + row * (kDqk * 2);
-      }
-    }
-    const int nch = nblk * 8;
-    for (int key = 0; key < kTile; ++key) {
-      const uint8_t* src = reinterpret_cast<const uint8_t*>(
-          __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(key < 32 ? r0 : r1), key & 31));
-      for (int ch = lane; ch < nch; ch += 32) {
-        const uint32_t d = dst + (ch >> 3) * kBlk + tc05::sw128(key, ch & 7);
-        if (src != nullptr) cp16(d, src + ch * 16);
-        else cp16_zero(d, pool);
-      }
-    }
-    cp_arrive_noinc(full);
+// Copies of column blocks kb0 .. kb0 + nb - 1 of a per-partner tile by TMA
+// boxes of box_rows rows: lane r issues run r's boxes (run_row: its pool row
+// from tile_run_row, -1: not copied), lane 0 counts the bytes (run_bytes a
+// block, all runs) on `full`.  The whole warp calls.
+__device__ __forceinline__ void load_unit_runs(const CUtensorMap* tmap, uint32_t dst, int kb0, int nb, uint32_t full,
+                                               int run_row, uint32_t run_bytes, int box_rows, int lane) {
+  if (lane == 0) tc05::mbar_arrive_expect_tx(full, nb * run_bytes);
+  if (run_row >= 0)
+    for (int kb = 0; kb < nb; ++kb)
+      tc05::tma_load_2d(dst + kb * kBlk + lane * box_rows * 128, tmap, (kb0 + kb) * 64, run_row, full);
+}
+
+// Copy path (no TMA): source rows of keys lane and 32 + lane of tile j
+// (nullptr: no data).
+__device__ __forceinline__ void cp_tile_rows(const PartialArgs& a, const MlaItem& it, int j, int pb0, int npg, int lane,
+                                             const uint8_t*& r0, const uint8_t*& r1) {
+  const uint8_t* pool = static_cast<const uint8_t*>(a.pool_k);
+  const int ka = it.k_begin + j * kTile + lane, kb = ka + 32;
+  r0 = nullptr;
+  r1 = nullptr;
+  if (ka < it.k_end) {
+    const int64_t row = pool_row(a, it, ka, pb0, npg, true);
+    if (row >= 0) r0 = pool + row * (kDqk * 2);
   }
+  if (kb < it.k_end) {
+    const int64_t row = pool_row(a, it, kb, pb0, npg, true);
+    if (row >= 0) r1 = pool + row * (kDqk * 2);
+  }
+}
+
+// Copy path: column blocks kb0 .. kb0 + nb - 1 of the tile by 16-byte
+// cp.async copies of the whole warp (zero fill for keys without data),
+// counted on `full` (32 arrivals).
+__device__ __forceinline__ void cp_tile_blocks(uint32_t dst, int kb0, int nb, const uint8_t* r0, const uint8_t* r1,
+                                               const void* any_gmem, uint32_t full, int lane) {
+  const int nch = nb * 8;  // 16-byte chunks of a key row
+  for (int idx = lane; idx < kTile * nch; idx += 32) {
+    const int key = idx / nch, ch = idx - key * nch;
+    const uintptr_t s0 = __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(r0), key & 31);
+    const uintptr_t s1 = __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(r1), key & 31);
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(key < 32 ? s0 : s1);
+    const uint32_t d = dst + (ch >> 3) * kBlk + tc05::sw128(key, ch & 7);
+    if (src != nullptr) cp16(d, src + (kb0 * 8 + ch) * 16);
+    else cp16_zero(d, any_gmem);
+  }
+  cp_arrive_noinc(full);
 }
 
 }  // namespace
 
 template <bool kTma, bool kGroup>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    mla_pair_kernel(const PartialArgs a, const __grid_constant__ CUtensorMap tmap, int box_rows) {
+    mla_pair_kernel(const PartialArgs a, const __grid_constant__ CUtensorMap tmap,
+                    const __grid_constant__ CUtensorMap tmap_v, int box_rows) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = tc05::smem_addr(base);
@@ -695,17 +722,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   if (tid == 0) {
     const uint32_t load_arrivals = kTma ? 1u : 32u;
-    for (int i = 0; i < kKStages; ++i) {
+    for (int i = 0; i < kKUnits; ++i) {
       tc05::mbar_init(bar(B_KFULL + i), load_arrivals);
       tc05::mbar_init(bar(B_KEMPTY + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       tc05::mbar_init(bar(B_SFULL + i), 1);
       tc05::mbar_init(bar(B_SEMPTY + i), 4);
-      tc05::mbar_init(bar(B_PEMPTY + i), 1);
-      tc05::mbar_init(bar(B_PFULL + i), 1);
       tc05::mbar_init(bar(B_READY + i), 4);
       tc05::mbar_init(bar(B_PVDONE + i), 1);
+    }
+    for (int i = 0; i < kPBufs; ++i) {
+      tc05::mbar_init(bar(B_PEMPTY + i), 1);
+      tc05::mbar_init(bar(B_PFULL + i), 1);
     }
     for (int i = 0; i < kVStages; ++i) {
       tc05::mbar_init(bar(B_VFULL + i), load_arrivals);
@@ -735,9 +764,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if constexpr (kGroup) return get_item_group(a, k, g_C, c, g_pre, g_sbase, g_W, n_items, it);
     else return get_item(a, k, C, c, n_items, items, it);
   };
-  auto mask_of = [&](const MlaItem& it, int j, int pb0, int npg) {
-    if constexpr (kGroup) return tile_mask_group(a, it, j, pb0, npg, lane);
-    else return tile_mask(a, it, j, pb0, npg, lane);
+  auto mask_words = [&](const MlaItem& it, int j, int pb0, int npg) {
+    return tile_mask_words<kGroup>(a, it, j, pb0, npg, lane);
   };
   auto ntiles = [](const MlaItem& it) {
     return it.t >= 0 && it.k_end > it.k_begin ? (it.k_end - it.k_begin + kTile - 1) / kTile : 0;
@@ -745,59 +773,142 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   bool ok = true;
 
   if (warp == kWLoad) {
-    // ---- loader (both CTAs): whole latent rows into the K ring (CTA 0), the value part into the V ring (CTA 1)
-    const int nstages = rank == 0 ? kKStages : kVStages;
-    const uint32_t stage_bytes = rank == 0 ? kKStage : kVStage;
-    const int nblk = rank == 0 ? kKB : kVB;
-    const int b_full = rank == 0 ? B_KFULL : B_VFULL, b_empty = rank == 0 ? B_KEMPTY : B_VEMPTY;
-    int g = 0, issued = 0;
-    for (int k = 0; ok; ++k) {
-      MlaItem it;
-      if (!item(k, it)) break;
-      const int nt = ntiles(it);
-      if (nt == 0) continue;
-      const int pb0 = __ldg(a.page_indptr + it.b), npg = __ldg(a.page_indptr + it.b + 1) - pb0;
-      // page rows of the next tile are looked up while the stage it goes to is still busy
-      auto rows_of = [&](int jt) {
-        if constexpr (kGroup) return lane == 0 ? group_page_row(a, it, jt, pb0, npg, true) : -1;
-        else return kTma ? tile_run_row(a, it, jt, pb0, npg, box_rows, lane) : -1;
-      };
-      int run_row = rows_of(0);
-      for (int j = 0; j < nt; ++j, ++g) {
-        const int st = g % nstages;
-        ok = wwait<false>(bar(b_empty + st), ((g / nstages) & 1) ^ 1, abort_flag);
-        // CTA 1 copies a tile's value rows once CTA 0 has the whole rows:
-        // they are in L2 by then, and CTA 1's copies do not race CTA 0's to HBM
-        if (ok && rank == 1) ok = wwait<true>(bar(B_KLAND + g % kLandRing), (g / kLandRing) & 1, abort_flag);
-        if (!ok) break;
-        if constexpr (kGroup) load_tile_group(&tmap, sb + st * stage_bytes, nblk, bar(b_full + st), run_row, lane);
-        else load_tile<kTma>(a, &tmap, it, j, pb0, npg, sb + st * stage_bytes, nblk, bar(b_full + st), box_rows, lane,
-                             run_row);
-        issued = g + 1;
-        if (j + 1 < nt) run_row = rows_of(j + 1);
-      }
-    }
-    if (!ok) raise_abort();
-    if (*abort_flag) {
-      // nothing may land after the CTA exits: wait (bounded) for the last copies issued into each stage
-      for (int g2 = max(0, issued - nstages); g2 < issued; ++g2) {
-        const uint32_t mb = bar(b_full + g2 % nstages), par = (g2 / nstages) & 1;
-        for (uint32_t i = 0; i < (1u << 20); ++i) {
-          uint32_t done;
-          asm volatile(
-              "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-              : "=r"(done)
-              : "r"(mb), "r"(par)
-              : "memory");
-          if (done) break;
+    // ---- loader (both CTAs).  CTA 0: whole latent rows in units of kUBlk
+    // column blocks into a ring of kKUnits units (a unit is free again once
+    // the S MMAs that read it are done).  CTA 1: the value part of the same
+    // tiles into a 2-stage ring of whole tiles.  The ring constants are
+    // compile-time per role: this warp shares its scheduler with a softmax
+    // warp, so every instruction it issues per unit counts.
+    auto run = [&](auto kU_, auto kUB_, auto kR_, auto kBytes_, int b_full, int b_empty, const CUtensorMap* map4) {
+      constexpr int kU = decltype(kU_)::value, kUB = decltype(kUB_)::value, kR = decltype(kR_)::value;
+      constexpr uint32_t kBytes = decltype(kBytes_)::value;
+      int g = 0, q = 0, issued = 0;  // tiles, next unit's slot, units issued
+      uint32_t par = 0;              // parity of the slot's next use
+      for (int k = 0; ok; ++k) {
+        MlaItem it;
+        if (!item(k, it)) break;
+        const int nt = ntiles(it);
+        if (nt == 0) continue;
+        const int pb0 = __ldg(a.page_indptr + it.b), npg = __ldg(a.page_indptr + it.b + 1) - pb0;
+        // page rows of the next tile are looked up while the stage it goes to is still busy
+        auto rows_of = [&](int jt) { return kTma ? tile_run_row(a, it, jt, pb0, npg, box_rows, lane) : -1; };
+        // grouped plans: lane l holds the page row of tile j0 + l of the current
+        // batch of 32 tiles, and the next batch is read while this one is used
+        auto batch_of = [&](int j0) { return j0 + lane < nt ? group_page_row(a, it, j0 + lane, pb0, npg, true) : -1; };
+        int cur_rows = 0, next_rows = 0;
+        if constexpr (kGroup) {
+          cur_rows = batch_of(0);
+          next_rows = batch_of(32);
+        } else {
+          (void)cur_rows;
+          (void)next_rows;
+        }
+        int run_row = kGroup ? 0 : rows_of(0);
+        for (int j = 0; j < nt; ++j, ++g) {
+          if constexpr (kGroup) {
+            if (j > 0 && (j & 31) == 0) {
+              cur_rows = next_rows;
+              next_rows = batch_of(j + 32);
+            }
+            run_row = __shfl_sync(0xffffffffu, cur_rows, j & 31);
+          }
+          // CTA 1 copies a tile's value rows once CTA 0 has the whole rows:
+          // they are in L2 by then, and CTA 1's copies do not race CTA 0's to HBM
+          if (rank == 1) ok = wwait<true>(bar(B_KLAND + g % kLandRing), (g / kLandRing) & 1, abort_flag);
+          if (!ok) break;
+          int nu = 0;  // units of this tile issued
+          if constexpr (kTma) {
+            // per-partner tiles: lane r < kTile / box_rows copies run r; grouped
+            // tiles: lane 0 copies the unit with one 4-D box
+            uint32_t run_bytes = 0;
+            if constexpr (!kGroup)
+              run_bytes = __popc(__ballot_sync(0xffffffffu, run_row >= 0)) * static_cast<uint32_t>(box_rows) * 128u;
+            int qq = q;
+            uint32_t pp = par;
+            if constexpr (kGroup) {
+              // lane 0 alone: no warp-wide step a unit
+              if (lane == 0) {
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                  if (!pwait<false>(bar(b_empty + qq), pp ^ 1u, abort_flag)) break;
+                  load_unit_group(map4, sb + qq * kBytes, u * kUB, kUB, bar(b_full + qq), run_row);
+                  ++nu;
+                  if (++qq == kR) {
+                    qq = 0;
+                    pp ^= 1u;
+                  }
+                }
+              }
+              nu = __shfl_sync(0xffffffffu, nu, 0);
+            } else {
+#pragma unroll
+              for (int u = 0; u < kU; ++u) {
+                if (!wwait<false>(bar(b_empty + qq), pp ^ 1u, abort_flag)) break;
+                load_unit_runs(&tmap, sb + qq * kBytes, u * kUB, kUB, bar(b_full + qq), run_row, run_bytes, box_rows,
+                               lane);
+                ++nu;
+                if (++qq == kR) {
+                  qq = 0;
+                  pp ^= 1u;
+                }
+              }
+            }
+          } else {
+            const uint8_t* r0;
+            const uint8_t* r1;
+            cp_tile_rows(a, it, j, pb0, npg, lane, r0, r1);
+            int qq = q;
+            uint32_t pp = par;
+            for (int u = 0; u < kU; ++u) {
+              if (!wwait<false>(bar(b_empty + qq), pp ^ 1u, abort_flag)) break;
+              cp_tile_blocks(sb + qq * kBytes, u * kUB, kUB, r0, r1, a.pool_k, bar(b_full + qq), lane);
+              ++nu;
+              if (++qq == kR) {
+                qq = 0;
+                pp ^= 1u;
+              }
+            }
+          }
+          issued += nu;
+          ok = nu == kU;
+          if (!ok) break;
+          q += kU;
+          if (q >= kR) {
+            q -= kR;
+            par ^= 1u;
+          }
+          if (!kGroup && j + 1 < nt) run_row = rows_of(j + 1);
         }
       }
-    }
+      if (!ok) raise_abort();
+      if (*abort_flag) {
+        // nothing may land after the CTA exits: wait (bounded) for the last copies issued into each slot
+        for (int n2 = max(0, issued - kR); n2 < issued; ++n2) {
+          const uint32_t mb = bar(b_full + n2 % kR), par2 = (n2 / kR) & 1;
+          for (uint32_t i = 0; i < (1u << 20); ++i) {
+            uint32_t done;
+            asm volatile(
+                "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+                : "=r"(done)
+                : "r"(mb), "r"(par2)
+                : "memory");
+            if (done) break;
+          }
+        }
+      }
+    };
+    if (rank == 0)
+      run(std::integral_constant<int, kUnitsK>{}, std::integral_constant<int, kUBlk>{},
+          std::integral_constant<int, kKUnits>{}, std::integral_constant<uint32_t, kKUnit>{}, B_KFULL, B_KEMPTY, &tmap);
+    else
+      run(std::integral_constant<int, 1>{}, std::integral_constant<int, kVB>{}, std::integral_constant<int, kVStages>{},
+          std::integral_constant<uint32_t, kVStage>{}, B_VFULL, B_VEMPTY, &tmap_v);
   } else if (rank == 0 && warp == kWMma) {
     // ---- CTA 0, MMA warp (one elected lane issues): S = Q K^T of each tile, Q from tensor memory
     const uint32_t id_s = tc05::idesc_bf16(128, kTile, false, false);
     const uint32_t r_kland = tc05::mapa(bar(B_KLAND), 1);
-    int g = 0, qi = 0;
+    int g = 0, qi = 0, kq = 0;  // kq, kpar: ring slot of the next tile's first unit and its use parity
+    uint32_t kpar = 0;
     for (int k = 0; ok; ++k) {
       MlaItem it;
       if (!item(k, it)) break;
@@ -805,24 +916,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (nt == 0) continue;
       ok = wwait<false>(bar(B_QFULL), qi & 1, abort_flag);
       for (int j = 0; j < nt && ok; ++j, ++g) {
-        const int st = g % kKStages, sbuf = g & 1;
-        ok = wwait<false>(bar(B_KFULL + st), (g / kKStages) & 1, abort_flag);
-        if (ok && lane == 0) tc05::mbar_arrive_remote(r_kland + (g % kLandRing) * 8);
-        ok = ok && wwait<false>(bar(B_SEMPTY + sbuf), ((g >> 1) & 1) ^ 1, abort_flag);
+        const int sbuf = g & 1;
+        ok = wwait<false>(bar(B_SEMPTY + sbuf), ((g >> 1) & 1) ^ 1, abort_flag);
         if (!ok) break;
+        bool fail = false;
         if (tc05::elect_one()) {
-          if constexpr (!kTma) tc05::fence_smem_to_async();  // the tile came through cp.async
-          tc05::fence_after_sync();
-          const uint64_t dk = tc05::desc_k128(sb + st * kKStage);
+          // unit u of the tile sits in ring slot kq + u (mod kKUnits); its 12
+          // MMAs go as soon as it landed, and a commit frees the slot
           const uint32_t dcol = tbase + sbuf * kTile;
+          int q = kq;
+          uint32_t par = kpar;
 #pragma unroll
-          for (int ks = 0; ks < kDqk / 16; ++ks)
-            tc05::mma_ts(dcol, tbase + kQCol + ks * 8, tc05::desc_add(dk, (ks >> 2) * kBlk + (ks & 3) * 32), id_s,
-                         ks > 0);
-          tc05::commit(bar(B_SFULL + sbuf));
-          tc05::commit(bar(B_KEMPTY + st));
+          for (int u = 0; u < kUnitsK; ++u) {
+            if (!pwait<false>(bar(B_KFULL + q), par, abort_flag)) {
+              fail = true;
+              break;
+            }
+            // the tile's last unit landed, so all its rows sit in L2: CTA 1 may
+            // copy their value part (a signal only, nothing to publish)
+            if (u == kUnitsK - 1) tc05::mbar_arrive_remote_relaxed(r_kland + (g % kLandRing) * 8);
+            if constexpr (!kTma) tc05::fence_smem_to_async();  // the unit came through cp.async
+            tc05::fence_after_sync();
+#pragma unroll
+            for (int b = 0; b < kUBlk; ++b) {
+              const uint64_t dk = tc05::desc_k128(sb + q * kKUnit + b * kBlk);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const int ks = (u * kUBlk + b) * 4 + kk;
+                tc05::mma_ts(dcol, tbase + kQCol + ks * 8, tc05::desc_add(dk, kk * 32), id_s, ks > 0);
+              }
+            }
+            tc05::commit(bar(B_KEMPTY + q));
+            if (++q == kKUnits) {
+              q = 0;
+              par ^= 1u;
+            }
+          }
+          if (!fail) tc05::commit(bar(B_SFULL + sbuf));
         }
-        __syncwarp();
+        ok = __ballot_sync(0xffffffffu, fail) == 0u;
+        kq += kUnitsK;
+        if (kq >= kKUnits) {
+          kq -= kKUnits;
+          kpar ^= 1u;
+        }
       }
       if (!ok) break;
       if (tc05::elect_one()) tc05::commit(bar(B_QEMPTY));
@@ -835,13 +972,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc05::mbar_wait(bar(B_DRAIN), 0, 1u << 20);
     }
     __syncwarp();
-  } else if (rank == 0) {
+  } else if (rank == 0 && warp < 4) {
     // ---- CTA 0, warps 0-3: Q into tensor memory, online softmax, P to CTA 1
     const float sl = a.scale * kLog2e;
     const uint32_t my_lane = tc05::taddr(tbase, warp * 32, 0);
     const uint32_t r_p = tc05::mapa(sb + OFF_P, 1), r_alpha = tc05::mapa(sb + OFF_ALPHA, 1);
     const uint32_t r_fin = tc05::mapa(sb + OFF_FIN, 1);
     const uint32_t r_pfull = tc05::mapa(bar(B_PFULL), 1), r_finfull = tc05::mapa(bar(B_FINFULL), 1);
+    const uint32_t pst = sb + OFF_PSTAGE + tid * 128;  // this row's place in the warp's staging slot
     int g = 0, qi = 0, prev_t = -1;
     for (int k = 0; ok; ++k) {
       MlaItem it;
@@ -886,9 +1024,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
       float m = -INFINITY, l = 0.f, lr = 0.f;
+      MaskWords next_words = mask_words(it, 0, pb0, npg);
       for (int j = 0; j < nt; ++j, ++g) {
         const int sbuf = g & 1;
-        const uint64_t vmask = mask_of(it, j, pb0, npg);
+        const MaskWords words = next_words;
+        if (j + 1 < nt) next_words = mask_words(it, j + 1, pb0, npg);
         ok = wwait<false>(bar(B_SFULL + sbuf), (g >> 1) & 1, abort_flag);
         if (!ok) break;
         tc05::fence_after_sync();
@@ -911,12 +1051,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc05::fence_before_sync();
         __syncwarp();
         if (lane == 0) arrive_local(bar(B_SEMPTY + sbuf));
-        float bm = -INFINITY;
+        // keys without data: -inf (so their probability is 0); the running max
+        // is kept in log2 units, the scores stay unscaled
+        const uint64_t vmask = tile_mask_from<kGroup>(a, it, j, words, lane);
+        if (vmask != ~0ull) {
 #pragma unroll
-        for (int e = 0; e < kTile; ++e) {
-          sv[e] = ((vmask >> e) & 1ull) ? sv[e] * sl : -INFINITY;
-          bm = fmaxf(bm, sv[e]);
+          for (int e = 0; e < kTile; ++e) sv[e] = ((vmask >> e) & 1ull) ? sv[e] : -INFINITY;
         }
+        float mx[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) mx[e] = fmaxf(fmaxf(sv[e], sv[16 + e]), fmaxf(sv[32 + e], sv[48 + e]));
+#pragma unroll
+        for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+          for (int e = 0; e < w; ++e) mx[e] = fmaxf(mx[e], mx[e + w]);
+        const float bm = mx[0] * sl;
         float alpha = 1.f;
         if (bm > m + 8.f) {
           alpha = m == -INFINITY ? 0.f : exp2f(m - bm);
@@ -924,28 +1073,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           lr *= alpha;
           m = bm;
         }
-        // P buffer `sbuf` of CTA 1 is free once its P V two tiles back is done;
-        // the row of P (bf16, 128-byte swizzle) and the rescale factor go there
-        // by asynchronous stores counted in bytes on CTA 1's barrier
-        ok = wwait<true>(bar(B_PEMPTY + sbuf), ((g >> 1) & 1) ^ 1, abort_flag);
-        if (!ok) break;
-        const uint32_t prow = r_p + sbuf * kPBuf + tid * 128, pfull = r_pfull + sbuf * 8;
+        // The row of P (bf16, 128-byte swizzle) goes to this warp's staging
+        // slot, once the slot's previous copy has read it; the slot then
+        // travels to P buffer `sbuf` of CTA 1 as one bulk copy, and the rescale
+        // factor by an asynchronous store, both counted in bytes on CTA 1's
+        // barrier.  The buffer is free once its P V two tiles back is done.
+        if (lane == 0) tc05::bulk_wait_read();
+        __syncwarp();
+        {
+          // p = 2^(s * scale * log2 e - m): one FMA and one ex2 a key (a key
+          // at -inf gives 0; while every key so far is masked m is -inf and
+          // every p is 0); four partial sums of p and of bf16(p) each
+          const float nm = m == -INFINITY ? 0.f : -m;
+          float ls[4] = {0.f, 0.f, 0.f, 0.f}, lrs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          uint32_t pk[4];
+          for (int cc = 0; cc < 8; ++cc) {
+            uint32_t pk[4];
 #pragma unroll
-          for (int e2 = 0; e2 < 4; ++e2) {
-            const int e = 8 * cc + 2 * e2;
-            const float p0 = sv[e] == -INFINITY ? 0.f : ex2_approx(sv[e] - m);
-            const float p1 = sv[e + 1] == -INFINITY ? 0.f : ex2_approx(sv[e + 1] - m);
-            l += p0 + p1;
-            __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-            lr += __low2float(pb) + __high2float(pb);
-            pk[e2] = *reinterpret_cast<uint32_t*>(&pb);
+            for (int e2 = 0; e2 < 4; ++e2) {
+              const int e = 8 * cc + 2 * e2;
+              const float p0 = ex2_approx(fmaf(sv[e], sl, nm));
+              const float p1 = ex2_approx(fmaf(sv[e + 1], sl, nm));
+              ls[e2] += p0 + p1;
+              __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+              pk[e2] = *reinterpret_cast<uint32_t*>(&pb);
+              lrs[e2] += __uint_as_float(pk[e2] << 16) + __uint_as_float(pk[e2] & 0xffff0000u);
+            }
+            tc05::st_shared_v4(pst + ((cc ^ (tid & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
           }
-          tc05::st_async_v4(prow + ((cc ^ (tid & 7)) << 4), pk[0], pk[1], pk[2], pk[3], pfull);
+          l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+          lr += (lrs[0] + lrs[1]) + (lrs[2] + lrs[3]);
         }
-        tc05::st_async_b32(r_alpha + (sbuf * kHeads + tid) * 4, __float_as_uint(alpha), pfull);
+        tc05::fence_smem_to_async();  // the copy engine reads what these threads wrote
+        const int pq = g % kPBufs;
+        ok = wwait<true>(bar(B_PEMPTY + pq), ((g / kPBufs) & 1) ^ 1, abort_flag);
+        if (!ok) break;
+        const uint32_t pfull = r_pfull + pq * 8;
+        tc05::st_async_b32(r_alpha + (pq * kHeads + tid) * 4, __float_as_uint(alpha), pfull);
+        if (lane == 0) {
+          tc05::bulk_s2cluster(r_p + pq * kPBuf + warp * kPSlot, sb + OFF_PSTAGE + warp * kPSlot, kPSlot, pfull);
+          tc05::bulk_commit();
+        }
       }
       if (!ok) break;
       // the item's row scale and LSE to CTA 1, once it read the previous item's
@@ -958,6 +1126,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ++qi;
     }
     if (!ok) raise_abort();
+    if (lane == 0) tc05::bulk_wait_all();  // the staging slot stays until its last copy is done
+    __syncwarp();
   } else if (warp == kWMma) {
     // ---- CTA 1, MMA warp (one elected lane issues): O += P V
     const uint32_t id_pv = tc05::idesc_bf16(128, 256, false, true);
@@ -973,7 +1143,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (tc05::elect_one()) {
           if constexpr (!kTma) tc05::fence_smem_to_async();
           tc05::fence_after_sync();
-          const uint64_t dp = tc05::desc_k128(sb + OFF_P + pbuf * kPBuf);
+          const uint64_t dp = tc05::desc_k128(sb + OFF_P + (g % kPBufs) * kPBuf);
           const uint64_t dv = tc05::desc_mn128(sb + vs * kVStage, kBlk);
 #pragma unroll
           for (int ks = 0; ks < kTile / 16; ++ks) {
@@ -984,7 +1154,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           tc05::commit(bar(B_PVDONE + pbuf));
           tc05::commit(bar(B_VEMPTY + vs));
-          tc05::commit_multicast(bar(B_PEMPTY + pbuf), 0x1);
+          tc05::commit_multicast(bar(B_PEMPTY + g % kPBufs), 0x1);
         }
         __syncwarp();
       }
@@ -1214,15 +1384,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         continue;
       }
       const int pb0 = __ldg(a.page_indptr + it.b), npg = __ldg(a.page_indptr + it.b + 1) - pb0;
+      MaskWords next_words = mask_words(it, 0, pb0, npg);
       for (int j = 0; j < nt; ++j, ++g) {
         const int pbuf = g & 1, vs = g % kVStages;
-        const uint64_t vmask = mask_of(it, j, pb0, npg);
+        const MaskWords words = next_words;
+        if (j + 1 < nt) next_words = mask_words(it, j + 1, pb0, npg);
         // P and the rescale factors arrive by bulk copies from CTA 0 (bytes counted)
-        if (tid == 0) tc05::mbar_arrive_expect_tx(bar(B_PFULL + pbuf), kPBuf + kHeads * 4);
-        ok = wwait<true>(bar(B_PFULL + pbuf), (g >> 1) & 1, abort_flag);
+        const int pq = g % kPBufs;
+        if (tid == 0) tc05::mbar_arrive_expect_tx(bar(B_PFULL + pq), kPBuf + kHeads * 4);
+        ok = wwait<true>(bar(B_PFULL + pq), (g / kPBufs) & 1, abort_flag);
         if (!ok) break;
-        tc05::fence_smem_to_async();  // P was written by CTA 0's stores; the tensor core reads it
-        const float alpha = alpha_s[pbuf * kHeads + tid];
+        const uint64_t vmask = tile_mask_from<kGroup>(a, it, j, words, lane);
+        tc05::fence_smem_to_async();  // the tensor core reads P next
+        const float alpha = alpha_s[pq * kHeads + tid];
         ok = wwait<false>(bar(B_VFULL + vs), (g / kVStages) & 1, abort_flag);
         if (!ok) break;
         if (kTma && vmask != ~0ull) {
@@ -1406,14 +1580,16 @@ bool encode_rows(CUtensorMap* map, const void* ptr, uint64_t rows, uint32_t box_
 
 // 3-D bf16 view [P][num_pages * ps_l][576] of an MLA pool: boxes of 64
 // values x ps_l rows x P partners (a logical page of every partner), 128-byte swizzle.
-bool encode_pages(CUtensorMap* map, const void* ptr, int P, uint64_t rows_per_partner, uint32_t ps_l) {
+bool encode_pages(CUtensorMap* map, const void* ptr, int P, uint64_t rows_per_partner, uint32_t ps_l, uint32_t nblk) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr || rows_per_partner == 0) return false;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDqk), rows_per_partner, static_cast<cuuint64_t>(P)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kDqk * 2), rows_per_partner * kDqk * 2};
-  const cuuint32_t box[3] = {64u, ps_l, static_cast<cuuint32_t>(P)};
-  const cuuint32_t estr[3] = {1u, 1u, 1u};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+  // dims: 64 values of a column block, rows of a partner's pool, partners,
+  // column blocks (128 bytes apart); a box is nblk blocks of a logical page
+  const cuuint64_t dims[4] = {64u, rows_per_partner, static_cast<cuuint64_t>(P), static_cast<cuuint64_t>(kKB)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kDqk * 2), rows_per_partner * kDqk * 2, 128u};
+  const cuuint32_t box[4] = {64u, ps_l, static_cast<cuuint32_t>(P), nblk};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -1463,13 +1639,16 @@ int launch_mla_partial(const PartialArgs& a, cudaStream_t s, cudaError_t* err) {
     return CPATTN_ERR_UNSUPPORTED_SHAPE;
   const int64_t pool_rows = static_cast<int64_t>(a.P) * a.num_pages * a.ps_l;
   if (pool_rows >= (int64_t{1} << 31)) return CPATTN_ERR_UNSUPPORTED_SHAPE;
-  CUtensorMap map;
+  CUtensorMap map, map_v;
   std::memset(&map, 0, sizeof(map));
+  std::memset(&map_v, 0, sizeof(map_v));
   // fused calls over logical pages of 64 slots: tiles are whole logical
-  // pages, one 3-D box per column block (the per-partner partials are merged
+  // pages, one 4-D box per ring unit (the per-partner partials are merged
   // inside the online softmax)
+  const uint64_t rows_pp = static_cast<uint64_t>(a.num_pages) * a.ps_l;
   const bool group = a.fused && a.page_size == kTile && a.num_tokens <= kGroupMaxTokens &&
-                     encode_pages(&map, a.pool_k, a.P, static_cast<uint64_t>(a.num_pages) * a.ps_l, a.ps_l);
+                     encode_pages(&map, a.pool_k, a.P, rows_pp, a.ps_l, kUBlk) &&
+                     encode_pages(&map_v, a.pool_k, a.P, rows_pp, a.ps_l, kVB);
   // per-partner tiles: TMA when every 64-key tile is a whole number of page
   // runs of >= 8 rows (so each box lands on a 1024-byte boundary of the
   // 128-byte swizzle pattern), or lies inside one page run
@@ -1498,7 +1677,7 @@ int launch_mla_partial(const PartialArgs& a, cudaStream_t s, cudaError_t* err) {
     cudaGetLastError();  // a failed query leaves no error behind
     fit[variant][dev & 63].store(C, std::memory_order_relaxed);
   }
-  kern<<<dim3(2 * C, 1, 1), kThreads, kSmemBytes, s>>>(a, map, box_rows);
+  kern<<<dim3(2 * C, 1, 1), kThreads, kSmemBytes, s>>>(a, map, map_v, box_rows);
   *err = cudaGetLastError();
   return *err == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
 }

@@ -224,6 +224,11 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(addr) : "memory");
 }
+// The same arrival without release semantics: a signal that carries no data
+// (nothing written before it needs to be seen by the waiter).
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(addr) : "memory");
+}
 // Make this thread's generic-proxy stores into any CTA's shared memory of the
 // cluster visible to the tensor core (async proxy).
 __device__ __forceinline__ void fence_cluster_smem_to_async() {
@@ -263,9 +268,16 @@ __device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t v, uint32_t
                "r"(mbar)
                : "memory");
 }
+// 16-byte store into this CTA's shared memory.
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
 // Wait until every bulk copy this thread committed has completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+// Wait until every bulk copy this thread committed has read its source (the
+// source may then be overwritten; the writes may still be in flight).
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
 
 // Every thread of every CTA of the cluster (warps converged).
 __device__ __forceinline__ void cluster_sync() {
