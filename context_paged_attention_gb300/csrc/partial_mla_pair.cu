@@ -1247,15 +1247,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // then batches of R rows of every entry come into shared memory by bulk
     // copies (two batches in flight) and the weighted rows go to row r of
     // dst0 (a row every 512 elements, fp32 or bf16) with coalesced stores; the
-    // row's LSE to put_lse.  Returns false (nothing done) when the entries do
-    // not fit the staging buffers.  All epilogue threads call.
+    // row's LSE to put_lse.  The staging area is the merge scratch, or, for the
+    // cluster's last item (no tile of it or after it still in flight), the
+    // value stages and P buffers too: the copies' latency sets the pace, so the
+    // batches should be large.  Returns false (nothing done) when the entries
+    // do not fit.  All epilogue threads call.
     int merge_phase = 0;  // batches issued on B_MERGE so far (parity tracking)
     auto merge_bulk = [&](int E0, int64_t sl0, const float* ext_o, const float* ext_lse, void* dst0, bool to_bf16,
-                          auto put_lse) -> bool {
+                          bool wide, auto put_lse) -> bool {
+      const uint32_t area = wide ? 0u : OFF_SCR;
+      const uint32_t area_bytes = wide ? OFF_ALPHA : static_cast<uint32_t>(kScrFloats) * 4u;
       const int E = E0 + (ext_o != nullptr ? 1 : 0);
-      float* wt = scratch;  // [E][128]
+      float* wt = reinterpret_cast<float*>(base + area);  // [E][128]
       const uint32_t wt_bytes = static_cast<uint32_t>((E * kHeads * 4 + 1023) & ~1023);
-      const uint32_t avail = static_cast<uint32_t>(kScrFloats) * 4u - wt_bytes;
+      if (wt_bytes >= area_bytes) return false;
+      const uint32_t avail = area_bytes - wt_bytes;
       const int R = static_cast<int>(avail / 2 / (static_cast<uint32_t>(E) * kDv * 4));
       if (R < 1) return false;
       {
@@ -1278,7 +1284,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         put_lse(tid, sum == 0.f ? -INFINITY : mx + logf(sum));
       }
-      uint8_t* buf0 = base + OFF_SCR + wt_bytes;
+      uint8_t* buf0 = base + area + wt_bytes;
       const uint32_t buf_bytes = static_cast<uint32_t>(E) * R * kDv * 4;
       const int nbatch = (kHeads + R - 1) / R;
       auto issue = [&](int k) {
@@ -1477,9 +1483,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int64_t sl0 = it.slot_base, trow = static_cast<int64_t>(it.t) * kHeads;
         const int esz = a.out_bf16 ? 2 : 4;
         const bool has_e = a.extra_lse != nullptr;
+        MlaItem nx;
+        const bool wide = !item(k + 1, nx);
         if (merge_bulk(it.npieces, sl0, has_e ? a.extra_o + trow * kDv : nullptr,
                        has_e ? a.extra_lse + trow : nullptr, static_cast<char*>(a.out) + trow * kDv * esz,
-                       a.out_bf16 != 0, [&](int r, float lv) {
+                       a.out_bf16 != 0, wide, [&](int r, float lv) {
                          if (a.lse_out != nullptr) a.lse_out[trow + r] = lv;
                        })) {
           if (tid == 0) a.ws_cnt[it.t] = 0;
@@ -1520,7 +1528,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!take_ticket<EpGroup>(a.ws_cnt + s_idx, it.npieces)) continue;
         const int64_t sl0 = it.slot_base;
         const int64_t prow0 = (static_cast<int64_t>(it.p) * a.num_tokens + it.t) * a.num_q_heads;
-        if (!merge_bulk(it.npieces, sl0, nullptr, nullptr, a.o_part + prow0 * kDv, false,
+        MlaItem nx;
+        const bool wide = !item(k + 1, nx);
+        if (!merge_bulk(it.npieces, sl0, nullptr, nullptr, a.o_part + prow0 * kDv, false, wide,
                         [&](int r, float lv) { a.lse_part[lse_slot(a, it.p, it.t, r)] = lv; }))
         merge_rows<kMergeUnroll, EpGroup>(
             kHeads, it.npieces, kDv, [&](int r, int e) { return __ldcg(a.ws_lse + (sl0 + e) * kHeads + r); },
