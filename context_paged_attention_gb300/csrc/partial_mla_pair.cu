@@ -1177,61 +1177,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // elements; fp32, or bf16 rounded to nearest even).  Staged through shared
     // memory in 128-byte chunks of every row, so that eight threads store each
     // line.  All epilogue threads call.
-    auto store_rows = [&](void* dst0, bool to_bf16, float wo, float we, const float* ext) {
-      const int cols = to_bf16 ? 64 : 32;
+    auto store_rows_t = [&](auto bf16_c, void* dst0, float wo, float we, const float* ext) {
+      constexpr bool kB = decltype(bf16_c)::value;
+      constexpr int cols = kB ? 64 : 32, nch = kDv / cols, esz = kB ? 2 : 4;
+      // the next chunk's tensor-memory loads (and extra rows) are in flight
+      // while this chunk goes out
+      float v[cols];
+      float4 xe[cols / 4];
+      auto fetch = [&](int ch) {
+#pragma unroll
+        for (int q = 0; q < cols / 16; ++q)
+          tc05::ld_x16(my_lane + ch * cols + 16 * q, *reinterpret_cast<float(*)[16]>(v + 16 * q));
+        if (ext != nullptr) {
+#pragma unroll
+          for (int e = 0; e < cols / 4; ++e)
+            xe[e] = __ldg(reinterpret_cast<const float4*>(ext + static_cast<int64_t>(tid) * kDv + ch * cols) + e);
+        }
+      };
+      fetch(0);
 #pragma unroll 1
-      for (int ch = 0; ch < kDv / cols; ++ch) {
+      for (int ch = 0; ch < nch; ++ch) {
         uint8_t* buf = base + OFF_SCR + (ch & 1) * (kHeads * 128);
-        const int c0 = ch * cols;
+        tc05::ld_wait();
         uint32_t wds[32];
-        if (!to_bf16) {
-          float v[32];
-          tc05::ld_x16(my_lane + c0, *reinterpret_cast<float(*)[16]>(v));
-          tc05::ld_x16(my_lane + c0 + 16, *reinterpret_cast<float(*)[16]>(v + 16));
-          tc05::ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] *= wo;
-          if (ext != nullptr) {
+        for (int e = 0; e < cols; ++e) v[e] *= wo;
+        if (ext != nullptr) {
 #pragma unroll
-            for (int e = 0; e < 32; e += 4) {
-              const float4 x = __ldg(reinterpret_cast<const float4*>(ext + static_cast<int64_t>(tid) * kDv + c0 + e));
-              v[e] = fmaf(we, x.x, v[e]);
-              v[e + 1] = fmaf(we, x.y, v[e + 1]);
-              v[e + 2] = fmaf(we, x.z, v[e + 2]);
-              v[e + 3] = fmaf(we, x.w, v[e + 3]);
-            }
+          for (int e = 0; e < cols / 4; ++e) {
+            v[4 * e] = fmaf(we, xe[e].x, v[4 * e]);
+            v[4 * e + 1] = fmaf(we, xe[e].y, v[4 * e + 1]);
+            v[4 * e + 2] = fmaf(we, xe[e].z, v[4 * e + 2]);
+            v[4 * e + 3] = fmaf(we, xe[e].w, v[4 * e + 3]);
           }
-#pragma unroll
-          for (int e = 0; e < 32; ++e) wds[e] = __float_as_uint(v[e]);
-        } else {
-          float v[64];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) tc05::ld_x16(my_lane + c0 + 16 * q, *reinterpret_cast<float(*)[16]>(v + 16 * q));
-          tc05::ld_wait();
-#pragma unroll
-          for (int e = 0; e < 64; ++e) v[e] *= wo;
-          if (ext != nullptr) {
-#pragma unroll
-            for (int e = 0; e < 64; e += 4) {
-              const float4 x = __ldg(reinterpret_cast<const float4*>(ext + static_cast<int64_t>(tid) * kDv + c0 + e));
-              v[e] = fmaf(we, x.x, v[e]);
-              v[e + 1] = fmaf(we, x.y, v[e + 1]);
-              v[e + 2] = fmaf(we, x.z, v[e + 2]);
-              v[e + 3] = fmaf(we, x.w, v[e + 3]);
-            }
-          }
+        }
+        if constexpr (kB) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
             wds[e] = *reinterpret_cast<uint32_t*>(&h);
           }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) wds[e] = __float_as_uint(v[e]);
         }
 #pragma unroll
         for (int q = 0; q < 8; ++q)
           *reinterpret_cast<uint4*>(buf + tc05::sw128(tid, q)) =
               make_uint4(wds[4 * q], wds[4 * q + 1], wds[4 * q + 2], wds[4 * q + 3]);
         EpGroup::sync();
-        const int esz = to_bf16 ? 2 : 4;
+        if (ch + 1 < nch) fetch(ch + 1);
 #pragma unroll
         for (int i2 = 0; i2 < 8; ++i2) {
           const int x = i2 * kHeads + tid, row = x >> 3, q = x & 7;
@@ -1240,6 +1235,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               val;
         }
       }
+    };
+    auto store_rows = [&](void* dst0, bool to_bf16, float wo, float we, const float* ext) {
+      if (to_bf16) store_rows_t(std::true_type{}, dst0, wo, we, ext);
+      else store_rows_t(std::false_type{}, dst0, wo, we, ext);
     };
     // Exact merge of E partials of all 128 rows (the LSE merge of lse_merge):
     // entry e < E0 is workspace slot sl0 + e (rows contiguous), entry E0 (when
@@ -1315,17 +1314,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int r0 = k * R, nr = min(R, kHeads - r0);
         const float4* bf = reinterpret_cast<const float4*>(buf0 + (k & 1) * buf_bytes);
         if (okm) {
-          for (int idx = tid; idx < nr * (kDv / 4); idx += kHeads) {
-            const int rr = idx / (kDv / 4), c4 = idx - rr * (kDv / 4);
+          // thread tid owns column group c4 = tid of every row (kDv / 4 ==
+          // kHeads); the loads of up to 8 entries go out together, since the
+          // 4 warps alone cannot hide shared-memory latency
+          static_assert(kDv / 4 == kHeads, "one column group a thread");
+          const int c4 = tid;
+          for (int rr = 0; rr < nr; ++rr) {
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int e = 0; e < E; ++e) {
-              const float w = wt[e * kHeads + r0 + rr];
-              if (w == 0.f) continue;  // empty entries' rows never enter the sum
-              const float4 v = bf[(e * nr + rr) * (kDv / 4) + c4];
-              acc.x = fmaf(w, v.x, acc.x);
-              acc.y = fmaf(w, v.y, acc.y);
-              acc.z = fmaf(w, v.z, acc.z);
-              acc.w = fmaf(w, v.w, acc.w);
+            for (int e0 = 0; e0 < E; e0 += 8) {
+              float w[8];
+              float4 v[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                w[e] = 0.f;
+                if (e0 + e < E) {
+                  w[e] = wt[(e0 + e) * kHeads + r0 + rr];
+                  v[e] = bf[((e0 + e) * nr + rr) * (kDv / 4) + c4];
+                }
+              }
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                if (w[e] == 0.f) continue;  // empty entries' rows never enter the sum
+                acc.x = fmaf(w[e], v[e].x, acc.x);
+                acc.y = fmaf(w[e], v[e].y, acc.y);
+                acc.z = fmaf(w[e], v[e].z, acc.z);
+                acc.w = fmaf(w[e], v[e].w, acc.w);
+              }
             }
             const int64_t oi = static_cast<int64_t>(r0 + rr) * kDv + c4 * 4;
             if (to_bf16) {
@@ -1375,6 +1389,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (a.lse_out != nullptr) a.lse_out[row] = le;
       }
     }
+    // Merge of the pieces of cut token t (slots sl0 .., and the extra partial
+    // when given) into its final output; the pieces are complete.
+    auto merge_token = [&](int t, int64_t sl0, int npieces, bool wide) {
+      const int64_t trow = static_cast<int64_t>(t) * kHeads;
+      const int esz = a.out_bf16 ? 2 : 4;
+      const bool has_e = a.extra_lse != nullptr;
+      if (!merge_bulk(npieces, sl0, has_e ? a.extra_o + trow * kDv : nullptr, has_e ? a.extra_lse + trow : nullptr,
+                      static_cast<char*>(a.out) + trow * kDv * esz, a.out_bf16 != 0, wide, [&](int r, float lv) {
+                        if (a.lse_out != nullptr) a.lse_out[trow + r] = lv;
+                      })) {
+        const int E = npieces + (has_e ? 1 : 0);
+        merge_rows<kMergeUnroll, EpGroup>(
+            kHeads, E, kDv,
+            [&](int r, int e) {
+              return e < npieces ? __ldcg(a.ws_lse + (sl0 + e) * kHeads + r) : __ldg(a.extra_lse + trow + r);
+            },
+            [&](int r, int e) {
+              return e < npieces ? a.ws_o + ((sl0 + e) * kHeads + r) * kDv : a.extra_o + (trow + r) * kDv;
+            },
+            [&](int r, int d, float4 v) {
+              const int64_t oi = (trow + r) * kDv + d;
+              if (a.out_bf16) {
+                __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+                *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + oi) =
+                    make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+              } else {
+                *reinterpret_cast<float4*>(static_cast<float*>(a.out) + oi) = v;
+              }
+            },
+            [&](int r, float lv) {
+              if (a.lse_out != nullptr) a.lse_out[trow + r] = lv;
+            },
+            scratch, kScrFloats);
+      }
+      if (tid == 0) a.ws_cnt[t] = 0;
+    };
+    constexpr int kMaxDefer = 4;
+    int n_defer = 0, defer_t[kMaxDefer], defer_np[kMaxDefer];
+    int64_t defer_sl0[kMaxDefer];
     for (int k = 0; ok; ++k) {
       MlaItem it;
       if (!item(k, it)) break;
@@ -1480,43 +1533,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // (and the extra partial) into the token's final output
         a.ws_lse[static_cast<int64_t>(it.slot) * kHeads + tid] = f.y;
         if (!take_ticket<EpGroup>(a.ws_cnt + it.t, it.npieces)) continue;
-        const int64_t sl0 = it.slot_base, trow = static_cast<int64_t>(it.t) * kHeads;
-        const int esz = a.out_bf16 ? 2 : 4;
-        const bool has_e = a.extra_lse != nullptr;
+        // this piece finished last: the merge runs now if this is the
+        // cluster's last item, else after it (with the wide staging area, and
+        // without holding up this cluster's tiles meanwhile)
         MlaItem nx;
-        const bool wide = !item(k + 1, nx);
-        if (merge_bulk(it.npieces, sl0, has_e ? a.extra_o + trow * kDv : nullptr,
-                       has_e ? a.extra_lse + trow : nullptr, static_cast<char*>(a.out) + trow * kDv * esz,
-                       a.out_bf16 != 0, wide, [&](int r, float lv) {
-                         if (a.lse_out != nullptr) a.lse_out[trow + r] = lv;
-                       })) {
-          if (tid == 0) a.ws_cnt[it.t] = 0;
+        if (item(k + 1, nx) && n_defer < kMaxDefer) {
+          defer_t[n_defer] = it.t;
+          defer_sl0[n_defer] = it.slot_base;
+          defer_np[n_defer] = it.npieces;
+          ++n_defer;
           continue;
         }
-        const int E = it.npieces + (a.extra_lse != nullptr ? 1 : 0);
-        merge_rows<kMergeUnroll, EpGroup>(
-            kHeads, E, kDv,
-            [&](int r, int e) {
-              return e < it.npieces ? __ldcg(a.ws_lse + (sl0 + e) * kHeads + r) : __ldg(a.extra_lse + trow + r);
-            },
-            [&](int r, int e) {
-              return e < it.npieces ? a.ws_o + ((sl0 + e) * kHeads + r) * kDv : a.extra_o + (trow + r) * kDv;
-            },
-            [&](int r, int d, float4 v) {
-              const int64_t oi = (trow + r) * kDv + d;
-              if (a.out_bf16) {
-                __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
-                *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + oi) =
-                    make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
-              } else {
-                *reinterpret_cast<float4*>(static_cast<float*>(a.out) + oi) = v;
-              }
-            },
-            [&](int r, float lv) {
-              if (a.lse_out != nullptr) a.lse_out[trow + r] = lv;
-            },
-            scratch, kScrFloats);
-        if (tid == 0) a.ws_cnt[it.t] = 0;
+        merge_token(it.t, it.slot_base, it.npieces, !item(k + 1, nx));
         continue;
       }
       if (it.slot < 0) {
@@ -1544,6 +1572,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       if (a.fused) pair_finish<kMergeUnroll, EpGroup>(a, it.t, 0, kHeads, kDv, scratch, kScrFloats);
     }
+    // merges put off until no tile of this cluster is in flight
+    for (int i = 0; i < n_defer && ok; ++i) merge_token(defer_t[i], defer_sl0[i], defer_np[i], true);
     if (!ok) raise_abort();
   }
 
