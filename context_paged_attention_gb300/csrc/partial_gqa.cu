@@ -246,7 +246,7 @@ bool plan_partial(int mla, int fused, int P, int interleave, int page_size, int 
     plan->max_chunks = slots;
     plan->ws_o_floats = static_cast<size_t>(slots) * num_q_heads * Dv;
     plan->ws_lse_floats = static_cast<size_t>(slots) * num_q_heads;
-    plan->ws_cnt_ints = stripes;
+    plan->ws_cnt_ints = stripes + (grouped ? 2 * static_cast<size_t>(num_tokens) : 0);  // + per-token records
     if (fused) {
       plan->ws_part_floats = stripes * num_q_heads * Dv;
       plan->ws_part_lse_floats = stripes * num_q_heads;

@@ -113,7 +113,7 @@ constexpr int kMergeUnroll = 8;
 constexpr uint32_t OFF_P = kVStages * kVStage;                   // CTA 1: P buffers [kPBufs]
 constexpr uint32_t OFF_ALPHA = OFF_P + kPBufs * kPBuf;           // CTA 1: [kPBufs][128] rescale factors
 constexpr uint32_t OFF_FIN = OFF_ALPHA + kPBufs * kHeads * 4;    // CTA 1: [128] (1 / sum, LSE)
-constexpr uint32_t OFF_SCR = OFF_FIN + kHeads * 8;               // CTA 1: merge scratch
+constexpr uint32_t OFF_SCR = (OFF_FIN + kHeads * 8 + 1023u) & ~1023u;  // CTA 1: output staging, merge scratch
 constexpr uint32_t OFF_PSTAGE = kKUnits * kKUnit;               // CTA 0: P rows of the 4 softmax warps
 constexpr uint32_t kPSlot = 32 * 128;                            //   (4 KB each) on their way to CTA 1
 constexpr uint32_t kAreaK = OFF_PSTAGE + 4 * kPSlot;              // CTA 0's part of the map
@@ -686,7 +686,8 @@ __device__ __forceinline__ void cp_tile_blocks(uint32_t dst, int kb0, int nb, co
 template <bool kTma, bool kGroup>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_pair_kernel(const PartialArgs a, const __grid_constant__ CUtensorMap tmap,
-                    const __grid_constant__ CUtensorMap tmap_v, int box_rows) {
+                    const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_out,
+                    const __grid_constant__ CUtensorMap tmap_ws, int box_rows) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = tc05::smem_addr(base);
@@ -704,6 +705,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     report(a.dev_status, CPATTN_DEV_TC_TIMEOUT);
   };
 
+  // the merge of cut tokens (grouped plans) may be scheduled already; it
+  // waits for this grid's completion before it reads anything
+  if (tid == 0) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   // ---- plan, barriers, tensor memory
   if (tid == 0) {
     misc[1] = 0;
@@ -1172,12 +1176,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const float* alpha_s = reinterpret_cast<const float*>(base + OFF_ALPHA);
     const float2* fin_s = reinterpret_cast<const float2*>(base + OFF_FIN);
     float* scratch = reinterpret_cast<float*>(base + OFF_SCR);
+    // grouped plans: per token (slot of its first piece, pieces; 1: whole)
+    int32_t* rec = a.ws_cnt + static_cast<int64_t>(a.num_tokens) * a.P;
     // O (tensor memory, this thread's row = head tid) times wo, plus we times
     // row tid of ext when given, into the 128 rows at dst0 (a row every 512
     // elements; fp32, or bf16 rounded to nearest even).  Staged through shared
     // memory in 128-byte chunks of every row, so that eight threads store each
     // line.  All epilogue threads call.
-    auto store_rows_t = [&](auto bf16_c, void* dst0, float wo, float we, const float* ext) {
+    // With `map` (grouped plans), each staged chunk leaves by a TMA store of
+    // the box at column ch * cols, row y0; else by the threads' stores.
+    auto store_rows_t = [&](auto bf16_c, void* dst0, const CUtensorMap* map, int y0, float wo, float we,
+                            const float* ext) {
       constexpr bool kB = decltype(bf16_c)::value;
       constexpr int cols = kB ? 64 : 32, nch = kDv / cols, esz = kB ? 2 : 4;
       // the next chunk's tensor-memory loads (and extra rows) are in flight
@@ -1225,20 +1234,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int q = 0; q < 8; ++q)
           *reinterpret_cast<uint4*>(buf + tc05::sw128(tid, q)) =
               make_uint4(wds[4 * q], wds[4 * q + 1], wds[4 * q + 2], wds[4 * q + 3]);
+        if (map != nullptr) {
+          tc05::fence_smem_to_async();  // the copy engine reads what these threads wrote
+          // the previous chunk's store has read its buffer (written again next chunk)
+          if (tid == 0) tc05::bulk_wait_read();
+          EpGroup::sync();
+          if (tid == 0) {
+            tc05::tma_store_2d(map, tc05::smem_addr(buf), ch * cols, y0);
+            tc05::bulk_commit();
+          }
+          if (ch + 1 < nch) fetch(ch + 1);
+          continue;
+        }
         EpGroup::sync();
         if (ch + 1 < nch) fetch(ch + 1);
+        // all eight loads first: the stores could alias them for all the
+        // compiler knows, so interleaving would wait out each load in turn
+        uint4 vals[8];
 #pragma unroll
         for (int i2 = 0; i2 < 8; ++i2) {
           const int x = i2 * kHeads + tid, row = x >> 3, q = x & 7;
-          const uint4 val = *reinterpret_cast<const uint4*>(buf + tc05::sw128(row, q));
+          vals[i2] = *reinterpret_cast<const uint4*>(buf + tc05::sw128(row, q));
+        }
+#pragma unroll
+        for (int i2 = 0; i2 < 8; ++i2) {
+          const int x = i2 * kHeads + tid, row = x >> 3, q = x & 7;
           *reinterpret_cast<uint4*>(static_cast<char*>(dst0) + static_cast<int64_t>(row) * kDv * esz + ch * 128 + q * 16) =
-              val;
+              vals[i2];
         }
       }
     };
     auto store_rows = [&](void* dst0, bool to_bf16, float wo, float we, const float* ext) {
-      if (to_bf16) store_rows_t(std::true_type{}, dst0, wo, we, ext);
-      else store_rows_t(std::false_type{}, dst0, wo, we, ext);
+      if (to_bf16) store_rows_t(std::true_type{}, dst0, nullptr, 0, wo, we, ext);
+      else store_rows_t(std::false_type{}, dst0, nullptr, 0, wo, we, ext);
+    };
+    // the same by TMA stores: rows y0 .. y0 + 127 of the map's tensor; the
+    // staging buffers are free again on return
+    auto store_rows_tma = [&](const CUtensorMap* map, int y0, bool to_bf16, float wo, float we, const float* ext) {
+      if (to_bf16) store_rows_t(std::true_type{}, nullptr, map, y0, wo, we, ext);
+      else store_rows_t(std::false_type{}, nullptr, map, y0, wo, we, ext);
+      if (tid == 0) tc05::bulk_wait_read();
+      EpGroup::sync();
     };
     // Exact merge of E partials of all 128 rows (the LSE merge of lse_merge):
     // entry e < E0 is workspace slot sl0 + e (rows contiguous), entry E0 (when
@@ -1315,39 +1351,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const float4* bf = reinterpret_cast<const float4*>(buf0 + (k & 1) * buf_bytes);
         if (okm) {
           // thread tid owns column group c4 = tid of every row (kDv / 4 ==
-          // kHeads); the loads of up to 8 entries go out together, since the
-          // 4 warps alone cannot hide shared-memory latency
+          // kHeads).  Two rows at a time, their loads (four entries each)
+          // all issued before any arithmetic and the stores after: the stores
+          // could alias the loads for all the compiler knows, so it keeps this
+          // order, and the 4 warps alone cannot hide shared-memory latency.
           static_assert(kDv / 4 == kHeads, "one column group a thread");
           const int c4 = tid;
-          for (int rr = 0; rr < nr; ++rr) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int e0 = 0; e0 < E; e0 += 8) {
-              float w[8];
-              float4 v[8];
+          for (int rr0 = 0; rr0 < nr; rr0 += 2) {
+            float4 acc[2];
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                w[e] = 0.f;
-                if (e0 + e < E) {
-                  w[e] = wt[(e0 + e) * kHeads + r0 + rr];
-                  v[e] = bf[((e0 + e) * nr + rr) * (kDv / 4) + c4];
+            for (int r = 0; r < 2; ++r) acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int e0 = 0; e0 < E; e0 += 4) {
+              float w[2][4];
+              float4 v[2][4];
+#pragma unroll
+              for (int r = 0; r < 2; ++r)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  w[r][e] = 0.f;
+                  if (rr0 + r < nr && e0 + e < E) {
+                    w[r][e] = wt[(e0 + e) * kHeads + r0 + rr0 + r];
+                    v[r][e] = bf[((e0 + e) * nr + rr0 + r) * (kDv / 4) + c4];
+                  }
                 }
-              }
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                if (w[e] == 0.f) continue;  // empty entries' rows never enter the sum
-                acc.x = fmaf(w[e], v[e].x, acc.x);
-                acc.y = fmaf(w[e], v[e].y, acc.y);
-                acc.z = fmaf(w[e], v[e].z, acc.z);
-                acc.w = fmaf(w[e], v[e].w, acc.w);
-              }
+              for (int r = 0; r < 2; ++r)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  if (w[r][e] == 0.f) continue;  // empty entries' rows never enter the sum
+                  acc[r].x = fmaf(w[r][e], v[r][e].x, acc[r].x);
+                  acc[r].y = fmaf(w[r][e], v[r][e].y, acc[r].y);
+                  acc[r].z = fmaf(w[r][e], v[r][e].z, acc[r].z);
+                  acc[r].w = fmaf(w[r][e], v[r][e].w, acc[r].w);
+                }
             }
-            const int64_t oi = static_cast<int64_t>(r0 + rr) * kDv + c4 * 4;
-            if (to_bf16) {
-              __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
-              *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(dst0) + oi) =
-                  make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
-            } else {
-              *reinterpret_cast<float4*>(static_cast<float*>(dst0) + oi) = acc;
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              if (rr0 + r >= nr) break;
+              const int64_t oi = static_cast<int64_t>(r0 + rr0 + r) * kDv + c4 * 4;
+              if (to_bf16) {
+                __nv_bfloat162 lo = __floats2bfloat162_rn(acc[r].x, acc[r].y),
+                               hi = __floats2bfloat162_rn(acc[r].z, acc[r].w);
+                *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(dst0) + oi) =
+                    make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+              } else {
+                *reinterpret_cast<float4*>(static_cast<float*>(dst0) + oi) = acc[r];
+              }
             }
           }
         }
@@ -1372,6 +1421,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // partial alone, or 0 / -inf; cluster c takes tokens c, c + C, ...
       for (int t = c; t < a.num_tokens; t += C) {
         if (g_pre[t + 1] != g_pre[t]) continue;
+        if (tid == 0) {
+          rec[2 * t] = 0;
+          rec[2 * t + 1] = 1;
+        }
         const int64_t row = static_cast<int64_t>(t) * kHeads + tid;
         const bool has_e = a.extra_lse != nullptr;
         const float le = has_e ? __ldg(a.extra_lse + row) : -INFINITY;
@@ -1389,45 +1442,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (a.lse_out != nullptr) a.lse_out[row] = le;
       }
     }
-    // Merge of the pieces of cut token t (slots sl0 .., and the extra partial
-    // when given) into its final output; the pieces are complete.
-    auto merge_token = [&](int t, int64_t sl0, int npieces, bool wide) {
-      const int64_t trow = static_cast<int64_t>(t) * kHeads;
-      const int esz = a.out_bf16 ? 2 : 4;
-      const bool has_e = a.extra_lse != nullptr;
-      if (!merge_bulk(npieces, sl0, has_e ? a.extra_o + trow * kDv : nullptr, has_e ? a.extra_lse + trow : nullptr,
-                      static_cast<char*>(a.out) + trow * kDv * esz, a.out_bf16 != 0, wide, [&](int r, float lv) {
-                        if (a.lse_out != nullptr) a.lse_out[trow + r] = lv;
-                      })) {
-        const int E = npieces + (has_e ? 1 : 0);
-        merge_rows<kMergeUnroll, EpGroup>(
-            kHeads, E, kDv,
-            [&](int r, int e) {
-              return e < npieces ? __ldcg(a.ws_lse + (sl0 + e) * kHeads + r) : __ldg(a.extra_lse + trow + r);
-            },
-            [&](int r, int e) {
-              return e < npieces ? a.ws_o + ((sl0 + e) * kHeads + r) * kDv : a.extra_o + (trow + r) * kDv;
-            },
-            [&](int r, int d, float4 v) {
-              const int64_t oi = (trow + r) * kDv + d;
-              if (a.out_bf16) {
-                __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
-                *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + oi) =
-                    make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
-              } else {
-                *reinterpret_cast<float4*>(static_cast<float*>(a.out) + oi) = v;
-              }
-            },
-            [&](int r, float lv) {
-              if (a.lse_out != nullptr) a.lse_out[trow + r] = lv;
-            },
-            scratch, kScrFloats);
-      }
-      if (tid == 0) a.ws_cnt[t] = 0;
-    };
-    constexpr int kMaxDefer = 4;
-    int n_defer = 0, defer_t[kMaxDefer], defer_np[kMaxDefer];
-    int64_t defer_sl0[kMaxDefer];
     for (int k = 0; ok; ++k) {
       MlaItem it;
       if (!item(k, it)) break;
@@ -1518,35 +1532,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           we = sum > 0.f ? w2 / sum : 0.f;
           lse = sum > 0.f ? M + logf(sum) : -INFINITY;
         }
-        const int esz = a.out_bf16 ? 2 : 4;
-        store_rows(static_cast<char*>(a.out) + static_cast<int64_t>(it.t) * kHeads * kDv * esz, a.out_bf16 != 0, wo,
-                   we, a.extra_lse != nullptr ? a.extra_o + static_cast<int64_t>(it.t) * kHeads * kDv : nullptr);
+        store_rows_tma(&tmap_out, it.t * kHeads, a.out_bf16 != 0, wo, we,
+                       a.extra_lse != nullptr ? a.extra_o + static_cast<int64_t>(it.t) * kHeads * kDv : nullptr);
         tc05::fence_before_sync();
         if (a.lse_out != nullptr) a.lse_out[row] = lse;
+        if (tid == 0) {
+          rec[2 * it.t] = 0;
+          rec[2 * it.t + 1] = 1;
+        }
+        continue;
+      }
+      if (kGroup) {
+        // a piece of a cut token: its normalised partial to its workspace
+        // slot; the merge kernel that follows combines the pieces (and the
+        // extra partial) into the token's final output
+        store_rows_tma(&tmap_ws, it.slot * kHeads, false, f.x, 0.f, nullptr);
+        tc05::fence_before_sync();
+        a.ws_lse[static_cast<int64_t>(it.slot) * kHeads + tid] = f.y;
+        if (tid == 0) {
+          rec[2 * it.t] = it.slot_base;
+          rec[2 * it.t + 1] = it.npieces;
+        }
         continue;
       }
       float* dst0 = it.slot < 0 ? a.o_part + (orow - tid) * kDv : a.ws_o + static_cast<int64_t>(it.slot) * kHeads * kDv;
       store_rows(dst0, false, f.x, 0.f, nullptr);
       tc05::fence_before_sync();
-      if (kGroup) {
-        // a piece of a cut token: the last piece to finish merges the pieces
-        // (and the extra partial) into the token's final output
-        a.ws_lse[static_cast<int64_t>(it.slot) * kHeads + tid] = f.y;
-        if (!take_ticket<EpGroup>(a.ws_cnt + it.t, it.npieces)) continue;
-        // this piece finished last: the merge runs now if this is the
-        // cluster's last item, else after it (with the wide staging area, and
-        // without holding up this cluster's tiles meanwhile)
-        MlaItem nx;
-        if (item(k + 1, nx) && n_defer < kMaxDefer) {
-          defer_t[n_defer] = it.t;
-          defer_sl0[n_defer] = it.slot_base;
-          defer_np[n_defer] = it.npieces;
-          ++n_defer;
-          continue;
-        }
-        merge_token(it.t, it.slot_base, it.npieces, !item(k + 1, nx));
-        continue;
-      }
       if (it.slot < 0) {
         a.lse_part[lse_slot(a, it.p, it.t, tid)] = f.y;
       } else {
@@ -1572,8 +1583,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       if (a.fused) pair_finish<kMergeUnroll, EpGroup>(a, it.t, 0, kHeads, kDv, scratch, kScrFloats);
     }
-    // merges put off until no tile of this cluster is in flight
-    for (int i = 0; i < n_defer && ok; ++i) merge_token(defer_t[i], defer_sl0[i], defer_np[i], true);
+    if (tid == 0) tc05::bulk_wait_all();  // the TMA stores are done before the CTA exits
     if (!ok) raise_abort();
   }
 
@@ -1584,6 +1594,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc05::fence_after_sync();
   if (warp == 0) tc05::tmem_dealloc(tbase, 512);
   tc05::cluster_sync();
+}
+
+// Grouped plans: the exact merge of the pieces of each cut token (and the
+// extra partial, when given) into its final output and LSE.  Block (t, rb)
+// takes rows 16 rb .. 16 rb + 15 of token t; the token's record (slot of its
+// first piece, pieces) comes from the partial kernel, which this grid follows
+// on the stream (it may start early and waits here for that grid to finish).
+constexpr int kMergeRows = 16;
+__global__ void __launch_bounds__(128) mla_merge_pieces_kernel(const PartialArgs a, int ws_slots) {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  __shared__ float scr[2048];
+  const int t = blockIdx.x, r0 = blockIdx.y * kMergeRows;
+  const int32_t* rec = a.ws_cnt + static_cast<int64_t>(a.num_tokens) * a.P;
+  const int npieces = __ldcg(rec + 2 * t + 1);
+  const int64_t sl0 = __ldcg(rec + 2 * t), trow = static_cast<int64_t>(t) * kHeads + r0;
+  // written whole by the partial kernel; or a record that kernel did not
+  // write (it gave up on a wait): never read outside the slots
+  if (npieces <= 1 || sl0 < 0 || sl0 + npieces > ws_slots) return;
+  const bool has_e = a.extra_lse != nullptr;
+  const int E = npieces + (has_e ? 1 : 0);
+  merge_rows<kMergeUnroll, CtaGroup>(
+      kMergeRows, E, kDv,
+      [&](int r, int e) {
+        return e < npieces ? __ldcg(a.ws_lse + (sl0 + e) * kHeads + r0 + r) : __ldg(a.extra_lse + trow + r);
+      },
+      [&](int r, int e) {
+        return e < npieces ? a.ws_o + ((sl0 + e) * kHeads + r0 + r) * kDv : a.extra_o + (trow + r) * kDv;
+      },
+      [&](int r, int d, float4 v) {
+        const int64_t oi = (trow + r) * kDv + d;
+        if (a.out_bf16) {
+          __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + oi) =
+              make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+        } else {
+          *reinterpret_cast<float4*>(static_cast<float*>(a.out) + oi) = v;
+        }
+      },
+      [&](int r, float lv) {
+        if (a.lse_out != nullptr) a.lse_out[trow + r] = lv;
+      },
+      scr, 2048);
 }
 
 namespace {
@@ -1634,6 +1686,21 @@ bool encode_pages(CUtensorMap* map, const void* ptr, int P, uint64_t rows_per_pa
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Rows of 512 values (fp32, or bf16) written as boxes of 128 rows x 128
+// bytes (the epilogue's staged chunks, 128-byte swizzle).
+bool encode_out(CUtensorMap* map, void* ptr, uint64_t rows, bool bf16) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr || rows == 0 || ptr == nullptr) return false;
+  const uint32_t esz = bf16 ? 2u : 4u;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDv), rows};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDv) * esz};
+  const cuuint32_t box[2] = {128u / esz, 128u};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // SMs of the current device (0 if unknown).
 int device_sms() {
   int dev = 0, sms = 0;
@@ -1679,16 +1746,22 @@ int launch_mla_partial(const PartialArgs& a, cudaStream_t s, cudaError_t* err) {
     return CPATTN_ERR_UNSUPPORTED_SHAPE;
   const int64_t pool_rows = static_cast<int64_t>(a.P) * a.num_pages * a.ps_l;
   if (pool_rows >= (int64_t{1} << 31)) return CPATTN_ERR_UNSUPPORTED_SHAPE;
-  CUtensorMap map, map_v;
+  CUtensorMap map, map_v, map_out, map_ws;
   std::memset(&map, 0, sizeof(map));
   std::memset(&map_v, 0, sizeof(map_v));
+  std::memset(&map_out, 0, sizeof(map_out));
+  std::memset(&map_ws, 0, sizeof(map_ws));
   // fused calls over logical pages of 64 slots: tiles are whole logical
   // pages, one 4-D box per ring unit (the per-partner partials are merged
   // inside the online softmax)
   const uint64_t rows_pp = static_cast<uint64_t>(a.num_pages) * a.ps_l;
+  // (outputs of whole tokens and the pieces of cut ones leave by TMA stores)
+  const int ws_slots = mla_ws_slots(a.P, a.interleave, a.num_tokens, a.max_kv_len, 1);
   const bool group = a.fused && a.page_size == kTile && a.num_tokens <= kGroupMaxTokens &&
                      encode_pages(&map, a.pool_k, a.P, rows_pp, a.ps_l, kUBlk) &&
-                     encode_pages(&map_v, a.pool_k, a.P, rows_pp, a.ps_l, kVB);
+                     encode_pages(&map_v, a.pool_k, a.P, rows_pp, a.ps_l, kVB) &&
+                     encode_out(&map_out, a.out, static_cast<uint64_t>(a.num_tokens) * kHeads, a.out_bf16 != 0) &&
+                     (ws_slots == 0 || encode_out(&map_ws, a.ws_o, static_cast<uint64_t>(ws_slots) * kHeads, false));
   // per-partner tiles: TMA when every 64-key tile is a whole number of page
   // runs of >= 8 rows (so each box lands on a 1024-byte boundary of the
   // 128-byte swizzle pattern), or lies inside one page run
@@ -1717,9 +1790,25 @@ int launch_mla_partial(const PartialArgs& a, cudaStream_t s, cudaError_t* err) {
     cudaGetLastError();  // a failed query leaves no error behind
     fit[variant][dev & 63].store(C, std::memory_order_relaxed);
   }
-  kern<<<dim3(2 * C, 1, 1), kThreads, kSmemBytes, s>>>(a, map, map_v, box_rows);
+  kern<<<dim3(2 * C, 1, 1), kThreads, kSmemBytes, s>>>(a, map, map_v, map_out, map_ws, box_rows);
   *err = cudaGetLastError();
-  return *err == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+  if (*err != cudaSuccess) return CPATTN_ERR_CUDA;
+  if (group && a.num_tokens > 0) {
+    // the cut tokens' merge, launched to overlap the partial kernel's tail
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.num_tokens), kHeads / kMergeRows, 1);
+    cfg.blockDim = dim3(128, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    *err = cudaLaunchKernelEx(&cfg, mla_merge_pieces_kernel, a, ws_slots);
+    if (*err != cudaSuccess) return CPATTN_ERR_CUDA;
+  }
+  return CPATTN_OK;
 }
 
 }  // namespace cpattn
