@@ -12,6 +12,15 @@ than L2, so no flush is needed between steps.
 Default workload: GQA decode, batch 64, 32 query / 8 KV heads, head_dim 128,
 page 16, P = 4, context lengths uniform in [512, 8192], bf16, fp32 LSE.
 
+Each timed measurement is ``--windows`` windows of exactly K steps (after W
+warm-up steps, a barrier and a synchronize around each window); the line
+reports the median window and the spread.  Besides the headline workload the
+line carries ``configs``: all five workloads of the specification, each timed
+on both paths (``unfused``: partial + lse_merge; ``fused``: the partials merged
+by the partial launch), with its partial launch's roofline (HBM, and for MLA
+the tensor pipe against the sustained bf16 peak), the end-to-end step through
+host buffers on its faster path, and the SM clocks sampled meanwhile.
+
 ``--impl reference`` times the float64 CPU oracle on the host cores instead
 (the pages publish no implementation or figures to run); under torchrun only
 rank 0 runs it.  ``--gpus N`` under torchrun runs N independent replicas (the
@@ -55,7 +64,7 @@ KERNEL_SOURCES = {
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="gqa_decode",
@@ -68,7 +77,15 @@ def parse_args():
                     help="unfused: partial + lse_merge (the faster on every workload measured); fused: partials "
                          "merged inside the partial launch")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
+    ap.add_argument("--windows", type=int, default=5,
+                    help="timed windows of K steps each (median and spread reported)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="time the headline workload only (skip the per-config object)")
     return ap.parse_args()
+
+
+# the five workloads of the specification, in its order; the headline is the second
+CONFIG_NAMES = ["tiny_fp32", "gqa_decode", "long_gqa_decode", "mla_decode", "mixed_step"]
 
 
 # ---------------------------------------------------------------- workloads
@@ -122,13 +139,24 @@ def algorithmic_bytes(w, fused=True):
 def launches_per_step(w, fused=True):
     """Kernels of one step: kv_write, the partial (a second kernel for the
     multi-token rows of a non-decode step), own_token (non-decode), and
-    lse_merge (unfused only)."""
+    lse_merge (unfused) or, for fused MLA steps over 64-slot logical pages,
+    the merge of the tokens cut between clusters."""
     n = 1 + 1
     if not w.decode:
         n += 2
     if not fused:
         n += 1
+    elif w.mla and w.page_size == 64:
+        n += 1
     return n
+
+
+def algorithmic_flops(w):
+    """Tensor-core FLOPs of the pool partial: 2 (D + Dv) per query head, per
+    new token of a row and per key it sees in the pool."""
+    kv = w.kv_len[: w.num_real_rows].astype("int64")
+    n = w.new_len[: w.num_real_rows].astype("int64")
+    return int(2 * (w.head_dim + w.head_dim_v) * w.num_q_heads * int((kv * n).sum()))
 
 
 # ---------------------------------------------------------------- environment
@@ -384,29 +412,17 @@ def sample_keys(w):
 
 # ---------------------------------------------------------------- our arm
 
-def run_ours(args, rank, world, local_rank):
-    import torch
+def load_tflops():
+    """Sustained dense bf16 TFLOP/s (for a kernel inside a long step)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 1700.0, "fallback"
 
-    import __graft_entry__
-    from context_paged_attention_gb300.step import StripedAttention
 
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-    torch.cuda.set_device(local_rank)
-    __graft_entry__.build()
-
-    # the oracle workers are spawned before the first GPU call
-    opool = OraclePool() if (rank == 0 and not args.no_cpu_baseline) else None
-
-    w = make_workload(args.config)
-    att = StripedAttention(w, device=f"cuda:{local_rank}")
-    torch.cuda.synchronize()
-    if att.status() != 0:
-        raise RuntimeError(f"device status {att.status()} after filling the pool")
-    fused = args.path == "fused"
-    alg = algorithmic_bytes(w, fused)
-    stream = torch.cuda.current_stream()
+def make_step(att, w, fused, stream):
+    """One step of the hot path; ev0/ev1 bracket the partial launch."""
 
     def step(ev0=None, ev1=None):
         att.write_new()
@@ -428,6 +444,123 @@ def run_ours(args, rank, world, local_rank):
             att.own()
         att.merge()
 
+    return step
+
+
+def time_windows(step, K, windows, warmup, stream, dist):
+    """W warm-up steps, then `windows` timed windows of exactly K steps, each
+    bracketed by a barrier and a synchronize.  Returns per-window ms per step
+    and mean partial-launch ms, and the wall-clock span of the windows."""
+    import torch
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    win, part = [], []
+    t0 = time.time()
+    for _ in range(windows):
+        e0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        e1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(K):
+            step(e0[i], e1[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+        win.append(start.elapsed_time(end) / K)
+        part.append(sum(e0[i].elapsed_time(e1[i]) for i in range(K)) / K)
+    t1 = time.time()
+    return win, part, (t0, t1)
+
+
+def spread(xs):
+    return {"median": round(statistics.median(xs), 5), "min": round(min(xs), 5), "max": round(max(xs), 5),
+            "windows": len(xs)}
+
+
+def measure_config(name, args, world, local_rank, dist, sampler, stream, paths=("unfused", "fused"), att_w=None):
+    """All of one workload's numbers: both paths timed in repeated windows,
+    the partial launch's roofline, the end-to-end step with host buffers and
+    the clocks seen meanwhile."""
+    import torch
+    from context_paged_attention_gb300.step import StripedAttention
+
+    if att_w is None:
+        w = make_workload(name)
+        att = StripedAttention(w, device=f"cuda:{local_rank}")
+    else:
+        att, w = att_w
+    torch.cuda.synchronize()
+    if att.status() != 0:
+        raise RuntimeError(f"{name}: device status {att.status()} after filling the pool")
+    peak, peak_src = load_peaks()
+    tflops, tf_src = load_tflops()
+    out = {"workload": describe(w)["workload"], "kv_bytes_per_step": int(w.kv_bytes_read())}
+    spans = []
+    best = None
+    for path in paths:
+        fused = path == "fused"
+        win, part, span = time_windows(make_step(att, w, fused, stream), args.steps, args.windows, args.warmup,
+                                       stream, dist)
+        spans.append(span)
+        if att.status() != 0:
+            raise RuntimeError(f"{name} ({path}): device status {att.status()} during the timed steps")
+        if dist is not None:
+            win = max_over_ranks(dist, win, f"cuda:{local_rank}")
+            part = max_over_ranks(dist, part, f"cuda:{local_rank}")
+        ms = statistics.median(win)
+        pms = statistics.median(part)
+        alg = algorithmic_bytes(w, fused)
+        achieved = alg["partial"] / (pms * 1e-3) / 1e9
+        roof = {"kernel": ("cp_paged_attn_fused" if fused else "cp_paged_attn_partial"), "bound": "hbm",
+                "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "algorithmic_bytes": alg["partial"], "ms_per_launch": round(pms, 5),
+                "launch_windows": spread(part), "peak_note": f"of {peak_src}"}
+        if w.mla:
+            fl = algorithmic_flops(w)
+            roof["tensor"] = {"achieved": round(fl / (pms * 1e-3) / 1e12, 1), "peak": tflops, "unit": "TFLOP/s",
+                              "frac": round(fl / (pms * 1e-3) / 1e12 / tflops, 4), "flops": fl,
+                              "peak_note": f"bf16_tflops_sustained, of {tf_src}"}
+        entry = {"ms_per_step": round(ms, 5), "step_windows": spread(win),
+                 "value": round(job_throughput(world, alg["kv"], ms), 2), "unit": "GB/s",
+                 "frac_of_peak": round(alg["kv"] / (ms * 1e-3) / 1e9 / peak, 4),
+                 "decode_tokens_per_s": round(world * int(w.qo_indptr[w.num_real_rows]) / (ms * 1e-3), 1),
+                 "roofline": roof, "gpu_launches_per_step": launches_per_step(w, fused)}
+        out[path] = entry
+        if best is None or ms < out[best]["ms_per_step"]:
+            best = path
+    out["best_path"] = best
+    if not args.no_e2e:
+        e = time_e2e(att, w, args, stream, best == "fused")
+        if dist is not None:
+            e["ms_per_step"] = max_over_ranks(dist, [e["ms_per_step"]], f"cuda:{local_rank}")[0]
+        out["e2e"] = {"value": round(world * w.kv_bytes_read() / (e["ms_per_step"] * 1e-3) / 1e9, 2), "unit": "GB/s",
+                      "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
+                      "ms_per_step": round(e["ms_per_step"], 5), "path": best}
+    if sampler is not None:
+        out["clocks"] = sampler.summary(spans[0][0], spans[-1][1])
+    return out, att, w
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import __graft_entry__
+    from context_paged_attention_gb300.step import StripedAttention
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    torch.cuda.set_device(local_rank)
+    __graft_entry__.build()
+
+    # the oracle workers are spawned before the first GPU call
+    opool = OraclePool() if (rank == 0 and not args.no_cpu_baseline) else None
+    stream = torch.cuda.current_stream()
+
     sampler = None
     if not args.no_clocks and rank == 0:
         try:
@@ -438,38 +571,16 @@ def run_ours(args, rank, world, local_rank):
         sampler.start()
         time.sleep(0.3)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
-    K = args.steps
-    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_wall0 = time.time()
-    start.record(stream)
-    for i in range(K):
-        step(e0[i], e1[i])
-    end.record(stream)
-    torch.cuda.synchronize()
-    t_wall1 = time.time()
-    if dist is not None:
-        dist.barrier()
-    total_ms = start.elapsed_time(end)
-    partial_ms = sum(e0[i].elapsed_time(e1[i]) for i in range(K)) / K
-    if sampler is not None:
-        time.sleep(0.25)
-        sampler.stop()
-    if att.status() != 0:
-        raise RuntimeError(f"device status {att.status()} during the timed steps")
+    # ---- the headline workload, on the requested path
+    w = make_workload(args.config)
+    att = StripedAttention(w, device=f"cuda:{local_rank}")
+    fused = args.path == "fused"
+    head, att, w = measure_config(args.config, args, world, local_rank, dist, sampler, stream, paths=(args.path,),
+                                  att_w=(att, w))
+    h = head[args.path]
+    ms = h["ms_per_step"]
 
-    # end-to-end through the public API with host buffers (pinned), copies inside the timed region
-    e2e = None
-    if not args.no_e2e:
-        e2e = time_e2e(att, w, args, stream, fused)
-
-    # the same fused step captured once as a CUDA graph and replayed K times
+    # the same step captured once as a CUDA graph and replayed K times
     graph = None
     if not args.no_graph:
         att.capture(fused)
@@ -478,62 +589,60 @@ def run_ours(args, rank, world, local_rank):
         g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         g0.record(stream)
-        for _ in range(K):
+        for _ in range(args.steps):
             att.replay()
         g1.record(stream)
         torch.cuda.synchronize()
-        gms = g0.elapsed_time(g1) / K
-        graph = {"ms_per_step": round(gms, 5), "value": round(world * alg["kv"] / (gms * 1e-3) / 1e9, 2),
+        gms = g0.elapsed_time(g1) / args.steps
+        graph = {"ms_per_step": round(gms, 5), "value": round(world * w.kv_bytes_read() / (gms * 1e-3) / 1e9, 2),
                  "unit": "GB/s", "note": "informational: the same step replayed from one captured CUDA graph"}
+    cpu_tasks = oracle_tasks(w, sample_keys(w)) if opool is not None else None
+    del att
+    torch.cuda.empty_cache()
 
-    if dist is not None:
-        total_ms, e2e_ms = max_over_ranks(dist, [total_ms, e2e["ms_per_step"] if e2e else 0.0], f"cuda:{local_rank}")
-        if e2e:
-            e2e["ms_per_step"] = e2e_ms
-    ms = total_ms / K
-    kv_bytes = alg["kv"]
-    value = job_throughput(world, kv_bytes, ms)
-    peak, peak_src = load_peaks()
+    # ---- every workload of the specification, both paths
+    configs = None
+    if not args.no_configs:
+        configs = {}
+        for name in CONFIG_NAMES:
+            entry, a2, _ = measure_config(name, args, world, local_rank, dist, sampler, stream)
+            configs[name] = entry
+            del a2
+            torch.cuda.empty_cache()
 
     if rank != 0:
         return
-    achieved = alg["partial"] / (partial_ms * 1e-3) / 1e9
-    traffic = recorded_traffic("mla_partial" if w.mla else ("gqa_partial" if w.decode else "gqa_mixed_partial"),
-                               args.config)
+    peak, peak_src = load_peaks()
+    roof = dict(h["roofline"])
+    roof["kernel"] += (" (MLA, tcgen05)" if w.mla else
+                       " (GQA, mma.sync decode rows + tcgen05 multi-token rows)" if w.dtype == "bf16" else
+                       " (GQA, CUDA cores)")
+    roof["traffic"] = recorded_traffic("mla_partial" if w.mla else ("gqa_partial" if w.decode else "gqa_mixed_partial"),
+                                       args.config)
     line = {
         "metric": METRIC,
-        "value": round(value, 2),
+        "value": h["value"],
         "unit": "GB/s",
         "n_gpus": world,
-        "steps": K,
+        "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(ms, 5),
+        "ms_per_step": ms,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": w.dtype,
         "data": "synthetic (seeded N(0,1) values, uniform lengths, random page permutation)",
-        "config": describe(w) | {"parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "frac_of_peak": round(value / world / peak, 4),
+        "config": describe(w) | {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                                 "timing": f"{args.windows} windows of {args.steps} steps after {args.warmup} "
+                                           f"warm-up steps; ms_per_step is the median window"},
+        "frac_of_peak": h["frac_of_peak"],
         "peak_source": f"{peak_src} hbm_gbs {peak}",
-        "decode_tokens_per_s": round(world * int(w.qo_indptr[w.num_real_rows]) / (ms * 1e-3), 1),
-        "roofline": {
-            "kernel": ("cp_paged_attn_fused" if fused else "cp_paged_attn_partial") +
-                      (" (MLA, tcgen05)" if w.mla else
-                       " (GQA, mma.sync decode rows + tcgen05 multi-token rows)" if w.dtype == "bf16" else
-                       " (GQA, CUDA cores)"),
-            "bound": "hbm",
-            "achieved": round(achieved, 1),
-            "peak": peak,
-            "unit": "GB/s",
-            "frac": round(achieved / peak, 4),
-            "traffic": traffic,
-            "algorithmic_bytes": alg["partial"],
-            "ms_per_launch": round(partial_ms, 5),
-            "peak_note": f"of {peak_src}",
-        },
-        "gpu_launches": K * launches_per_step(w, fused),
-        "launch_note": "per step: " + ("kv_write, the fused partial+merge" if fused else "kv_write, partial, lse_merge") +
+        "decode_tokens_per_s": h["decode_tokens_per_s"],
+        "step_windows": h["step_windows"],
+        "roofline": roof,
+        "gpu_launches": args.steps * launches_per_step(w, fused),
+        "launch_note": "per timed window of K steps: " +
+                       ("kv_write, the fused partial+merge" if fused else "kv_write, partial, lse_merge") +
                        (" (+ own_token and the multi-token-row partial kernel for non-decode steps)" if not w.decode
                         else "") + "; plus one cudaMemsetAsync of the split-KV tickets when a stripe splits "
                                    "or the call is fused",
@@ -541,14 +650,14 @@ def run_ours(args, rank, world, local_rank):
     }
     if graph is not None:
         line["graph"] = graph
-    if e2e is not None:
-        line["e2e"] = {"value": round(world * kv_bytes / (e2e["ms_per_step"] * 1e-3) / 1e9, 2), "unit": "GB/s",
-                       "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
-                       "ms_per_step": round(e2e["ms_per_step"], 5)}
-    if sampler is not None:
-        line["clocks"] = sampler.summary(t_wall0, t_wall1)
+    if "e2e" in head:
+        line["e2e"] = {k: v for k, v in head["e2e"].items() if k != "path"}
+    if "clocks" in head:
+        line["clocks"] = head["clocks"]
+    if configs is not None:
+        line["configs"] = configs
     if opool is not None:
-        tasks, nbytes = oracle_tasks(w, sample_keys(w))
+        tasks, nbytes = cpu_tasks
         secs, passes = opool.run_for(tasks)
         opool.close()
         line["cpu_baseline"] = {"value": round(passes * nbytes / secs / 1e9, 4), "unit": "GB/s",
@@ -556,6 +665,8 @@ def run_ours(args, rank, world, local_rank):
                                 "sample": f"float64 oracle over {len(tasks)} of {w.num_real_rows} rows of the same "
                                           f"step ({nbytes / 1e9:.3f} GB of KV), {passes} pass(es), one spawned "
                                           f"single-threaded worker per core, {secs:.2f} s"}
+    if sampler is not None:
+        sampler.stop()
     print(json.dumps(line), flush=True)
 
 
