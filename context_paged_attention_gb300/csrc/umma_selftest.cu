@@ -28,7 +28,9 @@ __global__ void __launch_bounds__(128) umma_selftest_kernel(int variant, const _
   uint8_t* sB;
   const uint4* gA = reinterpret_cast<const uint4*>(A);
   const uint4* gB = reinterpret_cast<const uint4*>(B);
-  if (variant == 0 || variant == 4) {
+  if (variant == 5) {
+    sB = sA;  // no operands: the completion wait below is on a barrier nothing arrives at
+  } else if (variant == 0 || variant == 4) {
     // A [128][K], B [N][K], both K-major SW128 in 64-element column blocks
     // (variant 4 reads A from tensor memory instead, written below)
     sB = sA + 128 * K * 2;
@@ -107,7 +109,7 @@ __global__ void __launch_bounds__(128) umma_selftest_kernel(int variant, const _
     tc05::fence_after_sync();
   }
 
-  if (tid == 0) {
+  if (tid == 0 && variant != 5) {
     const uint32_t a0 = tc05::smem_addr(sA), b0 = tc05::smem_addr(sB);
     if (variant == 0) {
       const uint32_t id = tc05::idesc_bf16(128, N, false, false);
@@ -139,7 +141,9 @@ __global__ void __launch_bounds__(128) umma_selftest_kernel(int variant, const _
     }
     tc05::commit(mb);
   }
-  const bool ok = tc05::mbar_wait(mb, 0);
+  // variant 5: no MMA is issued and nothing commits, so the wait runs out
+  // after a short poll limit and takes the timeout path (status, TMEM freed)
+  const bool ok = tc05::mbar_wait(mb, 0, variant == 5 ? (1u << 12) : (1u << 24));
   tc05::fence_after_sync();
   if (ok) {
     for (int col = 0; col < N; col += 16) {
@@ -168,6 +172,9 @@ extern "C" int cpattn_umma_selftest(int variant, const void* A, const void* B, f
     if (N < 16 || N > 256 || N % 16 != 0 || K < 64 || K > 256 || K % 64 != 0) return CPATTN_ERR_UNSUPPORTED_SHAPE;
   } else if (variant == 1 || variant == 2 || variant == 3) {
     if (N < 64 || N > 256 || N % 64 != 0 || K != 32) return CPATTN_ERR_UNSUPPORTED_SHAPE;
+  } else if (variant == 5) {
+    N = 16;  // nothing is read or written but the status
+    K = 64;
   } else {
     return CPATTN_ERR_INVALID_ARG;
   }

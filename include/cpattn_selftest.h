@@ -33,6 +33,11 @@ extern "C" {
  *              bf16 K elements a 32-bit column), written there by tcgen05.st.
  *   variant 4: variant 0 with A read from tensor memory the same way (the
  *              Q K^T pattern with Q held in TMEM, K/16 k-steps of 8 columns).
+ *   variant 5: the timeout path.  No MMA is issued and nothing arrives on the
+ *              completion barrier, so its wait gives up after a short poll
+ *              limit; the kernel stores CPATTN_DEV_TC_TIMEOUT, frees its
+ *              tensor memory and returns (A, B, D are not read or written,
+ *              N and K are ignored).  The context stays usable.
  * A completion wait that times out stores 4 in *dev_status (if not NULL).
  */
 CPATTN_API int cpattn_umma_selftest(int variant, const void* A, const void* B, float* D, int N, int K,

@@ -67,6 +67,30 @@ class OracleView:
             return O, L
         return oracle.stripe_partial(q, K, V, w.scale, w.P, p, w.interleave)
 
+    def stripe_abs(self, t, p, drop=None):
+        """Partner p's softmax weights applied to |V| (sum_k w_k |v_k| per head
+        and value), and the partial itself, for token t; `drop`: index (within
+        the stripe) of one key to leave out."""
+        w = self.w
+        b = self.row_of_token(t)
+        m = int(w.kv_len[b])
+        K, V = self.row_kv(b, m)
+        idx = oracle.stripe_positions(m, w.P, p, w.interleave)
+        if drop is not None:
+            idx = np.delete(idx, drop)
+        q = self.q[t]
+        g = w.num_q_heads // w.num_kv_heads
+        Hq = w.num_q_heads
+        O = np.zeros((Hq, w.head_dim_v))
+        A = np.zeros((Hq, w.head_dim_v))
+        L = np.zeros((Hq,))
+        for kh in range(w.num_kv_heads):
+            hs = slice(kh * g, (kh + 1) * g)
+            Kk, Vk = K[idx, kh: kh + 1], V[idx, kh: kh + 1]
+            O[hs], L[hs] = oracle.attention(q[hs], Kk, Vk, w.scale)
+            A[hs], _ = oracle.attention(q[hs], Kk, np.abs(Vk), w.scale)
+        return O, L, A, len(idx)
+
     def final(self, rows=None, heads=None):
         w = self.w
         if w.kv_dtype == "fp8":
@@ -120,6 +144,19 @@ def assert_close_lse(got, want, tol, what=""):
     if fin.any():
         err = np.max(np.abs(got[fin] - want[fin]))
         assert err <= tol, f"{what}: max |dLSE| {err:.3e} > {tol}"
+
+
+def within_bound(got, want, bound):
+    """Whether |got - want| <= bound elementwise (bound broadcast to the arrays)."""
+    d = np.abs(np.asarray(got, np.float64) - np.asarray(want, np.float64))
+    return bool(np.all(np.isfinite(d)) and np.all(d <= bound))
+
+
+def assert_within_bound(got, want, bound, what=""):
+    d = np.abs(np.asarray(got, np.float64) - np.asarray(want, np.float64))
+    ratio = float(np.max(d / bound)) if np.size(d) else 0.0
+    assert np.all(np.isfinite(d)) and ratio <= 1.0, f"{what}: max |d| / bound {ratio:.3f} > 1"
+    return ratio
 
 
 def assert_close(got, want, tol, what=""):

@@ -81,3 +81,21 @@ def test_pv_pattern_a_in_tmem(selftest, N):
 def test_qk_pattern_a_in_tmem(selftest, N, K):
     # Q K^T with Q in tensor memory over several k-steps
     assert _run(selftest, 4, N, K, seed=N + K + 11) <= 1e-3
+
+
+def test_bounded_wait_times_out_and_frees(selftest):
+    # a completion barrier nobody arrives at: the bounded wait gives up, the
+    # call reports CPATTN_DEV_TC_TIMEOUT (4), frees its tensor memory, and the
+    # next tensor-core call on the same stream allocates and runs normally
+    x = torch.zeros(16, device="cuda", dtype=torch.bfloat16)
+    D = torch.full((128, 16), float("nan"), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    for _ in range(3):
+        st.zero_()
+        rc = selftest(5, x.data_ptr(), x.data_ptr(), D.data_ptr(), 0, 0, st.data_ptr(), stream)
+        torch.cuda.synchronize()
+        assert rc == 0 and int(st.item()) == 4
+        assert torch.isnan(D).all()  # the timed-out call wrote nothing
+    assert _run(selftest, 0, 128, 128, seed=5) <= 1e-3
+    assert _run(selftest, 4, 256, 256, seed=6) <= 1e-3  # 512 TMEM columns: all of it was freed
