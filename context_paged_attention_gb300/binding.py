@@ -274,11 +274,12 @@ def lse_merge_views(views, num_tokens, num_heads, head_dim_v, out, out_stride_to
 
 
 def own_token_attn(q, k_new, v_new, qo_indptr, num_real_rows, max_q_len, scale, o_own, lse_own, stream=None):
-    """Causal attention of the step's new tokens (see ``own_token_attn`` in cpattn.h)."""
+    """Causal attention of the step's new tokens (see ``own_token_attn`` in cpattn.h);
+    with ``v_new`` None the value width is ``o_own``'s (MLA: the first 512 key values)."""
     lib = load_library()
     T, Hq, D = q.shape
     Hkv = k_new.shape[1]
-    Dv = D if v_new is None else v_new.shape[2]
+    Dv = o_own.shape[-1] if v_new is None else v_new.shape[2]
     dt = DTYPE_BF16 if q.dtype == torch.bfloat16 else DTYPE_FP32
     st = lib.own_token_attn(_ptr(q), _ptr(k_new), _ptr(v_new), Hq, Hkv, D, Dv, dt,
                             _i32_tensor(qo_indptr, "qo_indptr"), qo_indptr.numel() - 1, int(num_real_rows), T,

@@ -338,11 +338,14 @@ int own_token_attn(const void* q, const void* k_new, const void* v_new, int32_t 
   if (eb == 0 || num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads != 0 || num_tokens < 0 ||
       num_rows_bucket < 1 || num_real_rows < 0 || num_real_rows > num_rows_bucket || max_q_len < 0)
     return CPATTN_ERR_INVALID_ARG;
-  if (head_dim != head_dim_v) return CPATTN_ERR_UNSUPPORTED_SHAPE;
+  // MLA: one latent head, keys of 576 values whose first 512 are the value (v_new NULL)
+  const bool mla = num_kv_heads == 1 && head_dim == 576 && head_dim_v == 512;
+  if (mla ? (dtype != CPATTN_DTYPE_BF16 || v_new != nullptr) : head_dim != head_dim_v)
+    return CPATTN_ERR_UNSUPPORTED_SHAPE;
   if (num_tokens == 0) return CPATTN_OK;
   if (q == nullptr || k_new == nullptr || qo_indptr == nullptr || o_own == nullptr || lse_own == nullptr)
     return CPATTN_ERR_INVALID_ARG;
-  if (v_new == nullptr) v_new = k_new;  // value = prefix (here: all) of the key row
+  if (v_new == nullptr) v_new = k_new;  // value = prefix of the key row
   if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(o_own)) return CPATTN_ERR_MISALIGNED;
   OwnArgs a;
   a.q = q;

@@ -82,9 +82,74 @@ static int own_dispatch_g(const OwnArgs& a, int G, cudaStream_t s, cudaError_t* 
   }
 }
 
+// MLA (one latent KV head, keys of 576 values, values = their first 512):
+// warp w of CTA (token t, head block y) takes query head 8 y + w.  Lane l
+// holds bf16 pairs l + 32 i of the query and of each key (i < 9; the value
+// pairs are those with i < 8), so every key is read once a warp, coalesced,
+// and its value needs no second load.  Same row and padding rules as above.
+constexpr int kOwnMlaHeads = 8;
+__global__ void __launch_bounds__(kOwnMlaHeads * 32) own_token_mla_kernel(const OwnArgs a) {
+  constexpr int kPairs = 576 / 2, kPL = kPairs / 32, kVPL = 512 / 2 / 32;  // 9 pairs a lane, 8 of them values
+  const int t = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y * kOwnMlaHeads + warp;
+  if (h >= a.num_q_heads) return;
+  const int real_end = __ldg(a.qo_indptr + a.num_real_rows);
+  const bool real = t < real_end;
+  const int start = real ? __ldg(a.qo_indptr + find_row(a.qo_indptr, a.num_real_rows, t)) : 0;
+  const float sl = a.scale * kLog2e;
+  const uint32_t* qrow =
+      reinterpret_cast<const uint32_t*>(a.q) + (static_cast<int64_t>(t) * a.num_q_heads + h) * kPairs;
+  float qv[2 * kPL];
+#pragma unroll
+  for (int i = 0; i < kPL; ++i) {
+    const float2 f = real ? __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(qrow + lane + 32 * i))
+                          : make_float2(0.f, 0.f);
+    qv[2 * i] = f.x * sl;
+    qv[2 * i + 1] = f.y * sl;
+  }
+  float m = -INFINITY, l = 0.f, o[2 * kVPL];
+#pragma unroll
+  for (int i = 0; i < 2 * kVPL; ++i) o[i] = 0.f;
+  if (real) {
+    for (int j = start; j <= t; ++j) {
+      const uint32_t* krow = reinterpret_cast<const uint32_t*>(a.k_new) + static_cast<int64_t>(j) * kPairs;
+      float kv[2 * kPL];
+      float s = 0.f;
+#pragma unroll
+      for (int i = 0; i < kPL; ++i) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(krow + lane + 32 * i));
+        kv[2 * i] = f.x;
+        kv[2 * i + 1] = f.y;
+        s = fmaf(qv[2 * i], f.x, fmaf(qv[2 * i + 1], f.y, s));
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+      const float mn = fmaxf(m, s);
+      const float alpha = m == -INFINITY ? 0.f : exp2f(m - mn);
+      const float pj = exp2f(s - mn);
+      l = l * alpha + pj;
+#pragma unroll
+      for (int i = 0; i < 2 * kVPL; ++i) o[i] = fmaf(pj, kv[i], o[i] * alpha);
+      m = mn;
+    }
+  }
+  const int64_t orow = static_cast<int64_t>(t) * a.num_q_heads + h;
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  float2* dst = reinterpret_cast<float2*>(a.o_own + orow * 512);
+#pragma unroll
+  for (int i = 0; i < kVPL; ++i) dst[lane + 32 * i] = make_float2(o[2 * i] * inv, o[2 * i + 1] * inv);
+  if (lane == 0) a.lse_own[orow] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+}
+
 int launch_own_token(const OwnArgs& a, int dtype_bf16, cudaStream_t s, cudaError_t* err) {
   const int G = a.num_q_heads / a.num_kv_heads;
   if (a.num_tokens == 0) return CPATTN_OK;
+  if (a.head_dim == 576) {  // MLA (the caller checked the shape)
+    dim3 grid(a.num_tokens, (a.num_q_heads + kOwnMlaHeads - 1) / kOwnMlaHeads);
+    own_token_mla_kernel<<<grid, kOwnMlaHeads * 32, 0, s>>>(a);
+    *err = cudaGetLastError();
+    return *err == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+  }
   if (dtype_bf16) {
     return launch_own_token_mma(a, s, err);  // tensor cores (own_token_mma.cu)
   } else {

@@ -344,7 +344,9 @@ CPATTN_API size_t cp_paged_attn_noalloc_scratch_bytes(void);
  *          underestimate only costs time)
  *   o_own  [num_tokens][num_q_heads][head_dim_v] fp32, lse_own [num_tokens][num_q_heads]
  * Supported: head_dim == head_dim_v in {64, 128}; group size in {1, 2, 4, 8,
- * 16} (bf16, tensor cores) or {1, 2, 4, 8} (fp32).
+ * 16} (bf16, tensor cores) or {1, 2, 4, 8} (fp32).  MLA: num_kv_heads 1,
+ * head_dim 576, head_dim_v 512, bf16, v_new NULL (the value is the first 512
+ * values of each latent key row), any num_q_heads.
  */
 CPATTN_API int own_token_attn(const void* q, const void* k_new, const void* v_new, int32_t num_q_heads,
                    int32_t num_kv_heads, int32_t head_dim, int32_t head_dim_v, int32_t dtype,

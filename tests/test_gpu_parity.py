@@ -44,6 +44,11 @@ SMALL = {
     "mla_decode": lambda: W.mla_decode(seed=24, batch=3, len_lo=100, len_hi=5000),
     "mla_decode_split": lambda: W.mla_decode(seed=30, batch=3, len_lo=9000, len_hi=20000),
     "mla_decode_short": lambda: W.mla_decode(seed=31, batch=4, len_lo=1, len_hi=40),
+    # MLA rows of several new tokens (pool partial + causal own-token partial), padding rows after them
+    "mla_mixed": lambda: W.build_workload("mla_mixed", dtype="bf16", P=4, page_size=64, num_q_heads=128,
+                                          num_kv_heads=1, head_dim=576, head_dim_v=512, mla=True, decode=False,
+                                          scale=1.0 / 192 ** 0.5, ctx_len=[700, 0, 3000, 64, 1500],
+                                          new_len=[1, 9, 5, 33, 1], padding_spans=[0, 3], num_tokens=64, seed=40),
     # page 16 with P 4: 4-row page runs, copied with cp.async instead of TMA
     "mla_decode_ps16": lambda: W.build_workload("mla_ps16", dtype="bf16", P=4, page_size=16, num_q_heads=128,
                                                 num_kv_heads=1, head_dim=576, head_dim_v=512, mla=True,
@@ -337,7 +342,10 @@ def test_own_token_partial(small):
         s0 = int(w.seq_indptr[b])
         c, n = int(w.ctx_len[b]), int(w.new_len[b])
         K = oracle.raw_to_f64(w.k_seq[s0 + c: s0 + c + n])
-        V = oracle.raw_to_f64(w.v_seq[s0 + c: s0 + c + n])
+        if w.mla:
+            K, V = oracle.mla_kv(K, w.head_dim_v)
+        else:
+            V = oracle.raw_to_f64(w.v_seq[s0 + c: s0 + c + n])
         t0 = int(w.qo_indptr[b])
         O, L = oracle.causal_own_attention(ov.q[t0: t0 + n], K, V, w.scale)
         assert_close(o_own[t0: t0 + n], O, 1e-4, f"own O row {b}")
