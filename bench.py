@@ -518,7 +518,8 @@ def measure_config(name, args, world, local_rank, dist, sampler, stream, paths=(
         roof = {"kernel": ("cp_paged_attn_fused" if fused else "cp_paged_attn_partial"), "bound": "hbm",
                 "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "algorithmic_bytes": alg["partial"], "ms_per_launch": round(pms, 5),
-                "launch_windows": spread(part), "peak_note": f"of {peak_src}"}
+                "launch_windows": spread(part), "peak_note": f"of {peak_src}",
+                "traffic": recorded_traffic(traffic_kernel(w), name + (":fused" if fused else ""))}
         if w.mla:
             fl = algorithmic_flops(w)
             roof["tensor"] = {"achieved": round(fl / (pms * 1e-3) / 1e12, 1), "peak": tflops, "unit": "TFLOP/s",
@@ -543,6 +544,10 @@ def measure_config(name, args, world, local_rank, dist, sampler, stream, paths=(
     if sampler is not None:
         out["clocks"] = sampler.summary(spans[0][0], spans[-1][1])
     return out, att, w
+
+
+def traffic_kernel(w):
+    return "mla_partial" if w.mla else ("gqa_partial" if w.decode else "gqa_mixed_partial")
 
 
 def run_ours(args, rank, world, local_rank):
@@ -617,8 +622,7 @@ def run_ours(args, rank, world, local_rank):
     roof["kernel"] += (" (MLA, tcgen05)" if w.mla else
                        " (GQA, mma.sync decode rows + tcgen05 multi-token rows)" if w.dtype == "bf16" else
                        " (GQA, CUDA cores)")
-    roof["traffic"] = recorded_traffic("mla_partial" if w.mla else ("gqa_partial" if w.decode else "gqa_mixed_partial"),
-                                       args.config)
+    roof["traffic"] = recorded_traffic(traffic_kernel(w), args.config + (":fused" if fused else ""))
     line = {
         "metric": METRIC,
         "value": h["value"],
