@@ -12,6 +12,31 @@ namespace cpattn {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// Programmatic dependent launch.  A kernel launched by launch_pdl may start
+// while the previous kernel on its stream is still running: it calls
+// pdl_wait() before it reads anything written before it on the stream (the
+// wait returns once that work is complete and visible; without a
+// programmatic launch it returns at once), and pdl_trigger() lets the next
+// such kernel be scheduled (it only starts its own prologue early).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // Record the first device-detected inconsistency (0 stays 0 until something happens).
 __device__ __forceinline__ void report(int32_t* status, int code) {
   if (status != nullptr) atomicCAS(status, 0, code);

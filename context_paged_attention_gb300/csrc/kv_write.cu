@@ -59,6 +59,8 @@ __device__ __forceinline__ void store_fp8_chunk(const void* src, int64_t src_off
 }
 
 __global__ void __launch_bounds__(256) kv_write_kernel(const WriteArgs a, int chunks_per_row) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t per_token = static_cast<int64_t>(a.num_kv_heads) * chunks_per_row;
   const int64_t total = per_token * a.num_tokens;
@@ -125,8 +127,7 @@ cudaError_t launch_kv_write(const WriteArgs& a, cudaStream_t s) {
   if (total == 0) return cudaSuccess;
   const int threads = 256;
   const int64_t blocks = (total + threads - 1) / threads;
-  kv_write_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(a, chunks);
-  return cudaGetLastError();
+  return launch_pdl(kv_write_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, s, a, chunks);
 }
 
 }  // namespace cpattn

@@ -12,6 +12,8 @@
 namespace cpattn {
 
 __global__ void __launch_bounds__(256) lse_merge_kernel(const MergeArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int warps_per_block = blockDim.x / 32;
   const int64_t item = static_cast<int64_t>(blockIdx.x) * warps_per_block + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
@@ -120,6 +122,8 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const MergeArgs a) {
 // token-major one DCP's combine wants ([B, H]) (vLLM "[Core] Add explicit
 // layer parallel plans", _forward_with_dcp), and per-rank head slices.
 __global__ void __launch_bounds__(256) lse_merge_views_kernel(const MergeViewArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int warps_per_block = blockDim.x / 32;
   const int64_t item = static_cast<int64_t>(blockIdx.x) * warps_per_block + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
@@ -173,8 +177,7 @@ cudaError_t launch_lse_merge_views(const MergeViewArgs& a, cudaStream_t s) {
   if (items == 0) return cudaSuccess;
   const int threads = 256;
   const int64_t blocks = (items + 7) / 8;
-  lse_merge_views_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(lse_merge_views_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, s, a);
 }
 
 cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t s) {
@@ -182,8 +185,7 @@ cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t s) {
   if (items == 0) return cudaSuccess;
   const int threads = 256;
   const int64_t blocks = (items + 7) / 8;
-  lse_merge_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(lse_merge_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, s, a);
 }
 
 }  // namespace cpattn

@@ -86,6 +86,8 @@ __global__ void __launch_bounds__(kTWarps * 32, F8 ? 4 : 3) gqa_partial_mmat_ker
   const int g8 = lane >> 2;  // key row (S^T) / dim row (O^T) / head column of B fragments
   const int qi = lane & 3;   // heads 2 qi, 2 qi + 1 of the accumulators
 
+  pdl_trigger();
+  pdl_wait();  // every input may come from the kernels before this one
   const int b = ordered_row(a.row_order, blockIdx.z, gridDim.z, a.dev_status);
   if (b < 0) return;
   int t = b;
@@ -405,8 +407,7 @@ static int launch_mmat_t(const PartialArgs& a, cudaStream_t s, cudaError_t* err)
   *err = ensure_smem(kern, smem, smem_set);
   if (*err != cudaSuccess) return CPATTN_ERR_CUDA;
   dim3 grid(a.max_chunks, a.P * a.num_kv_heads, a.qo_indptr != nullptr ? a.num_rows : a.num_tokens);
-  kern<<<grid, kTWarps * 32, smem, s>>>(a);
-  *err = cudaGetLastError();
+  *err = launch_pdl(kern, grid, dim3(kTWarps * 32), smem, s, a);
   return *err == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
 }
 

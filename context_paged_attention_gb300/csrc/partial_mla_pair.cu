@@ -707,7 +707,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   // the merge of cut tokens (grouped plans) may be scheduled already; it
   // waits for this grid's completion before it reads anything
-  if (tid == 0) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  if (tid == 0) pdl_trigger();
+  pdl_wait();  // every input may come from the kernels before this one
   // ---- plan, barriers, tensor memory
   if (tid == 0) {
     misc[1] = 0;
@@ -1790,8 +1791,8 @@ int launch_mla_partial(const PartialArgs& a, cudaStream_t s, cudaError_t* err) {
     cudaGetLastError();  // a failed query leaves no error behind
     fit[variant][dev & 63].store(C, std::memory_order_relaxed);
   }
-  kern<<<dim3(2 * C, 1, 1), kThreads, kSmemBytes, s>>>(a, map, map_v, map_out, map_ws, box_rows);
-  *err = cudaGetLastError();
+  *err = launch_pdl(kern, dim3(2 * C, 1, 1), dim3(kThreads, 1, 1), kSmemBytes, s, a, map, map_v, map_out, map_ws,
+                    box_rows);
   if (*err != cudaSuccess) return CPATTN_ERR_CUDA;
   if (group && a.num_tokens > 0) {
     // the cut tokens' merge, launched to overlap the partial kernel's tail
