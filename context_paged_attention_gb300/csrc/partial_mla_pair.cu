@@ -1604,7 +1604,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // on the stream (it may start early and waits here for that grid to finish).
 constexpr int kMergeRows = 16;
 __global__ void __launch_bounds__(128) mla_merge_pieces_kernel(const PartialArgs a, int ws_slots) {
-  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  pdl_wait();
   __shared__ float scr[2048];
   const int t = blockIdx.x, r0 = blockIdx.y * kMergeRows;
   const int32_t* rec = a.ws_cnt + static_cast<int64_t>(a.num_tokens) * a.P;
