@@ -503,25 +503,34 @@ __global__ void __launch_bounds__(kWThreads, 2) gqa_partial_ext_ws_kernel(const 
         const uint32_t vmask = smask[i % kMaskSlots];  // written before tile i's K copies
         float sv[32];
         {
-          float v16[16];
-          tc05::ld_x16(my_lane + Lt::S_COL + 32 * bb, v16);
+          // both halves of the row's scores in flight at once
+          float v0[16], v1[16];
+          tc05::ld_x16(my_lane + Lt::S_COL + 32 * bb, v0);
+          tc05::ld_x16(my_lane + Lt::S_COL + 32 * bb + 16, v1);
           tc05::ld_wait();
 #pragma unroll
-          for (int e = 0; e < 16; ++e) sv[e] = v16[e];
-          tc05::ld_x16(my_lane + Lt::S_COL + 32 * bb + 16, v16);
-          tc05::ld_wait();
-#pragma unroll
-          for (int e = 0; e < 16; ++e) sv[16 + e] = v16[e];
+          for (int e = 0; e < 16; ++e) {
+            sv[e] = v0[e];
+            sv[16 + e] = v1[e];
+          }
         }
         tc05::fence_before_sync();
         __syncwarp();
         if (lane == 0) ws_arrive(bar(W_SFREE + bb));
-        float bm = -INFINITY;
+        // keys without data: -inf (probability 0); scores stay unscaled, the
+        // running max is in log2 units; the max as a tree, not a chain
+        if (vmask != 0xffffffffu) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          sv[e] = ((vmask >> e) & 1u) ? sv[e] * sl : -INFINITY;
-          bm = fmaxf(bm, sv[e]);
+          for (int e = 0; e < 32; ++e) sv[e] = ((vmask >> e) & 1u) ? sv[e] : -INFINITY;
         }
+        float mx[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) mx[e] = fmaxf(sv[e], sv[16 + e]);
+#pragma unroll
+        for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+          for (int e = 0; e < w; ++e) mx[e] = fmaxf(mx[e], mx[e + w]);
+        const float bm = mx[0] * sl;
         const bool up = bm > m + 8.f;
         if (__any_sync(0xffffffffu, up) && i > 0) {
           // rescale O rows whose max rose; P V of the previous tile must be done
@@ -549,16 +558,23 @@ __global__ void __launch_bounds__(kWThreads, 2) gqa_partial_ext_ws_kernel(const 
           if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
         }
         {
+          // p = 2^(s * scale * log2 e - m): one FMA and one ex2 a key (-inf
+          // gives 0; while every key so far is masked m is -inf and every p
+          // is 0); four partial sums of p and of bf16(p) each
+          const float nm = m == -INFINITY ? 0.f : -m;
+          float ls[4] = {0.f, 0.f, 0.f, 0.f}, lrs[4] = {0.f, 0.f, 0.f, 0.f};
           uint32_t pk[16];  // bf16 pairs of keys 2e, 2e+1: row `tid` of P, as the MMA reads it from TMEM
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float pa = sv[2 * e] == -INFINITY ? 0.f : ex2_approx(sv[2 * e] - m);
-            const float pb = sv[2 * e + 1] == -INFINITY ? 0.f : ex2_approx(sv[2 * e + 1] - m);
-            l += pa + pb;
+            const float pa = ex2_approx(fmaf(sv[2 * e], sl, nm));
+            const float pb = ex2_approx(fmaf(sv[2 * e + 1], sl, nm));
+            ls[e & 3] += pa + pb;
             __nv_bfloat162 h2 = __floats2bfloat162_rn(pa, pb);
-            lr += __low2float(h2) + __high2float(h2);
             pk[e] = *reinterpret_cast<uint32_t*>(&h2);
+            lrs[e & 3] += __uint_as_float(pk[e] << 16) + __uint_as_float(pk[e] & 0xffff0000u);
           }
+          l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+          lr += (lrs[0] + lrs[1]) + (lrs[2] + lrs[3]);
           tc05::st_x16_u32(my_lane + Lt::P_COL + 16 * bb, pk);
           asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
         }
