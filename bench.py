@@ -54,7 +54,6 @@ KERNEL_SOURCES = {
     "gqa_partial": ["partial_gqa.cu", "partial_gqa_mma.cu", "partial_gqa_mmat.cu", "gqa_core.cuh",
                     "split_combine.cuh", "common.cuh", "mma_sync.cuh"],
     # non-decode steps add the multi-token kernel
-    # (bf16 pools: the E4M3 multi-token kernel, partial_gqa_ext_tc.cu, is not in the launch)
     "gqa_mixed_partial": ["partial_gqa.cu", "partial_gqa_mma.cu", "partial_gqa_mmat.cu", "partial_gqa_ext_ws.cu",
                           "gqa_core.cuh", "split_combine.cuh", "common.cuh", "mma_sync.cuh", "tc05.cuh"],
     "mla_partial": ["partial_gqa.cu", "partial_mla_pair.cu", "tc05.cuh", "split_combine.cuh", "common.cuh"],

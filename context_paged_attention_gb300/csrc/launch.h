@@ -130,7 +130,7 @@ bool plan_partial(int mla, int fused, int P, int interleave, int page_size, int 
 int launch_gqa_partial(const PartialArgs& a, int dtype_bf16, cudaStream_t s, cudaError_t* err);
 int launch_gqa_partial_mma(const PartialArgs& a, cudaStream_t s, cudaError_t* err);
 int launch_gqa_partial_ext(const PartialArgs& a, cudaStream_t s, cudaError_t* err);
-int launch_gqa_partial_ext_ws(const PartialArgs& a, cudaStream_t s, cudaError_t* err);  // bf16 pools
+int launch_gqa_partial_ext_ws(const PartialArgs& a, cudaStream_t s, cudaError_t* err);  // bf16 and E4M3 pools
 int launch_mla_partial(const PartialArgs& a, cudaStream_t s, cudaError_t* err);
 // MLA kernel: workspace slots for the pieces of cut stripes (0: no stripe can be
 // cut); `grouped`: fused calls whose tiles are logical pages (cut tokens)

@@ -1,5 +1,5 @@
-// cp_paged_attn_partial, GQA rows with several query tokens over a bf16 pool,
-// on the tcgen05 tensor cores with specialised warps.
+// cp_paged_attn_partial, GQA rows with several query tokens over a bf16 or
+// E4M3 pool, on the tcgen05 tensor cores with specialised warps.
 //
 // A non-decode step attends the pool for its context only, and every new
 // token of a row sees the same context (mstar PR #1124 "Context / Sequence
@@ -28,7 +28,9 @@
 //     stage's tile is done; 16-byte cp.async, a warp instruction covering
 //     whole 128-byte blocks of rows.  Keys past the stripe end or on a
 //     rejected page are zero-filled, and each tile's valid-key mask is
-//     published for the softmax.
+//     published for the softmax.  E4M3 pools: the copy warps load each key
+//     row's codes and store it converted to bf16 (exact); the scores take
+//     k_descale and the output v_descale.
 // Tensor memory (256 columns, two CTAs an SM): S in two 32-column buffers,
 // O at column 64, P in two 16-column buffers after O.  O is normalised by the sum of the bf16-rounded
 // probabilities (an exact convex combination of the values); the LSE keeps
@@ -39,6 +41,7 @@
 // other wait, and the call reports CPATTN_DEV_TC_TIMEOUT.
 #include "common.cuh"
 #include "launch.h"
+#include "mma_sync.cuh"
 #include "split_combine.cuh"
 #include "tc05.cuh"
 
@@ -224,7 +227,11 @@ __device__ bool ws_merge_chunks_bulk(const PartialArgs& a, int p, int h, int s0,
   return true;
 }
 
-template <int D, int G>
+// F8: an E4M3 pool.  The copy warps read each key row's codes with 16-byte
+// loads, convert them exactly (every E4M3 value is a bf16 value) and store the
+// bf16 row into the ring in the MMA layout; the scores take k_descale and the
+// output v_descale.  Queries stay bf16.
+template <int D, int G, bool F8>
 __global__ void __launch_bounds__(kWThreads, 2) gqa_partial_ext_ws_kernel(const PartialArgs a) {
   using Lt = WsLayout<D>;
   constexpr int QB = kWRows / G;  // tokens per block
@@ -427,17 +434,56 @@ __global__ void __launch_bounds__(kWThreads, 2) gqa_partial_ext_ws_kernel(const 
           }
         }
         const uint32_t dst0 = ring + st * Lt::TILE;
-        // unrolled: the shuffles and addresses of all the warp's rows are
-        // formed before the copies issue (one chain a row is latency-bound)
-        const int kstep = is_k ? 2 * RPI : RPI;  // the K warps split the keys
+        if constexpr (F8) {
+          // lane: 16 codes (chunk c8 of a key row) -> two bf16 chunks; the
+          // warp's loads all go out before any conversion
+          constexpr int CH8 = D / 16, RPI8 = 32 / CH8;
+          constexpr int NK = kWTile / RPI8;  // keys a lane takes in the V warp (half that in a K warp)
+          const int ro8 = lane / CH8, c8 = lane - (lane / CH8) * CH8;
+          const int kstep8 = is_k ? 2 * RPI8 : RPI8;
+          uint4 codes[NK];
+#pragma unroll
+          for (int u = 0; u < NK; ++u) {
+            const int key = ro8 + (is_k ? khalf * RPI8 : 0) + u * kstep8;
+            const int row = __shfl_sync(0xffffffffu, myrow, key & 31);
+            codes[u] = make_uint4(0u, 0u, 0u, 0u);  // masked key: zero row
+            if (key < kWTile && row >= 0)
+              codes[u] = __ldg(reinterpret_cast<const uint4*>(pool + static_cast<int64_t>(row) * D + c8 * 16));
+          }
+#pragma unroll
+          for (int u = 0; u < NK; ++u) {
+            const int key = ro8 + (is_k ? khalf * RPI8 : 0) + u * kstep8;
+            if (key >= kWTile) continue;
+            const uint32_t w[4] = {codes[u].x, codes[u].y, codes[u].z, codes[u].w};
+            uint32_t bf[8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              bf[2 * q] = e4m3x2_to_bf16x2(w[q]);
+              bf[2 * q + 1] = e4m3x2_to_bf16x2(w[q] >> 16);
+            }
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const int cb = 2 * c8 + hh;  // bf16 chunk of the row (8 values)
+              *reinterpret_cast<uint4*>(base + (dst0 - tc05::smem_addr(base)) + (cb >> 3) * Lt::BLK +
+                                        tc05::sw128(key, cb & 7)) =
+                  make_uint4(bf[4 * hh], bf[4 * hh + 1], bf[4 * hh + 2], bf[4 * hh + 3]);
+            }
+          }
+          tc05::fence_smem_to_async();  // the tensor core reads what this lane wrote
+          ws_arrive(bar(b_full + st));
+        } else {
+          // unrolled: the shuffles and addresses of all the warp's rows are
+          // formed before the copies issue (one chain a row is latency-bound)
+          const int kstep = is_k ? 2 * RPI : RPI;  // the K warps split the keys
 #pragma unroll 8
-        for (int key = ro + khalf * RPI; key < kWTile; key += kstep) {
-          const int row = __shfl_sync(0xffffffffu, myrow, key);
-          const uint32_t dst = dst0 + coff + tc05::sw128(key, cc & 7);
-          if (row >= 0) ws_cp16(dst, pool + (static_cast<int64_t>(row) * D + cc * 8) * 2);
-          else ws_cp16_zero(dst, pool);  // masked key: zero row (finite scores, zero values)
+          for (int key = ro + khalf * RPI; key < kWTile; key += kstep) {
+            const int row = __shfl_sync(0xffffffffu, myrow, key);
+            const uint32_t dst = dst0 + coff + tc05::sw128(key, cc & 7);
+            if (row >= 0) ws_cp16(dst, pool + (static_cast<int64_t>(row) * D + cc * 8) * 2);
+            else ws_cp16_zero(dst, pool);  // masked key: zero row (finite scores, zero values)
+          }
+          ws_cp_arrive(bar(b_full + st));
         }
-        ws_cp_arrive(bar(b_full + st));
       }
       cp_async_wait<0>();  // nothing lands after the CTA moves on
       if (!alive) *s_abort = 1;
@@ -493,7 +539,7 @@ __global__ void __launch_bounds__(kWThreads, 2) gqa_partial_ext_ws_kernel(const 
     } else if (tid < kWRows) {
       // ================= softmax rows =================
       const uint32_t my_lane = tc05::taddr(tbase, warp * 32, 0);
-      const float sl = a.scale * kLog2e;
+      const float sl = a.scale * kLog2e * (F8 ? a.k_descale : 1.f);
       float m = -INFINITY, l = 0.f, lr = 0.f;  // running max (log2), fp32 sum, sum of bf16-rounded p
       for (int i = 0; i < ntiles; ++i) {
         const int bb = i & 1;
@@ -592,7 +638,7 @@ __global__ void __launch_bounds__(kWThreads, 2) gqa_partial_ext_ws_kernel(const 
       } else {
         // ---- row `tid`: normalised output and LSE, to o_part or the chunk workspace
         tc05::fence_after_sync();
-        const float inv = lr > 0.f ? 1.f / lr : 0.f;
+        const float inv = lr > 0.f ? (F8 ? a.v_descale : 1.f) / lr : 0.f;  // E4M3: value = code * v_descale
         const float lse = l == 0.f ? -INFINITY : (m + log2f(l)) * kLn2;
         float* dst = nullptr;
         float* ldst = nullptr;
@@ -651,7 +697,7 @@ __global__ void __launch_bounds__(kWThreads, 2) gqa_partial_ext_ws_kernel(const 
   }
 }
 
-template <int D, int G>
+template <int D, int G, bool F8>
 static int launch_ext_ws_t(const PartialArgs& a, cudaStream_t s, cudaError_t* err) {
   constexpr int QB = kWRows / G;
   const int page_slots = a.chunk / a.ps_l + 2;
@@ -660,7 +706,7 @@ static int launch_ext_ws_t(const PartialArgs& a, cudaStream_t s, cudaError_t* er
   // the copy warps exchange pool row indices as 32-bit values
   if (static_cast<int64_t>(a.P) * a.num_pages * a.num_kv_heads * a.ps_l >= (int64_t{1} << 31))
     return CPATTN_ERR_UNSUPPORTED_SHAPE;
-  auto kern = gqa_partial_ext_ws_kernel<D, G>;
+  auto kern = gqa_partial_ext_ws_kernel<D, G, F8>;
   static std::atomic<int> smem_set[64];
   *err = ensure_smem(kern, smem, smem_set);
   if (*err != cudaSuccess) return CPATTN_ERR_CUDA;
@@ -673,22 +719,31 @@ static int launch_ext_ws_t(const PartialArgs& a, cudaStream_t s, cudaError_t* er
   return *err == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
 }
 
-template <int D>
+template <int D, bool F8>
 static int ext_ws_dispatch_g(const PartialArgs& a, int G, cudaStream_t s, cudaError_t* err) {
   switch (G) {
-    case 1: return launch_ext_ws_t<D, 1>(a, s, err);
-    case 2: return launch_ext_ws_t<D, 2>(a, s, err);
-    case 4: return launch_ext_ws_t<D, 4>(a, s, err);
-    case 8: return launch_ext_ws_t<D, 8>(a, s, err);
-    case 16: return launch_ext_ws_t<D, 16>(a, s, err);
+    case 1: return launch_ext_ws_t<D, 1, F8>(a, s, err);
+    case 2: return launch_ext_ws_t<D, 2, F8>(a, s, err);
+    case 4: return launch_ext_ws_t<D, 4, F8>(a, s, err);
+    case 8: return launch_ext_ws_t<D, 8, F8>(a, s, err);
+    case 16: return launch_ext_ws_t<D, 16, F8>(a, s, err);
     default: return CPATTN_ERR_UNSUPPORTED_SHAPE;
   }
 }
 
+int launch_gqa_partial_ext(const PartialArgs& a, cudaStream_t s, cudaError_t* err) {
+  return launch_gqa_partial_ext_ws(a, s, err);
+}
+
 int launch_gqa_partial_ext_ws(const PartialArgs& a, cudaStream_t s, cudaError_t* err) {
   const int G = a.num_q_heads / a.num_kv_heads;
-  if (a.head_dim == 128) return ext_ws_dispatch_g<128>(a, G, s, err);
-  if (a.head_dim == 64) return ext_ws_dispatch_g<64>(a, G, s, err);
+  if (a.kv_fp8) {
+    if (a.head_dim == 128) return ext_ws_dispatch_g<128, true>(a, G, s, err);
+    if (a.head_dim == 64) return ext_ws_dispatch_g<64, true>(a, G, s, err);
+    return CPATTN_ERR_UNSUPPORTED_SHAPE;
+  }
+  if (a.head_dim == 128) return ext_ws_dispatch_g<128, false>(a, G, s, err);
+  if (a.head_dim == 64) return ext_ws_dispatch_g<64, false>(a, G, s, err);
   return CPATTN_ERR_UNSUPPORTED_SHAPE;
 }
 
