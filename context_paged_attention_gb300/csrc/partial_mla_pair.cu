@@ -94,7 +94,12 @@ constexpr int kUnitsK = kKB / kUBlk;  // units of a tile
 constexpr int kKUnits = 8;            // CTA 0: ring of units (2.7 tiles)
 constexpr uint32_t kKUnit = kUBlk * kBlk;
 static_assert(kKB % kUBlk == 0, "whole units a tile");
-constexpr int kVStages = 2;
+constexpr int kVStages = 2;           // CTA 1: tiles of value rows in flight
+constexpr int kVUB = 4;               // CTA 1: column blocks of a value unit (half a tile's columns, 32 KB)
+constexpr int kVUnits = kVB / kVUB;   // value units of a tile, each with its own barriers
+constexpr int kVRing = kVStages * kVUnits;
+constexpr uint32_t kVUnit = kVUB * kBlk;
+static_assert(kVB % kVUB == 0 && kVUB % 4 == 0, "whole units a tile, N = 256 a unit");
 constexpr int kLandRing = 16;        // CTA 1's "K tile landed on CTA 0" barriers
 constexpr int kPBuf = kHeads * 128;  // P of one tile: 128 rows x 64 bf16
 constexpr int kPBufs = 3;            // CTA 1: P buffers (the softmax runs up to 3 tiles ahead of P V)
@@ -131,9 +136,9 @@ enum : int {
   B_QEMPTY = B_QFULL + 1,           // CTA 0 [commit]: the item's last S done
   B_PEMPTY = B_QEMPTY + 1,          // x3 CTA 0 [multicast commit from CTA 1]: P V of the buffer done
   B_FINEMPTY = B_PEMPTY + kPBufs,   // CTA 0 [4 remote arrivals]: CTA 1 read the item's row scales
-  B_VFULL = B_FINEMPTY + 1,         // x2 CTA 1 [1 + bytes | 32]: V tile landed
-  B_VEMPTY = B_VFULL + kVStages,    // x2 CTA 1 [commit]: P V of the stage's tile done
-  B_PFULL = B_VEMPTY + kVStages,    // x3 CTA 1 [1 + bytes of CTA 0's copies]: P and rescale factors landed
+  B_VFULL = B_FINEMPTY + 1,         // x4 CTA 1 [1 + bytes | 32]: value unit landed
+  B_VEMPTY = B_VFULL + kVRing,      // x4 CTA 1 [commit]: the P V MMAs that read the unit done
+  B_PFULL = B_VEMPTY + kVRing,      // x3 CTA 1 [1 + bytes of CTA 0's copies]: P and rescale factors landed
   B_READY = B_PFULL + kPBufs,       // x2 CTA 1 [4 epilogue warps]: O rescaled, V rows fixed
   B_PVDONE = B_READY + 2,           // x2 CTA 1 [commit]: P V done
   B_FINFULL = B_PVDONE + 2,         // CTA 1 [128 remote arrivals]: the item's row scales and LSEs
@@ -741,7 +746,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc05::mbar_init(bar(B_PEMPTY + i), 1);
       tc05::mbar_init(bar(B_PFULL + i), 1);
     }
-    for (int i = 0; i < kVStages; ++i) {
+    for (int i = 0; i < kVRing; ++i) {
       tc05::mbar_init(bar(B_VFULL + i), load_arrivals);
       tc05::mbar_init(bar(B_VEMPTY + i), 1);
     }
@@ -906,8 +911,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       run(std::integral_constant<int, kUnitsK>{}, std::integral_constant<int, kUBlk>{},
           std::integral_constant<int, kKUnits>{}, std::integral_constant<uint32_t, kKUnit>{}, B_KFULL, B_KEMPTY, &tmap);
     else
-      run(std::integral_constant<int, 1>{}, std::integral_constant<int, kVB>{}, std::integral_constant<int, kVStages>{},
-          std::integral_constant<uint32_t, kVStage>{}, B_VFULL, B_VEMPTY, &tmap_v);
+      run(std::integral_constant<int, kVUnits>{}, std::integral_constant<int, kVUB>{},
+          std::integral_constant<int, kVRing>{}, std::integral_constant<uint32_t, kVUnit>{}, B_VFULL, B_VEMPTY, &tmap_v);
   } else if (rank == 0 && warp == kWMma) {
     // ---- CTA 0, MMA warp (one elected lane issues): S = Q K^T of each tile, Q from tensor memory
     const uint32_t id_s = tc05::idesc_bf16(128, kTile, false, false);
@@ -997,20 +1002,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc05::fence_after_sync();
       if (it.t != prev_t) {
-        const uint4* src = reinterpret_cast<const uint4*>(
-            static_cast<const uint8_t*>(a.q) + (static_cast<int64_t>(it.t) * a.num_q_heads + tid) * (kDqk * 2));
+        // coalesced: a lane loads 16-byte chunk (lane & 7) of rows 4 i + lane / 8
+        // of its warp's 32 (four whole 128-byte lines an instruction), a
+        // 64-value column block at a time through the warp's P staging slot,
+        // where thread r then reads its row's block for tcgen05.st
+        if (lane == 0) tc05::bulk_wait_read();  // the slot's last P copy has read it
+        __syncwarp();
+        const uint8_t* qrows =
+            static_cast<const uint8_t*>(a.q) + (static_cast<int64_t>(it.t) * a.num_q_heads + warp * 32) * (kDqk * 2);
+        uint8_t* slot = base + OFF_PSTAGE + warp * kPSlot;
+        const int lr8 = lane >> 3, lc = lane & 7;
+        constexpr int kGrp = 3;  // column blocks whose loads are in flight together
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {  // 36 loads in flight a thread, two rounds
-          uint4 u[kDqk / 16];
+        for (int g0 = 0; g0 < kKB; g0 += kGrp) {
+          uint4 u[kGrp][8];
 #pragma unroll
-          for (int i = 0; i < kDqk / 16; ++i) u[i] = __ldg(src + half * (kDqk / 16) + i);
+          for (int b = 0; b < kGrp; ++b)
 #pragma unroll
-          for (int cb = 0; cb < kDqk / 64; ++cb) {
-            const uint32_t w[16] = {u[4 * cb].x,     u[4 * cb].y,     u[4 * cb].z,     u[4 * cb].w,
-                                    u[4 * cb + 1].x, u[4 * cb + 1].y, u[4 * cb + 1].z, u[4 * cb + 1].w,
-                                    u[4 * cb + 2].x, u[4 * cb + 2].y, u[4 * cb + 2].z, u[4 * cb + 2].w,
-                                    u[4 * cb + 3].x, u[4 * cb + 3].y, u[4 * cb + 3].z, u[4 * cb + 3].w};
-            tc05::st_x16_u32(my_lane + kQCol + half * (kDqk / 4) + cb * 16, w);
+            for (int i = 0; i < 8; ++i)
+              u[b][i] = __ldg(reinterpret_cast<const uint4*>(qrows + (4 * i + lr8) * (kDqk * 2) + (g0 + b) * 128 + lc * 16));
+#pragma unroll
+          for (int b = 0; b < kGrp; ++b) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) *reinterpret_cast<uint4*>(slot + tc05::sw128(4 * i + lr8, lc)) = u[b][i];
+            __syncwarp();
+            uint32_t w[32];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const uint4 v = *reinterpret_cast<const uint4*>(slot + tc05::sw128(lane, c));
+              w[4 * c] = v.x;
+              w[4 * c + 1] = v.y;
+              w[4 * c + 2] = v.z;
+              w[4 * c + 3] = v.w;
+            }
+            __syncwarp();  // the slot is rewritten for the next block
+            tc05::st_x16_u32(my_lane + kQCol + (g0 + b) * 32, *reinterpret_cast<uint32_t(*)[16]>(w));
+            tc05::st_x16_u32(my_lane + kQCol + (g0 + b) * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(w + 16));
           }
         }
         tc05::st_wait();
@@ -1142,26 +1169,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!item(k, it)) break;
       const int nt = ntiles(it);
       for (int j = 0; j < nt; ++j, ++g) {
-        const int pbuf = g & 1, vs = g % kVStages;
+        const int pbuf = g & 1;
         ok = wwait<false>(bar(B_READY + pbuf), (g >> 1) & 1, abort_flag);
         if (!ok) break;
+        bool fail = false;
         if (tc05::elect_one()) {
-          if constexpr (!kTma) tc05::fence_smem_to_async();
           tc05::fence_after_sync();
           const uint64_t dp = tc05::desc_k128(sb + OFF_P + (g % kPBufs) * kPBuf);
-          const uint64_t dv = tc05::desc_mn128(sb + vs * kVStage, kBlk);
+          // value unit h (columns 256 h ..) of the tile: its MMAs go as soon as
+          // it landed, and a commit frees its ring slot
 #pragma unroll
-          for (int ks = 0; ks < kTile / 16; ++ks) {
-            const uint64_t ad = tc05::desc_add(dp, ks * 32);
-            const uint64_t bd = tc05::desc_add(dv, ks * 16 * 128);
-            tc05::mma_ss(tbase, ad, bd, id_pv, j > 0 || ks > 0);
-            tc05::mma_ss(tbase + 256, ad, tc05::desc_add(bd, 4 * kBlk), id_pv, j > 0 || ks > 0);
+          for (int h = 0; h < kVUnits; ++h) {
+            const int n = g * kVUnits + h, vq = n % kVRing;
+            if (!pwait<false>(bar(B_VFULL + vq), (n / kVRing) & 1, abort_flag)) {
+              fail = true;
+              break;
+            }
+            if constexpr (!kTma) tc05::fence_smem_to_async();  // the unit came through cp.async
+            tc05::fence_after_sync();
+            const uint64_t dv = tc05::desc_mn128(sb + vq * kVUnit, kBlk);
+#pragma unroll
+            for (int ks = 0; ks < kTile / 16; ++ks) {
+              const uint64_t ad = tc05::desc_add(dp, ks * 32);
+              const uint64_t bd = tc05::desc_add(dv, ks * 16 * 128);
+#pragma unroll
+              for (int c = 0; c < kVUB / 4; ++c)
+                tc05::mma_ss(tbase + (h * kVUB + 4 * c) * 64, ad, tc05::desc_add(bd, 4 * c * kBlk), id_pv,
+                             j > 0 || ks > 0);
+            }
+            tc05::commit(bar(B_VEMPTY + vq));
           }
-          tc05::commit(bar(B_PVDONE + pbuf));
-          tc05::commit(bar(B_VEMPTY + vs));
-          tc05::commit_multicast(bar(B_PEMPTY + g % kPBufs), 0x1);
+          if (!fail) {
+            tc05::commit(bar(B_PVDONE + pbuf));
+            tc05::commit_multicast(bar(B_PEMPTY + g % kPBufs), 0x1);
+          }
         }
-        __syncwarp();
+        ok = __ballot_sync(0xffffffffu, fail) == 0u;
+        if (!ok) break;
       }
     }
     if (!ok) raise_abort();
@@ -1471,10 +1515,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint64_t vmask = tile_mask_from<kGroup>(a, it, j, words, lane);
         tc05::fence_smem_to_async();  // the tensor core reads P next
         const float alpha = alpha_s[pq * kHeads + tid];
-        ok = wwait<false>(bar(B_VFULL + vs), (g / kVStages) & 1, abort_flag);
-        if (!ok) break;
         if (kTma && vmask != ~0ull) {
-          // value rows of keys without data (past the item, rejected pages, runs not copied): zero
+          // value rows of keys without data (past the item, rejected pages, runs
+          // not copied): zero, once the tile's units landed (they sit together,
+          // stage vs of the ring); the MMA warp waits for them by itself
+          for (int h = 0; h < kVUnits && ok; ++h) {
+            const int n = g * kVUnits + h;
+            ok = wwait<false>(bar(B_VFULL + n % kVRing), (n / kVRing) & 1, abort_flag);
+          }
+          if (!ok) break;
           uint8_t* st = base + vs * kVStage;
           for (int idx = tid; idx < kTile * kVB * 8; idx += 128) {
             const int key = idx / (kVB * 8);
@@ -1599,44 +1648,93 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 // Grouped plans: the exact merge of the pieces of each cut token (and the
 // extra partial, when given) into its final output and LSE.  Block (t, rb)
-// takes rows 16 rb .. 16 rb + 15 of token t; the token's record (slot of its
-// first piece, pieces) comes from the partial kernel, which this grid follows
-// on the stream (it may start early and waits here for that grid to finish).
-constexpr int kMergeRows = 16;
+// takes rows 4 rb .. 4 rb + 3 of token t, a warp a row: lane e holds the
+// weight of piece e (32 at a time), lane l accumulates 16-byte columns
+// l + 32 i of the row, with the loads of four pieces in flight.  The
+// token's record (slot of its first piece, pieces) comes from the partial
+// kernel, which this grid follows on the stream (it may start early and
+// waits here for that grid to finish).
+constexpr int kMergeRows = 4;
 __global__ void __launch_bounds__(128) mla_merge_pieces_kernel(const PartialArgs a, int ws_slots) {
   pdl_wait();
-  __shared__ float scr[2048];
-  const int t = blockIdx.x, r0 = blockIdx.y * kMergeRows;
+  const int t = blockIdx.x, lane = threadIdx.x & 31;
+  const int r = blockIdx.y * kMergeRows + (threadIdx.x >> 5);
   const int32_t* rec = a.ws_cnt + static_cast<int64_t>(a.num_tokens) * a.P;
   const int npieces = __ldcg(rec + 2 * t + 1);
-  const int64_t sl0 = __ldcg(rec + 2 * t), trow = static_cast<int64_t>(t) * kHeads + r0;
+  const int64_t sl0 = __ldcg(rec + 2 * t), trow = static_cast<int64_t>(t) * kHeads + r;
   // written whole by the partial kernel; or a record that kernel did not
   // write (it gave up on a wait): never read outside the slots
   if (npieces <= 1 || sl0 < 0 || sl0 + npieces > ws_slots) return;
   const bool has_e = a.extra_lse != nullptr;
   const int E = npieces + (has_e ? 1 : 0);
-  merge_rows<kMergeUnroll, CtaGroup>(
-      kMergeRows, E, kDv,
-      [&](int r, int e) {
-        return e < npieces ? __ldcg(a.ws_lse + (sl0 + e) * kHeads + r0 + r) : __ldg(a.extra_lse + trow + r);
-      },
-      [&](int r, int e) {
-        return e < npieces ? a.ws_o + ((sl0 + e) * kHeads + r0 + r) * kDv : a.extra_o + (trow + r) * kDv;
-      },
-      [&](int r, int d, float4 v) {
-        const int64_t oi = (trow + r) * kDv + d;
-        if (a.out_bf16) {
-          __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
-          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + oi) =
-              make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
-        } else {
-          *reinterpret_cast<float4*>(static_cast<float*>(a.out) + oi) = v;
+  auto lse_of = [&](int e) {
+    return e < npieces ? __ldcg(a.ws_lse + (sl0 + e) * kHeads + r) : __ldg(a.extra_lse + trow);
+  };
+  auto row_of = [&](int e) {
+    return reinterpret_cast<const float4*>(e < npieces ? a.ws_o + ((sl0 + e) * kHeads + r) * kDv
+                                                       : a.extra_o + trow * kDv);
+  };
+  float mx = -INFINITY;
+  for (int e = lane; e < E; e += 32) mx = fmaxf(mx, lse_of(e));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float sum = 0.f;
+  for (int e = lane; e < E; e += 32) {
+    const float l = lse_of(e);
+    sum += (mx == -INFINITY || l == -INFINITY) ? 0.f : expf(l - mx);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const float inv = sum > 0.f ? 1.f / sum : 0.f;
+  float4 acc[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c0 = 0; c0 < E; c0 += 32) {
+    // lane e: the weight of piece c0 + e (0 for an empty one, whose row is never read)
+    float w_l = 0.f;
+    if (c0 + lane < E) {
+      const float l = lse_of(c0 + lane);
+      w_l = (sum > 0.f && l != -INFINITY) ? expf(l - mx) * inv : 0.f;
+    }
+    const int ne = min(32, E - c0);
+    for (int e0 = 0; e0 < ne; e0 += 4) {
+      float w[4];
+      float4 v[4][4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        w[b] = __shfl_sync(0xffffffffu, w_l, (e0 + b) & 31);
+        if (e0 + b >= ne) w[b] = 0.f;
+        if (w[b] != 0.f) {
+          const float4* src = row_of(c0 + e0 + b);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) v[b][i] = __ldcg(src + lane + 32 * i);
         }
-      },
-      [&](int r, float lv) {
-        if (a.lse_out != nullptr) a.lse_out[trow + r] = lv;
-      },
-      scr, 2048);
+      }
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        if (w[b] == 0.f) continue;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[i].x = fmaf(w[b], v[b][i].x, acc[i].x);
+          acc[i].y = fmaf(w[b], v[b][i].y, acc[i].y);
+          acc[i].z = fmaf(w[b], v[b][i].z, acc[i].z);
+          acc[i].w = fmaf(w[b], v[b][i].w, acc[i].w);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int64_t oi = trow * kDv + (lane + 32 * i) * 4;
+    if (a.out_bf16) {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(acc[i].x, acc[i].y), hi = __floats2bfloat162_rn(acc[i].z, acc[i].w);
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + oi) =
+          make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+    } else {
+      *reinterpret_cast<float4*>(static_cast<float*>(a.out) + oi) = acc[i];
+    }
+  }
+  if (lane == 0 && a.lse_out != nullptr) a.lse_out[trow] = sum > 0.f ? mx + logf(sum) : -INFINITY;
 }
 
 namespace {
@@ -1760,7 +1858,7 @@ int launch_mla_partial(const PartialArgs& a, cudaStream_t s, cudaError_t* err) {
   const int ws_slots = mla_ws_slots(a.P, a.interleave, a.num_tokens, a.max_kv_len, 1);
   const bool group = a.fused && a.page_size == kTile && a.num_tokens <= kGroupMaxTokens &&
                      encode_pages(&map, a.pool_k, a.P, rows_pp, a.ps_l, kUBlk) &&
-                     encode_pages(&map_v, a.pool_k, a.P, rows_pp, a.ps_l, kVB) &&
+                     encode_pages(&map_v, a.pool_k, a.P, rows_pp, a.ps_l, kVUB) &&
                      encode_out(&map_out, a.out, static_cast<uint64_t>(a.num_tokens) * kHeads, a.out_bf16 != 0) &&
                      (ws_slots == 0 || encode_out(&map_ws, a.ws_o, static_cast<uint64_t>(ws_slots) * kHeads, false));
   // per-partner tiles: TMA when every 64-key tile is a whole number of page
