@@ -95,18 +95,27 @@ constexpr int kKUnits = 8;            // CTA 0: ring of units (2.7 tiles)
 constexpr uint32_t kKUnit = kUBlk * kBlk;
 static_assert(kKB % kUBlk == 0, "whole units a tile");
 constexpr int kVStages = 2;           // CTA 1: tiles of value rows in flight
-constexpr int kVUB = 4;               // CTA 1: column blocks of a value unit (half a tile's columns, 32 KB)
-constexpr int kVUnits = kVB / kVUB;   // value units of a tile, each with its own barriers
+constexpr int kVUB = kVB;             // CTA 1: column blocks of a value unit (a whole tile's, 64 KB:
+                                      // measured faster than two 32 KB halves with their own barriers)
+constexpr int kVUnits = kVB / kVUB;   // value units of a tile
 constexpr int kVRing = kVStages * kVUnits;
 constexpr uint32_t kVUnit = kVUB * kBlk;
 static_assert(kVB % kVUB == 0 && kVUB % 4 == 0, "whole units a tile, N = 256 a unit");
 constexpr int kLandRing = 16;        // CTA 1's "K tile landed on CTA 0" barriers
 constexpr int kPBuf = kHeads * 128;  // P of one tile: 128 rows x 64 bf16
 constexpr int kPBufs = 3;            // CTA 1: P buffers (the softmax runs up to 3 tiles ahead of P V)
+// CTA 1: barriers a tile for "O ready for the tile's P V" and "P V done".  The
+// epilogue warps wait for P V only now and then (a rescale, an item's end),
+// and may run up to kPBufs tiles ahead of the MMAs (their one per-tile wait
+// is for P, which needs the P V kPBufs tiles back done), so a parity wait is
+// unambiguous only with a ring of more than kPBufs barriers.
+constexpr int kTileRing = 4;
+static_assert(kTileRing > kPBufs, "parity waits on the tile ring");
 constexpr int kThreads = 192;
 constexpr int kWMma = 4;
 constexpr int kWLoad = 5;
 constexpr int kMinChunkTiles = 16;   // cut pieces hold at least 1024 keys
+constexpr int kItemCostTiles = 16;   // grouped plans: what starting a token costs a cluster, in tiles
 constexpr int kSortMax = 512;        // stripes ranked in shared memory
 constexpr int kItemsBytes = 4096;    // per-cluster item list (stripes), or the token tables (grouped)
 constexpr int kGroupMaxTokens = kItemsBytes / 8 - 1;  // grouped plans: pre[T + 1] and sbase[T] ints
@@ -139,9 +148,9 @@ enum : int {
   B_VFULL = B_FINEMPTY + 1,         // x4 CTA 1 [1 + bytes | 32]: value unit landed
   B_VEMPTY = B_VFULL + kVRing,      // x4 CTA 1 [commit]: the P V MMAs that read the unit done
   B_PFULL = B_VEMPTY + kVRing,      // x3 CTA 1 [1 + bytes of CTA 0's copies]: P and rescale factors landed
-  B_READY = B_PFULL + kPBufs,       // x2 CTA 1 [4 epilogue warps]: O rescaled, V rows fixed
-  B_PVDONE = B_READY + 2,           // x2 CTA 1 [commit]: P V done
-  B_FINFULL = B_PVDONE + 2,         // CTA 1 [128 remote arrivals]: the item's row scales and LSEs
+  B_READY = B_PFULL + kPBufs,       // x4 CTA 1 [4 epilogue warps]: O rescaled, V rows fixed
+  B_PVDONE = B_READY + kTileRing,   // x4 CTA 1 [commit]: P V done
+  B_FINFULL = B_PVDONE + kTileRing,         // CTA 1 [1 + bytes of CTA 0's asynchronous stores]: the item's row scales and LSEs
   B_DRAIN = B_FINFULL + 1,          // both [commit]: the MMA thread's last MMAs done
   B_EPSYNC = B_DRAIN + 1,           // CTA 1 [128 epilogue threads]: their group barrier (merges)
   B_KLAND = B_EPSYNC + 1,           // x16 CTA 1 [1 remote arrival]: the tile's rows reached CTA 0 (so they sit in L2)
@@ -431,23 +440,28 @@ __device__ __forceinline__ int tile_cluster(int64_t x, int64_t W, int C) {
   return static_cast<int>(((x + 1) * C + W - 1) / W) - 1;
 }
 
-// The grouped plan (all threads; both CTAs compute the same one): pre[t] =
-// first tile of token t in the sequence of all tokens' pages, pre[T] = W;
-// sbase[t] = first workspace slot of a cut token (the pieces of cut tokens
-// numbered in token order).  The W tiles go to Ce = min(C, ceil(W / 16))
-// clusters in equal contiguous ranges, so no range is shorter than 16 tiles
-// (clusters from Ce on get none).  misc[3] = W, misc[4] = Ce, misc[2] = first
-// token of cluster c.
+// The grouped plan (all threads; both CTAs compute the same one).  Token t
+// with n > 0 pages spans kItemCostTiles + n positions of a sequence of all
+// tokens -- a token's start (its Q load, its output store) costs a cluster
+// about as much as that many tiles, so a cluster whose range starts a token
+// inside it gets that many fewer pages -- and its pages sit at the last n of
+// them.  pre[t] = first position of token t, pre[T] = W; sbase[t] = first
+// workspace slot of a cut token (the pieces of cut tokens numbered in token
+// order).  The W positions go to Ce = min(C, ceil(pages / 16)) clusters in
+// equal contiguous ranges (clusters from Ce on get none).  misc[3] = W,
+// misc[4] = Ce, misc[2] = first token of cluster c.
 __device__ void mla_plan_group(const PartialArgs& a, int C, int c, int* pre, int* sbase, int* misc) {
   const int T = a.num_tokens;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (warp == 0) {
     const int per = (T + 31) / 32;
     const int i0 = min(T, lane * per), i1 = min(T, i0 + per);
-    int sp = 0;
+    int sp = 0, sr = 0;  // positions, pages
     for (int t = i0; t < i1; ++t) {
       int b;
-      sp += (token_len(a, t, &b, true) + kTile - 1) / kTile;
+      const int n = (token_len(a, t, &b, true) + kTile - 1) / kTile;
+      sr += n;
+      sp += n > 0 ? n + kItemCostTiles : 0;
     }
     int ip = sp;
 #pragma unroll
@@ -459,21 +473,25 @@ __device__ void mla_plan_group(const PartialArgs& a, int C, int c, int* pre, int
     for (int t = i0; t < i1; ++t) {
       int b;
       pre[t] = ep;
-      ep += (token_len(a, t, &b, false) + kTile - 1) / kTile;
+      const int n = (token_len(a, t, &b, false) + kTile - 1) / kTile;
+      ep += n > 0 ? n + kItemCostTiles : 0;
     }
     if (lane == 31) pre[T] = ip;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sr += __shfl_xor_sync(0xffffffffu, sr, o);
     __syncwarp();
     // workspace slots of cut tokens (pieces in token order)
     const int64_t W = pre[T];
     {
-      const int64_t cap = (W + kMinChunkTiles - 1) / kMinChunkTiles;
+      const int64_t cap = (static_cast<int64_t>(sr) + kMinChunkTiles - 1) / kMinChunkTiles;
       if (cap < C) C = static_cast<int>(cap);
     }
     if (C < 1) C = 1;
     int ss = 0;
     for (int t = i0; t < i1; ++t) {
       const int n = pre[t + 1] - pre[t];
-      const int pcs = n > 0 && W > 0 ? tile_cluster(pre[t + 1] - 1, W, C) - tile_cluster(pre[t], W, C) + 1 : 1;
+      const int pcs =
+          n > 0 && W > 0 ? tile_cluster(pre[t + 1] - 1, W, C) - tile_cluster(pre[t] + kItemCostTiles, W, C) + 1 : 1;
       ss += pcs > 1 ? pcs : 0;
     }
     int is = ss;
@@ -485,7 +503,8 @@ __device__ void mla_plan_group(const PartialArgs& a, int C, int c, int* pre, int
     int es = is - ss;
     for (int t = i0; t < i1; ++t) {
       const int n = pre[t + 1] - pre[t];
-      const int pcs = n > 0 && W > 0 ? tile_cluster(pre[t + 1] - 1, W, C) - tile_cluster(pre[t], W, C) + 1 : 1;
+      const int pcs =
+          n > 0 && W > 0 ? tile_cluster(pre[t + 1] - 1, W, C) - tile_cluster(pre[t] + kItemCostTiles, W, C) + 1 : 1;
       sbase[t] = es;
       es += pcs > 1 ? pcs : 0;
     }
@@ -507,7 +526,8 @@ __device__ void mla_plan_group(const PartialArgs& a, int C, int c, int* pre, int
 }
 
 // Item k of cluster c in the grouped plan: token t_first + k, the part of its
-// pages inside the cluster's range (k_begin / k_end in positions of the row).
+// pages inside the cluster's range (k_begin / k_end in positions of the row;
+// none when the range holds only the token's start cost).
 __device__ __forceinline__ bool get_item_group(const PartialArgs& a, int k, int C, int c, const int* pre,
                                                const int* sbase, int64_t W, int t_first, MlaItem& it) {
   const int t = t_first + k;
@@ -517,15 +537,19 @@ __device__ __forceinline__ bool get_item_group(const PartialArgs& a, int k, int 
   int b;
   const int L = token_len(a, t, &b, false);
   const int64_t pt0 = pre[t], pt1 = pre[t + 1];
-  const int64_t lo = pt0 > s0 ? pt0 : s0, hi = pt1 < s1 ? pt1 : s1;
+  const int64_t f0 = pt1 > pt0 ? pt0 + kItemCostTiles : pt0;  // position of the token's first page
+  const int64_t lo = f0 > s0 ? f0 : s0, hi = pt1 < s1 ? pt1 : s1;
   it.t = t;
   it.p = 0;
   it.b = b;
-  it.k_begin = static_cast<int>(lo - pre[t]) * kTile;
-  it.k_end = min(L, static_cast<int>(hi - pre[t]) * kTile);
-  if (hi <= lo) it.k_end = it.k_begin;  // a token of no pages: nothing here (written by the zero pass)
+  it.k_begin = 0;
+  it.k_end = 0;
+  if (hi > lo) {  // else: a token of no pages (written by the zero pass), or only its start cost here
+    it.k_begin = static_cast<int>(lo - f0) * kTile;
+    it.k_end = min(L, static_cast<int>(hi - f0) * kTile);
+  }
   const int n = pre[t + 1] - pre[t];
-  const int c0 = n > 0 ? tile_cluster(pre[t], W, C) : c;
+  const int c0 = n > 0 ? tile_cluster(f0, W, C) : c;
   const int pcs = n > 0 ? tile_cluster(pre[t + 1] - 1, W, C) - c0 + 1 : 1;
   it.npieces = pcs;
   it.slot_base = sbase[t];
@@ -739,6 +763,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       tc05::mbar_init(bar(B_SFULL + i), 1);
       tc05::mbar_init(bar(B_SEMPTY + i), 4);
+    }
+    for (int i = 0; i < kTileRing; ++i) {
       tc05::mbar_init(bar(B_READY + i), 4);
       tc05::mbar_init(bar(B_PVDONE + i), 1);
     }
@@ -753,7 +779,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc05::mbar_init(bar(B_QFULL), 4);
     tc05::mbar_init(bar(B_QEMPTY), 1);
     tc05::mbar_init(bar(B_FINEMPTY), 4);
-    tc05::mbar_init(bar(B_FINFULL), kHeads);
+    tc05::mbar_init(bar(B_FINFULL), 1);
     tc05::mbar_init(bar(B_DRAIN), 1);
     tc05::mbar_init(bar(B_EPSYNC), kHeads);
     tc05::mbar_init(bar(B_MERGE), 1);
@@ -786,7 +812,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ---- loader (both CTAs).  CTA 0: whole latent rows in units of kUBlk
     // column blocks into a ring of kKUnits units (a unit is free again once
     // the S MMAs that read it are done).  CTA 1: the value part of the same
-    // tiles into a 2-stage ring of whole tiles.  The ring constants are
+    // tiles into a ring of kVRing units of kVUB column blocks.  The ring constants are
     // compile-time per role: this warp shares its scheduler with a softmax
     // warp, so every instruction it issues per unit counts.
     auto run = [&](auto kU_, auto kUB_, auto kR_, auto kBytes_, int b_full, int b_empty, const CUtensorMap* map4) {
@@ -1020,9 +1046,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int b = 0; b < kGrp; ++b)
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              u[b][i] = __ldg(reinterpret_cast<const uint4*>(qrows + (4 * i + lr8) * (kDqk * 2) + (g0 + b) * 128 + lc * 16));
+              if (g0 + b < kKB)
+                u[b][i] =
+                    __ldg(reinterpret_cast<const uint4*>(qrows + (4 * i + lr8) * (kDqk * 2) + (g0 + b) * 128 + lc * 16));
 #pragma unroll
           for (int b = 0; b < kGrp; ++b) {
+            if (g0 + b >= kKB) break;
 #pragma unroll
             for (int i = 0; i < 8; ++i) *reinterpret_cast<uint4*>(slot + tc05::sw128(4 * i + lr8, lc)) = u[b][i];
             __syncwarp();
@@ -1046,19 +1075,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc05::fence_before_sync();
       __syncwarp();
       if (lane == 0) arrive_local(bar(B_QFULL));
+      // the next item's Q row goes into L2 some eight tiles before this item ends
+      int next_t = -1;
       {
-        // the next item's Q row into L2 while this one runs
         MlaItem nx;
-        if (item(k + 1, nx) && nx.t >= 0 && nx.t != it.t) {
-          const char* q2 = static_cast<const char*>(a.q) + (static_cast<int64_t>(nx.t) * a.num_q_heads + tid) * (kDqk * 2);
-#pragma unroll
-          for (int ln = 0; ln < (kDqk * 2) / 128; ++ln) asm volatile("prefetch.global.L2 [%0];\n" ::"l"(q2 + ln * 128));
-        }
+        if (item(k + 1, nx) && nx.t >= 0 && nx.t != it.t) next_t = nx.t;
       }
+      const int j_pf = nt > 8 ? nt - 8 : 0;
       float m = -INFINITY, l = 0.f, lr = 0.f;
       MaskWords next_words = mask_words(it, 0, pb0, npg);
       for (int j = 0; j < nt; ++j, ++g) {
         const int sbuf = g & 1;
+        if (j == j_pf && next_t >= 0) {
+          const char* q2 = static_cast<const char*>(a.q) + (static_cast<int64_t>(next_t) * a.num_q_heads + tid) * (kDqk * 2);
+#pragma unroll
+          for (int ln = 0; ln < (kDqk * 2) / 128; ++ln) asm volatile("prefetch.global.L2 [%0];\n" ::"l"(q2 + ln * 128));
+        }
         const MaskWords words = next_words;
         if (j + 1 < nt) next_words = mask_words(it, j + 1, pb0, npg);
         ok = wwait<false>(bar(B_SFULL + sbuf), (g >> 1) & 1, abort_flag);
@@ -1153,8 +1185,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!ok) break;
       const float inv = lr > 0.f ? 1.f / lr : 0.f;
       const float lse = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
-      tc05::st_cluster_v2f32(r_fin + tid * 8, inv, lse);
-      tc05::mbar_arrive_remote(r_finfull);
+      // an asynchronous store counted in bytes on CTA 1's barrier: no
+      // cluster-scope release, which would wait for this CTA's copies in flight
+      tc05::st_async_v2(r_fin + tid * 8, __float_as_uint(inv), __float_as_uint(lse), r_finfull);
       ++qi;
     }
     if (!ok) raise_abort();
@@ -1169,15 +1202,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!item(k, it)) break;
       const int nt = ntiles(it);
       for (int j = 0; j < nt; ++j, ++g) {
-        const int pbuf = g & 1;
-        ok = wwait<false>(bar(B_READY + pbuf), (g >> 1) & 1, abort_flag);
+        const int pbuf = g % kTileRing;
+        ok = wwait<false>(bar(B_READY + pbuf), (g / kTileRing) & 1, abort_flag);
         if (!ok) break;
         bool fail = false;
         if (tc05::elect_one()) {
           tc05::fence_after_sync();
           const uint64_t dp = tc05::desc_k128(sb + OFF_P + (g % kPBufs) * kPBuf);
-          // value unit h (columns 256 h ..) of the tile: its MMAs go as soon as
-          // it landed, and a commit frees its ring slot
+          // value unit h (columns 64 kVUB h ..) of the tile: its MMAs go as
+          // soon as it landed, and a commit frees its ring slot
 #pragma unroll
           for (int h = 0; h < kVUnits; ++h) {
             const int n = g * kVUnits + h, vq = n % kVRing;
@@ -1275,6 +1308,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) wds[e] = __float_as_uint(v[e]);
         }
+        if (ch + 1 < nch) fetch(ch + 1);  // the values are in wds: the next chunk's loads go now
 #pragma unroll
         for (int q = 0; q < 8; ++q)
           *reinterpret_cast<uint4*>(buf + tc05::sw128(tid, q)) =
@@ -1288,11 +1322,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc05::tma_store_2d(map, tc05::smem_addr(buf), ch * cols, y0);
             tc05::bulk_commit();
           }
-          if (ch + 1 < nch) fetch(ch + 1);
           continue;
         }
         EpGroup::sync();
-        if (ch + 1 < nch) fetch(ch + 1);
         // all eight loads first: the stores could alias them for all the
         // compiler knows, so interleaving would wait out each load in turn
         uint4 vals[8];
@@ -1504,7 +1536,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int pb0 = __ldg(a.page_indptr + it.b), npg = __ldg(a.page_indptr + it.b + 1) - pb0;
       MaskWords next_words = mask_words(it, 0, pb0, npg);
       for (int j = 0; j < nt; ++j, ++g) {
-        const int pbuf = g & 1, vs = g % kVStages;
+        const int pbuf = g % kTileRing, vs = g % kVStages;
         const MaskWords words = next_words;
         if (j + 1 < nt) next_words = mask_words(it, j + 1, pb0, npg);
         // P and the rescale factors arrive by bulk copies from CTA 0 (bytes counted)
@@ -1518,7 +1550,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (kTma && vmask != ~0ull) {
           // value rows of keys without data (past the item, rejected pages, runs
           // not copied): zero, once the tile's units landed (they sit together,
-          // stage vs of the ring); the MMA warp waits for them by itself
+          // stage vs of the ring); the MMA warp waits for them by itself.  This
+          // warp may be ahead of the MMAs: the P V two tiles back first (its
+          // units then landed), so that the parity waits below are unambiguous.
+          if (g >= kVStages)
+            ok = wwait<false>(bar(B_PVDONE + (g - kVStages) % kTileRing), ((g - kVStages) / kTileRing) & 1,
+                              abort_flag);
           for (int h = 0; h < kVUnits && ok; ++h) {
             const int n = g * kVUnits + h;
             ok = wwait<false>(bar(B_VFULL + n % kVRing), (n / kVRing) & 1, abort_flag);
@@ -1535,7 +1572,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
           // O (all 512 columns) of the rows whose max rose, after the previous P V
-          ok = wwait<false>(bar(B_PVDONE + ((g - 1) & 1)), ((g - 1) >> 1) & 1, abort_flag);
+          ok = wwait<false>(bar(B_PVDONE + (g - 1) % kTileRing), ((g - 1) / kTileRing) & 1, abort_flag);
           if (!ok) break;
           tc05::fence_after_sync();
 #pragma unroll 1
@@ -1560,12 +1597,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // ---- epilogue of the item: O / sum -> o_part (whole stripe) or the piece's workspace slot
+      if (tid == 0) tc05::mbar_arrive_expect_tx(bar(B_FINFULL), kHeads * 8);
       ok = wwait<true>(bar(B_FINFULL), fi & 1, abort_flag);
       if (!ok) break;
       const float2 f = fin_s[tid];
       __syncwarp();
       if (lane == 0) tc05::mbar_arrive_remote(r_finempty);
-      ok = wwait<false>(bar(B_PVDONE + ((g - 1) & 1)), ((g - 1) >> 1) & 1, abort_flag);
+      ok = wwait<false>(bar(B_PVDONE + (g - 1) % kTileRing), ((g - 1) / kTileRing) & 1, abort_flag);
       if (!ok) break;
       tc05::fence_after_sync();
       ++fi;
