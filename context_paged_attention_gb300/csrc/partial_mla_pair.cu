@@ -16,23 +16,27 @@
 //   * CTA 0 (scores) holds Q in tensor memory as the A operand of S (columns
 //     128..415, two bf16 a column) and two 64-column S buffers (0 and 64).
 //     Warp 5 streams 64-key tiles of whole latent rows (9 column blocks of
-//     64 values, 128-byte swizzle) into a 2-stage ring by TMA; warp 4 issues
-//     the 36 S MMAs of a tile (N = 64 keys, A from tensor memory, so only K
-//     is read from shared memory) as soon as the tile landed and the S
-//     buffer is free; warps 0-3 (thread = head = TMEM lane) read S, run the
-//     online softmax (running max raised only when it grows by more than 8
-//     in log2 units, so a rescale is rare and every probability stays
-//     <= 2^8) and store their row of P as bf16 (with the row's rescale
-//     factor) straight into CTA 1's shared memory with asynchronous stores
-//     counted in bytes on CTA 1's barrier.
+//     64 values, 128-byte swizzle) by TMA into a ring of 24 KB units (3
+//     column blocks each); warp 4 issues a tile's 36 S MMAs (N = 64 keys, A
+//     from tensor memory, so only K is read from shared memory) a unit at a
+//     time as the units land and the S buffer is free; warps 0-3 (thread =
+//     head = TMEM lane) read S, run the online softmax (running max raised
+//     only when it grows by more than 8 in log2 units, so a rescale is rare
+//     and every probability stays <= 2^8), write their rows of P as bf16
+//     into a per-warp staging slot and send the slot to CTA 1 with one bulk
+//     copy, the row's rescale factor with an asynchronous store, both counted
+//     in bytes on CTA 1's barrier.
 //   * CTA 1 (values) holds O in all 512 columns.  Warp 5 streams the value
-//     part of the same tiles (8 column blocks) into a 2-stage ring, each
-//     tile once CTA 0 reports that its rows landed there (so CTA 1's copies
-//     find them in L2 instead of racing CTA 0's to HBM); warps 0-3 rescale
-//     their O row when CTA 0 raised the max, zero the value rows of keys
-//     outside the stripe, and at the end of an item normalise O and write it
-//     out; warp 4 issues P V (two N = 256 MMAs per 16 keys) and, through a
-//     multicast commit, tells CTA 0 when a P buffer may be overwritten.
+//     part of the same tiles (8 column blocks) into a 2-tile ring, each tile
+//     once CTA 0 reports that its rows landed there (so CTA 1's copies find
+//     them in L2 instead of racing CTA 0's to HBM); warp 4 waits for each
+//     value tile and issues P V (two N = 256 MMAs per 16 keys) and, through a
+//     multicast commit, tells CTA 0 when a P buffer may be overwritten; warps
+//     0-3 rescale their O row when CTA 0 raised the max, zero the value rows
+//     of keys outside the stripe (waiting for that tile only then), and at
+//     the end of an item normalise O and write it out.  Those warps can run
+//     up to three tiles ahead of the MMAs, so their "O ready" and "P V done"
+//     barriers form a ring of four tiles (a parity wait stays unambiguous).
 // O is normalised by the sum of the bf16-rounded probabilities (an exact
 // convex combination of the values); the LSE keeps the fp32 sum.
 //
@@ -48,19 +52,21 @@
 //
 // Fused calls over pages of 64 slots (P * page_size / P = 64) take another
 // grouping.  The P partners hold the 64 slots of a logical page as P runs of
-// page_size / P rows at the same page id of their pools, so one 3-D TMA box
-// per column block -- 64 values x page_size / P rows x P partners, 8 KB --
-// brings the whole logical page into a 64-key tile (row r = partner r /
-// (page_size / P), slot r % (page_size / P); the placement, interleave
-// included, says which position each row holds).  An item is then a token,
-// its tiles are its logical pages, and the online softmax runs over every
-// partner's keys at once: the exact merge of the partner partials happens
-// tile by tile inside it, and the kernel writes the token's final output.
-// With page runs of 16 rows this needs a quarter of the TMA boxes of the
-// per-partner tiles, and the copy engines, not the boxes, set the pace.  The
-// clusters split the sequence of all tiles into equal contiguous ranges; a
-// token that straddles a boundary is cut, its pieces go to workspace slots
-// and the last to finish merges them (with the optional extra partial).
+// page_size / P rows at the same page id of their pools, so one 4-D TMA box
+// -- 64 values x page_size / P rows x P partners x the unit's column blocks
+// -- brings a unit of the whole logical page into a 64-key tile (row r =
+// partner r / (page_size / P), slot r % (page_size / P); the placement,
+// interleave included, says which position each row holds).  An item is
+// then a token, its tiles are its logical pages, and the online softmax runs
+// over every partner's keys at once: the exact merge of the partner partials
+// happens tile by tile inside it, and the kernel writes the token's final
+// output.  With page runs of 16 rows this needs a quarter of the TMA boxes
+// of the per-partner tiles, and the copy engines, not the boxes, set the
+// pace.  The clusters split the sequence of all tiles into contiguous
+// ranges of equal cost, a token start counted as kItemCostTiles tiles; a
+// token that straddles a boundary is cut, its pieces go to workspace slots,
+// and a follow-up kernel (mla_merge_pieces_kernel) merges them with the
+// optional extra partial.
 //
 // Every wait is bounded; one that runs out raises the abort flag of both
 // CTAs, which ends their other waits, and the call reports
@@ -859,6 +865,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t run_bytes = 0;
             if constexpr (!kGroup)
               run_bytes = __popc(__ballot_sync(0xffffffffu, run_row >= 0)) * static_cast<uint32_t>(box_rows) * 128u;
+            else
+              (void)run_bytes;
             int qq = q;
             uint32_t pp = par;
             if constexpr (kGroup) {
