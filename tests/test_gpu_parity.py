@@ -44,6 +44,10 @@ SMALL = {
     "mla_decode": lambda: W.mla_decode(seed=24, batch=3, len_lo=100, len_hi=5000),
     "mla_decode_split": lambda: W.mla_decode(seed=30, batch=3, len_lo=9000, len_hi=20000),
     "mla_decode_short": lambda: W.mla_decode(seed=31, batch=4, len_lo=1, len_hi=40),
+    # many tokens of 1-4 logical pages: the fused split over clusters charges
+    # each token start as 16 pages, so some cluster ranges end inside a
+    # token's start cost and hold none of its pages
+    "mla_many_short": lambda: W.mla_decode(seed=50, batch=40, len_lo=1, len_hi=200),
     # MLA rows of several new tokens (pool partial + causal own-token partial), padding rows after them
     "mla_mixed": lambda: W.build_workload("mla_mixed", dtype="bf16", P=4, page_size=64, num_q_heads=128,
                                           num_kv_heads=1, head_dim=576, head_dim_v=512, mla=True, decode=False,
