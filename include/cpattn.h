@@ -231,20 +231,25 @@ CPATTN_API int cp_paged_attn_partial_ex(const cpattn_pool_desc* desc, const void
 
 /*
  * cp_paged_attn_fused -- the partials of all P partners and their exact merge
- * in one launch: the final attention output of every query token.
+ * in one call: the final attention output of every query token.
  *
  * The method computes one partial (output, LSE) per partner over its stripe
  * and combines them exactly (mstar PR #1124 "Context / Sequence Parallel
  * 1/5", description: each partner returns its partial with its log-sum-exp,
  * merged on the device; vLLM "[Core] Add explicit layer parallel plans",
  * _forward_with_dcp: merge_attn_states of the context and query partials).
- * Here the merge is fused into the partial kernels: every chunk of every
- * partner leaves its partial in the workspace and the last CTA of each
- * (token, KV head) merges them.  The exact merge is associative, so the
- * result is the one cp_paged_attn_partial followed by lse_merge gives, with
- * one launch and no [P, T, Hq, Dv] partial tensor round trip.  Pages give the
- * captured buckets of a step (fixed shapes, replayed as a graph); this call
- * makes no host synchronisation and no allocation, so it can be captured.
+ * Here the merge is fused into the partial kernels.  GQA heads: every chunk
+ * of every partner leaves its partial in the workspace and the last CTA of
+ * each (token, KV head) merges them.  MLA over pages of 64 slots: one tile
+ * holds a logical page of every partner, so the online softmax merges the
+ * partners as it goes and the kernel writes final rows; a token whose pages
+ * are split between two CTA pairs leaves normalised pieces in the workspace,
+ * merged by a second kernel on the same stream.  The exact merge is
+ * associative, so the result is the one cp_paged_attn_partial followed by
+ * lse_merge gives (up to rounding order), without the [P, T, Hq, Dv] partial
+ * tensor round trip.  Pages give the captured buckets of a step (fixed
+ * shapes, replayed as a graph); this call makes no host synchronisation and
+ * no allocation, so it can be captured.
  *
  * Arguments as cp_paged_attn_partial, except:
  *   row_order   optional device [num_rows] permutation of the rows: the order
